@@ -1,0 +1,458 @@
+"""Draft-round benchmark: draft blocks/s and achieved HBM GB/s on one GB300 (replicas for N > 1).
+
+A step is one speculative round for every request of the workload: dflash_project_ctx (the
+round's new context rows), dflash_draft_block, dflash_accept. Default workload: the page-1 DFlash2
+geometry, 4-bit (config c3). Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c3] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dflash_synth as syn  # noqa: E402
+
+Q4_BYTES_PER_PARAM = 0.5 + 4.0 / 64.0   # 4-bit code + bf16 scale and bias per 64 inputs
+BYTES_PER_PARAM = {"q4": Q4_BYTES_PER_PARAM, "bf16": 2.0, "f32": 4.0}
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work of one round
+# ---------------------------------------------------------------------------------------------
+def round_params(cfg) -> dict:
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    layer = cfg.d * (qd + 2 * kvd) + qd * cfg.d + 3 * cfg.d * cfg.inter
+    p = {"W_c": cfg.d * cfg.n_taps * cfg.target_hidden, "layers": cfg.n_layers * layer,
+         "lm_head": cfg.vocab * cfg.target_hidden}
+    if cfg.d != cfg.target_hidden:
+        p["tok_out_proj"] = 2 * cfg.d * cfg.target_hidden
+    return p
+
+
+def round_bytes(cfg, ctx_lens) -> dict:
+    bpp = BYTES_PER_PARAM[cfg.wdtype]
+    b = {k: v * bpp for k, v in round_params(cfg).items()}
+    kvd = cfg.n_kv_heads * cfg.head_dim
+    act = 4 if cfg.adtype == "f32" else 2
+    keys = sum(min(int(P), cfg.window) if cfg.window else int(P) for P in ctx_lens)
+    b["kv"] = cfg.n_layers * keys * kvd * 2 * act
+    b["total"] = sum(b.values())
+    return b
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def load_traffic(kernel: str):
+    """ncu DRAM bytes per launch of `kernel`, if captured on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[kernel]
+        if ent.get("source_hash") != kernel_source_hash():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_block_draft_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [x.strip() for x in vis.split(",")] if vis else []
+        self.dev = ids[device_index] if device_index < len(ids) else str(device_index)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed helpers (replicas: no data-path collective; timing max over ranks)
+# ---------------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_over_ranks(elapsed_s: float, units: float, group=None):
+    """(max elapsed over ranks, sum of units over ranks); identity when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------------------------
+def oracle_round_seconds(cfg, model, rounds: int = 1, scale_rows: int = 1):
+    """Wall time of the oracle for one round of request 0 (ctx rows projected, block drafted over
+    a full window, accept). The context window's K/V are drawn from the generator (the oracle's
+    cost does not depend on their values), so no multi-minute prefill is needed.
+    scale_rows > 1 times only 1/scale_rows of every matrix's output rows and scales up."""
+    import oracle
+    n_new = cfg.appends()[0]
+    P = cfg.ctx_len
+    nwin = min(P, cfg.window) if cfg.window else P
+    kvd = cfg.n_kv_heads * cfg.head_dim
+    k = syn.normal(cfg.seed, "bench.kctx", (cfg.n_layers, nwin, kvd), 1.0).astype(np.float64)
+    v = syn.normal(cfg.seed, "bench.vctx", (cfg.n_layers, nwin, kvd), 1.0).astype(np.float64)
+    taps = syn.taps_to_f32(cfg, syn.taps_rows(cfg, cfg.seed, 0, P, n_new)).astype(np.float64)
+    if scale_rows == 1:
+        o = oracle.Oracle(model)
+        times = []
+        for r in range(rounds):
+            t0 = time.perf_counter()
+            kn, vn = o.ctx_rows(taps)
+            kk = np.concatenate([k, kn], axis=1)[:, -nwin:] if cfg.window else np.concatenate([k, kn], axis=1)
+            vv = np.concatenate([v, vn], axis=1)[:, -nwin:] if cfg.window else np.concatenate([v, vn], axis=1)
+            out = o.draft(int(syn.anchors(cfg.seed, 1, r, cfg.vocab)[0]), np.ascontiguousarray(kk),
+                          np.ascontiguousarray(vv))
+            t = syn.target_tokens(cfg.seed, 0, r, out["tokens"], cfg.agree or 0.0, cfg.vocab)
+            oracle.accept(out["tokens"], t)
+            times.append(time.perf_counter() - t0)
+        return times
+    # sampled step: the oracle's projections on a row slice of every matrix of the round
+    import dflash_synth
+    G = cfg.gamma
+    xs = {}
+    t0 = time.perf_counter()
+    for name, hm in model.mats.items():
+        if name == "embed":
+            continue
+        rows = max(16, hm.n_out // scale_rows)
+        part = dflash_synth.HostMatrix(hm.fmt, rows, hm.n_in, hm.data[:rows],
+                                       None if hm.scale is None else hm.scale[:rows],
+                                       None if hm.bias is None else hm.bias[:rows])
+        nrow = n_new if name == "W_c" else (G - 1 if name in ("lm_head", "out_proj") else G)
+        if name not in xs or xs[name].shape != (nrow, hm.n_in):
+            xs[name] = syn.normal(cfg.seed, "bench.x", (nrow, hm.n_in), 1.0).astype(np.float64)
+        oracle.linear(part, xs[name])
+        if name.endswith((".k", ".v")):
+            oracle.linear(part, xs[name][:1].repeat(n_new, axis=0))
+    return [(time.perf_counter() - t0) * scale_rows]
+
+
+def run_reference(args, cfg):
+    """The CPU oracle as the reference arm, on this arm's workload and metric."""
+    rank, ws, _ = dist_env()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(threads))
+    model = syn.make_model(cfg)
+    est = oracle_round_seconds(cfg, model, rounds=1)[0]
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    scale = max(1, int(np.ceil(est / per_step)))
+    for _ in range(args.warmup):
+        oracle_round_seconds(cfg, model, rounds=1, scale_rows=scale)
+    times = []
+    for _ in range(args.steps):
+        times.extend(oracle_round_seconds(cfg, model, rounds=1, scale_rows=scale))
+    total = sum(times)
+    value = len(times) / total     # blocks of one request per second
+    sample = ("one full round of request 0 per step" if scale == 1 else
+              f"per step the round's projections on 1/{scale} of every matrix's rows, time x{scale}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg),
+            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "draft blocks/s (4-bit 5120-wide DFlash2 drafter round: context projection + block draft + accept)"
+
+
+def workload_config(cfg) -> dict:
+    return {"workload": (f"{cfg.name}: L{cfg.n_layers} d{cfg.d} {cfg.n_q_heads}/{cfg.n_kv_heads}x{cfg.head_dim} "
+                         f"I{cfg.inter} taps {cfg.n_taps}xH{cfg.target_hidden} V{cfg.vocab} gamma{cfg.gamma} "
+                         f"window{cfg.window} ctx{cfg.ctx_len} batch{cfg.batch} weights {cfg.wdtype}"),
+            "requests": cfg.batch, "gamma": cfg.gamma, "ctx_len": cfg.ctx_len, "window": cfg.window,
+            "new_ctx_rows_per_round": list(cfg.appends()),
+            "l2": "no flush: every round streams >1.4 GB of weights, far above the 129 MB L2"}
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c3")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    cfg = syn.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+    import torch.distributed as dist
+
+    import speculative_block_draft_gb300 as pkg
+    from speculative_block_draft_gb300.session import Session
+
+    rank, ws, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.build()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    # ---- drafter, context, per-step inputs resident in HBM -----------------------------------
+    model = syn.make_model(cfg)
+    B, G, n = cfg.batch, cfg.gamma, cfg.gamma - 1
+    sess = Session(model, max_batch=B, ctx_capacity=(cfg.window if cfg.window else
+                                                      cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + 8)))
+    h, stream = sess.h, sess.stream
+    lengths = syn.ctx_lengths(cfg)
+    width = cfg.n_taps * cfg.target_hidden
+    for b in range(B):
+        done = 0
+        while done < int(lengths[b]):
+            m = min(4096, int(lengths[b]) - done)
+            rows = syn.taps_rows(cfg, cfg.seed + rank, b, done, m)
+            assert sess.project([b], [m], rows) == 0
+            done += m
+    total_steps = args.warmup + args.steps
+    counts = [syn.append_counts(cfg, s) for s in range(total_steps + args.e2e_steps)]
+    pos = lengths.astype(np.int64).copy()
+    step_taps, step_anchor, step_target = [], [], []
+    for s in range(total_steps + args.e2e_steps):
+        rows = [syn.taps_rows(cfg, cfg.seed + rank, b, int(pos[b]), int(counts[s][b])) for b in range(B)]
+        pos += counts[s]
+        step_taps.append(np.concatenate(rows))
+        step_anchor.append(syn.anchors(cfg.seed + rank, B, s, cfg.vocab))
+        step_target.append(syn.tokens(cfg.seed + rank, "bench.target", B * G, cfg.vocab, offset=s * B * G)
+                           .reshape(B, G))
+    dev_taps = [sess.upload(t) for t in step_taps[:total_steps]]
+    dev_anchor = [sess.upload(a) for a in step_anchor[:total_steps]]
+    dev_target = [sess.upload(t) for t in step_target[:total_steps]]
+    draft = torch.empty((B, n), dtype=torch.int32, device=dev)
+    conf = torch.empty((B, n), dtype=torch.float32, device=dev)
+    acc_len = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    req = list(range(B))
+
+    def step(s, probe=None):
+        c = [int(x) for x in counts[s]]
+        h.project_ctx(req, c, dev_taps[s], stream=stream)
+        if probe is not None:
+            h.set_probe(*probe)
+        rc = h.draft_block(req, dev_anchor[s], draft, conf, None, stream=stream)
+        assert rc == 0
+        h.accept(draft, dev_target[s], acc_len, nxt, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s)
+    stream.synchronize()
+    assert h.check_errors(stream) == 0
+
+    # ---- timed region: K rounds, inputs resident ---------------------------------------------
+    probes = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = h.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        torch.cuda.nvtx.range_push("timed")
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                step(args.warmup + i, probe=probes[i])
+            ev1.record(stream)
+        stream.synchronize()
+        torch.cuda.nvtx.range_pop()
+    barrier()
+    torch.cuda.synchronize()
+    launches = h.launch_count() - launches0
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    assert h.check_errors(stream) == 0
+    lm_ms = float(np.mean([a.elapsed_time(b) for a, b in probes]))
+    t_max, blocks = reduce_over_ranks(elapsed, float(B * args.steps))
+    value = blocks / t_max
+
+    # ---- end to end through the C ABI with host buffers --------------------------------------
+    pin_taps = [torch.from_numpy(t.view(np.int16) if t.dtype == np.uint16 else t).pin_memory()
+                for t in step_taps[total_steps:]]
+    pin_anchor = [torch.from_numpy(a).pin_memory() for a in step_anchor[total_steps:]]
+    pin_target = [torch.from_numpy(t).pin_memory() for t in step_target[total_steps:]]
+    out_draft = torch.empty((B, n), dtype=torch.int32).pin_memory()
+    out_len = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_nxt = torch.empty(B, dtype=torch.int32).pin_memory()
+    d_taps = torch.empty((max(t.shape[0] for t in pin_taps), width), dtype=pin_taps[0].dtype, device=dev)
+    d_anchor = torch.empty(B, dtype=torch.int32, device=dev)
+    d_target = torch.empty((B, G), dtype=torch.int32, device=dev)
+    h2d = d2h = 0
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.e2e_steps):
+            s = total_steps + i
+            nt = pin_taps[i].shape[0]
+            d_taps[:nt].copy_(pin_taps[i], non_blocking=True)
+            d_anchor.copy_(pin_anchor[i], non_blocking=True)
+            d_target.copy_(pin_target[i], non_blocking=True)
+            h.project_ctx(req, [int(x) for x in counts[s]], d_taps, stream=stream)
+            assert h.draft_block(req, d_anchor, draft, conf, None, stream=stream) == 0
+            h.accept(draft, d_target, acc_len, nxt, stream=stream)
+            out_draft.copy_(draft, non_blocking=True)
+            out_len.copy_(acc_len, non_blocking=True)
+            out_nxt.copy_(nxt, non_blocking=True)
+            stream.synchronize()          # the host needs the accepted length before the next round
+            h2d += pin_taps[i][:nt].numel() * pin_taps[i].element_size() + 4 * B + 4 * B * G
+            d2h += 4 * B * n + 8 * B
+        e1.record(stream)
+    stream.synchronize()
+    e2e_t, e2e_blocks = reduce_over_ranks(e0.elapsed_time(e1) / 1e3, float(B * args.e2e_steps))
+    e2e_value = e2e_blocks / e2e_t
+
+    if rank != 0:
+        sess.close()
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    rb = round_bytes(cfg, lengths)
+    lm_bytes = round_bytes(cfg, lengths)["lm_head"]
+    lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
+    traffic = load_traffic("lm_head")
+    line = {
+        "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(cfg),
+        "round_hbm": {"algorithmic_bytes": rb["total"], "breakdown_mb": {k: round(v / 1e6, 1) for k, v in rb.items()},
+                      "achieved_gbs": rb["total"] / (t_max / args.steps) / 1e9,
+                      "peak_gbs": peaks["hbm_gbs"],
+                      "frac": rb["total"] / (t_max / args.steps) / 1e9 / peaks["hbm_gbs"],
+                      "peak_source": peaks["source"]},
+        "roofline": {"kernel": "LM head (4-bit GEMV + fused argmax/softmax confidence), 1 launch per round",
+                     "bound": "hbm", "achieved": lm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": lm_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": lm_bytes, "avg_launch_ms": lm_ms,
+                     "peak_source": f"{peaks['source']} (burst copy, MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": e2e_value, "unit": "blocks/s", "h2d_bytes_per_step": h2d // max(1, args.e2e_steps),
+                "d2h_bytes_per_step": d2h // max(1, args.e2e_steps), "steps": args.e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and ws >= 1:
+        threads = os.cpu_count() or 1
+        times = oracle_round_seconds(cfg, model, rounds=2)
+        cpu_v = 1.0 / (sum(times) / len(times))
+        line["cpu_baseline"] = {"value": cpu_v, "unit": "blocks/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{len(times)} rounds of request 0 (project {cfg.appends()[0]} ctx rows, "
+                                          f"draft one block over the full window, accept); window K/V drawn "
+                                          f"from the generator"}
+    print(json.dumps(line), flush=True)
+    sess.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

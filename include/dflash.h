@@ -1,0 +1,183 @@
+/*
+ * dflash.h -- C ABI of the GB300 (sm_103a) DFlash / DFlash2 block-drafter round.
+ *
+ * One speculative round is three calls on one CUDA stream:
+ *   dflash_project_ctx  context rows: Eq 2 of the dflash.ts page (H_ctx = RMSNorm(W_c [H^l1;..;H^lm]))
+ *                       and each layer's K_i = W_k^i RMSNorm(H_ctx), V_i = W_v^i RMSNorm(H_ctx),
+ *                       appended to a per-layer context K/V cache ("projectContextRows": the rows do
+ *                       not depend on the block, so each position is projected once).
+ *   dflash_draft_block  the block pass: block rows (anchor embedding + block_pos, mask_emb + block_pos),
+ *                       the Eq 3 KV-injection layers (non-causal attention of the block over
+ *                       [windowed context ++ block], SwiGLU MLP), out_norm, the borrowed target LM head,
+ *                       greedy token and softmax confidence for block rows 1..gamma-1.
+ *   dflash_accept       greedy acceptance: longest prefix of drafts equal to the target's greedy
+ *                       tokens; the bonus token becomes the next anchor ("Inco Hacks Native: DFlash 2
+ *                       Speculation", section 3: bs=8 accepted=7 committed=8).
+ *
+ * Conventions
+ *  - Every projection matrix is output-major W[n_out][n_in] (y = W x) in one storage format:
+ *      DFLASH_F32   float      [n_out][n_in]
+ *      DFLASH_BF16  bf16 bits  [n_out][n_in]
+ *      DFLASH_Q4G64 uint32     [n_out][n_in/8] (nibble i of word j = input 8j+i, low nibble first)
+ *                   + scale, bias bf16 bits [n_out][n_in/64]; element = scale*q + bias
+ *    Norm weights, mask_emb [gamma-1][d] and block_pos [gamma][d] are float32.
+ *  - All pointers passed to the calls below are DEVICE pointers unless stated otherwise.
+ *  - Ownership: the caller allocates every device buffer (weights, workspace, inputs, outputs).
+ *    The library never calls cudaMalloc/cudaFree. dflash_create copies and re-lays-out the
+ *    drafter weights and the target LM head into the workspace; the source weight buffers may be
+ *    freed once the create stream has been synchronised. The target embedding table is BORROWED
+ *    (the drafter has no embedding of its own, "A Refusal Is Not A Failure", section "What the port
+ *    taught"): it must stay alive and unchanged for the handle's lifetime.
+ *  - Calls only enqueue work on the given stream and never synchronise, except dflash_check_errors.
+ *  - Calls are validated on the host before any launch; a rejected call changes no state.
+ *  - Temperature != 0, or the environment variable DFLASH_DISABLE=1, make dflash_draft_block return
+ *    DFLASH_DECLINED without doing any work: the caller falls back to plain autoregressive decoding
+ *    ("A Refusal Is Not A Failure", section "The rule it earned": an acceleration path may decline a
+ *    request, it must never fail one).
+ *  - Handles are not thread-safe; use one handle per thread or serialise calls.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_MAX_LAYERS 8
+#define DFLASH_MAX_BATCH 64
+#define DFLASH_MAX_GAMMA 16
+
+enum dflash_status {
+  DFLASH_OK = 0,
+  DFLASH_DECLINED = 1,    /* not drafted on purpose (temperature > 0, kill switch); not an error */
+  DFLASH_EINVAL = -1,     /* bad shape, null pointer, unsupported combination */
+  DFLASH_ECAPACITY = -2,  /* context cache or batch capacity exceeded */
+  DFLASH_ECUDA = -3,      /* a CUDA runtime call failed */
+  DFLASH_ETIMEOUT = -4,   /* a bounded device-side wait gave up (reported by dflash_check_errors) */
+};
+
+enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_Q4G64 = 2 };
+
+typedef struct {
+  int n_layers;       /* drafter layers L (<= DFLASH_MAX_LAYERS) */
+  int d;              /* draft width; n_q_heads * head_dim == d */
+  int n_q_heads, n_kv_heads, head_dim;   /* head_dim in {64, 128, 256}; n_q_heads % n_kv_heads == 0 */
+  int inter;          /* SwiGLU inner width */
+  int n_taps;         /* m tapped target layers */
+  int target_hidden;  /* H; tok_proj / out_proj exist iff d != H */
+  int vocab;          /* V */
+  int gamma;          /* block size (2..DFLASH_MAX_GAMMA); gamma-1 drafts per block */
+  int window;         /* sliding window over context rows; 0 = the whole context */
+  int max_batch;      /* request slots (<= DFLASH_MAX_BATCH) */
+  int ctx_capacity;   /* context rows kept per request and layer. With window > 0 the cache is a
+                         ring of this many rows and must hold >= window rows; with window == 0 it
+                         bounds the total context length of a request. */
+  float eps;          /* RMSNorm epsilon */
+  int wdtype;         /* storage of every projection matrix, the embedding and the LM head */
+  int adtype;         /* DFLASH_F32 (fp32 taps, cache and CUDA-core arithmetic) or DFLASH_BF16
+                         (bf16 taps and cache, tensor-core projections with fp32 accumulation).
+                         DFLASH_F32 requires wdtype DFLASH_F32. */
+} dflash_config;
+
+typedef struct {
+  const void* data;   /* see the storage formats above */
+  const void* scale;  /* DFLASH_Q4G64 only */
+  const void* bias;   /* DFLASH_Q4G64 only */
+} dflash_matrix;
+
+typedef struct {
+  dflash_matrix wq, wk, wv, wo;        /* [Hq*hd][d], [Hkv*hd][d], [Hkv*hd][d], [d][Hq*hd] */
+  dflash_matrix w_gate, w_up, w_down;  /* [inter][d], [inter][d], [d][inter] */
+  const float* attn_norm;              /* [d]; used for the block rows AND the context rows */
+  const float* ff_norm;                /* [d] */
+} dflash_layer_weights;
+
+typedef struct {
+  dflash_matrix w_c;        /* [d][n_taps*H]  Eq 2 context projection */
+  dflash_matrix tok_proj;   /* [d][H]  only when d != H */
+  dflash_matrix out_proj;   /* [H][d]  only when d != H */
+  dflash_matrix embed;      /* [V][H]  the target's embedding table (borrowed, see above) */
+  dflash_matrix lm_head;    /* [V][H]  the target's output head (copied into the workspace) */
+  const float* ctx_norm;    /* [d] */
+  const float* mask_emb;    /* [gamma-1][d] */
+  const float* block_pos;   /* [gamma][d] */
+  const float* out_norm;    /* [d] */
+  dflash_layer_weights layer[DFLASH_MAX_LAYERS];
+} dflash_weights;
+
+typedef struct dflash_handle dflash_handle;
+
+typedef struct {
+  uint64_t rounds;          /* successful dflash_draft_block calls */
+  uint64_t blocks;          /* request-blocks drafted */
+  uint64_t declined;        /* dflash_draft_block calls that returned DFLASH_DECLINED */
+  uint64_t ctx_rows;        /* context rows projected */
+  uint64_t accept_calls;    /* dflash_accept calls */
+} dflash_stats;
+
+/* Bytes of device workspace dflash_create needs for this configuration (0 if invalid). */
+size_t dflash_workspace_bytes(const dflash_config* cfg);
+
+/* Validate cfg, lay out the workspace (>= dflash_workspace_bytes, 256-byte aligned, device
+ * memory owned by the caller), re-lay-out the weights into it and zero all state, all on
+ * `stream` (a cudaStream_t; NULL = legacy default stream). *out receives a host-side handle. */
+int dflash_create(const dflash_config* cfg, const dflash_weights* weights, void* workspace,
+                  size_t workspace_bytes, void* stream, dflash_handle** out);
+
+/* Append context rows (Eq 2 plus each layer's K/V projection of the retained context).
+ * req_ids [n_req], n_new [n_req]: HOST arrays; request slots are 0..max_batch-1, each at most once.
+ * taps: device [sum(n_new)][n_taps*H] (fp32 or bf16 per adtype), rows of request i after those of
+ * request i-1; row j of request i is context position P_i + j, where P_i is the request's
+ * current context length. Every request's P grows by n_new[i].
+ * Returns DFLASH_ECAPACITY if window == 0 and a request would exceed ctx_capacity. */
+int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, const int32_t* n_new,
+                       const void* taps, void* stream);
+
+/* Draft one block per request. req_ids: HOST [n_req]. anchor: device int32 [n_req], the last
+ * committed token of each request. Outputs (device): draft int32 [n_req][gamma-1] (greedy tokens of
+ * block rows 1..gamma-1), conf float [n_req][gamma-1] (softmax probability of the drafted token;
+ * may be NULL), logits float [n_req][gamma-1][V] (may be NULL; written only when given).
+ * Attention of each request reads its context rows [max(0, P - window), P) (all when window == 0)
+ * and all gamma block rows, with no causal mask. temperature != 0 -> DFLASH_DECLINED. */
+int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, const int32_t* anchor,
+                       float temperature, int32_t* draft, float* conf, float* logits, void* stream);
+
+/* Greedy acceptance for n_req requests (independent of any handle state except gamma).
+ * draft int32 [n_req][gamma-1], target int32 [n_req][gamma] (the target's greedy tokens after
+ * [anchor, d_1..d_{gamma-1}]). Outputs: accept_len int32 [n_req] = longest prefix with
+ * draft == target; next_anchor int32 [n_req] = target[accept_len]; accept_len + 1 tokens commit. */
+int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* target,
+                  int32_t* accept_len, int32_t* next_anchor, void* stream);
+
+/* Forget a request slot's context (its length returns to 0). Host-only; no device work. */
+int dflash_reset_request(dflash_handle* h, int req_id);
+
+/* Current context length of a request slot (host mirror), or -1 for a bad slot. */
+int64_t dflash_ctx_len(const dflash_handle* h, int req_id);
+
+/* Synchronise `stream`, then read and clear the device error word. Returns DFLASH_ETIMEOUT if a
+ * bounded device wait gave up since the last check, DFLASH_ECUDA on a CUDA error, else DFLASH_OK. */
+int dflash_check_errors(dflash_handle* h, void* stream);
+
+/* Host-side counters. */
+int dflash_get_stats(const dflash_handle* h, dflash_stats* out);
+
+/* Record two caller-created CUDA events (cudaEvent_t) around the launch of one kernel of the
+ * next dflash_draft_block call, for live per-kernel timing. kernel: 0 = the LM head (the largest
+ * launch of the round). Events are used once, then forgotten. */
+int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop_event);
+
+/* Kernel launches issued by this handle since create (all calls), for launch accounting. */
+uint64_t dflash_launch_count(const dflash_handle* h);
+
+void dflash_destroy(dflash_handle* h);
+
+const char* dflash_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,282 @@
+"""Python binding of the GB300 DFlash draft-round library (include/dflash.h).
+
+Argument marshalling only: every step of the round runs in the CUDA kernels of ``libdflash.so``
+(built in-tree from ``csrc/`` for sm_103a). PyTorch provides device memory and streams. There is
+no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
+_BUILD = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_BUILD, "libdflash.so")
+_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu"]
+_HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh"]
+NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a",
+              "-Xcompiler", "-fPIC"]
+
+DFLASH_OK, DFLASH_DECLINED, DFLASH_EINVAL, DFLASH_ECAPACITY, DFLASH_ECUDA, DFLASH_ETIMEOUT = 0, 1, -1, -2, -3, -4
+DFLASH_F32, DFLASH_BF16, DFLASH_Q4G64 = 0, 1, 2
+DFLASH_MAX_LAYERS = 8
+DFLASH_MAX_BATCH = 64
+DTYPE = {"f32": DFLASH_F32, "bf16": DFLASH_BF16, "q4": DFLASH_Q4G64}
+
+
+def _nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a (one -gencode) into _build/libdflash.so, in parallel."""
+    os.makedirs(_BUILD, exist_ok=True)
+    deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS] + [os.path.join(_INCLUDE, "dflash.h")]
+    newest = max(os.path.getmtime(p) for p in deps)
+    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
+        return LIB_PATH
+    nvcc = _nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(_BUILD, src.replace(".cu", ".o"))
+        cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(_CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+        if verbose and r.stderr:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, _SOURCES))
+    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    r = subprocess.run([nvcc, "-shared", "-cudart", "shared", *objs, "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+# ---------------------------------------------------------------------------------------------
+# ctypes mirrors of include/dflash.h
+# ---------------------------------------------------------------------------------------------
+class dflash_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter", "n_taps", "target_hidden", "vocab",
+        "gamma", "window", "max_batch", "ctx_capacity")] + \
+        [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int)]
+
+
+class dflash_matrix(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+
+
+class dflash_layer_weights(ctypes.Structure):
+    _fields_ = [(n, dflash_matrix) for n in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")] + \
+               [("attn_norm", ctypes.c_void_p), ("ff_norm", ctypes.c_void_p)]
+
+
+class dflash_weights(ctypes.Structure):
+    _fields_ = [(n, dflash_matrix) for n in ("w_c", "tok_proj", "out_proj", "embed", "lm_head")] + \
+               [(n, ctypes.c_void_p) for n in ("ctx_norm", "mask_emb", "block_pos", "out_norm")] + \
+               [("layer", dflash_layer_weights * DFLASH_MAX_LAYERS)]
+
+
+class dflash_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("rounds", "blocks", "declined", "ctx_rows", "accept_calls")]
+
+
+_lib = None
+SYMBOLS = ["dflash_workspace_bytes", "dflash_create", "dflash_project_ctx", "dflash_draft_block",
+           "dflash_accept", "dflash_reset_request", "dflash_ctx_len", "dflash_check_errors",
+           "dflash_get_stats", "dflash_set_probe", "dflash_launch_count", "dflash_destroy",
+           "dflash_status_str"]
+
+
+def lib():
+    """Load libdflash.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdflash.so is not built ({LIB_PATH}); run speculative_block_draft_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        P = ctypes.POINTER
+        L.dflash_workspace_bytes.restype = ctypes.c_size_t
+        L.dflash_workspace_bytes.argtypes = [P(dflash_config)]
+        L.dflash_create.restype = i32
+        L.dflash_create.argtypes = [P(dflash_config), P(dflash_weights), vp, ctypes.c_size_t, vp, P(vp)]
+        L.dflash_project_ctx.restype = i32
+        L.dflash_project_ctx.argtypes = [vp, i32, vp, vp, vp, vp]
+        L.dflash_draft_block.restype = i32
+        L.dflash_draft_block.argtypes = [vp, i32, vp, vp, f32, vp, vp, vp, vp]
+        L.dflash_accept.restype = i32
+        L.dflash_accept.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+        L.dflash_reset_request.restype = i32
+        L.dflash_reset_request.argtypes = [vp, i32]
+        L.dflash_ctx_len.restype = ctypes.c_int64
+        L.dflash_ctx_len.argtypes = [vp, i32]
+        L.dflash_check_errors.restype = i32
+        L.dflash_check_errors.argtypes = [vp, vp]
+        L.dflash_get_stats.restype = i32
+        L.dflash_get_stats.argtypes = [vp, P(dflash_stats)]
+        L.dflash_set_probe.restype = i32
+        L.dflash_set_probe.argtypes = [vp, i32, vp, vp]
+        L.dflash_launch_count.restype = ctypes.c_uint64
+        L.dflash_launch_count.argtypes = [vp]
+        L.dflash_destroy.restype = None
+        L.dflash_destroy.argtypes = [vp]
+        L.dflash_status_str.restype = ctypes.c_char_p
+        L.dflash_status_str.argtypes = [i32]
+        _lib = L
+    return _lib
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lib().dflash_status_str(status).decode()} ({status})")
+
+
+def _check(status: int, what: str) -> int:
+    if status < 0:
+        raise DFlashError(status, what)
+    return status
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _int_array(xs):
+    arr = (ctypes.c_int32 * len(xs))(*[int(x) for x in xs])
+    return arr
+
+
+def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = None) -> dflash_config:
+    """dflash_config for a dflash_synth.DraftConfig."""
+    mb = max_batch or cfg.batch
+    if ctx_capacity is None:
+        ctx_capacity = cfg.window if cfg.window > 0 else cfg.ctx_len + 64 * cfg.gamma
+    return dflash_config(cfg.n_layers, cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.inter, cfg.n_taps,
+                         cfg.target_hidden, cfg.vocab, cfg.gamma, cfg.window, mb, ctx_capacity, cfg.eps,
+                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype])
+
+
+class DeviceModel:
+    """A dflash_synth.HostModel uploaded to device tensors, plus the dflash_weights pointing at them."""
+
+    def __init__(self, host_model, device="cuda"):
+        import torch
+        self.cfg = host_model.cfg
+        self.tensors = {}
+
+        def t(name, a):
+            x = torch.from_numpy(a).to(device)
+            self.tensors.setdefault(name, []).append(x)
+            return x.data_ptr()
+
+        def m(name):
+            hm = host_model.mats.get(name)
+            if hm is None:
+                return dflash_matrix(None, None, None)
+            view = {"uint32": "int32", "uint16": "int16"}.get(hm.data.dtype.name)
+            data = hm.data.view(view) if view else hm.data
+            if hm.scale is None:
+                return dflash_matrix(t(name, data), None, None)
+            return dflash_matrix(t(name, data), t(name, hm.scale.view("int16")), t(name, hm.bias.view("int16")))
+
+        w = dflash_weights()
+        w.w_c, w.tok_proj, w.out_proj = m("W_c"), m("tok_proj"), m("out_proj")
+        w.embed, w.lm_head = m("embed"), m("lm_head")
+        v = host_model.vecs
+        w.ctx_norm, w.block_pos, w.out_norm = t("ctx_norm", v["ctx_norm"]), t("block_pos", v["block_pos"]), \
+            t("out_norm", v["out_norm"])
+        w.mask_emb = t("mask_emb", v["mask_emb"]) if v["mask_emb"].size else None
+        for i in range(self.cfg.n_layers):
+            L = w.layer[i]
+            L.wq, L.wk, L.wv, L.wo = (m(f"bb.{i}.{n}") for n in ("q", "k", "v", "o"))
+            L.w_gate, L.w_up, L.w_down = (m(f"bb.{i}.{n}") for n in ("gate", "up", "down"))
+            L.attn_norm = t(f"bb.{i}.attn_norm", v[f"bb.{i}.attn_norm"])
+            L.ff_norm = t(f"bb.{i}.ff_norm", v[f"bb.{i}.ff_norm"])
+        self.weights = w
+
+    def free(self, keep=("embed",)):
+        """Drop the device copies the handle no longer needs after dflash_create (the embedding
+        table is borrowed by the handle and must be kept)."""
+        self.tensors = {k: v for k, v in self.tensors.items() if k in keep}
+
+
+class Handle:
+    """Owns a workspace tensor and a dflash_handle. Methods map 1:1 onto the C calls."""
+
+    def __init__(self, cfg: dflash_config, weights: dflash_weights, stream=None, device="cuda"):
+        import torch
+        self.cfg = cfg
+        nbytes = lib().dflash_workspace_bytes(ctypes.byref(cfg))
+        if nbytes == 0:
+            raise DFlashError(DFLASH_EINVAL, "dflash_workspace_bytes")
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        base = (self.workspace.data_ptr() + 255) // 256 * 256
+        self.workspace_bytes = nbytes
+        h = ctypes.c_void_p()
+        _check(lib().dflash_create(ctypes.byref(cfg), ctypes.byref(weights), base, nbytes, _stream_ptr(stream),
+                                   ctypes.byref(h)), "dflash_create")
+        self.h = h
+
+    def project_ctx(self, req_ids, n_new, taps, stream=None) -> int:
+        return _check(lib().dflash_project_ctx(self.h, len(req_ids), _int_array(req_ids), _int_array(n_new),
+                                               taps.data_ptr() if taps is not None else None, _stream_ptr(stream)),
+                      "dflash_project_ctx")
+
+    def draft_block(self, req_ids, anchor, draft, conf=None, logits=None, temperature=0.0, stream=None) -> int:
+        return _check(lib().dflash_draft_block(self.h, len(req_ids), _int_array(req_ids), anchor.data_ptr(),
+                                               float(temperature), draft.data_ptr(),
+                                               conf.data_ptr() if conf is not None else None,
+                                               logits.data_ptr() if logits is not None else None,
+                                               _stream_ptr(stream)), "dflash_draft_block")
+
+    def accept(self, draft, target, accept_len, next_anchor, stream=None) -> int:
+        return _check(lib().dflash_accept(self.h, draft.shape[0], draft.data_ptr(), target.data_ptr(),
+                                          accept_len.data_ptr(), next_anchor.data_ptr(), _stream_ptr(stream)),
+                      "dflash_accept")
+
+    def reset_request(self, req_id: int) -> int:
+        return _check(lib().dflash_reset_request(self.h, req_id), "dflash_reset_request")
+
+    def ctx_len(self, req_id: int) -> int:
+        return lib().dflash_ctx_len(self.h, req_id)
+
+    def check_errors(self, stream=None) -> int:
+        return _check(lib().dflash_check_errors(self.h, _stream_ptr(stream)), "dflash_check_errors")
+
+    def stats(self) -> dict:
+        s = dflash_stats()
+        _check(lib().dflash_get_stats(self.h, ctypes.byref(s)), "dflash_get_stats")
+        return {n: getattr(s, n) for n, _ in dflash_stats._fields_}
+
+    def set_probe(self, start_event, stop_event, kernel: int = 0) -> int:
+        return _check(lib().dflash_set_probe(self.h, kernel, start_event.cuda_event, stop_event.cuda_event),
+                      "dflash_set_probe")
+
+    def launch_count(self) -> int:
+        return lib().dflash_launch_count(self.h)
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,867 @@
+// Host side of the C ABI in include/dflash.h: validation, workspace layout, weight re-layout at
+// create, launch planning and the three calls of a draft round.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "internal.h"
+
+using namespace dfl;
+
+namespace {
+
+struct PackedMat {
+  uint8_t* w = nullptr;
+  int n_rows = 0;    // logical rows
+  int n_strips = 0;  // ceil(n_rows / 16)
+  int k = 0, groups = 0;
+};
+
+struct GemvPlan {
+  int n_slices, gps, ctas_per_slice, grid;
+};
+
+}  // namespace
+
+struct dflash_handle {
+  dflash_config cfg;
+  int fmt = 0, act_f32 = 0, act_bytes = 2;
+  int d = 0, H = 0, qd = 0, kvd = 0, I = 0, L = 0, G = 0, V = 0, mH = 0, cap = 0;
+  int n_sm = 148, r_blk = 0, ssq_ld = 0;
+  size_t ws_bytes = 0;
+
+  PackedMat wc, qkv[DFLASH_MAX_LAYERS], wo[DFLASH_MAX_LAYERS], gu[DFLASH_MAX_LAYERS], down[DFLASH_MAX_LAYERS],
+      tok, outp, lm;
+  dflash_matrix embed{};
+  float *ctx_norm = nullptr, *mask_emb = nullptr, *block_pos = nullptr, *out_norm = nullptr;
+  float *attn_norm = nullptr, *ff_norm = nullptr;  // [L][d]
+  void *kc = nullptr, *vc = nullptr;               // [L][max_batch][Hkv][cap][hd]
+  float* h = nullptr;
+  void *xn = nullptr, *q = nullptr, *kb = nullptr, *vb = nullptr, *attn = nullptr, *act = nullptr, *hout = nullptr,
+       *emb = nullptr, *xw = nullptr;
+  float *tokrow = nullptr, *ssq = nullptr, *ssq_ctx = nullptr;
+  float* partials = nullptr;
+  int* tickets = nullptr;
+  float* lm_part = nullptr;
+  int* lm_ticket = nullptr;
+  float *att_o = nullptr, *att_ml = nullptr;
+  int* att_tickets = nullptr;
+  unsigned* err = nullptr;
+  size_t partial_floats = 0;
+  int ticket_count = 0, lm_grid_max = 0, att_pairs_max = 0;
+  CUtensorMap kmap{}, vmap{};
+
+  int64_t ctx_len[DFLASH_MAX_BATCH] = {};
+  dflash_stats stats{};
+  uint64_t launches = 0;
+  cudaEvent_t probe_start = nullptr, probe_stop = nullptr;
+};
+
+namespace {
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int packed_bytes_per_strip(int fmt, int k) {
+  if (fmt == FMT_Q4) return (k / 64) * kQ4GroupBytes;
+  if (fmt == FMT_BF16) return (k / 64) * kBf16GroupBytes;
+  return 16 * k * 4;
+}
+
+int nt_for(int R) { return R <= 8 ? 1 : (R <= 16 ? 2 : 4); }
+
+GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R) {
+  GemvPlan p{};
+  if (h->fmt == FMT_F32) {
+    p.n_slices = 1;
+    p.gps = groups;
+    p.ctas_per_slice = std::max(1, std::min((n_strips + kF32Warps - 1) / kF32Warps, 4 * h->n_sm));
+    p.grid = p.ctas_per_slice;
+    return p;
+  }
+  const int rp = nt_for(R) * 8;
+  const int gps_max = std::max(1, (kXBudget / rp - 16) / 128);
+  const int ctas = std::max(1, std::min((n_strips + kWarps - 1) / kWarps, h->n_sm));
+  int s = std::max(1, (int)lround((double)h->n_sm / ctas));
+  s = std::min(s, groups);
+  int gps = (groups + s - 1) / s;
+  gps = std::min(gps, gps_max);
+  s = (groups + gps - 1) / gps;
+  p.n_slices = s;
+  p.gps = gps;
+  p.ctas_per_slice = ctas;
+  p.grid = s * ctas;
+  return p;
+}
+
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t bytes) {
+    off = round_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+bool valid_config(const dflash_config* c) {
+  if (!c) return false;
+  if (c->n_layers < 1 || c->n_layers > DFLASH_MAX_LAYERS) return false;
+  if (c->d <= 0 || c->d % 64 || c->inter <= 0 || c->inter % 64 || c->target_hidden <= 0 || c->target_hidden % 64)
+    return false;
+  if (c->n_taps < 1 || c->vocab < 2 || c->gamma < 2 || c->gamma > DFLASH_MAX_GAMMA) return false;
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return false;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return false;
+  if (c->n_q_heads * c->head_dim != c->d) return false;
+  if (c->window < 0 || c->max_batch < 1 || c->max_batch > DFLASH_MAX_BATCH || c->ctx_capacity < 1) return false;
+  if (c->window > 0 && c->ctx_capacity < c->window) return false;
+  if (!(c->eps >= 0.f)) return false;
+  if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
+  if (c->adtype == DFLASH_F32) {
+    if (c->wdtype != DFLASH_F32) return false;
+  } else if (c->adtype == DFLASH_BF16) {
+    if (c->wdtype == DFLASH_F32) return false;
+    if ((c->n_q_heads / c->n_kv_heads) * c->gamma > 64) return false;  // query rows per KV head
+  } else {
+    return false;
+  }
+  return true;
+}
+
+// Lay out the workspace; with base == nullptr only sizes are computed.
+size_t carve(dflash_handle* h, uint8_t* base) {
+  const dflash_config& c = h->cfg;
+  Carver cv{base};
+  auto mat = [&](PackedMat& m, int rows, int k) {
+    m.n_rows = rows;
+    m.n_strips = (rows + 15) / 16;
+    m.k = k;
+    m.groups = k / 64;
+    m.w = cv.take<uint8_t>((size_t)m.n_strips * packed_bytes_per_strip(h->fmt, k));
+  };
+  mat(h->wc, h->d, h->mH);
+  for (int i = 0; i < h->L; i++) {
+    mat(h->qkv[i], h->qd + 2 * h->kvd, h->d);
+    mat(h->wo[i], h->d, h->qd);
+    mat(h->gu[i], 2 * h->I, h->d);
+    mat(h->down[i], h->d, h->I);
+  }
+  if (h->d != h->H) {
+    mat(h->tok, h->d, h->H);
+    mat(h->outp, h->H, h->d);
+  }
+  mat(h->lm, h->V, h->H);
+
+  const size_t ab = h->act_bytes;
+  h->ctx_norm = cv.take<float>(h->d * 4);
+  h->mask_emb = cv.take<float>((size_t)(h->G - 1) * h->d * 4);
+  h->block_pos = cv.take<float>((size_t)h->G * h->d * 4);
+  h->out_norm = cv.take<float>(h->d * 4);
+  h->attn_norm = cv.take<float>((size_t)h->L * h->d * 4);
+  h->ff_norm = cv.take<float>((size_t)h->L * h->d * 4);
+  const size_t state_begin = round_up(cv.off, 256);
+  const size_t cache_elems = (size_t)h->L * c.max_batch * c.n_kv_heads * h->cap * c.head_dim;
+  h->kc = cv.take<void>(cache_elems * ab);
+  h->vc = cv.take<void>(cache_elems * ab);
+  const int R = h->r_blk;
+  h->h = cv.take<float>((size_t)R * h->d * 4);
+  h->xn = cv.take<void>((size_t)R * h->d * ab);
+  h->q = cv.take<void>((size_t)R * h->qd * ab);
+  h->kb = cv.take<void>((size_t)R * h->kvd * ab);
+  h->vb = cv.take<void>((size_t)R * h->kvd * ab);
+  h->attn = cv.take<void>((size_t)R * h->qd * ab);
+  h->act = cv.take<void>((size_t)R * h->I * ab);
+  h->hout = cv.take<void>((size_t)R * h->H * ab);
+  h->emb = cv.take<void>((size_t)c.max_batch * h->H * ab);
+  h->tokrow = cv.take<float>((size_t)c.max_batch * h->d * 4);
+  h->ssq_ld = (h->d + 15) / 16;
+  h->ssq = cv.take<float>((size_t)R * h->ssq_ld * 4);
+  h->ssq_ctx = cv.take<float>((size_t)kMaxCtxChunk * h->ssq_ld * 2 * 4);
+  h->xw = cv.take<void>((size_t)h->L * kMaxCtxChunk * h->d * ab);
+
+  // split-K partials / tickets: the largest plan over every matrix and row count
+  size_t pf = 0;
+  int tk = 0, lmg = 0;
+  auto consider = [&](const PackedMat& m, int strips) {
+    for (int r : {8, 16, 32}) {
+      const GemvPlan p = plan_gemv(h, strips, m.groups, r);
+      if (p.n_slices > 1) pf = std::max(pf, (size_t)strips * p.n_slices * 32 * nt_for(r) * 4);
+      lmg = std::max(lmg, p.grid);
+    }
+    tk = std::max(tk, strips);
+  };
+  consider(h->wc, h->wc.n_strips);
+  for (int i = 0; i < h->L; i++) {
+    consider(h->qkv[i], h->qkv[i].n_strips);
+    consider(h->qkv[i], (2 * h->kvd) / 16);
+    consider(h->wo[i], h->wo[i].n_strips);
+    consider(h->gu[i], h->gu[i].n_strips);
+    consider(h->down[i], h->down[i].n_strips);
+  }
+  if (h->d != h->H) {
+    consider(h->tok, h->tok.n_strips);
+    consider(h->outp, h->outp.n_strips);
+  }
+  consider(h->lm, h->lm.n_strips);
+  h->partial_floats = pf;
+  h->ticket_count = tk;
+  h->lm_grid_max = lmg;
+  h->partials = cv.take<float>(std::max<size_t>(pf, 4) * 4);
+  h->tickets = cv.take<int>((size_t)tk * 4);
+  h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4);
+  h->lm_ticket = cv.take<int>(4);
+  // attention split partials: n_req * Hkv * splits stays below ~2 waves of CTAs (see draft)
+  h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
+  h->att_o = cv.take<float>((size_t)h->att_pairs_max * 64 * c.head_dim * 4);
+  h->att_ml = cv.take<float>((size_t)h->att_pairs_max * 64 * 2 * 4);
+  h->att_tickets = cv.take<int>((size_t)c.max_batch * c.n_kv_heads * 4);
+  h->err = cv.take<unsigned>(4);
+  (void)state_begin;
+  return round_up(cv.off, 256);
+}
+
+void init_dims(dflash_handle* h, const dflash_config* c) {
+  h->cfg = *c;
+  h->fmt = c->wdtype == DFLASH_Q4G64 ? FMT_Q4 : (c->wdtype == DFLASH_BF16 ? FMT_BF16 : FMT_F32);
+  h->act_f32 = c->adtype == DFLASH_F32;
+  h->act_bytes = h->act_f32 ? 4 : 2;
+  h->d = c->d;
+  h->H = c->target_hidden;
+  h->qd = c->n_q_heads * c->head_dim;
+  h->kvd = c->n_kv_heads * c->head_dim;
+  h->I = c->inter;
+  h->L = c->n_layers;
+  h->G = c->gamma;
+  h->V = c->vocab;
+  h->mH = c->n_taps * c->target_hidden;
+  // ring rows: at least the requested capacity, a multiple of the 64-row attention tile
+  h->cap = (int)round_up((size_t)std::max(c->ctx_capacity, 64), 64);
+  h->r_blk = c->max_batch * c->gamma;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA; }
+
+bool disabled_by_env() {
+  const char* v = getenv("DFLASH_DISABLE");
+  return v && v[0] == '1';
+}
+
+typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
+  static EncodeTiled encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return DFLASH_ECUDA;
+    encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  const dflash_config& c = h->cfg;
+  const cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)h->cap,
+                              (cuuint64_t)h->L * c.max_batch * c.n_kv_heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)h->cap * c.head_dim * 2};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
+}
+
+bool mat_ok(const dflash_matrix& m, int fmt) {
+  if (!m.data) return false;
+  if (fmt == FMT_Q4 && (!m.scale || !m.bias)) return false;
+  return true;
+}
+
+RepackSrc src_of(const dflash_matrix& m, int rows) {
+  return RepackSrc{m.data, static_cast<const uint16_t*>(m.scale), static_cast<const uint16_t*>(m.bias), rows};
+}
+
+int repack(dflash_handle* h, const PackedMat& dst, const RepackSrc* srcs, int n_src, int interleave, cudaStream_t s) {
+  RepackArgs a{};
+  for (int i = 0; i < n_src; i++) a.src[i] = srcs[i];
+  a.n_src = n_src;
+  a.interleave = interleave;
+  a.fmt = h->fmt;
+  a.k = dst.k;
+  a.n_strips = dst.n_strips;
+  a.dst = dst.w;
+  h->launches++;
+  return status_of(launch_repack(a, s));
+}
+
+// ---- one GEMV over rows [0, R) ------------------------------------------------------------------
+struct GemvCall {
+  const PackedMat* m;
+  int strip0 = 0, n_strips = -1;
+  int R = 0;
+  const void* x = nullptr;
+  int ldx = 0;
+  RowMap xmap{1 << 30, 0, 0};
+  int norm_mode = NORM_NONE;
+  const float* ssq = nullptr;
+  int ssq_ld = 0, ssq_parts = 0;
+  float inv_dim = 1.f;
+  int epi = EPI_STORE;
+  EpiArgs e{};
+};
+
+int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
+  const PackedMat& m = *c.m;
+  const int strips = c.n_strips < 0 ? m.n_strips : c.n_strips;
+  if (c.R <= 0 || strips <= 0) return DFLASH_OK;
+  const GemvPlan p = plan_gemv(h, strips, m.groups, c.R);
+  GemvArgs a{};
+  a.w = m.w;
+  a.strip0 = c.strip0;
+  a.n_strips = strips;
+  a.k = m.k;
+  a.groups = m.groups;
+  a.n_slices = p.n_slices;
+  a.gps = p.gps;
+  a.ctas_per_slice = p.ctas_per_slice;
+  a.R = c.R;
+  a.x = c.x;
+  a.ldx = c.ldx;
+  a.xmap = c.xmap;
+  a.norm_mode = c.norm_mode;
+  a.ssq = c.ssq;
+  a.ssq_ld = c.ssq_ld;
+  a.ssq_parts = c.ssq_parts;
+  a.inv_dim = c.inv_dim;
+  a.eps = h->cfg.eps;
+  a.partials = h->partials;
+  a.tickets = h->tickets;
+  a.err = h->err;
+  a.e = c.e;
+  if (c.epi == EPI_LMHEAD) {
+    a.e.lm_part = h->lm_part;
+    a.e.lm_ticket = h->lm_ticket;
+  }
+  h->launches++;
+  return status_of(launch_gemv(h->fmt, c.epi, nt_for(c.R), a, p.grid, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dflash_workspace_bytes(const dflash_config* cfg) {
+  if (!valid_config(cfg)) return 0;
+  dflash_handle* h = new (std::nothrow) dflash_handle();
+  if (!h) return 0;
+  init_dims(h, cfg);
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const size_t b = carve(h, nullptr);
+  delete h;
+  return b;
+}
+
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* workspace, size_t workspace_bytes,
+                  void* stream, dflash_handle** out) {
+  if (!out) return DFLASH_EINVAL;
+  *out = nullptr;
+  if (!valid_config(cfg) || !w || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return DFLASH_EINVAL;
+  dflash_handle* h = new (std::nothrow) dflash_handle();
+  if (!h) return DFLASH_EINVAL;
+  init_dims(h, cfg);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete h;
+    return DFLASH_ECUDA;
+  }
+  const size_t need = carve(h, nullptr);
+  if (workspace_bytes < need) {
+    delete h;
+    return DFLASH_ECAPACITY;
+  }
+  h->ws_bytes = carve(h, static_cast<uint8_t*>(workspace));
+
+  const int f = h->fmt;
+  bool ok = mat_ok(w->w_c, f) && mat_ok(w->embed, f) && mat_ok(w->lm_head, f) && w->ctx_norm && w->block_pos &&
+            w->out_norm && (h->G < 2 || w->mask_emb);
+  if (h->d != h->H) ok = ok && mat_ok(w->tok_proj, f) && mat_ok(w->out_proj, f);
+  for (int i = 0; i < h->L && ok; i++) {
+    const dflash_layer_weights& l = w->layer[i];
+    ok = mat_ok(l.wq, f) && mat_ok(l.wk, f) && mat_ok(l.wv, f) && mat_ok(l.wo, f) && mat_ok(l.w_gate, f) &&
+         mat_ok(l.w_up, f) && mat_ok(l.w_down, f) && l.attn_norm && l.ff_norm;
+  }
+  if (!ok) {
+    delete h;
+    return DFLASH_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int st = DFLASH_OK;
+  auto chk = [&](int r) {
+    if (st == DFLASH_OK) st = r;
+  };
+  // zero everything after the weights (caches, activations, tickets, error word)
+  chk(status_of(cudaMemsetAsync(h->kc, 0, h->ws_bytes - (static_cast<uint8_t*>(h->kc) - static_cast<uint8_t*>(workspace)), s)));
+  {
+    RepackSrc a = src_of(w->w_c, h->d);
+    chk(repack(h, h->wc, &a, 1, 0, s));
+  }
+  for (int i = 0; i < h->L; i++) {
+    const dflash_layer_weights& l = w->layer[i];
+    RepackSrc qkv[3] = {src_of(l.wq, h->qd), src_of(l.wk, h->kvd), src_of(l.wv, h->kvd)};
+    chk(repack(h, h->qkv[i], qkv, 3, 0, s));
+    RepackSrc o = src_of(l.wo, h->d);
+    chk(repack(h, h->wo[i], &o, 1, 0, s));
+    RepackSrc gu[2] = {src_of(l.w_gate, h->I), src_of(l.w_up, h->I)};
+    chk(repack(h, h->gu[i], gu, 2, 1, s));
+    RepackSrc dn = src_of(l.w_down, h->d);
+    chk(repack(h, h->down[i], &dn, 1, 0, s));
+    chk(status_of(cudaMemcpyAsync(h->attn_norm + (size_t)i * h->d, l.attn_norm, h->d * 4, cudaMemcpyDefault, s)));
+    chk(status_of(cudaMemcpyAsync(h->ff_norm + (size_t)i * h->d, l.ff_norm, h->d * 4, cudaMemcpyDefault, s)));
+  }
+  if (h->d != h->H) {
+    RepackSrc t = src_of(w->tok_proj, h->d), o = src_of(w->out_proj, h->H);
+    chk(repack(h, h->tok, &t, 1, 0, s));
+    chk(repack(h, h->outp, &o, 1, 0, s));
+  }
+  {
+    RepackSrc l = src_of(w->lm_head, h->V);
+    chk(repack(h, h->lm, &l, 1, 0, s));
+  }
+  chk(status_of(cudaMemcpyAsync(h->ctx_norm, w->ctx_norm, h->d * 4, cudaMemcpyDefault, s)));
+  if (h->G > 1)
+    chk(status_of(cudaMemcpyAsync(h->mask_emb, w->mask_emb, (size_t)(h->G - 1) * h->d * 4, cudaMemcpyDefault, s)));
+  chk(status_of(cudaMemcpyAsync(h->block_pos, w->block_pos, (size_t)h->G * h->d * 4, cudaMemcpyDefault, s)));
+  chk(status_of(cudaMemcpyAsync(h->out_norm, w->out_norm, h->d * 4, cudaMemcpyDefault, s)));
+  h->embed = w->embed;
+  if (!h->act_f32 && st == DFLASH_OK) {
+    chk(make_cache_map(h, h->kc, &h->kmap));
+    chk(make_cache_map(h, h->vc, &h->vmap));
+  }
+  if (st != DFLASH_OK) {
+    delete h;
+    return st;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, const int32_t* n_new, const void* taps,
+                       void* stream) {
+  if (!h || n_req < 0 || n_req > h->cfg.max_batch) return DFLASH_EINVAL;
+  if (n_req == 0) return DFLASH_OK;
+  if (!req_ids || !n_new) return DFLASH_EINVAL;
+  bool seen[DFLASH_MAX_BATCH] = {};
+  int64_t total = 0;
+  for (int i = 0; i < n_req; i++) {
+    const int r = req_ids[i];
+    if (r < 0 || r >= h->cfg.max_batch || seen[r] || n_new[i] < 0) return DFLASH_EINVAL;
+    seen[r] = true;
+    total += n_new[i];
+    if (h->cfg.window == 0 && h->ctx_len[r] + n_new[i] > h->cfg.ctx_capacity) return DFLASH_ECAPACITY;
+  }
+  if (total == 0) return DFLASH_OK;
+  if (!taps) return DFLASH_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t ab = h->act_bytes;
+  const uint8_t* tp = static_cast<const uint8_t*>(taps);
+  const int parts = h->ssq_ld;
+  const size_t layer_cache = (size_t)h->cfg.max_batch * h->cfg.n_kv_heads * h->cap * h->cfg.head_dim * ab;
+
+  // rows in call order: (slot, position)
+  int req_i = 0, j_in = 0;
+  int64_t row = 0;
+  while (row < total) {
+    const int rc = (int)std::min<int64_t>(kMaxCtxChunk, total - row);
+    int slots[kMaxCtxChunk], pos[kMaxCtxChunk];
+    for (int r = 0; r < rc; r++) {
+      while (j_in >= n_new[req_i]) {
+        req_i++;
+        j_in = 0;
+      }
+      slots[r] = req_ids[req_i];
+      pos[r] = (int)((h->ctx_len[req_ids[req_i]] + j_in) % h->cap);
+      j_in++;
+    }
+    // Eq 2: x = W_c taps; epilogue writes x*ctx_norm*attn_norm_i for every layer + sums of squares
+    GemvCall c1;
+    c1.m = &h->wc;
+    c1.R = rc;
+    c1.x = tp + (size_t)row * h->mH * ab;
+    c1.ldx = h->mH;
+    c1.epi = EPI_CTX;
+    c1.e.row_base = 0;
+    c1.e.n_rows = h->d;
+    c1.e.ldo = h->d;
+    c1.e.ctx_norm = h->ctx_norm;
+    c1.e.attn_norms = h->attn_norm;
+    c1.e.n_layers = h->L;
+    c1.e.xw = h->xw;
+    c1.e.xw_rows = kMaxCtxChunk;
+    c1.e.ssq_out = h->ssq_ctx;
+    c1.e.ssq_ld = h->ssq_ld;
+    int st = run_gemv(h, c1, s);
+    if (st) return st;
+    // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache
+    for (int i = 0; i < h->L; i++) {
+      GemvCall c2;
+      c2.m = &h->qkv[i];
+      c2.strip0 = h->qd / 16;
+      c2.n_strips = (2 * h->kvd) / 16;
+      c2.R = rc;
+      c2.x = static_cast<const uint8_t*>(h->xw) + (size_t)i * kMaxCtxChunk * h->d * ab;
+      c2.ldx = h->d;
+      c2.norm_mode = NORM_CTX;
+      c2.ssq = h->ssq_ctx;
+      c2.ssq_ld = h->ssq_ld;
+      c2.ssq_parts = parts;
+      c2.inv_dim = 1.f / h->d;
+      c2.epi = EPI_KV;
+      c2.e.row_base = h->qd;
+      c2.e.n_rows = 2 * h->kvd;
+      c2.e.kc = static_cast<uint8_t*>(h->kc) + i * layer_cache;
+      c2.e.vc = static_cast<uint8_t*>(h->vc) + i * layer_cache;
+      c2.e.cap = h->cap;
+      c2.e.hd = h->cfg.head_dim;
+      c2.e.n_kv = h->cfg.n_kv_heads;
+      c2.e.kvd = h->kvd;
+      for (int r = 0; r < rc; r++) {
+        c2.e.kv_slot[r] = slots[r];
+        c2.e.kv_pos[r] = pos[r];
+      }
+      st = run_gemv(h, c2, s);
+      if (st) return st;
+    }
+    row += rc;
+  }
+  for (int i = 0; i < n_req; i++) h->ctx_len[req_ids[i]] += n_new[i];
+  h->stats.ctx_rows += (uint64_t)total;
+  return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, const int32_t* anchor, float temperature,
+                       int32_t* draft, float* conf, float* logits, void* stream) {
+  if (!h) return DFLASH_EINVAL;
+  if (temperature != 0.0f || disabled_by_env()) {
+    h->stats.declined++;
+    return DFLASH_DECLINED;
+  }
+  if (n_req < 0 || n_req > h->cfg.max_batch) return DFLASH_EINVAL;
+  if (n_req == 0) return DFLASH_OK;
+  if (!req_ids || !anchor || !draft) return DFLASH_EINVAL;
+  bool seen[DFLASH_MAX_BATCH] = {};
+  for (int i = 0; i < n_req; i++) {
+    const int r = req_ids[i];
+    if (r < 0 || r >= h->cfg.max_batch || seen[r]) return DFLASH_EINVAL;
+    seen[r] = true;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dflash_config& c = h->cfg;
+  const size_t ab = h->act_bytes;
+  const int G = h->G, n = G - 1, d = h->d;
+  const int parts = h->ssq_ld;
+  const size_t layer_cache = (size_t)c.max_batch * c.n_kv_heads * h->cap * c.head_dim * ab;
+  auto off = [&](void* p, size_t rows, size_t width) -> void* {
+    return static_cast<uint8_t*>(p) + rows * width * ab;
+  };
+  int st = DFLASH_OK;
+
+  // block construction
+  BlockArgs ba{};
+  ba.n_req = n_req;
+  ba.gamma = G;
+  ba.d = d;
+  ba.H = h->H;
+  ba.vocab = h->V;
+  ba.fmt = h->fmt;
+  ba.act_f32 = h->act_f32;
+  ba.anchor = anchor;
+  ba.emb = h->embed.data;
+  ba.emb_scale = static_cast<const uint16_t*>(h->embed.scale);
+  ba.emb_bias = static_cast<const uint16_t*>(h->embed.bias);
+  ba.mask_emb = h->mask_emb;
+  ba.block_pos = h->block_pos;
+  ba.attn_norm0 = h->attn_norm;
+  ba.h = h->h;
+  ba.xn = h->xn;
+  ba.ssq = h->ssq;
+  ba.ssq_ld = h->ssq_ld;
+  ba.emb_out = h->emb;
+  if (d != h->H) {
+    h->launches++;
+    if ((st = status_of(launch_embed_gather(ba, s)))) return st;
+    for (int b0 = 0; b0 < n_req; b0 += kMaxRows) {
+      const int rb = std::min(kMaxRows, n_req - b0);
+      GemvCall ct;
+      ct.m = &h->tok;
+      ct.R = rb;
+      ct.x = off(h->emb, b0, h->H);
+      ct.ldx = h->H;
+      ct.epi = EPI_STORE;
+      ct.e.n_rows = d;
+      ct.e.out = h->tokrow + (size_t)b0 * d;
+      ct.e.ldo = d;
+      ct.e.out_f32 = 1;
+      if ((st = run_gemv(h, ct, s))) return st;
+    }
+    ba.tokrow = h->tokrow;
+  }
+  h->launches++;
+  if ((st = status_of(launch_block_init(ba, s)))) return st;
+
+  const int req_per_chunk = std::max(1, kMaxRows / G);
+  for (int i = 0; i < h->L; i++) {
+    const int in_parts = i == 0 ? 1 : parts;
+    // Q, K_d, V_d of RMSNorm_attn_i(H_d)
+    for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
+      const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
+      GemvCall cq;
+      cq.m = &h->qkv[i];
+      cq.R = nb * G;
+      cq.x = off(h->xn, r0, d);
+      cq.ldx = d;
+      cq.norm_mode = NORM_ONE;
+      cq.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
+      cq.ssq_ld = h->ssq_ld;
+      cq.ssq_parts = in_parts;
+      cq.inv_dim = 1.f / d;
+      cq.epi = EPI_QKV;
+      cq.e.n_rows = h->qd + 2 * h->kvd;
+      cq.e.q = off(h->q, r0, h->qd);
+      cq.e.kb = off(h->kb, r0, h->kvd);
+      cq.e.vb = off(h->vb, r0, h->kvd);
+      cq.e.qd = h->qd;
+      cq.e.kvd = h->kvd;
+      if ((st = run_gemv(h, cq, s))) return st;
+    }
+    // attention over [windowed context ++ block], no causal mask
+    {
+      AttnArgs aa{};
+      aa.q = h->q;
+      aa.kb = h->kb;
+      aa.vb = h->vb;
+      aa.out = h->attn;
+      aa.kc = static_cast<uint8_t*>(h->kc) + i * layer_cache;
+      aa.vc = static_cast<uint8_t*>(h->vc) + i * layer_cache;
+      aa.qd = h->qd;
+      aa.kvd = h->kvd;
+      aa.hd = c.head_dim;
+      aa.hq = c.n_q_heads;
+      aa.hkv = c.n_kv_heads;
+      aa.gamma = G;
+      aa.window = c.window;
+      aa.cap = h->cap;
+      aa.max_batch = c.max_batch;
+      aa.plane0 = i * c.max_batch * c.n_kv_heads;
+      aa.n_req = n_req;
+      aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+      aa.part_o = h->att_o;
+      aa.part_ml = h->att_ml;
+      aa.tickets = h->att_tickets;
+      aa.err = h->err;
+      int max_tiles = 0;
+      for (int b = 0; b < n_req; b++) {
+        const int64_t P = h->ctx_len[req_ids[b]];
+        const int64_t nw = c.window > 0 ? std::min<int64_t>(P, c.window) : P;
+        aa.req[b] = AttnReq{req_ids[b], (int)P, b * G};
+        max_tiles = std::max(max_tiles, (int)((nw + 63) / 64) + 1);
+      }
+      if (h->act_f32) {
+        aa.n_splits = 1;
+        h->launches++;
+        if ((st = status_of(launch_attn_f32(aa, s)))) return st;
+      } else {
+        const int pairs = n_req * c.n_kv_heads;
+        int splits = std::max(1, (2 * h->n_sm + pairs - 1) / pairs);
+        splits = std::min(splits, max_tiles);
+        splits = std::max(1, std::min(splits, h->att_pairs_max / pairs));
+        aa.n_splits = splits;
+        h->launches++;
+        if ((st = status_of(launch_attn_tc(aa, h->kmap, h->vmap, s)))) return st;
+      }
+    }
+    for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
+      const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
+      // H_d += W_o attn; next input = H_d * ff_norm_i (+ sums of squares)
+      GemvCall co;
+      co.m = &h->wo[i];
+      co.R = nb * G;
+      co.x = off(h->attn, r0, h->qd);
+      co.ldx = h->qd;
+      co.epi = EPI_RESID;
+      co.e.n_rows = d;
+      co.e.ldo = d;
+      co.e.h = h->h + (size_t)r0 * d;
+      co.e.wnext = h->ff_norm + (size_t)i * d;
+      co.e.xnext = off(h->xn, r0, d);
+      co.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
+      co.e.ssq_ld = h->ssq_ld;
+      if ((st = run_gemv(h, co, s))) return st;
+    }
+    for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
+      const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
+      // a = SiLU(W_gate n2) * (W_up n2), n2 = RMSNorm_ff_i(H_d)
+      GemvCall cg;
+      cg.m = &h->gu[i];
+      cg.R = nb * G;
+      cg.x = off(h->xn, r0, d);
+      cg.ldx = d;
+      cg.norm_mode = NORM_ONE;
+      cg.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
+      cg.ssq_ld = h->ssq_ld;
+      cg.ssq_parts = parts;
+      cg.inv_dim = 1.f / d;
+      cg.epi = EPI_SWIGLU;
+      cg.e.n_rows = 2 * h->I;
+      cg.e.act = off(h->act, r0, h->I);
+      cg.e.inter = h->I;
+      if ((st = run_gemv(h, cg, s))) return st;
+    }
+    for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
+      const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
+      // H_d += W_down a; next input = H_d * (attn_norm_{i+1} | out_norm)
+      GemvCall cd;
+      cd.m = &h->down[i];
+      cd.R = nb * G;
+      cd.x = off(h->act, r0, h->I);
+      cd.ldx = h->I;
+      cd.epi = EPI_RESID;
+      cd.e.n_rows = d;
+      cd.e.ldo = d;
+      cd.e.h = h->h + (size_t)r0 * d;
+      cd.e.wnext = i + 1 < h->L ? h->attn_norm + (size_t)(i + 1) * d : h->out_norm;
+      cd.e.xnext = off(h->xn, r0, d);
+      cd.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
+      cd.e.ssq_ld = h->ssq_ld;
+      if ((st = run_gemv(h, cd, s))) return st;
+    }
+  }
+
+  // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (rows 1..gamma-1)
+  const int lm_req_per_chunk = std::max(1, kMaxRows / n);
+  if (h->probe_start) cudaEventRecord(h->probe_start, s);
+  for (int b0 = 0; b0 < n_req; b0 += lm_req_per_chunk) {
+    const int nb = std::min(lm_req_per_chunk, n_req - b0);
+    const int r0 = b0 * G, l0 = b0 * n, R = nb * n;
+    GemvCall cl;
+    cl.m = &h->lm;
+    cl.R = R;
+    if (d != h->H) {
+      GemvCall cp;
+      cp.m = &h->outp;
+      cp.R = R;
+      cp.x = off(h->xn, r0, d);
+      cp.ldx = d;
+      cp.xmap = RowMap{n, G, 1};
+      cp.norm_mode = NORM_ONE;
+      cp.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
+      cp.ssq_ld = h->ssq_ld;
+      cp.ssq_parts = parts;
+      cp.inv_dim = 1.f / d;
+      cp.epi = EPI_STORE;
+      cp.e.n_rows = h->H;
+      cp.e.out = h->hout;
+      cp.e.ldo = h->H;
+      if ((st = run_gemv(h, cp, s))) return st;
+      cl.x = h->hout;
+      cl.ldx = h->H;
+    } else {
+      cl.x = off(h->xn, r0, d);
+      cl.ldx = d;
+      cl.xmap = RowMap{n, G, 1};
+      cl.norm_mode = NORM_ONE;
+      cl.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
+      cl.ssq_ld = h->ssq_ld;
+      cl.ssq_parts = parts;
+      cl.inv_dim = 1.f / d;
+    }
+    cl.epi = EPI_LMHEAD;
+    cl.e.n_rows = h->V;
+    cl.e.logits = logits ? logits + (size_t)l0 * h->V : nullptr;
+    cl.e.vocab = h->V;
+    cl.e.rows_per_req = n;
+    cl.e.tok_out = draft + l0;
+    cl.e.conf_out = conf ? conf + l0 : nullptr;
+    if ((st = run_gemv(h, cl, s))) return st;
+  }
+  if (h->probe_stop) cudaEventRecord(h->probe_stop, s);
+  h->probe_start = h->probe_stop = nullptr;
+  h->stats.rounds++;
+  h->stats.blocks += (uint64_t)n_req;
+  return DFLASH_OK;
+}
+
+int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* target, int32_t* accept_len,
+                  int32_t* next_anchor, void* stream) {
+  if (!h || n_req < 0) return DFLASH_EINVAL;
+  if (n_req == 0) return DFLASH_OK;
+  if (!draft || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
+  h->launches++;
+  h->stats.accept_calls++;
+  return status_of(launch_accept(n_req, h->G - 1, draft, target, accept_len, next_anchor,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int dflash_reset_request(dflash_handle* h, int req_id) {
+  if (!h || req_id < 0 || req_id >= h->cfg.max_batch) return DFLASH_EINVAL;
+  h->ctx_len[req_id] = 0;
+  return DFLASH_OK;
+}
+
+int64_t dflash_ctx_len(const dflash_handle* h, int req_id) {
+  if (!h || req_id < 0 || req_id >= h->cfg.max_batch) return -1;
+  return h->ctx_len[req_id];
+}
+
+int dflash_check_errors(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_EINVAL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DFLASH_ECUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_ECUDA;
+  if (word) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(h->err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) return DFLASH_ECUDA;
+    return DFLASH_ETIMEOUT;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_get_stats(const dflash_handle* h, dflash_stats* out) {
+  if (!h || !out) return DFLASH_EINVAL;
+  *out = h->stats;
+  return DFLASH_OK;
+}
+
+int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop_event) {
+  if (!h || kernel != 0) return DFLASH_EINVAL;
+  h->probe_start = static_cast<cudaEvent_t>(start_event);
+  h->probe_stop = static_cast<cudaEvent_t>(stop_event);
+  return DFLASH_OK;
+}
+
+uint64_t dflash_launch_count(const dflash_handle* h) { return h ? h->launches : 0; }
+
+void dflash_destroy(dflash_handle* h) { delete h; }
+
+const char* dflash_status_str(int s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_DECLINED: return "declined (temperature > 0 or DFLASH_DISABLE=1): fall back to plain decoding";
+    case DFLASH_EINVAL: return "invalid argument";
+    case DFLASH_ECAPACITY: return "capacity exceeded";
+    case DFLASH_ECUDA: return "CUDA error";
+    case DFLASH_ETIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

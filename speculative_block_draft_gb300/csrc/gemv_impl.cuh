@@ -1,0 +1,595 @@
+// Skinny GEMM Y[R][N] = X[R][K] W[N][K]^T for the drafter's projections, R <= 32 activation
+// rows, with the RMSNorm scale, residual, SwiGLU, cache-append and vocab argmax epilogues fused.
+//
+// Tensor-core path (bf16 / 4-bit weights), one CTA per SM:
+//  * A CTA owns one K slice and a range of 16-row strips. It stages its activation slice
+//    X[R][slice] (bf16) into shared memory with 1-D bulk copies (TMA) once.
+//  * Each of its 8 warps streams the weight bytes of its strips through a private ring of
+//    kStages shared-memory stages filled by cp.async.bulk, so ~74 KB per SM are in flight.
+//  * 4-bit codes are turned into bf16 (128 + q, exact) with one lop3 per pair and fed to
+//    mma.sync m16n8k16 (weights = A, 16 rows; activations = B, 8 columns per n-tile). The
+//    group-64 affine code is folded per group in fp32:  sum_k (s q_k + b) x_k =
+//    s * sum_k (128 + q_k) x_k + (b - 128 s) * sum_k x_k, so the MMA sees exact integers.
+//  * When a strip's K is split over several CTAs, each writes a partial tile; the last to
+//    arrive (atomic ticket, no waiting) sums them in slice order and runs the epilogue.
+// CUDA-core path (fp32 weights and activations): one warp per strip, fp32 FMA.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace dfl {
+
+struct LmState {
+  float m, s;
+  int i;
+};
+
+__device__ __forceinline__ void lm_merge(LmState& a, const LmState& b) {
+  if (b.m > a.m || (b.m == a.m && b.i < a.i)) {
+    const float s = (a.m == -INFINITY) ? b.s : b.s + a.s * __expf(a.m - b.m);
+    a.m = b.m;
+    a.i = b.i;
+    a.s = s;
+  } else {
+    if (b.m != -INFINITY) a.s += b.s * __expf(b.m - a.m);
+  }
+}
+
+__device__ __forceinline__ void lm_push(LmState& st, float v, int n) {
+  if (v > st.m) {
+    st.s = (st.m == -INFINITY) ? 1.0f : st.s * __expf(st.m - v) + 1.0f;
+    st.m = v;
+    st.i = n;
+  } else {
+    st.s += __expf(v - st.m);
+    if (v == st.m && n < st.i) st.i = n;
+  }
+}
+
+__device__ __forceinline__ int map_row(const RowMap& m, int r) {
+  return (r / m.per) * m.stride + m.off + r % m.per;
+}
+
+template <typename XT>
+__device__ __forceinline__ void store_act(void* base, size_t idx, float v) {
+  static_cast<XT*>(base)[idx] = from_f<XT>(v);
+}
+
+// Per-row RMSNorm scale from the producer's per-strip sum-of-squares partials.
+__device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* srow, int nrows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  for (int r = warp; r < nrows; r += nw) {
+    float s = 1.0f;
+    if (r < a.R && a.norm_mode != NORM_NONE) {
+      const int src = map_row(a.xmap, r);
+      if (a.norm_mode == NORM_ONE) {
+        float acc = 0.f;
+        for (int p = lane; p < a.ssq_parts; p += 32) acc += a.ssq[(size_t)src * a.ssq_ld + p];
+        acc = warp_sum(acc);
+        s = rsqrtf(acc * a.inv_dim + a.eps);
+      } else {
+        float sa = 0.f, sb = 0.f;
+        for (int p = lane; p < a.ssq_parts; p += 32) {
+          sa += a.ssq[((size_t)src * a.ssq_ld + p) * 2 + 0];
+          sb += a.ssq[((size_t)src * a.ssq_ld + p) * 2 + 1];
+        }
+        sa = warp_sum(sa);
+        sb = warp_sum(sb);
+        const float inv1 = rsqrtf(sa * a.inv_dim + a.eps);
+        s = inv1 * rsqrtf(inv1 * inv1 * sb * a.inv_dim + a.eps);
+      }
+    }
+    if (lane == 0) srow[r] = s;
+  }
+}
+
+// Epilogue of one complete 16-row strip. Lane (g, t) holds, for n-tile nt, rows strip*16+g
+// (y[nt][0..1]) and strip*16+g+8 (y[nt][2..3]) at activation columns nt*8+2t and nt*8+2t+1.
+template <int EPI, int NT, typename XT>
+__device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, float (&y)[NT][4],
+                                               const float* srow, LmState (&lm)[NT][2]) {
+  const EpiArgs& e = a.e;
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
+  const bool v0 = nr0 >= 0 && nr0 < e.n_rows, v1 = nr1 >= 0 && nr1 < e.n_rows;
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+      const int c = nt * 8 + 2 * t + p;
+      const bool cv = c < a.R;
+      const float sc = srow[c];
+      const float ya = y[nt][p] * sc, yb = y[nt][2 + p] * sc;
+      if constexpr (EPI == EPI_STORE) {
+        if (cv) {
+          const size_t base = (size_t)c * e.ldo;
+          if (e.out_f32) {
+            if (v0) static_cast<float*>(e.out)[base + nr0] = ya;
+            if (v1) static_cast<float*>(e.out)[base + nr1] = yb;
+          } else {
+            if (v0) store_act<XT>(e.out, base + nr0, ya);
+            if (v1) store_act<XT>(e.out, base + nr1, yb);
+          }
+        }
+      } else if constexpr (EPI == EPI_QKV) {
+        if (cv) {
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int nr = h ? nr1 : nr0;
+            const float v = h ? yb : ya;
+            if (!(h ? v1 : v0)) continue;
+            if (nr < e.qd) store_act<XT>(e.q, (size_t)c * e.qd + nr, v);
+            else if (nr < e.qd + e.kvd) store_act<XT>(e.kb, (size_t)c * e.kvd + nr - e.qd, v);
+            else store_act<XT>(e.vb, (size_t)c * e.kvd + nr - e.qd - e.kvd, v);
+          }
+        }
+      } else if constexpr (EPI == EPI_KV) {
+        if (cv) {
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int nr = h ? nr1 : nr0;
+            if (!(h ? v1 : v0)) continue;
+            const float v = h ? yb : ya;
+            const int half = nr >= e.kvd;
+            const int f = nr - half * e.kvd;
+            const size_t idx =
+                (((size_t)e.kv_slot[c] * e.n_kv + f / e.hd) * e.cap + e.kv_pos[c]) * e.hd + f % e.hd;
+            store_act<XT>(half ? e.vc : e.kc, idx, v);
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        const int j = strip * 8 + g;
+        if (cv && j < e.inter) {
+          const float silu = ya / (1.0f + __expf(-ya));
+          store_act<XT>(e.act, (size_t)c * e.inter + j, silu * yb);
+        }
+      } else if constexpr (EPI == EPI_LMHEAD) {
+        if (cv) {
+          if (v0) {
+            if (e.logits) e.logits[(size_t)c * e.vocab + nr0] = ya;
+            lm_push(lm[nt][p], ya, nr0);
+          }
+          if (v1) {
+            if (e.logits) e.logits[(size_t)c * e.vocab + nr1] = yb;
+            lm_push(lm[nt][p], yb, nr1);
+          }
+        }
+      }
+    }
+  }
+  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
+    // residual update / context rows, then this strip's sum-of-squares partial per column
+    float sq[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+      for (int p = 0; p < 2; p++) {
+        const int c = nt * 8 + 2 * t + p;
+        const bool cv = c < a.R;
+        const float sc = srow[c];
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const int nr = h ? nr1 : nr0;
+          if (!cv || !(h ? v1 : v0)) continue;
+          const float v = y[nt][2 * h + p] * sc;
+          if constexpr (EPI == EPI_RESID) {
+            const size_t idx = (size_t)c * e.ldo + nr;
+            const float hn = e.h[idx] + v;
+            e.h[idx] = hn;
+            store_act<XT>(e.xnext, idx, e.wnext ? hn * e.wnext[nr] : hn);
+            s0 += hn * hn;
+          } else {
+            const float cn = e.ctx_norm[nr];
+            for (int i = 0; i < e.n_layers; i++)
+              store_act<XT>(e.xw, ((size_t)i * e.xw_rows + c) * e.ldo + nr, v * cn * e.attn_norms[(size_t)i * e.ldo + nr]);
+            s0 += v * v;
+            s1 += (v * cn) * (v * cn);
+          }
+        }
+        sq[nt][p][0] = s0;
+        sq[nt][p][1] = s1;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int p = 0; p < 2; p++)
+#pragma unroll
+        for (int q = 0; q < 2; q++)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) sq[nt][p][q] += __shfl_xor_sync(0xffffffffu, sq[nt][p][q], o);
+    if (g == 0) {
+      const int part = strip - e.row_base / 16;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+          const int c = nt * 8 + 2 * t + p;
+          if (c >= a.R) continue;
+          if constexpr (EPI == EPI_RESID) {
+            e.ssq_out[(size_t)c * e.ssq_ld + part] = sq[nt][p][0];
+          } else {
+            e.ssq_out[((size_t)c * e.ssq_ld + part) * 2 + 0] = sq[nt][p][0];
+            e.ssq_out[((size_t)c * e.ssq_ld + part) * 2 + 1] = sq[nt][p][1];
+          }
+        }
+    }
+  }
+}
+
+// Vocab reduction of the LM-head epilogue: lanes -> warps -> CTA partial -> last CTA.
+template <int NT>
+__device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2], LmState* sm_lm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int p = 0; p < 2; p++)
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        LmState other;
+        other.m = __shfl_xor_sync(0xffffffffu, lm[nt][p].m, o);
+        other.s = __shfl_xor_sync(0xffffffffu, lm[nt][p].s, o);
+        other.i = __shfl_xor_sync(0xffffffffu, lm[nt][p].i, o);
+        lm_merge(lm[nt][p], other);
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int p = 0; p < 2; p++) sm_lm[warp * kMaxRows + nt * 8 + 2 * t + p] = lm[nt][p];
+  }
+  __syncthreads();
+  const EpiArgs& e = a.e;
+  if ((int)threadIdx.x < a.R) {
+    LmState acc{-INFINITY, 0.f, 0x7fffffff};
+    for (int w = 0; w < nw; w++) lm_merge(acc, sm_lm[w * kMaxRows + threadIdx.x]);
+    float* dst = e.lm_part + ((size_t)blockIdx.x * kMaxRows + threadIdx.x) * 3;
+    dst[0] = acc.m;
+    dst[1] = acc.s;
+    dst[2] = __int_as_float(acc.i);
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int last;
+  if (threadIdx.x == 0) last = atomicAdd(e.lm_ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if ((int)threadIdx.x < a.R) {
+    LmState acc{-INFINITY, 0.f, 0x7fffffff};
+    for (int b = 0; b < (int)gridDim.x; b++) {
+      const float* src = e.lm_part + ((size_t)b * kMaxRows + threadIdx.x) * 3;
+      LmState o{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))};
+      lm_merge(acc, o);
+    }
+    e.tok_out[threadIdx.x] = acc.i;
+    if (e.conf_out) e.conf_out[threadIdx.x] = 1.0f / acc.s;
+  }
+  if (threadIdx.x == 0) *e.lm_ticket = 0;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tensor-core kernel (bf16 or 4-bit weights, bf16 activations)
+// ------------------------------------------------------------------------------------------------
+template <int FMT, int NT, int EPI>
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_constant__ GemvArgs a) {
+  using XT = __nv_bfloat16;
+  constexpr int GS = FMT == FMT_Q4 ? kQ4GroupsPerStage : kBf16GroupsPerStage;
+  constexpr int GB = FMT == FMT_Q4 ? kQ4GroupBytes : kBf16GroupBytes;
+  constexpr int RP = NT * 8;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+
+  const int slice = blockIdx.x / a.ctas_per_slice, cis = blockIdx.x % a.ctas_per_slice;
+  const int gbeg = slice * a.gps, gend = min(a.groups, gbeg + a.gps), ng = gend - gbeg;
+  const int sbeg = (int)((long long)cis * a.n_strips / a.ctas_per_slice);
+  const int send = (int)((long long)(cis + 1) * a.n_strips / a.ctas_per_slice);
+  const int xstride = a.gps * 128 + 16;
+
+  uint8_t* ring = sm;
+  uint8_t* xs = sm + kWarps * kStages * kStageBytes;
+  float* xsum = reinterpret_cast<float*>(xs + RP * xstride);
+  float* srow = xsum + (FMT == FMT_Q4 ? RP * a.gps : 0);
+  LmState* sm_lm = reinterpret_cast<LmState*>(srow + kMaxRows);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(sm_lm + (EPI == EPI_LMHEAD ? kWarps * kMaxRows : 0)) + 15) & ~uintptr_t(15));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 1 + kWarps * kStages; i++) mbar_init(smem_u32(&bars[i]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // this warp's strips: sbeg + warp, sbeg + warp + kWarps, ...
+  const int first = sbeg + warp;
+  const int n_my = first < send ? (send - 1 - first) / kWarps + 1 : 0;
+  const int sps = (ng + GS - 1) / GS;  // stages per strip
+  const int n_q = n_my * sps;
+  int issued = 0;
+  auto issue = [&](int q) {
+    const int si = q / sps, st = q % sps;
+    const int strip = a.strip0 + first + si * kWarps;
+    const int g0 = gbeg + st * GS, gn = min(GS, gend - g0);
+    const uint8_t* src = a.w + ((size_t)strip * a.groups + g0) * GB;
+    const int slot = warp * kStages + q % kStages;
+    const uint32_t bar = smem_u32(&bars[1 + slot]);
+    mbar_arrive_expect_tx(bar, gn * GB);
+    bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);
+  };
+  if (lane == 0)
+    for (int q = 0; q < min(kStages, n_q); q++) issue(q);
+  issued = min(kStages, n_q);
+
+  // activation slice -> shared (bulk copies), pad rows zeroed
+  const int k0 = gbeg * 64, kbytes = ng * 128;
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_u32(&bars[0]);
+    mbar_arrive_expect_tx(bar, a.R * kbytes);
+    for (int r = 0; r < a.R; r++) {
+      const int src = map_row(a.xmap, r);
+      bulk_g2s(smem_u32(xs + (size_t)r * xstride),
+               static_cast<const uint8_t*>(a.x) + ((size_t)src * a.ldx + k0) * 2, kbytes, bar);
+    }
+  }
+  for (int i = threadIdx.x; i < (RP - a.R) * (kbytes / 16); i += blockDim.x) {
+    const int r = a.R + i / (kbytes / 16), c = i % (kbytes / 16);
+    *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
+  }
+  compute_row_scales(a, srow, RP);
+  bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
+  ok = __syncthreads_and(ok);
+  if (FMT == FMT_Q4 && ok) {
+    for (int i = threadIdx.x; i < RP * ng; i += blockDim.x) {
+      const int r = i / ng, gl = i % ng;
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(xs + (size_t)r * xstride + gl * 128);
+      float s = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < 32; j++) {
+        const float2 f = __bfloat1622float2(p[j]);
+        s += f.x + f.y;
+      }
+      xsum[r * a.gps + gl] = s;
+    }
+  }
+  __syncthreads();
+
+  LmState lm[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
+
+  int consumed = 0;
+  for (int si = 0; ok && si < n_my; si++) {
+    const int strip_local = first + si * kWarps;
+    const int strip = a.strip0 + strip_local;
+    float y[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+
+    for (int st = 0; st < sps; st++) {
+      const int q = si * sps + st;
+      const int slot = warp * kStages + q % kStages;
+      bool w_ok = mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, a.err, kErrTimeoutGemv);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok) {
+        ok = false;
+        break;
+      }
+      consumed = q + 1;
+      const uint8_t* stg = ring + (size_t)slot * kStageBytes;
+      const int g0 = gbeg + st * GS, gn = min(GS, gend - g0);
+      for (int gi = 0; gi < gn; gi++) {
+        const int gl = g0 - gbeg + gi;
+        if constexpr (FMT == FMT_Q4) {
+          const uint8_t* gp = stg + gi * kQ4GroupBytes;
+          const uint4 A = *reinterpret_cast<const uint4*>(gp + lane * 16);
+          const uint32_t sb0 = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * g);
+          const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g + 8));
+          const float s0 = __uint_as_float(sb0 << 16), s1 = __uint_as_float(sb1 << 16);
+          const float b0 = fmaf(-128.f, s0, __uint_as_float(sb0 & 0xFFFF0000u));
+          const float b1 = fmaf(-128.f, s1, __uint_as_float(sb1 & 0xFFFF0000u));
+          const uint32_t u[4] = {A.x, A.y, A.z, A.w};
+          uint32_t af[4][4];
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            af[j][0] = nib2_to_bf16x2_plus128(u[j]);
+            af[j][1] = nib2_to_bf16x2_plus128(u[j] >> 4);
+            af[j][2] = nib2_to_bf16x2_plus128(u[j] >> 8);
+            af[j][3] = nib2_to_bf16x2_plus128(u[j] >> 12);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            const uint8_t* xr = xs + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+            const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
+            const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(acc, af[0][0], af[0][1], af[0][2], af[0][3], x01.x, x01.y);
+            mma_bf16(acc, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
+            mma_bf16(acc, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
+            mma_bf16(acc, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
+            const float xa = xsum[(nt * 8 + 2 * t) * a.gps + gl];
+            const float xb = xsum[(nt * 8 + 2 * t + 1) * a.gps + gl];
+            y[nt][0] = fmaf(s0, acc[0], fmaf(b0, xa, y[nt][0]));
+            y[nt][1] = fmaf(s0, acc[1], fmaf(b0, xb, y[nt][1]));
+            y[nt][2] = fmaf(s1, acc[2], fmaf(b1, xa, y[nt][2]));
+            y[nt][3] = fmaf(s1, acc[3], fmaf(b1, xb, y[nt][3]));
+          }
+        } else {
+          const uint8_t* gp = stg + gi * kBf16GroupBytes;
+          uint4 A[4];
+#pragma unroll
+          for (int j = 0; j < 4; j++) A[j] = *reinterpret_cast<const uint4*>(gp + j * 512 + lane * 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            const uint8_t* xr = xs + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+            const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
+            const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
+            mma_bf16(y[nt], A[0].x, A[0].y, A[0].z, A[0].w, x01.x, x01.y);
+            mma_bf16(y[nt], A[1].x, A[1].y, A[1].z, A[1].w, x01.z, x01.w);
+            mma_bf16(y[nt], A[2].x, A[2].y, A[2].z, A[2].w, x23.x, x23.y);
+            mma_bf16(y[nt], A[3].x, A[3].y, A[3].z, A[3].w, x23.z, x23.w);
+          }
+        }
+      }
+      // every lane is done reading this slot before the copy engine refills it
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0 && q + kStages < n_q) issue(q + kStages);
+      if (q + kStages < n_q) issued = q + kStages + 1;
+    }
+    if (!ok) break;
+
+    bool have = true;
+    if (a.n_slices > 1) {
+      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * (NT * 4);
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+      __threadfence();
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.tickets[strip_local], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev != a.n_slices - 1) {
+        have = false;
+      } else {
+        __threadfence();
+        float tot[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+          for (int j = 0; j < 4; j++) tot[nt][j] = 0.f;
+        for (int s2 = 0; s2 < a.n_slices; s2++) {
+          const float* src = a.partials + (((size_t)strip_local * a.n_slices + s2) * 32 + lane) * (NT * 4);
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            float4 v;
+            if (s2 == slice) v = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+            else v = __ldcg(reinterpret_cast<const float4*>(src + nt * 4));
+            tot[nt][0] += v.x;
+            tot[nt][1] += v.y;
+            tot[nt][2] += v.z;
+            tot[nt][3] += v.w;
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+          for (int j = 0; j < 4; j++) y[nt][j] = tot[nt][j];
+        if (lane == 0) a.tickets[strip_local] = 0;
+      }
+    }
+    if (have) strip_epilogue<EPI, NT, XT>(a, strip, y, srow, lm);
+  }
+
+  if (!ok && lane == 0) {
+    // leave no copy in flight into this CTA's shared memory
+    if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bars[0]), 0, nullptr, 0);
+    for (int q = consumed; q < issued; q++) {
+      const int slot = warp * kStages + q % kStages;
+      mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, nullptr, 0);
+    }
+  }
+  if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
+}
+
+// ------------------------------------------------------------------------------------------------
+// CUDA-core kernel (fp32 weights and activations): one warp per strip
+// ------------------------------------------------------------------------------------------------
+template <int NT, int EPI>
+__global__ void __launch_bounds__(kF32Warps * 32) gemv_f32_kernel(const __grid_constant__ GemvArgs a) {
+  constexpr int RP = NT * 8;
+  __shared__ float srow[kMaxRows];
+  __shared__ LmState sm_lm[kF32Warps * kMaxRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  compute_row_scales(a, srow, RP);
+  __syncthreads();
+  const float* X = static_cast<const float*>(a.x);
+  const float* W = reinterpret_cast<const float*>(a.w);
+  LmState lm[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
+
+  for (int sl = blockIdx.x * kF32Warps + warp; sl < a.n_strips; sl += gridDim.x * kF32Warps) {
+    const int strip = a.strip0 + sl;
+    float y[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+    for (int m = 0; m < 16; m++) {
+      const float* wr = W + (size_t)(strip * 16 + m) * a.k;
+      float part[RP];
+#pragma unroll
+      for (int c = 0; c < RP; c++) part[c] = 0.f;
+      for (int k = lane; k < a.k; k += 32) {
+        const float w = wr[k];
+#pragma unroll
+        for (int c = 0; c < RP; c++)
+          if (c < a.R) part[c] = fmaf(w, X[(size_t)map_row(a.xmap, c) * a.ldx + k], part[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < RP; c++) {
+        const float v = warp_sum(part[c]);
+        if ((c % 8) / 2 == t) {
+          if (m == g) y[c / 8][c & 1] = v;
+          if (m == g + 8) y[c / 8][2 + (c & 1)] = v;
+        }
+      }
+    }
+    strip_epilogue<EPI, NT, float>(a, strip, y, srow, lm);
+  }
+  if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
+}
+
+template <int FMT, int NT>
+cudaError_t launch_gemv_fmt_nt(int epi, const GemvArgs& a, int grid, size_t smem, cudaStream_t s) {
+#define DFL_CASE(E)                                                                              \
+  case E: {                                                                                      \
+    if constexpr (FMT == FMT_F32) {                                                              \
+      gemv_f32_kernel<NT, E><<<grid, kF32Warps * 32, 0, s>>>(a);                                 \
+    } else {                                                                                     \
+      auto k = gemv_tc_kernel<FMT, NT, E>;                                                       \
+      cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+      if (err != cudaSuccess) return err;                                                        \
+      k<<<grid, kGemvThreads, smem, s>>>(a);                                                     \
+    }                                                                                            \
+    return cudaGetLastError();                                                                   \
+  }
+  switch (epi) {
+    DFL_CASE(EPI_STORE)
+    DFL_CASE(EPI_CTX)
+    DFL_CASE(EPI_KV)
+    DFL_CASE(EPI_QKV)
+    DFL_CASE(EPI_RESID)
+    DFL_CASE(EPI_SWIGLU)
+    DFL_CASE(EPI_LMHEAD)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef DFL_CASE
+}
+
+template <int FMT>
+cudaError_t launch_gemv_fmt(int epi, int nt, const GemvArgs& a, int grid, size_t smem, cudaStream_t s) {
+  switch (nt) {
+    case 1: return launch_gemv_fmt_nt<FMT, 1>(epi, a, grid, smem, s);
+    case 2: return launch_gemv_fmt_nt<FMT, 2>(epi, a, grid, smem, s);
+    case 4: return launch_gemv_fmt_nt<FMT, 4>(epi, a, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dfl

@@ -1,0 +1,133 @@
+// Internal declarations shared by the host side (abi.cu) and the kernels (gemv.cu, attn.cu,
+// misc.cu) of the DFlash draft-round library. Not part of the public ABI (include/dflash.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace dfl {
+
+// ---- GEMV (skinny GEMM) geometry ---------------------------------------------------------------
+// Weights are re-laid-out at create time into 16-row strips. Per strip and per 64-input group:
+//   q4   : 576 B = 512 B of nibbles in mma.sync A-fragment order (16 B per lane) + 16 x (scale, bias)
+//   bf16 : 2048 B = 4 k16 steps x 32 lanes x 16 B, A-fragment order
+//   f32  : row-major float rows (CUDA-core path), strips of 16 consecutive logical rows
+constexpr int kWarps = 8;                 // consumer warps per tensor-core GEMV CTA
+constexpr int kStages = 4;                // ring depth per warp (bulk copies in flight)
+constexpr int kQ4GroupBytes = 576;
+constexpr int kBf16GroupBytes = 2048;
+constexpr int kQ4GroupsPerStage = 4;      // 2304 B per stage
+constexpr int kBf16GroupsPerStage = 1;    // 2048 B per stage
+constexpr int kStageBytes = 2304;         // max over formats
+constexpr int kMaxRows = 32;              // activation rows per launch (4 n-tiles of 8)
+constexpr int kXBudget = 120 * 1024;      // shared bytes for the staged activation slice
+constexpr int kMaxCtxChunk = 32;          // context rows per projection chunk
+constexpr int kGemvThreads = kWarps * 32;
+constexpr int kF32Warps = 8;
+
+enum Fmt { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q4 = 2 };
+enum Epi { EPI_STORE = 0, EPI_CTX = 1, EPI_KV = 2, EPI_QKV = 3, EPI_RESID = 4, EPI_SWIGLU = 5, EPI_LMHEAD = 6 };
+enum NormMode { NORM_NONE = 0, NORM_ONE = 1, NORM_CTX = 2 };
+
+// Device error word bits.
+constexpr unsigned kErrTimeoutGemv = 1u;
+constexpr unsigned kErrTimeoutAttn = 2u;
+
+struct RowMap {      // activation row r of a launch reads source row (r/per)*stride + off + r%per
+  int per, stride, off;
+};
+
+struct EpiArgs {
+  int row_base;      // first logical matrix row of the epilogue's output space
+  int n_rows;        // valid output features (rows >= row_base + n_rows are padding)
+  // EPI_STORE
+  void* out; int ldo; int out_f32;
+  // EPI_RESID: h[r][n] += y; xnext[r][n] = act(h[r][n] * wnext[n]); ssq_out[r*ssq_ld + strip]
+  float* h; const float* wnext; void* xnext; float* ssq_out; int ssq_ld;
+  // EPI_CTX: x = y; xw[i][r][n] = act(x*ctx_norm*attn_norm_i); ssq_out[(r*ssq_ld+strip)*2+{0,1}]
+  const float* ctx_norm; const float* attn_norms; int n_layers; void* xw; int xw_rows;
+  // EPI_QKV
+  void* q; void* kb; void* vb; int qd, kvd;
+  // EPI_KV (append to a ring of cap rows per (slot, kv head)); cache layout [slot][Hkv][cap][hd]
+  void* kc; void* vc; int cap, hd, n_kv;
+  int kv_slot[kMaxRows];
+  int kv_pos[kMaxRows];
+  // EPI_SWIGLU
+  void* act; int inter;
+  // EPI_LMHEAD
+  float* logits; int vocab; int rows_per_req; int32_t* tok_out; float* conf_out;
+  float* lm_part; int* lm_ticket;
+};
+
+struct GemvArgs {
+  const uint8_t* w;        // packed matrix base
+  int strip0, n_strips;    // strip range of this launch
+  int k, groups;           // inputs and 64-input groups
+  int n_slices, gps;       // K slices per strip, groups per slice
+  int ctas_per_slice;
+  int R;                   // activation rows (<= kMaxRows)
+  const void* x; int ldx; RowMap xmap;
+  int norm_mode; const float* ssq; int ssq_ld; int ssq_parts; float inv_dim; float eps;
+  float* partials; int* tickets;
+  unsigned* err;
+  EpiArgs e;
+};
+
+// ---- attention ---------------------------------------------------------------------------------
+struct AttnReq {
+  int slot;      // cache slot of the request
+  int ctx_len;   // context length P
+  int row0;      // first block row of the request
+};
+
+struct AttnArgs {
+  const void* q; const void* kb; const void* vb; void* out;   // q/out [rows][qd], kb/vb [rows][kvd]
+  const void* kc; const void* vc;                             // layer base of the cache
+  int qd, kvd, hd, hq, hkv, gamma, window, cap, max_batch;
+  int plane0;                                                 // layer * max_batch * hkv
+  int n_req, n_splits;
+  float scale_log2;                                           // log2(e) / sqrt(hd)
+  float* part_o; float* part_ml; int* tickets;
+  unsigned* err;
+  AttnReq req[DFLASH_MAX_BATCH];
+};
+
+// ---- misc --------------------------------------------------------------------------------------
+struct RepackSrc {
+  const void* data; const uint16_t* scale; const uint16_t* bias; int rows;
+};
+
+struct RepackArgs {
+  RepackSrc src[3]; int n_src;
+  int interleave;          // 1: strip rows 0-7 from src[0] (gate), 8-15 from src[1] (up)
+  int fmt, k, n_strips;
+  uint8_t* dst;
+};
+
+struct BlockArgs {
+  int n_req, gamma, d, H, vocab, fmt, act_f32;
+  const int32_t* anchor;
+  const void* emb; const uint16_t* emb_scale; const uint16_t* emb_bias;
+  const float* tokrow;        // [n_req][d] tok_proj(E[anchor]) when d != H
+  const float* mask_emb; const float* block_pos; const float* attn_norm0;
+  float* h; void* xn; float* ssq; int ssq_ld;
+  void* emb_out;              // gather mode: [n_req][H] activation rows
+};
+
+// ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
+cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s);
+size_t gemv_smem_bytes(int fmt, int R, int gps, int k);
+cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t s);
+size_t attn_smem_bytes(int hd);
+cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
+cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s);
+cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s);
+cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* target,
+                          int32_t* accept_len, int32_t* next_anchor, cudaStream_t s);
+
+}  // namespace dfl

@@ -1,0 +1,175 @@
+// Small kernels of the draft round: weight re-layout (once, at create), block construction,
+// embedding gather and greedy acceptance.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace dfl {
+
+namespace {
+
+// logical matrix row n -> (source, source row); false for padding rows
+__device__ __forceinline__ bool resolve_row(const RepackArgs& a, int n, int& src, int& row) {
+  if (a.interleave) {
+    const int strip = n / 16, m = n % 16;
+    src = m < 8 ? 0 : 1;
+    row = strip * 8 + (m % 8);
+    return row < a.src[src].rows;
+  }
+  for (int s = 0; s < a.n_src; s++) {
+    if (n < a.src[s].rows) {
+      src = s;
+      row = n;
+      return true;
+    }
+    n -= a.src[s].rows;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint32_t q4_code(const RepackArgs& a, int n, int k) {
+  int s, r;
+  if (!resolve_row(a, n, s, r)) return 0u;
+  const uint32_t w = static_cast<const uint32_t*>(a.src[s].data)[(size_t)r * (a.k / 8) + k / 8];
+  return (w >> (4 * (k % 8))) & 15u;
+}
+
+__device__ __forceinline__ uint32_t bf16_code(const RepackArgs& a, int n, int k) {
+  int s, r;
+  if (!resolve_row(a, n, s, r)) return 0u;
+  return static_cast<const uint16_t*>(a.src[s].data)[(size_t)r * a.k + k];
+}
+
+// Destination layouts (per 16-row strip, per 64-input group; k0 = 64*grp + 16*t + 4*j for
+// lane = 4*g + t and mma step j):
+//  q4  : 144 words. Word lane*4 + j packs the 8 codes lane (g,t) feeds mma j, nibble positions
+//        0..7 = (g,k0) (g+8,k0) (g,k0+2) (g+8,k0+2) (g,k0+1) (g+8,k0+1) (g,k0+3) (g+8,k0+3),
+//        so that (w >> 4i) & 0x000F000F yields A register i. Words 128 + m hold row m's
+//        (scale | bias << 16) bf16 pair.
+//  bf16: 512 words. Word j*128 + lane*4 + i is A register i of mma j:
+//        i=0 (g,k0..k0+1), 1 (g+8,k0..k0+1), 2 (g,k0+2..k0+3), 3 (g+8,k0+2..k0+3).
+//  f32 : row-major rows.
+__global__ void repack_kernel(const __grid_constant__ RepackArgs a) {
+  const int groups = a.k / 64;
+  const size_t words_per = a.fmt == FMT_Q4 ? 144 : 512;
+  const size_t total = a.fmt == FMT_F32 ? (size_t)a.n_strips * 16 * a.k : (size_t)a.n_strips * groups * words_per;
+  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < total; w += (size_t)gridDim.x * blockDim.x) {
+    if (a.fmt == FMT_F32) {
+      const int n = (int)(w / a.k), k = (int)(w % a.k);
+      int s, r;
+      float v = 0.f;
+      if (resolve_row(a, n, s, r)) v = static_cast<const float*>(a.src[s].data)[(size_t)r * a.k + k];
+      reinterpret_cast<float*>(a.dst)[w] = v;
+      continue;
+    }
+    const int strip = (int)(w / (groups * words_per));
+    const int rem = (int)(w % (groups * words_per));
+    const int grp = rem / (int)words_per, wi = rem % (int)words_per;
+    uint32_t out = 0;
+    if (a.fmt == FMT_Q4) {
+      if (wi < 128) {
+        const int lane = wi / 4, j = wi % 4, g = lane / 4, t = lane % 4;
+        const int k0 = grp * 64 + 16 * t + 4 * j;
+        const int r0 = strip * 16 + g, r1 = r0 + 8;
+        const uint32_t c[8] = {q4_code(a, r0, k0),     q4_code(a, r1, k0),     q4_code(a, r0, k0 + 2),
+                               q4_code(a, r1, k0 + 2), q4_code(a, r0, k0 + 1), q4_code(a, r1, k0 + 1),
+                               q4_code(a, r0, k0 + 3), q4_code(a, r1, k0 + 3)};
+#pragma unroll
+        for (int p = 0; p < 8; p++) out |= c[p] << (4 * p);
+      } else {
+        const int n = strip * 16 + (wi - 128);
+        int s, r;
+        if (resolve_row(a, n, s, r)) {
+          const size_t gi = (size_t)r * groups + grp;
+          out = (uint32_t)a.src[s].scale[gi] | ((uint32_t)a.src[s].bias[gi] << 16);
+        }
+      }
+    } else {
+      const int j = wi / 128, lane = (wi % 128) / 4, i = wi % 4, g = lane / 4, t = lane % 4;
+      const int k0 = grp * 64 + 16 * t + 4 * j + ((i >> 1) << 1);
+      const int row = strip * 16 + g + ((i & 1) << 3);
+      out = bf16_code(a, row, k0) | (bf16_code(a, row, k0 + 1) << 16);
+    }
+    reinterpret_cast<uint32_t*>(a.dst)[w] = out;
+  }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__ BlockArgs a) {
+  const int r = blockIdx.x, b = r / a.gamma, k = r % a.gamma;
+  __shared__ float red[8];
+  int tok = a.anchor[b];
+  tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);  // clamped: no read outside the table
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < a.d; j += blockDim.x) {
+    float v;
+    if (k == 0) {
+      const float e = a.tokrow ? a.tokrow[(size_t)b * a.d + j]
+                               : load_weight(a.fmt, a.emb, a.emb_scale, a.emb_bias, a.H, tok, j);
+      v = e + a.block_pos[j];
+    } else {
+      v = a.mask_emb[(size_t)(k - 1) * a.d + j] + a.block_pos[(size_t)k * a.d + j];
+    }
+    a.h[(size_t)r * a.d + j] = v;
+    static_cast<XT*>(a.xn)[(size_t)r * a.d + j] = from_f<XT>(v * a.attn_norm0[j]);
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) s += red[w];
+    a.ssq[(size_t)r * a.ssq_ld] = s;
+  }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant__ BlockArgs a) {
+  const int b = blockIdx.x;
+  int tok = a.anchor[b];
+  tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);
+  for (int j = threadIdx.x; j < a.H; j += blockDim.x)
+    static_cast<XT*>(a.emb_out)[(size_t)b * a.H + j] =
+        from_f<XT>(load_weight(a.fmt, a.emb, a.emb_scale, a.emb_bias, a.H, tok, j));
+}
+
+// One warp per request: first mismatch via ballot.
+__global__ void accept_kernel(int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
+                              int32_t* next_anchor) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const bool miss = lane < n && draft[(size_t)b * n + lane] != target[(size_t)b * (n + 1) + lane];
+  const unsigned mask = __ballot_sync(0xffffffffu, miss);
+  const int acc = mask ? __ffs(mask) - 1 : n;
+  if (lane == 0) {
+    accept_len[b] = acc;
+    next_anchor[b] = target[(size_t)b * (n + 1) + acc];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s) {
+  repack_kernel<<<1024, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s) {
+  if (a.act_f32) block_init_kernel<float><<<a.n_req * a.gamma, 256, 0, s>>>(a);
+  else block_init_kernel<__nv_bfloat16><<<a.n_req * a.gamma, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
+  if (a.act_f32) embed_gather_kernel<float><<<a.n_req, 256, 0, s>>>(a);
+  else embed_gather_kernel<__nv_bfloat16><<<a.n_req, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
+                          int32_t* next_anchor, cudaStream_t s) {
+  accept_kernel<<<n_req, 32, 0, s>>>(n, draft, target, accept_len, next_anchor);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

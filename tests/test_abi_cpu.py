@@ -1,0 +1,67 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every entry point the
+header declares; the ctypes mirrors have the C layout; host-side validation needs no GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import speculative_block_draft_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return pkg.lib()
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[a-z_0-9 ]+\*?\s*(dflash_[a-z_]+)\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (dflash_\w+)", out))
+    assert set(names) <= exported
+    assert set(pkg.SYMBOLS) == set(names)
+
+
+def test_struct_layouts_match_c(tmp_path):
+    src = tmp_path / "sz.c"
+    src.write_text('#include "dflash.h"\n#include <stdio.h>\n#include <stddef.h>\nint main(){printf("%zu %zu %zu %zu %zu %zu",'
+                   'sizeof(dflash_config), sizeof(dflash_matrix), sizeof(dflash_layer_weights), sizeof(dflash_weights),'
+                   'sizeof(dflash_stats), offsetof(dflash_weights, layer));return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = list(map(int, subprocess.check_output([str(exe)]).split()))
+    want = [ctypes.sizeof(pkg.dflash_config), ctypes.sizeof(pkg.dflash_matrix), ctypes.sizeof(pkg.dflash_layer_weights),
+            ctypes.sizeof(pkg.dflash_weights), ctypes.sizeof(pkg.dflash_stats), pkg.dflash_weights.layer.offset]
+    assert got == want
+
+
+def test_host_validation_without_gpu(lib):
+    bad = pkg.dflash_config()
+    assert lib.dflash_workspace_bytes(ctypes.byref(bad)) == 0
+    import dflash_synth as syn
+    good = pkg.make_config(syn.CONFIGS["c3"])
+    assert lib.dflash_workspace_bytes(ctypes.byref(good)) > 1_400_000_000   # repacked drafter + head
+    for field, val in (("head_dim", 96), ("gamma", 1), ("gamma", 17), ("max_batch", 65), ("adtype", 7)):
+        c = pkg.make_config(syn.CONFIGS["c3"])
+        setattr(c, field, val)
+        assert lib.dflash_workspace_bytes(ctypes.byref(c)) == 0, field
+    c = pkg.make_config(syn.CONFIGS["c3"], ctx_capacity=1000)        # ring smaller than the window
+    assert lib.dflash_workspace_bytes(ctypes.byref(c)) == 0
+    h = ctypes.c_void_p()
+    assert lib.dflash_create(ctypes.byref(good), None, None, 0, None, ctypes.byref(h)) == pkg.DFLASH_EINVAL
+    assert lib.dflash_draft_block(None, 1, None, None, 0.0, None, None, None, None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_ctx_len(None, 0) == -1
+    assert b"declined" in lib.dflash_status_str(pkg.DFLASH_DECLINED)

@@ -1,0 +1,43 @@
+"""The bench's multi-GPU host logic (replicas: max elapsed over ranks, units summed) on CPU with
+gloo, world size 2."""
+import os
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2")
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    t, u = bench.reduce_over_ranks(1.5 + rank, 10.0 * (rank + 1))
+    q.put((rank, t, u, bench.dist_env()[:2]))
+    dist.destroy_process_group()
+
+
+def test_reduce_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+    assert [r[1:3] for r in res] == [(2.5, 30.0), (2.5, 30.0)]
+    assert [r[3] for r in res] == [(0, 2), (1, 2)]
+
+
+def test_round_bytes_match_the_c3_budget():
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    b = bench.round_bytes(syn.CONFIGS["c3"], [4096])
+    assert abs(b["total"] / 1e6 - 1482.2) < 0.5          # layers 929.0 + head 437.6 + W_c 73.7 + KV 41.9
+    assert abs(b["lm_head"] / 1e6 - 437.6) < 0.1

@@ -1,0 +1,263 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Small configurations span several tiles, ragged tails, ring wrap-around, padding strips, split-K
+and row chunking; the full-size workloads (page-3 default bf16, the page-1 4-bit drafter, the
+block/head sweep and the batched case) run in the launch configuration the bench times.
+"""
+import numpy as np
+import pytest
+
+import dflash_synth as syn
+from dflash_synth import CONFIGS, DraftConfig
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import speculative_block_draft_gb300 as pkg
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkg.build()
+    yield
+
+
+def small(name, **kw):
+    base = dict(n_layers=2, d=256, n_q_heads=4, n_kv_heads=2, head_dim=64, inter=512, n_taps=2, target_hidden=256,
+                vocab=1000, gamma=5, window=0, ctx_len=70, wdtype="q4", adtype="bf16", seed=99)
+    base.update(kw)
+    return DraftConfig(name, **base)
+
+
+def run(cfg, rounds=3, jitter=0.1, max_batch=None, ctx_capacity=None, lengths=None, model=None, oracle_ctx=None,
+        appends=None):
+    from parity_util import Pair
+    model = model or syn.make_model(cfg, norm_jitter=jitter)
+    pair = Pair(cfg, model, max_batch=max_batch, ctx_capacity=ctx_capacity, oracle_ctx=oracle_ctx)
+    lengths = syn.ctx_lengths(cfg) if lengths is None else lengths
+    pair.prefill(lengths)
+    report = {}
+    for r in range(rounds):
+        if r:
+            counts = appends(r) if appends else syn.append_counts(cfg, r)
+            pair.append(counts)
+        pair.round(r, report)
+    assert pair.gpu.check() == 0
+    pair.gpu.close()
+    return report
+
+
+# ---------------------------------------------------------------------------------------------
+# small cases: every code path, several tiles, ragged tails
+# ---------------------------------------------------------------------------------------------
+def test_c1_tiny_fp32():
+    rep = run(CONFIGS["c1"], rounds=3)
+    assert rep["max_logit_err"] < 1e-4
+
+
+@pytest.mark.parametrize("wdtype", ["q4", "bf16"])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_small_formats_and_head_dims(wdtype, hd):
+    cfg = small(f"s_{wdtype}_{hd}", wdtype=wdtype, head_dim=hd, n_q_heads=512 // hd, n_kv_heads=max(1, 256 // hd),
+                d=512, target_hidden=512, inter=1024)
+    run(cfg, rounds=2)
+
+
+def test_small_d_ne_h_bf16():
+    """tok_proj / out_proj present (d != H)."""
+    run(small("s_proj", wdtype="bf16", target_hidden=512), rounds=2)
+
+
+@pytest.mark.parametrize("gamma", [2, 4, 8, 16])
+def test_small_block_sizes(gamma):
+    run(small(f"s_g{gamma}", gamma=gamma, n_q_heads=4, n_kv_heads=4 if gamma == 16 else 2), rounds=2)
+
+
+def test_sliding_window_ring_wraps():
+    """window 100 in a ring of 128 rows; 12 rounds of 7 new rows wrap the ring several times."""
+    cfg = small("s_ring", window=100, ctx_len=90)
+    run(cfg, rounds=12, ctx_capacity=100, appends=lambda r: np.array([7]))
+
+
+def test_empty_context():
+    cfg = small("s_p0", ctx_len=0)
+    run(cfg, rounds=2, lengths=np.array([0]), appends=lambda r: np.array([0]))
+
+
+def test_batch_ragged_and_row_chunks():
+    """8 requests x gamma 5 = 40 block rows (> 32: row chunks), ragged contexts, U{1..8} appends."""
+    cfg = small("s_batch", batch=8, ctx_len=300, ctx_min=1, window=128, append_min=1, append_max=8, agree=0.6)
+    run(cfg, rounds=3, ctx_capacity=160)
+
+
+def test_deterministic_repeat():
+    """Same inputs, two handles: bit-identical logits, tokens and confidence."""
+    from speculative_block_draft_gb300.session import Session
+    cfg = small("s_det")
+    m = syn.make_model(cfg, norm_jitter=0.1)
+    outs = []
+    for _ in range(2):
+        s = Session(m)
+        s.project([0], [70], syn.taps_rows(cfg, cfg.seed, 0, 0, 70))
+        outs.append(s.draft([0], np.array([3], dtype=np.int32)))
+        s.close()
+    for k in ("tokens", "conf", "logits"):
+        assert np.array_equal(outs[0][k], outs[1][k])
+
+
+def test_accept_kernel_exhaustive_vs_oracle():
+    import oracle
+    from speculative_block_draft_gb300.session import Session
+    cfg = small("s_acc", gamma=8)
+    s = Session(syn.make_model(cfg), max_batch=1)
+    rng = np.random.default_rng(0)
+    d = rng.integers(0, 3, size=(4096, 7)).astype(np.int32)
+    t = rng.integers(0, 3, size=(4096, 8)).astype(np.int32)
+    a, nxt = s.accept(d, t)
+    for i in range(4096):
+        assert (a[i], nxt[i]) == oracle.accept(d[i], t[i])
+    s.close()
+
+
+def test_abi_errors_and_decline(monkeypatch):
+    import speculative_block_draft_gb300 as pkg
+    from speculative_block_draft_gb300.session import Session
+    cfg = small("s_err", ctx_len=10)
+    s = Session(syn.make_model(cfg), max_batch=2, ctx_capacity=64)
+    h = s.h
+    taps = syn.taps_rows(cfg, cfg.seed, 0, 0, 10)
+    assert s.project([0], [10], taps) == 0
+    # temperature > 0 and the kill switch decline without touching the outputs
+    anchor = torch.zeros(1, dtype=torch.int32, device="cuda")
+    draft = torch.full((1, cfg.gamma - 1), -7, dtype=torch.int32, device="cuda")
+    assert h.draft_block([0], anchor, draft, temperature=0.4) == pkg.DFLASH_DECLINED
+    monkeypatch.setenv("DFLASH_DISABLE", "1")
+    assert h.draft_block([0], anchor, draft) == pkg.DFLASH_DECLINED
+    monkeypatch.delenv("DFLASH_DISABLE")
+    torch.cuda.synchronize()
+    assert int(draft.min()) == -7 and h.stats()["declined"] == 2
+    # rejected calls change no state
+    with pytest.raises(pkg.DFlashError) as e:
+        h.project_ctx([0, 0], [1, 1], torch.zeros(2, 512, dtype=torch.int16, device="cuda"))
+    assert e.value.status == pkg.DFLASH_EINVAL
+    with pytest.raises(pkg.DFlashError) as e:
+        h.project_ctx([5], [1], torch.zeros(1, 512, dtype=torch.int16, device="cuda"))
+    assert e.value.status == pkg.DFLASH_EINVAL
+    with pytest.raises(pkg.DFlashError) as e:   # window 0: capacity 64 rows per request
+        h.project_ctx([0], [60], torch.zeros(60, 512, dtype=torch.int16, device="cuda"))
+    assert e.value.status == pkg.DFLASH_ECAPACITY
+    assert h.ctx_len(0) == 10
+    assert h.draft_block([], anchor, draft) == 0
+    assert h.reset_request(1) == 0 and h.ctx_len(1) == 0
+    assert s.check() == 0
+    s.close()
+
+
+# ---------------------------------------------------------------------------------------------
+# full-size workloads
+# ---------------------------------------------------------------------------------------------
+def test_c2_p3_default_bf16_full():
+    rep = run(CONFIGS["c2"], rounds=2, jitter=0.0)
+    print("c2", rep)
+
+
+_C3_MODEL = {}
+
+
+def c3_model():
+    if "m" not in _C3_MODEL:
+        _C3_MODEL["m"] = syn.make_model(CONFIGS["c3"])
+    return _C3_MODEL["m"]
+
+
+def test_c3_dflash2_q4_full():
+    """The bench workload: 4-bit 5120-wide drafter, block 8, window 2048 over context 4096."""
+    rep = run(CONFIGS["c3"], rounds=2, jitter=0.0, model=c3_model())
+    print("c3", rep)
+
+
+def _c4_oracle_ctx(cfg, model):
+    """Window rows of the sweep's context (positions 6144..8191): the K/V rows do not depend on
+    gamma or on how head_dim splits the 1024 K/V features, so all sweep points share them."""
+    import oracle
+    key = ("c4ctx", cfg.window)
+    if key not in _C3_MODEL:
+        P = cfg.ctx_len
+        first = P - cfg.window if cfg.window else 0
+        taps = syn.taps_to_f32(cfg, syn.taps_rows(cfg, cfg.seed, 0, first, P - first)).astype(np.float64)
+        k, v = oracle.Oracle(model).ctx_rows(taps)
+        _C3_MODEL[key] = (first, k, v)
+    return {0: _C3_MODEL[key]}
+
+
+@pytest.mark.parametrize("cfg", syn.configs.C4[:6], ids=lambda c: c.name)
+def test_c4_sweep_full(cfg):
+    m = c3_model()
+    model = syn.HostModel(cfg, m.mats, dict(m.vecs))
+    model.vecs["block_pos"] = syn.normal(cfg.seed, "block_pos", (32, cfg.d), 0.02)[: cfg.gamma].copy()
+    model.vecs["mask_emb"] = syn.normal(cfg.seed, "mask_emb", (32, cfg.d), 0.02)[: cfg.gamma - 1].copy()
+    rep = run(cfg, rounds=1, jitter=0.0, model=model, oracle_ctx=_c4_oracle_ctx(cfg, m))
+    print(cfg.name, rep)
+
+
+@pytest.mark.slow
+def test_c4_full_context_window0():
+    cfg = syn.configs.C4[6]
+    m = c3_model()
+    model = syn.HostModel(cfg, m.mats, dict(m.vecs))
+    rep = run(cfg, rounds=1, jitter=0.0, model=model, oracle_ctx=_c4_oracle_ctx(cfg, m),
+              ctx_capacity=cfg.ctx_len + 64)
+    print(cfg.name, rep)
+
+
+def test_c5_batched_sampled_requests():
+    """32 requests, gamma 5, ragged contexts in [512, 16384], U{1..8} appends, agreement 0.6.
+    The GPU runs all 32; the oracle recomputes requests 0 and 17 (requests are independent)."""
+    from parity_util import MARGIN, Pair, accept_checked, compare_block
+    import oracle
+    cfg = CONFIGS["c5"]
+    m = c3_model()
+    model = syn.HostModel(cfg, m.mats, dict(m.vecs))
+    model.vecs["block_pos"] = syn.normal(cfg.seed, "block_pos", (32, cfg.d), 0.02)[: cfg.gamma].copy()
+    model.vecs["mask_emb"] = syn.normal(cfg.seed, "mask_emb", (32, cfg.d), 0.02)[: cfg.gamma - 1].copy()
+    from speculative_block_draft_gb300.session import Session
+    s = Session(model, max_batch=cfg.batch, ctx_capacity=cfg.window + 64)
+    lengths = syn.ctx_lengths(cfg)
+    B = cfg.batch
+    # the window is all that matters: rows before P - W never enter attention
+    first = [max(0, int(P) - cfg.window) for P in lengths]
+    rows = [syn.taps_rows(cfg, cfg.seed, b, first[b], int(lengths[b]) - first[b]) for b in range(B)]
+    # the GPU walks through the skipped prefix too (positions decide ring slots and the window);
+    # those rows never enter attention, so zero taps stand in for them
+    zeros = torch.zeros((4096, cfg.n_taps * cfg.target_hidden), dtype=torch.int16, device="cuda")
+    for b in range(B):
+        done = 0
+        while done < first[b]:
+            n = min(4096, first[b] - done)
+            with torch.cuda.stream(s.stream):
+                assert s.h.project_ctx([b], [n], zeros, stream=s.stream) == 0
+            done += n
+    s.stream.synchronize()
+    assert s.project(list(range(B)), [r.shape[0] for r in rows], np.concatenate(rows)) == 0
+    counts = syn.append_counts(cfg, 1)
+    app = [syn.taps_rows(cfg, cfg.seed, b, int(lengths[b]), int(counts[b])) for b in range(B)]
+    assert s.project(list(range(B)), [int(c) for c in counts], np.concatenate(app)) == 0
+    anchors = syn.anchors(cfg.seed, B, 1, cfg.vocab)
+    g = s.draft(list(range(B)), anchors, logits=True)
+    orc = oracle.Oracle(model)
+    rep = {}
+    for b in (0, 17):
+        taps = np.concatenate([rows[b], app[b]])
+        k, v = orc.ctx_rows(syn.taps_to_f32(cfg, taps).astype(np.float64))
+        if k.shape[1] > cfg.window:
+            k, v = k[:, -cfg.window:], v[:, -cfg.window:]
+        o = orc.draft(int(anchors[b]), np.ascontiguousarray(k), np.ascontiguousarray(v))
+        compare_block(cfg, g, o, b, rep)
+        t = syn.target_tokens(cfg.seed, b, 1, o["tokens"], cfg.agree, cfg.vocab)
+        ga, _ = s.accept(g["tokens"][b:b + 1], t[None, :])
+        accept_checked(o["tokens"], g["tokens"][b], o["margin"], t, int(ga[0]), rep)
+    assert s.check() == 0
+    s.close()
+    print("c5", rep)
