@@ -77,9 +77,10 @@ typedef struct {
                          bounds the total context length of a request. */
   float eps;          /* RMSNorm epsilon */
   int wdtype;         /* storage of every projection matrix, the embedding and the LM head */
-  int adtype;         /* DFLASH_F32 (fp32 taps, cache and CUDA-core arithmetic) or DFLASH_BF16
-                         (bf16 taps and cache, tensor-core projections with fp32 accumulation).
-                         DFLASH_F32 requires wdtype DFLASH_F32. */
+  int adtype;         /* DFLASH_F32: fp32 taps, fp32 cache, CUDA-core fp32 arithmetic (requires
+                         wdtype DFLASH_F32). DFLASH_BF16: bf16 taps; internally the tensor-core
+                         path runs f16 activations and an f16 context cache with fp32
+                         accumulation (bf16 weights are stored as f16 in the workspace). */
 } dflash_config;
 
 typedef struct {

@@ -49,6 +49,7 @@ struct dflash_handle {
   int* tickets = nullptr;
   float* lm_part = nullptr;
   int* lm_ticket = nullptr;
+  float* lm_strip = nullptr;
   float *att_o = nullptr, *att_ml = nullptr;
   int* att_tickets = nullptr;
   unsigned* err = nullptr;
@@ -216,6 +217,7 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->tickets = cv.take<int>((size_t)tk * 4);
   h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4);
   h->lm_ticket = cv.take<int>(4);
+  h->lm_strip = cv.take<float>((size_t)tk * kMaxRows * 3 * 4);
   // attention split partials: n_req * Hkv * splits stays below ~2 waves of CTAs (see draft)
   h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
   h->att_o = cv.take<float>((size_t)h->att_pairs_max * 64 * c.head_dim * 4);
@@ -273,7 +275,7 @@ int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
   const cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)h->cap * c.head_dim * 2};
   const cuuint32_t box[3] = {64, 64, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
@@ -310,6 +312,7 @@ struct GemvCall {
   const void* x = nullptr;
   int ldx = 0;
   RowMap xmap{1 << 30, 0, 0};
+  int x_bf16 = 0;
   int norm_mode = NORM_NONE;
   const float* ssq = nullptr;
   int ssq_ld = 0, ssq_parts = 0;
@@ -336,6 +339,7 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
   a.x = c.x;
   a.ldx = c.ldx;
   a.xmap = c.xmap;
+  a.x_bf16 = c.x_bf16;
   a.norm_mode = c.norm_mode;
   a.ssq = c.ssq;
   a.ssq_ld = c.ssq_ld;
@@ -349,6 +353,7 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
   if (c.epi == EPI_LMHEAD) {
     a.e.lm_part = h->lm_part;
     a.e.lm_ticket = h->lm_ticket;
+    a.e.lm_strip = h->lm_strip;
   }
   h->launches++;
   return status_of(launch_gemv(h->fmt, c.epi, nt_for(c.R), a, p.grid, s));
@@ -498,6 +503,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.R = rc;
     c1.x = tp + (size_t)row * h->mH * ab;
     c1.ldx = h->mH;
+    c1.x_bf16 = !h->act_f32;   // caller taps are bf16; the tensor-core path computes in f16
     c1.epi = EPI_CTX;
     c1.e.row_base = 0;
     c1.e.n_rows = h->d;

@@ -2,7 +2,7 @@
 // one request attend, with NO causal mask, over [context rows in the window ++ all gamma block
 // rows]; query head h reads K/V head h / (Hq/Hkv).
 //
-// Tensor-core path (bf16 cache): grid = (kv head, key split, request), flash-decoding style.
+// Tensor-core path (f16 cache): grid = (kv head, key split, request), flash-decoding style.
 //  * The CTA's query rows are the GQA group x gamma rows of one KV head (<= 64 rows, one 16-row
 //    m-tile per warp), held in shared memory.
 //  * Context K/V tiles of 64 rows x head_dim come from the per-layer ring cache
@@ -10,12 +10,12 @@
 //    ldmatrix reads are bank-conflict free. A tile never crosses the ring's wrap point; rows past
 //    the ring end read as zeros and are masked.
 //  * The last split also takes the 16-row block tile (K_d, V_d of this block, not cached).
-//  * S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate) with an online
+//  * S = Q K^T and O += P V run on mma.sync m16n8k16 (f16 in, fp32 accumulate) with an online
 //    softmax in fp32 (base-2 exponent, scores pre-scaled by log2(e)/sqrt(hd)).
 //  * Each split writes (O, m, l); the last split to arrive (atomic ticket, no waiting) merges them
-//    in split order and writes the bf16 attention output.
+//    in split order and writes the f16 attention output.
 // CUDA-core path (fp32 cache): one warp per (query head, block row), online softmax over keys.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -56,8 +56,8 @@ __device__ __forceinline__ void qk_tile(uint32_t q_base, uint32_t k_base, int su
       const int chunk = chunk0 + ((lane >> 3) & 1);
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(k_base + sub * sub_bytes + swz(key, chunk), b0, b1, b2, b3);
-      mma_bf16(S[nb], a0, a1, a2, a3, b0, b1);
-      mma_bf16(S[nb + 1], a0, a1, a2, a3, b2, b3);
+      mma_f16(S[nb], a0, a1, a2, a3, b0, b1);
+      mma_f16(S[nb + 1], a0, a1, a2, a3, b2, b3);
     }
   }
 }
@@ -108,10 +108,10 @@ __device__ __forceinline__ void softmax_pv(float (&S)[NKEY / 8][4], int nvalid, 
   }
 #pragma unroll
   for (int kb = 0; kb < NKEY / 16; kb++) {
-    const uint32_t a0 = pack_bf16x2(S[2 * kb][0], S[2 * kb][1]);
-    const uint32_t a1 = pack_bf16x2(S[2 * kb][2], S[2 * kb][3]);
-    const uint32_t a2 = pack_bf16x2(S[2 * kb + 1][0], S[2 * kb + 1][1]);
-    const uint32_t a3 = pack_bf16x2(S[2 * kb + 1][2], S[2 * kb + 1][3]);
+    const uint32_t a0 = pack_f16x2(S[2 * kb][0], S[2 * kb][1]);
+    const uint32_t a1 = pack_f16x2(S[2 * kb][2], S[2 * kb][3]);
+    const uint32_t a2 = pack_f16x2(S[2 * kb + 1][0], S[2 * kb + 1][1]);
+    const uint32_t a3 = pack_f16x2(S[2 * kb + 1][2], S[2 * kb + 1][3]);
 #pragma unroll
     for (int nd = 0; nd < HD / 8; nd += 2) {
       const int key = kb * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -119,8 +119,8 @@ __device__ __forceinline__ void softmax_pv(float (&S)[NKEY / 8][4], int nvalid, 
       const int sub = col8 / 8, chunk = col8 % 8;
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4_trans(v_base + sub * sub_bytes + swz(key, chunk), b0, b1, b2, b3);
-      mma_bf16(O[nd], a0, a1, a2, a3, b0, b1);
-      mma_bf16(O[nd + 1], a0, a1, a2, a3, b2, b3);
+      mma_f16(O[nd], a0, a1, a2, a3, b0, b1);
+      mma_f16(O[nd + 1], a0, a1, a2, a3, b2, b3);
     }
   }
 }
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
   }
 
   // Q rows (query row i = head-in-group * gamma + block row), pad rows zero
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+  const __half* qg = static_cast<const __half*>(a.q);
   for (int idx = threadIdx.x; idx < 64 * (HD / 8); idx += blockDim.x) {
     const int i = idx / (HD / 8), c8 = idx % (HD / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     *reinterpret_cast<uint4*>(q_s + (c8 / 8) * kSub + swz(i, c8 % 8)) = v;
   }
   if (with_block) {
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.kb);
-    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.vb);
+    const __half* kg = static_cast<const __half*>(a.kb);
+    const __half* vg = static_cast<const __half*>(a.vb);
     for (int idx = threadIdx.x; idx < 16 * (HD / 8); idx += blockDim.x) {
       const int k = idx / (HD / 8), c8 = idx % (HD / 8);
       uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
 
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  __half* out = static_cast<__half*>(a.out);
   if (a.n_splits == 1) {
     if (active) {
 #pragma unroll
@@ -273,10 +273,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
         if (i >= M) continue;
         const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
         const float inv = 1.0f / l_run[h];
-        __nv_bfloat16* o = out + (size_t)(rq.row0 + k) * a.qd + head * HD;
+        __half* o = out + (size_t)(rq.row0 + k) * a.qd + head * HD;
 #pragma unroll
         for (int nd = 0; nd < HD / 8; nd++)
-          *reinterpret_cast<uint32_t*>(o + nd * 8 + 2 * t) = pack_bf16x2(O[nd][2 * h] * inv, O[nd][2 * h + 1] * inv);
+          *reinterpret_cast<uint32_t*>(o + nd * 8 + 2 * t) = pack_f16x2(O[nd][2 * h] * inv, O[nd][2 * h + 1] * inv);
       }
     }
     return;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
       acc += wgt * __ldcg(&a.part_o[(ps * 64 + i) * HD + c]);
     }
     const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
-    out[(size_t)(rq.row0 + k) * a.qd + head * HD + c] = __float2bfloat16_rn(acc / L);
+    out[(size_t)(rq.row0 + k) * a.qd + head * HD + c] = from_f<__half>(acc / L);
   }
   if (threadIdx.x == 0) a.tickets[pair] = 0;
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "internal.h"
@@ -85,11 +86,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+// D = A * B + D, m16n8k16, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -116,15 +117,18 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return r;
 }
 
-// Two 4-bit codes (bits 0-3 and 16-19 of u) -> bf16x2 holding 128 + q (exact).
-__device__ __forceinline__ uint32_t nib2_to_bf16x2_plus128(uint32_t u) {
-  return lop3_and_or(u, 0x000F000Fu, 0x43004300u);
+// Two 4-bit codes at bits 3-6 and 19-22 of u -> f16x2 holding 128 + q (exact: the f16 ulp at
+// 128 is 1/8, so q lands in mantissa bits 3-6 of 0x5800 = 128.0).
+__device__ __forceinline__ uint32_t nib2_to_f16x2_plus128(uint32_t u_at_bit3) {
+  return lop3_and_or(u_at_bit3, 0x00780078u, 0x58005800u);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+constexpr float kF16Max = 65504.0f;
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -135,14 +139,16 @@ __device__ __forceinline__ float to_f(T v);
 template <>
 __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
 
 template <typename T>
 __device__ __forceinline__ T from_f(float v);
 template <>
 __device__ __forceinline__ float from_f<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <>  // saturating: activations never become inf
+__device__ __forceinline__ __half from_f<__half>(float v) {
+  return __float2half_rn(fminf(fmaxf(v, -kF16Max), kF16Max));
+}
 
 // Element k of row n of a matrix in its caller-side storage format (used for gathers).
 __device__ __forceinline__ float load_weight(int fmt, const void* data, const uint16_t* scale,

@@ -6,10 +6,11 @@
 //    X[R][slice] (bf16) into shared memory with 1-D bulk copies (TMA) once.
 //  * Each of its 8 warps streams the weight bytes of its strips through a private ring of
 //    kStages shared-memory stages filled by cp.async.bulk, so ~74 KB per SM are in flight.
-//  * 4-bit codes are turned into bf16 (128 + q, exact) with one lop3 per pair and fed to
-//    mma.sync m16n8k16 (weights = A, 16 rows; activations = B, 8 columns per n-tile). The
-//    group-64 affine code is folded per group in fp32:  sum_k (s q_k + b) x_k =
+//  * 4-bit codes are turned into f16 (128 + q, exact) with one shift and one lop3 per pair and
+//    fed to mma.sync m16n8k16 (weights = A, 16 rows; f16 activations = B, 8 columns per
+//    n-tile). The group-64 affine code is folded per group in fp32:  sum_k (s q_k + b) x_k =
 //    s * sum_k (128 + q_k) x_k + (b - 128 s) * sum_k x_k, so the MMA sees exact integers.
+//    bf16 weights are stored as f16 (converted once at create); activations are f16.
 //  * When a strip's K is split over several CTAs, each writes a partial tile; the last to
 //    arrive (atomic ticket, no waiting) sums them in slice order and runs the epilogue.
 // CUDA-core path (fp32 weights and activations): one warp per strip, fp32 FMA.
@@ -95,6 +96,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
   const EpiArgs& e = a.e;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
+  LmState lm_strip_state[NT][2];
   const bool v0 = nr0 >= 0 && nr0 < e.n_rows, v1 = nr1 >= 0 && nr1 < e.n_rows;
 #pragma unroll
   for (int nt = 0; nt < NT; nt++) {
@@ -148,16 +150,47 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
           store_act<XT>(e.act, (size_t)c * e.inter + j, silu * yb);
         }
       } else if constexpr (EPI == EPI_LMHEAD) {
+        // Which CTA finishes a split strip varies between runs, so split launches keep one
+        // state per strip (merged later in strip order) to stay bit-reproducible.
+        LmState& st = a.n_slices > 1 ? lm_strip_state[nt][p] : lm[nt][p];
+        if (a.n_slices > 1) st = LmState{-INFINITY, 0.f, 0x7fffffff};
         if (cv) {
           if (v0) {
             if (e.logits) e.logits[(size_t)c * e.vocab + nr0] = ya;
-            lm_push(lm[nt][p], ya, nr0);
+            lm_push(st, ya, nr0);
           }
           if (v1) {
             if (e.logits) e.logits[(size_t)c * e.vocab + nr1] = yb;
-            lm_push(lm[nt][p], yb, nr1);
+            lm_push(st, yb, nr1);
           }
         }
+      }
+    }
+  }
+  if constexpr (EPI == EPI_LMHEAD) {
+    if (a.n_slices > 1) {
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int p = 0; p < 2; p++)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            LmState other;
+            other.m = __shfl_xor_sync(0xffffffffu, lm_strip_state[nt][p].m, o);
+            other.s = __shfl_xor_sync(0xffffffffu, lm_strip_state[nt][p].s, o);
+            other.i = __shfl_xor_sync(0xffffffffu, lm_strip_state[nt][p].i, o);
+            lm_merge(lm_strip_state[nt][p], other);
+          }
+      if (g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+          for (int p = 0; p < 2; p++) {
+            float* dst = e.lm_strip + ((size_t)(strip - a.strip0) * kMaxRows + nt * 8 + 2 * t + p) * 3;
+            dst[0] = lm_strip_state[nt][p].m;
+            dst[1] = lm_strip_state[nt][p].s;
+            dst[2] = __int_as_float(lm_strip_state[nt][p].i);
+          }
       }
     }
   }
@@ -222,11 +255,49 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
   }
 }
 
+// Split-K head: the last CTA merges the per-strip states of each column with a fixed order
+// (thread j takes strips j, j + blockDim, ...; then a pairwise tree). Needs blockDim <= 256 and
+// scratch for blockDim states.
+__device__ __forceinline__ void lm_finish_split(const GemvArgs& a, LmState* sm) {
+  const EpiArgs& e = a.e;
+  __threadfence();
+  __syncthreads();
+  __shared__ int last_split;
+  if (threadIdx.x == 0) last_split = atomicAdd(e.lm_ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last_split) return;
+  __threadfence();
+  for (int c = 0; c < a.R; c++) {
+    LmState acc{-INFINITY, 0.f, 0x7fffffff};
+    for (int j = threadIdx.x; j < a.n_strips; j += blockDim.x) {
+      const float* src = e.lm_strip + ((size_t)j * kMaxRows + c) * 3;
+      LmState o{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))};
+      lm_merge(acc, o);
+    }
+    sm[threadIdx.x] = acc;
+    __syncthreads();
+    for (int off = blockDim.x / 2; off > 0; off >>= 1) {
+      if ((int)threadIdx.x < off) lm_merge(sm[threadIdx.x], sm[threadIdx.x + off]);
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      e.tok_out[c] = sm[0].i;
+      if (e.conf_out) e.conf_out[c] = 1.0f / sm[0].s;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *e.lm_ticket = 0;
+}
+
 // Vocab reduction of the LM-head epilogue: lanes -> warps -> CTA partial -> last CTA.
 template <int NT>
 __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2], LmState* sm_lm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int nw = blockDim.x >> 5;
+  if (a.n_slices > 1) {
+    lm_finish_split(a, sm_lm);
+    return;
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; nt++)
 #pragma unroll
@@ -280,7 +351,7 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
 // ------------------------------------------------------------------------------------------------
 template <int FMT, int NT, int EPI>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_constant__ GemvArgs a) {
-  using XT = __nv_bfloat16;
+  using XT = __half;
   constexpr int GS = FMT == FMT_Q4 ? kQ4GroupsPerStage : kBf16GroupsPerStage;
   constexpr int GB = FMT == FMT_Q4 ? kQ4GroupBytes : kBf16GroupBytes;
   constexpr int RP = NT * 8;
@@ -345,14 +416,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   compute_row_scales(a, srow, RP);
   bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
   ok = __syncthreads_and(ok);
+  if (a.x_bf16 && ok) {  // caller-side bf16 rows (context taps) -> f16 in place
+    for (int i = threadIdx.x; i < a.R * (kbytes / 4); i += blockDim.x) {
+      uint32_t* p = reinterpret_cast<uint32_t*>(xs + (size_t)(i / (kbytes / 4)) * xstride) + i % (kbytes / 4);
+      const uint32_t u = *p;
+      const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
+      *p = pack_f16x2(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
+    }
+    __syncthreads();
+  }
   if (FMT == FMT_Q4 && ok) {
     for (int i = threadIdx.x; i < RP * ng; i += blockDim.x) {
       const int r = i / ng, gl = i % ng;
-      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(xs + (size_t)r * xstride + gl * 128);
+      const __half2* p = reinterpret_cast<const __half2*>(xs + (size_t)r * xstride + gl * 128);
       float s = 0.f;
 #pragma unroll 8
       for (int j = 0; j < 32; j++) {
-        const float2 f = __bfloat1622float2(p[j]);
+        const float2 f = __half22float2(p[j]);
         s += f.x + f.y;
       }
       xsum[r * a.gps + gl] = s;
@@ -402,10 +482,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
           uint32_t af[4][4];
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            af[j][0] = nib2_to_bf16x2_plus128(u[j]);
-            af[j][1] = nib2_to_bf16x2_plus128(u[j] >> 4);
-            af[j][2] = nib2_to_bf16x2_plus128(u[j] >> 8);
-            af[j][3] = nib2_to_bf16x2_plus128(u[j] >> 12);
+            af[j][0] = nib2_to_f16x2_plus128(u[j] << 3);
+            af[j][1] = nib2_to_f16x2_plus128(u[j] >> 1);
+            af[j][2] = nib2_to_f16x2_plus128(u[j] >> 5);
+            af[j][3] = nib2_to_f16x2_plus128(u[j] >> 9);
           }
 #pragma unroll
           for (int nt = 0; nt < NT; nt++) {
@@ -413,10 +493,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
             const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
             const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_bf16(acc, af[0][0], af[0][1], af[0][2], af[0][3], x01.x, x01.y);
-            mma_bf16(acc, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
-            mma_bf16(acc, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
-            mma_bf16(acc, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
+            mma_f16(acc, af[0][0], af[0][1], af[0][2], af[0][3], x01.x, x01.y);
+            mma_f16(acc, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
+            mma_f16(acc, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
+            mma_f16(acc, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
             const float xa = xsum[(nt * 8 + 2 * t) * a.gps + gl];
             const float xb = xsum[(nt * 8 + 2 * t + 1) * a.gps + gl];
             y[nt][0] = fmaf(s0, acc[0], fmaf(b0, xa, y[nt][0]));
@@ -434,10 +514,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
             const uint8_t* xr = xs + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
             const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
             const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
-            mma_bf16(y[nt], A[0].x, A[0].y, A[0].z, A[0].w, x01.x, x01.y);
-            mma_bf16(y[nt], A[1].x, A[1].y, A[1].z, A[1].w, x01.z, x01.w);
-            mma_bf16(y[nt], A[2].x, A[2].y, A[2].z, A[2].w, x23.x, x23.y);
-            mma_bf16(y[nt], A[3].x, A[3].y, A[3].z, A[3].w, x23.z, x23.w);
+            mma_f16(y[nt], A[0].x, A[0].y, A[0].z, A[0].w, x01.x, x01.y);
+            mma_f16(y[nt], A[1].x, A[1].y, A[1].z, A[1].w, x01.z, x01.w);
+            mma_f16(y[nt], A[2].x, A[2].y, A[2].z, A[2].w, x23.x, x23.y);
+            mma_f16(y[nt], A[3].x, A[3].y, A[3].z, A[3].w, x23.z, x23.w);
           }
         }
       }

@@ -13,7 +13,7 @@ namespace dfl {
 // ---- GEMV (skinny GEMM) geometry ---------------------------------------------------------------
 // Weights are re-laid-out at create time into 16-row strips. Per strip and per 64-input group:
 //   q4   : 576 B = 512 B of nibbles in mma.sync A-fragment order (16 B per lane) + 16 x (scale, bias)
-//   bf16 : 2048 B = 4 k16 steps x 32 lanes x 16 B, A-fragment order
+//   bf16 : 2048 B = 4 k16 steps x 32 lanes x 16 B, A-fragment order, values stored as f16
 //   f32  : row-major float rows (CUDA-core path), strips of 16 consecutive logical rows
 constexpr int kWarps = 8;                 // consumer warps per tensor-core GEMV CTA
 constexpr int kStages = 4;                // ring depth per warp (bulk copies in flight)
@@ -60,6 +60,7 @@ struct EpiArgs {
   // EPI_LMHEAD
   float* logits; int vocab; int rows_per_req; int32_t* tok_out; float* conf_out;
   float* lm_part; int* lm_ticket;
+  float* lm_strip;   // split-K launches: per-strip (max, sum, index) per column, merged in strip order
 };
 
 struct GemvArgs {
@@ -70,6 +71,7 @@ struct GemvArgs {
   int ctas_per_slice;
   int R;                   // activation rows (<= kMaxRows)
   const void* x; int ldx; RowMap xmap;
+  int x_bf16;              // tensor-core path: x rows are bf16 (converted to f16 after staging)
   int norm_mode; const float* ssq; int ssq_ld; int ssq_parts; float inv_dim; float eps;
   float* partials; int* tickets;
   unsigned* err;

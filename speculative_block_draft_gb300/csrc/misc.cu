@@ -1,6 +1,6 @@
 // Small kernels of the draft round: weight re-layout (once, at create), block construction,
 // embedding gather and greedy acceptance.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -34,10 +34,12 @@ __device__ __forceinline__ uint32_t q4_code(const RepackArgs& a, int n, int k) {
   return (w >> (4 * (k % 8))) & 15u;
 }
 
-__device__ __forceinline__ uint32_t bf16_code(const RepackArgs& a, int n, int k) {
+// bf16 weight -> f16 bits (exact for |w| in the f16 normal range; the tensor-core path runs f16)
+__device__ __forceinline__ uint32_t bf16_as_f16_bits(const RepackArgs& a, int n, int k) {
   int s, r;
   if (!resolve_row(a, n, s, r)) return 0u;
-  return static_cast<const uint16_t*>(a.src[s].data)[(size_t)r * a.k + k];
+  const float w = bf16_bits_to_float(static_cast<const uint16_t*>(a.src[s].data)[(size_t)r * a.k + k]);
+  return __half_as_ushort(__float2half_rn(w));
 }
 
 // Destination layouts (per 16-row strip, per 64-input group; k0 = 64*grp + 16*t + 4*j for
@@ -46,7 +48,7 @@ __device__ __forceinline__ uint32_t bf16_code(const RepackArgs& a, int n, int k)
 //        0..7 = (g,k0) (g+8,k0) (g,k0+2) (g+8,k0+2) (g,k0+1) (g+8,k0+1) (g,k0+3) (g+8,k0+3),
 //        so that (w >> 4i) & 0x000F000F yields A register i. Words 128 + m hold row m's
 //        (scale | bias << 16) bf16 pair.
-//  bf16: 512 words. Word j*128 + lane*4 + i is A register i of mma j:
+//  bf16: 512 words of f16 pairs. Word j*128 + lane*4 + i is A register i of mma j:
 //        i=0 (g,k0..k0+1), 1 (g+8,k0..k0+1), 2 (g,k0+2..k0+3), 3 (g+8,k0+2..k0+3).
 //  f32 : row-major rows.
 __global__ void repack_kernel(const __grid_constant__ RepackArgs a) {
@@ -88,7 +90,7 @@ __global__ void repack_kernel(const __grid_constant__ RepackArgs a) {
       const int j = wi / 128, lane = (wi % 128) / 4, i = wi % 4, g = lane / 4, t = lane % 4;
       const int k0 = grp * 64 + 16 * t + 4 * j + ((i >> 1) << 1);
       const int row = strip * 16 + g + ((i & 1) << 3);
-      out = bf16_code(a, row, k0) | (bf16_code(a, row, k0 + 1) << 16);
+      out = bf16_as_f16_bits(a, row, k0) | (bf16_as_f16_bits(a, row, k0 + 1) << 16);
     }
     reinterpret_cast<uint32_t*>(a.dst)[w] = out;
   }
@@ -156,13 +158,13 @@ cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s) {
 
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s) {
   if (a.act_f32) block_init_kernel<float><<<a.n_req * a.gamma, 256, 0, s>>>(a);
-  else block_init_kernel<__nv_bfloat16><<<a.n_req * a.gamma, 256, 0, s>>>(a);
+  else block_init_kernel<__half><<<a.n_req * a.gamma, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
   if (a.act_f32) embed_gather_kernel<float><<<a.n_req, 256, 0, s>>>(a);
-  else embed_gather_kernel<__nv_bfloat16><<<a.n_req, 256, 0, s>>>(a);
+  else embed_gather_kernel<__half><<<a.n_req, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
