@@ -176,6 +176,24 @@ uint64_t dflash_launch_count(const dflash_handle* h);
 
 void dflash_destroy(dflash_handle* h);
 
+/* Allocation-free greedy token and softmax confidence for logits the caller already holds.
+ * The pages describe no such call; it exists for callers that cannot allocate device memory on
+ * their request path (an engine whose memory pool already owns the GPU, or a host process that
+ * forbids the library from calling cudaMalloc) and therefore cannot provide a dflash_create
+ * workspace. It runs the same vocab reduction as the LM-head epilogue of dflash_draft_block:
+ * token[r] = argmax_j logits[r][j] (lowest index on ties), conf[r] = 1 / sum_j exp(l_rj - max)
+ * (conf may be NULL). logits: device fp32 [rows][vocab]; token: device int32 [rows].
+ * It allocates nothing: its scratch is a fixed ~49 KB array inside the library that every
+ * device loading the library keeps until the process exits. Limits: rows <= 64
+ * (DFLASH_NOALLOC_MAX_ROWS; more returns DFLASH_ECAPACITY), 2 <= vocab < 2^31.
+ * The first call on each device looks up that array's device address (with the device
+ * current), so make that first call before any stream capture. All calls share the array:
+ * calls that can overlap on the GPU (different streams, different threads) race and must be
+ * serialised by the caller. No handle is needed. */
+#define DFLASH_NOALLOC_MAX_ROWS 64
+int dflash_greedy_from_logits_noalloc(const float* logits, int rows, int vocab, int32_t* token, float* conf,
+                                      void* stream);
+
 const char* dflash_status_str(int status);
 
 #ifdef __cplusplus

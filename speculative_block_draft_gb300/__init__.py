@@ -16,7 +16,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash.so")
-_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu"]
+_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu"]
 _HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a",
               "-Xcompiler", "-fPIC"]
@@ -25,6 +25,7 @@ DFLASH_OK, DFLASH_DECLINED, DFLASH_EINVAL, DFLASH_ECAPACITY, DFLASH_ECUDA, DFLAS
 DFLASH_F32, DFLASH_BF16, DFLASH_Q4G64 = 0, 1, 2
 DFLASH_MAX_LAYERS = 8
 DFLASH_MAX_BATCH = 64
+DFLASH_NOALLOC_MAX_ROWS = 64
 DTYPE = {"f32": DFLASH_F32, "bf16": DFLASH_BF16, "q4": DFLASH_Q4G64}
 
 
@@ -95,7 +96,7 @@ _lib = None
 SYMBOLS = ["dflash_workspace_bytes", "dflash_create", "dflash_project_ctx", "dflash_draft_block",
            "dflash_accept", "dflash_reset_request", "dflash_ctx_len", "dflash_check_errors",
            "dflash_get_stats", "dflash_set_probe", "dflash_launch_count", "dflash_destroy",
-           "dflash_status_str"]
+           "dflash_status_str", "dflash_greedy_from_logits_noalloc"]
 
 
 def lib():
@@ -133,8 +134,19 @@ def lib():
         L.dflash_destroy.argtypes = [vp]
         L.dflash_status_str.restype = ctypes.c_char_p
         L.dflash_status_str.argtypes = [i32]
+        L.dflash_greedy_from_logits_noalloc.restype = i32
+        L.dflash_greedy_from_logits_noalloc.argtypes = [vp, i32, i32, vp, vp, vp]
         _lib = L
     return _lib
+
+
+def greedy_from_logits_noalloc(logits, token, conf=None, stream=None) -> int:
+    """dflash_greedy_from_logits_noalloc on device tensors: logits fp32 [rows][vocab] ->
+    token int32 [rows], conf fp32 [rows] (optional). Allocates nothing on the device."""
+    rows, vocab = logits.shape
+    return _check(lib().dflash_greedy_from_logits_noalloc(logits.data_ptr(), rows, vocab, token.data_ptr(),
+                                                          conf.data_ptr() if conf is not None else None,
+                                                          _stream_ptr(stream)), "dflash_greedy_from_logits_noalloc")
 
 
 class DFlashError(RuntimeError):
