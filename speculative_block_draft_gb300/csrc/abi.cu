@@ -75,6 +75,9 @@ int packed_bytes_per_strip(int fmt, int k) {
 
 int nt_for(int R) { return R <= 8 ? 1 : (R <= 16 ? 2 : 4); }
 
+// Split of one launch over the SMs. Every warp of a CTA works on every strip of that CTA, so the
+// time of a launch is about (strips per CTA) x (groups per K slice); a K split over several
+// CTAs costs a partial tile per strip, counted here as one extra group.
 GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R) {
   GemvPlan p{};
   if (h->fmt == FMT_F32) {
@@ -84,18 +87,30 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R) {
     p.grid = p.ctas_per_slice;
     return p;
   }
-  const int rp = nt_for(R) * 8;
-  const int gps_max = std::max(1, (kXBudget / rp - 16) / 128);
-  const int ctas = std::max(1, std::min((n_strips + kWarps - 1) / kWarps, h->n_sm));
-  int s = std::max(1, (int)lround((double)h->n_sm / ctas));
-  s = std::min(s, groups);
-  int gps = (groups + s - 1) / s;
-  gps = std::min(gps, gps_max);
-  s = (groups + gps - 1) / gps;
-  p.n_slices = s;
-  p.gps = gps;
-  p.ctas_per_slice = ctas;
-  p.grid = s * ctas;
+  constexpr size_t kSmemLimit = 225 * 1024;
+  long best = -1;
+  for (int s = 1; s <= std::max(1, std::min(16, groups / kWarps)); s++) {
+    const int gps = (groups + s - 1) / s;
+    if (gemv_smem_bytes(h->fmt, R, gps, 0) > kSmemLimit) continue;
+    const int slices = (groups + gps - 1) / gps;
+    const int ctas = std::max(1, std::min(n_strips, h->n_sm / slices));
+    const long per_cta = (n_strips + ctas - 1) / ctas;
+    const long cost = per_cta * (gps + (slices > 1 ? 1 : 0));
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.n_slices = slices;
+      p.gps = gps;
+      p.ctas_per_slice = ctas;
+    }
+  }
+  if (best < 0) {  // the activation slice must shrink further: split K until it fits
+    int gps = groups;
+    while (gps > 1 && gemv_smem_bytes(h->fmt, R, gps, 0) > kSmemLimit) gps = (gps + 1) / 2;
+    p.gps = gps;
+    p.n_slices = (groups + gps - 1) / gps;
+    p.ctas_per_slice = std::max(1, std::min(n_strips, h->n_sm / p.n_slices));
+  }
+  p.grid = p.n_slices * p.ctas_per_slice;
   return p;
 }
 
@@ -626,7 +641,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
 
   const int req_per_chunk = std::max(1, kMaxRows / G);
   for (int i = 0; i < h->L; i++) {
-    const int in_parts = i == 0 ? 1 : parts;
+    const int in_parts = i == 0 ? (d + kBlockCols - 1) / kBlockCols : parts;
     // Q, K_d, V_d of RMSNorm_attn_i(H_d)
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
@@ -686,10 +701,11 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         h->launches++;
         if ((st = status_of(launch_attn_f32(aa, s)))) return st;
       } else {
+        // about four 64-key tiles per split, but enough splits to spread over the SMs
         const int pairs = n_req * c.n_kv_heads;
         int splits = std::max(1, (2 * h->n_sm + pairs - 1) / pairs);
-        splits = std::min(splits, max_tiles);
-        splits = std::max(1, std::min(splits, h->att_pairs_max / pairs));
+        splits = std::min(splits, std::max(1, (max_tiles + 3) / 4));
+        splits = std::max(1, std::min(std::min(splits, 64), h->att_pairs_max / pairs));
         aa.n_splits = splits;
         h->launches++;
         if ((st = status_of(launch_attn_tc(aa, h->kmap, h->vmap, s)))) return st;

@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     mbar_init(smem_u32(&bars[1]), 1);
     fence_barrier_init();
   }
+  pdl_launch_dependents();
+  pdl_wait();   // the cache rows and Q/K/V of this round were written by earlier kernels
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 0; i < min(2, n_tiles); i++) issue(i);
@@ -306,22 +308,45 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int idx = threadIdx.x; idx < M * HD; idx += blockDim.x) {
-    const int i = idx / HD, c = idx % HD;
+  // merge: per query row, the weight of each split (computed once), then O row-wise
+  float* wgt = reinterpret_cast<float*>(stage_s);   // [2][64 splits][64 rows] (the K/V stages are free now)
+  const size_t pbase = (size_t)pair * a.n_splits;
+  if ((int)threadIdx.x < M) {
+    const int i = threadIdx.x;
     float mx = -INFINITY;
-    for (int s = 0; s < a.n_splits; s++)
-      mx = fmaxf(mx, __ldcg(&a.part_ml[(((size_t)pair * a.n_splits + s) * 64 + i) * 2]));
-    float L = 0.f, acc = 0.f;
-    for (int s = 0; s < a.n_splits; s++) {
-      const size_t ps = (size_t)pair * a.n_splits + s;
-      const float ms = __ldcg(&a.part_ml[(ps * 64 + i) * 2]);
-      if (ms == -INFINITY) continue;
-      const float wgt = exp2f(ms - mx);
-      L += wgt * __ldcg(&a.part_ml[(ps * 64 + i) * 2 + 1]);
-      acc += wgt * __ldcg(&a.part_o[(ps * 64 + i) * HD + c]);
+#pragma unroll 8
+    for (int s2 = 0; s2 < a.n_splits; s2++) {   // stage (m, l) of every split in shared memory
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
+      wgt[s2 * 64 + i] = ml.x;
+      wgt[(64 + s2) * 64 + i] = ml.y;
+      mx = fmaxf(mx, ml.x);
+    }
+    float L = 0.f;
+    for (int s2 = 0; s2 < a.n_splits; s2++) {
+      const float ms = wgt[s2 * 64 + i];
+      const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+      wgt[s2 * 64 + i] = w;
+      L += w * wgt[(64 + s2) * 64 + i];
+    }
+    const float inv = 1.0f / L;
+    for (int s2 = 0; s2 < a.n_splits; s2++) wgt[s2 * 64 + i] *= inv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < M * (HD / 4); idx += blockDim.x) {
+    const int i = idx / (HD / 4), c4 = idx % (HD / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s2 = 0; s2 < a.n_splits; s2++) {
+      const float w = wgt[s2 * 64 + i];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + ((pbase + s2) * 64 + i) * HD) + c4);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
     const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
-    out[(size_t)(rq.row0 + k) * a.qd + head * HD + c] = from_f<__half>(acc / L);
+    __half* o = out + (size_t)(rq.row0 + k) * a.qd + head * HD + c4 * 4;
+    *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(acc.x, acc.y), pack_f16x2(acc.z, acc.w));
   }
   if (threadIdx.x == 0) a.tickets[pair] = 0;
 }
@@ -400,10 +425,15 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUt
   const size_t smem = attn_smem_bytes(a.hd);
   cudaError_t err;
 #define DFL_ATTN(HD)                                                                                \
-  err = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-  if (err != cudaSuccess) return err;                                                               \
-  attn_tc_kernel<HD><<<grid, kAttnWarps * 32, smem, s>>>(a, kmap, vmap);                            \
-  return cudaGetLastError();
+  {                                                                                                 \
+    static int smem_set = 0;                                                                        \
+    if ((int)smem > smem_set) {                                                                     \
+      err = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+      if (err != cudaSuccess) return err;                                                           \
+      smem_set = (int)smem;                                                                         \
+    }                                                                                               \
+  }                                                                                                 \
+  return launch_pdl(attn_tc_kernel<HD>, grid, dim3(kAttnWarps * 32), smem, s, a, kmap, vmap);
   switch (a.hd) {
     case 64: { DFL_ATTN(64) }
     case 128: { DFL_ATTN(128) }

@@ -117,11 +117,16 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return r;
 }
 
-// Two 4-bit codes at bits 3-6 and 19-22 of u -> f16x2 holding 128 + q (exact: the f16 ulp at
-// 128 is 1/8, so q lands in mantissa bits 3-6 of 0x5800 = 128.0).
-__device__ __forceinline__ uint32_t nib2_to_f16x2_plus128(uint32_t u_at_bit3) {
+// 4-bit codes -> f16x2 with one lop3 each; both forms are exact and the caller undoes the offset
+// (and the factor 16) in fp32, once per 64-input group:
+//   codes at bits 3-6 / 19-22 with 0x5800 (128.0, ulp 1/8) -> 128 + q
+//   codes at bits 4-7 / 20-23 with 0x6400 (1024.0, ulp 1)  -> 1024 + 16 q   (no shift needed)
+// The offsets are kept small relative to q (about 17x and 8.5x) because the fp32 group sum loses
+// that factor when the offset is removed.
+__device__ __forceinline__ uint32_t nib128_to_f16x2(uint32_t u_at_bit3) {
   return lop3_and_or(u_at_bit3, 0x00780078u, 0x58005800u);
 }
+__device__ __forceinline__ uint32_t nib_hi_to_f16x2(uint32_t u) { return lop3_and_or(u, 0x00F000F0u, 0x64006400u); }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
@@ -160,6 +165,13 @@ __device__ __forceinline__ float load_weight(int fmt, const void* data, const ui
   const int64_t g = n * (n_in / 64) + k / 64;
   return fmaf(bf16_bits_to_float(scale[g]), q, bf16_bits_to_float(bias[g]));
 }
+
+// Programmatic dependent launch: let the next kernel of the stream start launching, and wait
+// until every earlier kernel of the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

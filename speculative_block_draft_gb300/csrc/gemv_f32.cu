@@ -15,6 +15,7 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int k) {
   if (fmt == FMT_Q4) b += (size_t)rp * gps * 4;        // per-group activation sums
   b += kMaxRows * 4;                                   // row scales
   b += (size_t)kWarps * kMaxRows * sizeof(LmState);    // vocab reduction scratch
+  b += (size_t)2 * kWarps * 32 * (rp / 2) * 4;         // per-strip reduction buffers (2 x warps x 32 x NT*4)
   b += 16 + (1 + kWarps * kStages) * 8;                // mbarriers
   return b;
 }

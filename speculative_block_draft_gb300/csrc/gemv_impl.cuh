@@ -4,15 +4,24 @@
 // Tensor-core path (bf16 / 4-bit weights), one CTA per SM:
 //  * A CTA owns one K slice and a range of 16-row strips. It stages its activation slice
 //    X[R][slice] (bf16) into shared memory with 1-D bulk copies (TMA) once.
-//  * Each of its 8 warps streams the weight bytes of its strips through a private ring of
-//    kStages shared-memory stages filled by cp.async.bulk, so ~74 KB per SM are in flight.
-//  * 4-bit codes are turned into f16 (128 + q, exact) with one shift and one lop3 per pair and
-//    fed to mma.sync m16n8k16 (weights = A, 16 rows; f16 activations = B, 8 columns per
-//    n-tile). The group-64 affine code is folded per group in fp32:  sum_k (s q_k + b) x_k =
-//    s * sum_k (128 + q_k) x_k + (b - 128 s) * sum_k x_k, so the MMA sees exact integers.
-//    bf16 weights are stored as f16 (converted once at create); activations are f16.
-//  * When a strip's K is split over several CTAs, each writes a partial tile; the last to
-//    arrive (atomic ticket, no waiting) sums them in slice order and runs the epilogue.
+//  * Its warps stream weights through private rings of kStages shared-memory stages filled by
+//    cp.async.bulk. Strips are dealt out in whole rounds (one strip per warp, no
+//    synchronisation); the fewer-than-kWarps leftover strips are shared by all warps, each
+//    taking an equal share of the slice's 64-input groups, and summed through shared memory
+//    (double buffered, in warp order). Work is balanced to within one group.
+//  * 4-bit codes become f16 with one lop3 per register (plus a shift for three of four): the
+//    re-laid-out word of a lane holds rows g and g+8 in alternating nibbles, so row g decodes
+//    to 128 + q (magic 0x5800) and row g+8 to 1024 + 16 q (magic 0x6400, no shift). mma.sync
+//    m16n8k16 (weights = A, 16 rows; f16 activations = B, 8 columns per n-tile) accumulates per
+//    64-input group in fp32, and the group-64 affine code is folded once per group:
+//    sum_k (s q_k + b) x_k equals
+//      row g  :  s      * sum (128 + q) x    + (b - 128 s) * sum x
+//      row g+8:  s / 16 * sum (1024 + 16q) x + (b -  64 s) * sum x
+//    so the MMA sees exact integers; the offsets stay small next to q (17x, 8.5x) because the
+//    fp32 group sum loses that factor when they are removed. bf16 weights are stored as f16.
+//  * When a strip's K is split over several CTAs, each writes a partial tile; after its last
+//    strip every CTA settles its tickets, and the last slice to arrive (atomic ticket, no
+//    waiting) sums the partials in slice order and runs the epilogue.
 // CUDA-core path (fp32 weights and activations): one warp per strip, fp32 FMA.
 #pragma once
 
@@ -276,8 +285,11 @@ __device__ __forceinline__ void lm_finish_split(const GemvArgs& a, LmState* sm) 
     }
     sm[threadIdx.x] = acc;
     __syncthreads();
-    for (int off = blockDim.x / 2; off > 0; off >>= 1) {
-      if ((int)threadIdx.x < off) lm_merge(sm[threadIdx.x], sm[threadIdx.x + off]);
+    int span = 1;
+    while (span < (int)blockDim.x) span <<= 1;
+    for (int off = span / 2; off > 0; off >>= 1) {
+      if ((int)threadIdx.x < off && (int)threadIdx.x + off < (int)blockDim.x)
+        lm_merge(sm[threadIdx.x], sm[threadIdx.x + off]);
       __syncthreads();
     }
     if (threadIdx.x == 0) {
@@ -333,15 +345,31 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
   __syncthreads();
   if (!last) return;
   __threadfence();
-  if ((int)threadIdx.x < a.R) {
-    LmState acc{-INFINITY, 0.f, 0x7fffffff};
-    for (int b = 0; b < (int)gridDim.x; b++) {
-      const float* src = e.lm_part + ((size_t)b * kMaxRows + threadIdx.x) * 3;
+  // last CTA: thread j of row c merges CTAs j, j + P, j + 2P, ... (P threads per row), then a
+  // pairwise tree per row; the order is fixed, so the result is reproducible.
+  const int P = max(1, (int)blockDim.x / a.R);
+  int span = 1;
+  while (span < P) span <<= 1;
+  const int c = threadIdx.x / P, j = threadIdx.x % P;
+  LmState acc{-INFINITY, 0.f, 0x7fffffff};
+  if (c < a.R) {
+#pragma unroll 4
+    for (int b = j; b < (int)gridDim.x; b += P) {
+      const float* src = e.lm_part + ((size_t)b * kMaxRows + c) * 3;
       LmState o{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))};
       lm_merge(acc, o);
     }
-    e.tok_out[threadIdx.x] = acc.i;
-    if (e.conf_out) e.conf_out[threadIdx.x] = 1.0f / acc.s;
+  }
+  __syncthreads();
+  sm_lm[threadIdx.x] = acc;
+  __syncthreads();
+  for (int off = span / 2; off > 0; off >>= 1) {
+    if (c < a.R && j < off && j + off < P) lm_merge(sm_lm[threadIdx.x], sm_lm[threadIdx.x + off]);
+    __syncthreads();
+  }
+  if (c < a.R && j == 0) {
+    e.tok_out[c] = sm_lm[threadIdx.x].i;
+    if (e.conf_out) e.conf_out[c] = 1.0f / sm_lm[threadIdx.x].s;
   }
   if (threadIdx.x == 0) *e.lm_ticket = 0;
 }
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   constexpr int GS = FMT == FMT_Q4 ? kQ4GroupsPerStage : kBf16GroupsPerStage;
   constexpr int GB = FMT == FMT_Q4 ? kQ4GroupBytes : kBf16GroupBytes;
   constexpr int RP = NT * 8;
+  constexpr int NT4 = NT * 4;
   extern __shared__ __align__(1024) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 
@@ -362,15 +391,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   const int gbeg = slice * a.gps, gend = min(a.groups, gbeg + a.gps), ng = gend - gbeg;
   const int sbeg = (int)((long long)cis * a.n_strips / a.ctas_per_slice);
   const int send = (int)((long long)(cis + 1) * a.n_strips / a.ctas_per_slice);
+  const int n_cta = send - sbeg;                 // strips of this CTA; every warp works on each
   const int xstride = a.gps * 128 + 16;
+  // this warp's share of the slice's 64-input groups (the same share of every strip)
+  const int wg0 = gbeg + (int)((long long)warp * ng / kWarps);
+  const int wg1 = gbeg + (int)((long long)(warp + 1) * ng / kWarps);
 
   uint8_t* ring = sm;
   uint8_t* xs = sm + kWarps * kStages * kStageBytes;
   float* xsum = reinterpret_cast<float*>(xs + RP * xstride);
   float* srow = xsum + (FMT == FMT_Q4 ? RP * a.gps : 0);
   LmState* sm_lm = reinterpret_cast<LmState*>(srow + kMaxRows);
+  float* red = reinterpret_cast<float*>(sm_lm + (EPI == EPI_LMHEAD ? kWarps * kMaxRows : 0));
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(sm_lm + (EPI == EPI_LMHEAD ? kWarps * kMaxRows : 0)) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(red + 2 * kWarps * 32 * NT4) + 15) & ~uintptr_t(15));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 1 + kWarps * kStages; i++) mbar_init(smem_u32(&bars[i]), 1);
@@ -378,25 +412,42 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   }
   __syncthreads();
 
-  // this warp's strips: sbeg + warp, sbeg + warp + kWarps, ...
-  const int first = sbeg + warp;
-  const int n_my = first < send ? (send - 1 - first) / kWarps + 1 : 0;
-  const int sps = (ng + GS - 1) / GS;  // stages per strip
-  const int n_q = n_my * sps;
+  // Work of this warp: full rounds first (strip sbeg + r*kWarps + warp, all groups of the slice,
+  // no synchronisation), then the n_cta % kWarps leftover strips shared by all warps (this
+  // warp's groups [wg0, wg1) of each), summed through shared memory.
+  const int rounds = n_cta / kWarps, n_left = n_cta % kWarps;
+  const int sps_full = (ng + GS - 1) / GS;
+  const int sps_part = (wg1 - wg0 + GS - 1) / GS;   // may be 0
+  const int n_qa = rounds * sps_full;
+  const int n_q = n_qa + n_left * sps_part;
+  auto stage_of = [&](int q, int& strip_local, int& g0, int& gn) {
+    if (q < n_qa) {
+      const int si = q / sps_full, st = q % sps_full;
+      strip_local = sbeg + si * kWarps + warp;
+      g0 = gbeg + st * GS;
+      gn = min(GS, gend - g0);
+    } else {
+      const int li = (q - n_qa) / sps_part, st = (q - n_qa) % sps_part;
+      strip_local = sbeg + rounds * kWarps + li;
+      g0 = wg0 + st * GS;
+      gn = min(GS, wg1 - g0);
+    }
+  };
   int issued = 0;
   auto issue = [&](int q) {
-    const int si = q / sps, st = q % sps;
-    const int strip = a.strip0 + first + si * kWarps;
-    const int g0 = gbeg + st * GS, gn = min(GS, gend - g0);
-    const uint8_t* src = a.w + ((size_t)strip * a.groups + g0) * GB;
+    int sl, g0, gn;
+    stage_of(q, sl, g0, gn);
+    const uint8_t* src = a.w + ((size_t)(a.strip0 + sl) * a.groups + g0) * GB;
     const int slot = warp * kStages + q % kStages;
     const uint32_t bar = smem_u32(&bars[1 + slot]);
     mbar_arrive_expect_tx(bar, gn * GB);
     bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);
   };
   if (lane == 0)
-    for (int q = 0; q < min(kStages, n_q); q++) issue(q);
+    for (int q = 0; q < min(kStages, n_q); q++) issue(q);   // weights never change: no wait needed
   issued = min(kStages, n_q);
+  pdl_launch_dependents();
+  pdl_wait();   // from here on, everything earlier kernels wrote is visible
 
   // activation slice -> shared (bulk copies), pad rows zeroed
   const int k0 = gbeg * 64, kbytes = ng * 128;
@@ -435,7 +486,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         const float2 f = __half22float2(p[j]);
         s += f.x + f.y;
       }
-      xsum[r * a.gps + gl] = s;
+      xsum[gl * RP + r] = s;
     }
   }
   __syncthreads();
@@ -447,17 +498,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
 
   int consumed = 0;
-  for (int si = 0; ok && si < n_my; si++) {
-    const int strip_local = first + si * kWarps;
-    const int strip = a.strip0 + strip_local;
-    float y[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-
-    for (int st = 0; st < sps; st++) {
-      const int q = si * sps + st;
+  // consume stages [q0, q0 + n) into y
+  auto consume = [&](int q0, int n, float (&y)[NT][4]) {
+    for (int q = q0; ok && q < q0 + n; q++) {
       const int slot = warp * kStages + q % kStages;
       bool w_ok = mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, a.err, kErrTimeoutGemv);
       w_ok = __all_sync(0xffffffffu, w_ok);
@@ -466,9 +509,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         break;
       }
       consumed = q + 1;
+      int sl_unused, g0, gn;
+      stage_of(q, sl_unused, g0, gn);
       const uint8_t* stg = ring + (size_t)slot * kStageBytes;
-      const int g0 = gbeg + st * GS, gn = min(GS, gend - g0);
-      for (int gi = 0; gi < gn; gi++) {
+#pragma unroll
+      for (int gi = 0; gi < GS; gi++) {
+        if (gi >= gn) break;
         const int gl = g0 - gbeg + gi;
         if constexpr (FMT == FMT_Q4) {
           const uint8_t* gp = stg + gi * kQ4GroupBytes;
@@ -477,32 +523,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
           const uint32_t sb1 = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g + 8));
           const float s0 = __uint_as_float(sb0 << 16), s1 = __uint_as_float(sb1 << 16);
           const float b0 = fmaf(-128.f, s0, __uint_as_float(sb0 & 0xFFFF0000u));
-          const float b1 = fmaf(-128.f, s1, __uint_as_float(sb1 & 0xFFFF0000u));
+          const float b1 = fmaf(-64.f, s1, __uint_as_float(sb1 & 0xFFFF0000u));
+          const float s1q = s1 * 0.0625f;
           const uint32_t u[4] = {A.x, A.y, A.z, A.w};
           uint32_t af[4][4];
 #pragma unroll
           for (int j = 0; j < 4; j++) {
-            af[j][0] = nib2_to_f16x2_plus128(u[j] << 3);
-            af[j][1] = nib2_to_f16x2_plus128(u[j] >> 1);
-            af[j][2] = nib2_to_f16x2_plus128(u[j] >> 5);
-            af[j][3] = nib2_to_f16x2_plus128(u[j] >> 9);
+            af[j][0] = nib128_to_f16x2(u[j] << 3);
+            af[j][1] = nib_hi_to_f16x2(u[j]);
+            af[j][2] = nib128_to_f16x2(u[j] >> 5);
+            af[j][3] = nib_hi_to_f16x2(u[j] >> 8);
           }
 #pragma unroll
           for (int nt = 0; nt < NT; nt++) {
             const uint8_t* xr = xs + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
             const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
             const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16(acc, af[0][0], af[0][1], af[0][2], af[0][3], x01.x, x01.y);
-            mma_f16(acc, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
-            mma_f16(acc, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
-            mma_f16(acc, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
-            const float xa = xsum[(nt * 8 + 2 * t) * a.gps + gl];
-            const float xb = xsum[(nt * 8 + 2 * t + 1) * a.gps + gl];
-            y[nt][0] = fmaf(s0, acc[0], fmaf(b0, xa, y[nt][0]));
-            y[nt][1] = fmaf(s0, acc[1], fmaf(b0, xb, y[nt][1]));
-            y[nt][2] = fmaf(s1, acc[2], fmaf(b1, xa, y[nt][2]));
-            y[nt][3] = fmaf(s1, acc[3], fmaf(b1, xb, y[nt][3]));
+            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16(acc0, af[0][0], af[0][1], af[0][2], af[0][3], x01.x, x01.y);
+            mma_f16(acc1, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
+            mma_f16(acc0, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
+            mma_f16(acc1, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
+            const float2 xab = *reinterpret_cast<const float2*>(xsum + gl * RP + nt * 8 + 2 * t);
+            y[nt][0] = fmaf(s0, acc0[0] + acc1[0], fmaf(b0, xab.x, y[nt][0]));
+            y[nt][1] = fmaf(s0, acc0[1] + acc1[1], fmaf(b0, xab.y, y[nt][1]));
+            y[nt][2] = fmaf(s1q, acc0[2] + acc1[2], fmaf(b1, xab.x, y[nt][2]));
+            y[nt][3] = fmaf(s1q, acc0[3] + acc1[3], fmaf(b1, xab.y, y[nt][3]));
           }
         } else {
           const uint8_t* gp = stg + gi * kBf16GroupBytes;
@@ -527,49 +573,58 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       if (lane == 0 && q + kStages < n_q) issue(q + kStages);
       if (q + kStages < n_q) issued = q + kStages + 1;
     }
-    if (!ok) break;
-
-    bool have = true;
+  };
+  // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
+  auto finish = [&](int strip_local, float (&y)[NT][4]) {
     if (a.n_slices > 1) {
-      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * (NT * 4);
+      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * NT4;
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
         *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
-      __threadfence();
-      __syncwarp();
-      int prev = 0;
-      if (lane == 0) prev = atomicAdd(&a.tickets[strip_local], 1);
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev != a.n_slices - 1) {
-        have = false;
-      } else {
-        __threadfence();
-        float tot[NT][4];
+    } else {
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
+    }
+  };
+
+  for (int r = 0; r < rounds && ok; r++) {   // whole strips, one per warp
+    float y[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
+    for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-          for (int j = 0; j < 4; j++) tot[nt][j] = 0.f;
-        for (int s2 = 0; s2 < a.n_slices; s2++) {
-          const float* src = a.partials + (((size_t)strip_local * a.n_slices + s2) * 32 + lane) * (NT * 4);
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+    consume(r * sps_full, sps_full, y);
+    if (ok) finish(sbeg + r * kWarps + warp, y);
+  }
+  ok = __syncthreads_and(ok);
+  for (int li = 0; li < n_left && ok; li++) {   // leftover strips, K shared by all warps
+    float y[NT][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; nt++) {
-            float4 v;
-            if (s2 == slice) v = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
-            else v = __ldcg(reinterpret_cast<const float4*>(src + nt * 4));
-            tot[nt][0] += v.x;
-            tot[nt][1] += v.y;
-            tot[nt][2] += v.z;
-            tot[nt][3] += v.w;
-          }
-        }
+    for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+    consume(n_qa + li * sps_part, sps_part, y);
+    float* mine = red + ((size_t)((li & 1) * kWarps + warp) * 32 + lane) * NT4;
 #pragma unroll
-          for (int j = 0; j < 4; j++) y[nt][j] = tot[nt][j];
-        if (lane == 0) a.tickets[strip_local] = 0;
+    for (int nt = 0; nt < NT; nt++)
+      *reinterpret_cast<float4*>(mine + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+    ok = __syncthreads_and(ok);
+    if (!ok || warp != li) continue;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+    for (int w = 0; w < kWarps; w++) {
+      const float* src = red + ((size_t)((li & 1) * kWarps + w) * 32 + lane) * NT4;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) {
+        const float4 v = *reinterpret_cast<const float4*>(src + nt * 4);
+        y[nt][0] += v.x;
+        y[nt][1] += v.y;
+        y[nt][2] += v.z;
+        y[nt][3] += v.w;
       }
     }
-    if (have) strip_epilogue<EPI, NT, XT>(a, strip, y, srow, lm);
+    finish(sbeg + rounds * kWarps + li, y);
   }
 
   if (!ok && lane == 0) {
@@ -578,6 +633,50 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int q = consumed; q < issued; q++) {
       const int slot = warp * kStages + q % kStages;
       mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, nullptr, 0);
+    }
+  }
+
+  if (ok && a.n_slices > 1) {
+    // tickets of the strips this warp reduced; the last slice to arrive sums all slices in
+    // slice order and runs the epilogue
+    __threadfence();
+    __syncwarp();
+    for (int si = warp; si < n_cta; si += kWarps) {   // round strips of this warp, then leftover li == warp
+      const int strip_local = sbeg + si;
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.tickets[strip_local], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev != a.n_slices - 1) continue;
+      __threadfence();
+      float y[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+      for (int s0 = 0; s0 < a.n_slices; s0 += 4) {
+        float4 v[4][NT];   // four slices' loads in flight, then summed in slice order
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const float* src = a.partials + (((size_t)strip_local * a.n_slices + s0 + q) * 32 + lane) * NT4;
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++)
+            v[q][nt] = s0 + q < a.n_slices ? __ldcg(reinterpret_cast<const float4*>(src + nt * 4))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (s0 + q >= a.n_slices) break;
+#pragma unroll
+          for (int nt = 0; nt < NT; nt++) {
+            y[nt][0] += v[q][nt].x;
+            y[nt][1] += v[q][nt].y;
+            y[nt][2] += v[q][nt].z;
+            y[nt][3] += v[q][nt].w;
+          }
+        }
+      }
+      if (lane == 0) a.tickets[strip_local] = 0;
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
     }
   }
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
@@ -642,9 +741,13 @@ cudaError_t launch_gemv_fmt_nt(int epi, const GemvArgs& a, int grid, size_t smem
       gemv_f32_kernel<NT, E><<<grid, kF32Warps * 32, 0, s>>>(a);                                 \
     } else {                                                                                     \
       auto k = gemv_tc_kernel<FMT, NT, E>;                                                       \
-      cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-      if (err != cudaSuccess) return err;                                                        \
-      k<<<grid, kGemvThreads, smem, s>>>(a);                                                     \
+      static int smem_set = 0;                                                                   \
+      if ((int)smem > smem_set) {                                                                \
+        cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        if (err != cudaSuccess) return err;                                                      \
+        smem_set = (int)smem;                                                                    \
+      }                                                                                          \
+      return launch_pdl(k, dim3(grid), dim3(kGemvThreads), smem, s, a);                          \
     }                                                                                            \
     return cudaGetLastError();                                                                   \
   }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dflash.h"
 
 namespace dfl {
@@ -15,15 +17,26 @@ namespace dfl {
 //   q4   : 576 B = 512 B of nibbles in mma.sync A-fragment order (16 B per lane) + 16 x (scale, bias)
 //   bf16 : 2048 B = 4 k16 steps x 32 lanes x 16 B, A-fragment order, values stored as f16
 //   f32  : row-major float rows (CUDA-core path), strips of 16 consecutive logical rows
-constexpr int kWarps = 8;                 // consumer warps per tensor-core GEMV CTA
-constexpr int kStages = 4;                // ring depth per warp (bulk copies in flight)
+#ifndef DFL_GEMV_WARPS
+#define DFL_GEMV_WARPS 12
+#endif
+#ifndef DFL_GEMV_STAGES
+#define DFL_GEMV_STAGES 3
+#endif
+#ifndef DFL_Q4_GROUPS_PER_STAGE
+#define DFL_Q4_GROUPS_PER_STAGE 4
+#endif
+constexpr int kWarps = DFL_GEMV_WARPS;    // consumer warps per tensor-core GEMV CTA
+constexpr int kStages = DFL_GEMV_STAGES;  // ring depth per warp (bulk copies in flight)
 constexpr int kQ4GroupBytes = 576;
 constexpr int kBf16GroupBytes = 2048;
-constexpr int kQ4GroupsPerStage = 4;      // 2304 B per stage
-constexpr int kBf16GroupsPerStage = 1;    // 2048 B per stage
-constexpr int kStageBytes = 2304;         // max over formats
+constexpr int kQ4GroupsPerStage = DFL_Q4_GROUPS_PER_STAGE;
+constexpr int kBf16GroupsPerStage = (kQ4GroupsPerStage * kQ4GroupBytes) / kBf16GroupBytes > 0
+                                        ? (kQ4GroupsPerStage * kQ4GroupBytes) / kBf16GroupBytes : 1;
+constexpr int kStageBytes = kQ4GroupsPerStage * kQ4GroupBytes > kBf16GroupsPerStage * kBf16GroupBytes
+                                ? kQ4GroupsPerStage * kQ4GroupBytes : kBf16GroupsPerStage * kBf16GroupBytes;
 constexpr int kMaxRows = 32;              // activation rows per launch (4 n-tiles of 8)
-constexpr int kXBudget = 120 * 1024;      // shared bytes for the staged activation slice
+constexpr int kXBudget = 112 * 1024;      // shared bytes for the staged activation slice
 constexpr int kMaxCtxChunk = 32;          // context rows per projection chunk
 constexpr int kGemvThreads = kWarps * 32;
 constexpr int kF32Warps = 8;
@@ -109,6 +122,8 @@ struct RepackArgs {
   uint8_t* dst;
 };
 
+constexpr int kBlockCols = 1024;           // block-init columns per CTA (one ssq part each)
+
 struct BlockArgs {
   int n_req, gamma, d, H, vocab, fmt, act_f32;
   const int32_t* anchor;
@@ -118,6 +133,28 @@ struct BlockArgs {
   float* h; void* xn; float* ssq; int ssq_ld;
   void* emb_out;              // gather mode: [n_req][H] activation rows
 };
+
+// Launch with programmatic stream serialization: the kernel may start while the previous kernel
+// of the stream drains; it must call pdl_wait() before reading anything earlier kernels wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+#ifdef DFL_NO_PDL
+  cfg.numAttrs = 0;
+#else
+  cfg.numAttrs = 1;
+#endif
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s);

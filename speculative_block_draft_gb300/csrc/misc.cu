@@ -96,14 +96,20 @@ __global__ void repack_kernel(const __grid_constant__ RepackArgs a) {
   }
 }
 
+// grid (column chunks of kBlockCols, block rows): row 0 of a request is its anchor's embedding
+// (or tok_proj of it) plus block_pos[0]; row k >= 1 is mask_emb[k-1] + block_pos[k]. Writes the
+// residual h, the next input h * attn_norm_0 and one sum-of-squares part per chunk.
 template <typename XT>
 __global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__ BlockArgs a) {
-  const int r = blockIdx.x, b = r / a.gamma, k = r % a.gamma;
+  const int r = blockIdx.y, chunk = blockIdx.x, b = r / a.gamma, k = r % a.gamma;
   __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
   int tok = a.anchor[b];
   tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);  // clamped: no read outside the table
   float ss = 0.f;
-  for (int j = threadIdx.x; j < a.d; j += blockDim.x) {
+  const int j0 = chunk * kBlockCols, j1 = min(a.d, j0 + kBlockCols);
+  for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
     float v;
     if (k == 0) {
       const float e = a.tokrow ? a.tokrow[(size_t)b * a.d + j]
@@ -122,13 +128,15 @@ __global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     float s = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); w++) s += red[w];
-    a.ssq[(size_t)r * a.ssq_ld] = s;
+    a.ssq[(size_t)r * a.ssq_ld + chunk] = s;
   }
 }
 
 template <typename XT>
 __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant__ BlockArgs a) {
   const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   int tok = a.anchor[b];
   tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);
   for (int j = threadIdx.x; j < a.H; j += blockDim.x)
@@ -140,6 +148,8 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant
 __global__ void accept_kernel(int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
                               int32_t* next_anchor) {
   const int b = blockIdx.x, lane = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   const bool miss = lane < n && draft[(size_t)b * n + lane] != target[(size_t)b * (n + 1) + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
   const int acc = mask ? __ffs(mask) - 1 : n;
@@ -157,21 +167,19 @@ cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s) {
-  if (a.act_f32) block_init_kernel<float><<<a.n_req * a.gamma, 256, 0, s>>>(a);
-  else block_init_kernel<__half><<<a.n_req * a.gamma, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  const dim3 grid((a.d + kBlockCols - 1) / kBlockCols, a.n_req * a.gamma);
+  if (a.act_f32) return launch_pdl(block_init_kernel<float>, grid, dim3(256), 0, s, a);
+  return launch_pdl(block_init_kernel<__half>, grid, dim3(256), 0, s, a);
 }
 
 cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
-  if (a.act_f32) embed_gather_kernel<float><<<a.n_req, 256, 0, s>>>(a);
-  else embed_gather_kernel<__half><<<a.n_req, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.act_f32) return launch_pdl(embed_gather_kernel<float>, dim3(a.n_req), dim3(256), 0, s, a);
+  return launch_pdl(embed_gather_kernel<__half>, dim3(a.n_req), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
                           int32_t* next_anchor, cudaStream_t s) {
-  accept_kernel<<<n_req, 32, 0, s>>>(n, draft, target, accept_len, next_anchor);
-  return cudaGetLastError();
+  return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, target, accept_len, next_anchor);
 }
 
 }  // namespace dfl

@@ -46,6 +46,7 @@ def run(cfg, rounds=3, jitter=0.1, max_batch=None, ctx_capacity=None, lengths=No
         pair.round(r, report)
     assert pair.gpu.check() == 0
     pair.gpu.close()
+    print(f"\n[{cfg.name}] {report}")
     return report
 
 
