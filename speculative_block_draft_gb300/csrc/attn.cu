@@ -12,7 +12,7 @@
 //  * The last split also takes the 16-row block tile (K_d, V_d of this block, not cached).
 //  * S = Q K^T and O += P V run on mma.sync m16n8k16 (f16 in, fp32 accumulate) with an online
 //    softmax in fp32 (base-2 exponent, scores pre-scaled by log2(e)/sqrt(hd)).
-//  * Each split writes (O, m, l); the last split to arrive (atomic ticket, no waiting) merges them
+//  * Each split writes (O, m, l); a second, wide kernel (one CTA per query row) merges the splits
 //    in split order and writes the f16 attention output.
 // CUDA-core path (fp32 cache): one warp per (query head, block row), online softmax over keys.
 #include <cuda_fp16.h>
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     return;
   }
 
-  // split partials, then the last split of this (request, kv head) merges them
+  // split partials (unnormalised O, running max m and sum l, base 2); attn_merge_kernel combines them
   const int pair = b * a.hkv + kvh;
   const size_t pidx = (size_t)pair * a.n_splits + split;
   if (active) {
@@ -295,60 +295,41 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
 #pragma unroll
       for (int nd = 0; nd < HD / 8; nd++)
         *reinterpret_cast<float2*>(po + nd * 8 + 2 * t) = make_float2(O[nd][2 * h], O[nd][2 * h + 1]);
-      if (t == 0) {
-        a.part_ml[(pidx * 64 + i) * 2 + 0] = m_run[h];
-        a.part_ml[(pidx * 64 + i) * 2 + 1] = l_run[h];
-      }
+      if (t == 0) *reinterpret_cast<float2*>(&a.part_ml[(pidx * 64 + i) * 2]) = make_float2(m_run[h], l_run[h]);
     }
   }
-  __threadfence();
-  __syncthreads();
-  __shared__ int last;
-  if (threadIdx.x == 0) last = atomicAdd(&a.tickets[pair], 1) == a.n_splits - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // merge: per query row, the weight of each split (computed once), then O row-wise
-  float* wgt = reinterpret_cast<float*>(stage_s);   // [2][64 splits][64 rows] (the K/V stages are free now)
+}
+
+// Combine the key splits of one query row: grid (request * kv head, query row), one float4 of
+// head_dim per thread. Split weights exp2(m_s - max) are recomputed by every thread (broadcast
+// loads), then O = sum_s w_s O_s / sum_s w_s l_s in split order.
+template <int HD>
+__global__ void __launch_bounds__(HD / 4) attn_merge_kernel(const __grid_constant__ AttnArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int pair = blockIdx.x, i = blockIdx.y, c4 = threadIdx.x;
+  const int b = pair / a.hkv, kvh = pair % a.hkv, grp = a.hq / a.hkv;
   const size_t pbase = (size_t)pair * a.n_splits;
-  if ((int)threadIdx.x < M) {
-    const int i = threadIdx.x;
-    float mx = -INFINITY;
+  float mx = -INFINITY;
 #pragma unroll 8
-    for (int s2 = 0; s2 < a.n_splits; s2++) {   // stage (m, l) of every split in shared memory
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
-      wgt[s2 * 64 + i] = ml.x;
-      wgt[(64 + s2) * 64 + i] = ml.y;
-      mx = fmaxf(mx, ml.x);
-    }
-    float L = 0.f;
-    for (int s2 = 0; s2 < a.n_splits; s2++) {
-      const float ms = wgt[s2 * 64 + i];
-      const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-      wgt[s2 * 64 + i] = w;
-      L += w * wgt[(64 + s2) * 64 + i];
-    }
-    const float inv = 1.0f / L;
-    for (int s2 = 0; s2 < a.n_splits; s2++) wgt[s2 * 64 + i] *= inv;
+  for (int s2 = 0; s2 < a.n_splits; s2++) mx = fmaxf(mx, __ldcg(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int s2 = 0; s2 < a.n_splits; s2++) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + ((pbase + s2) * 64 + i) * HD) + c4);
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
+    L = fmaf(w, ml.y, L);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < M * (HD / 4); idx += blockDim.x) {
-    const int i = idx / (HD / 4), c4 = idx % (HD / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s2 = 0; s2 < a.n_splits; s2++) {
-      const float w = wgt[s2 * 64 + i];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + ((pbase + s2) * 64 + i) * HD) + c4);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
-    __half* o = out + (size_t)(rq.row0 + k) * a.qd + head * HD + c4 * 4;
-    *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(acc.x, acc.y), pack_f16x2(acc.z, acc.w));
-  }
-  if (threadIdx.x == 0) a.tickets[pair] = 0;
+  const float inv = 1.0f / L;
+  const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
+  __half* o = static_cast<__half*>(a.out) + (size_t)(a.req[b].row0 + k) * a.qd + head * HD + c4 * 4;
+  *reinterpret_cast<uint2*>(o) = make_uint2(pack_f16x2(acc.x * inv, acc.y * inv), pack_f16x2(acc.z * inv, acc.w * inv));
 }
 
 // fp32 path: warp per (query head, block row)
@@ -441,6 +422,16 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUt
     default: return cudaErrorInvalidValue;
   }
 #undef DFL_ATTN
+}
+
+cudaError_t launch_attn_merge(const AttnArgs& a, cudaStream_t s) {
+  const dim3 grid(a.n_req * a.hkv, (a.hq / a.hkv) * a.gamma);
+  switch (a.hd) {
+    case 64: return launch_pdl(attn_merge_kernel<64>, grid, dim3(16), 0, s, a);
+    case 128: return launch_pdl(attn_merge_kernel<128>, grid, dim3(32), 0, s, a);
+    case 256: return launch_pdl(attn_merge_kernel<256>, grid, dim3(64), 0, s, a);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s) {

@@ -155,6 +155,17 @@ __device__ __forceinline__ __half from_f<__half>(float v) {
   return __float2half_rn(fminf(fmaxf(v, -kF16Max), kF16Max));
 }
 
+// Store an activation; for f16 with lo_off != 0 also store the rounding remainder v - f16(v) at
+// base[idx + lo_off], so that hi + lo carries v to about 22 bits.
+template <typename T>
+__device__ __forceinline__ void store_act_split(void* base, size_t idx, size_t lo_off, float v) {
+  const T hi = from_f<T>(v);
+  static_cast<T*>(base)[idx] = hi;
+  if constexpr (sizeof(T) == 2) {
+    if (lo_off) static_cast<T*>(base)[idx + lo_off] = from_f<T>(v - to_f<T>(hi));
+  }
+}
+
 // Element k of row n of a matrix in its caller-side storage format (used for gathers).
 __device__ __forceinline__ float load_weight(int fmt, const void* data, const uint16_t* scale,
                                              const uint16_t* bias, int n_in, int64_t n, int k) {

@@ -6,12 +6,11 @@ namespace dfl {
 cudaError_t launch_gemv_q4(int epi, int nt, const GemvArgs& a, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemv_bf16(int epi, int nt, const GemvArgs& a, int grid, size_t smem, cudaStream_t s);
 
-size_t gemv_smem_bytes(int fmt, int R, int gps, int k) {
-  (void)k;
+size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo) {
   if (fmt == FMT_F32) return 0;
   const int rp = R <= 8 ? 8 : (R <= 16 ? 16 : 32);
   size_t b = (size_t)kWarps * kStages * kStageBytes;   // weight rings
-  b += (size_t)rp * (gps * 128 + 16);                  // activation slice
+  b += (size_t)rp * (gps * 128 + 16) * (x_lo ? 2 : 1); // activation slice (and its f16 remainder)
   if (fmt == FMT_Q4) b += (size_t)rp * gps * 4;        // per-group activation sums
   b += kMaxRows * 4;                                   // row scales
   b += (size_t)kWarps * kMaxRows * sizeof(LmState);    // vocab reduction scratch
@@ -21,7 +20,7 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int k) {
 }
 
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s) {
-  const size_t smem = gemv_smem_bytes(fmt, a.R, a.gps, a.k);
+  const size_t smem = gemv_smem_bytes(fmt, a.R, a.gps, a.x_lo_off != 0);
   switch (fmt) {
     case FMT_Q4: return launch_gemv_q4(epi, nt, a, grid, smem, s);
     case FMT_BF16: return launch_gemv_bf16(epi, nt, a, grid, smem, s);

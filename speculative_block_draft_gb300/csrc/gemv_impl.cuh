@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace dfl {
@@ -223,12 +225,13 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             const size_t idx = (size_t)c * e.ldo + nr;
             const float hn = e.h[idx] + v;
             e.h[idx] = hn;
-            store_act<XT>(e.xnext, idx, e.wnext ? hn * e.wnext[nr] : hn);
+            store_act_split<XT>(e.xnext, idx, e.x_lo_off, e.wnext ? hn * e.wnext[nr] : hn);
             s0 += hn * hn;
           } else {
             const float cn = e.ctx_norm[nr];
             for (int i = 0; i < e.n_layers; i++)
-              store_act<XT>(e.xw, ((size_t)i * e.xw_rows + c) * e.ldo + nr, v * cn * e.attn_norms[(size_t)i * e.ldo + nr]);
+              store_act_split<XT>(e.xw, ((size_t)i * e.xw_rows + c) * e.ldo + nr, e.x_lo_off,
+                                  v * cn * e.attn_norms[(size_t)i * e.ldo + nr]);
             s0 += v * v;
             s1 += (v * cn) * (v * cn);
           }
@@ -397,9 +400,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   const int wg0 = gbeg + (int)((long long)warp * ng / kWarps);
   const int wg1 = gbeg + (int)((long long)(warp + 1) * ng / kWarps);
 
+  const bool has_lo = a.x_lo_off != 0;
   uint8_t* ring = sm;
   uint8_t* xs = sm + kWarps * kStages * kStageBytes;
-  float* xsum = reinterpret_cast<float*>(xs + RP * xstride);
+  uint8_t* xs_lo = xs + RP * xstride;   // f16 remainder rows (when the input carries them)
+  float* xsum = reinterpret_cast<float*>(xs_lo + (has_lo ? RP * xstride : 0));
   float* srow = xsum + (FMT == FMT_Q4 ? RP * a.gps : 0);
   LmState* sm_lm = reinterpret_cast<LmState*>(srow + kMaxRows);
   float* red = reinterpret_cast<float*>(sm_lm + (EPI == EPI_LMHEAD ? kWarps * kMaxRows : 0));
@@ -453,16 +458,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   const int k0 = gbeg * 64, kbytes = ng * 128;
   if (threadIdx.x == 0) {
     const uint32_t bar = smem_u32(&bars[0]);
-    mbar_arrive_expect_tx(bar, a.R * kbytes);
+    mbar_arrive_expect_tx(bar, a.R * kbytes * (has_lo ? 2 : 1));
     for (int r = 0; r < a.R; r++) {
       const int src = map_row(a.xmap, r);
-      bulk_g2s(smem_u32(xs + (size_t)r * xstride),
-               static_cast<const uint8_t*>(a.x) + ((size_t)src * a.ldx + k0) * 2, kbytes, bar);
+      const uint8_t* row = static_cast<const uint8_t*>(a.x) + ((size_t)src * a.ldx + k0) * 2;
+      bulk_g2s(smem_u32(xs + (size_t)r * xstride), row, kbytes, bar);
+      if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride), row + a.x_lo_off * 2, kbytes, bar);
     }
   }
   for (int i = threadIdx.x; i < (RP - a.R) * (kbytes / 16); i += blockDim.x) {
     const int r = a.R + i / (kbytes / 16), c = i % (kbytes / 16);
     *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
+    if (has_lo) *reinterpret_cast<uint4*>(xs_lo + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
   }
   compute_row_scales(a, srow, RP);
   bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
@@ -480,11 +487,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int i = threadIdx.x; i < RP * ng; i += blockDim.x) {
       const int r = i / ng, gl = i % ng;
       const __half2* p = reinterpret_cast<const __half2*>(xs + (size_t)r * xstride + gl * 128);
+      const __half2* pl = reinterpret_cast<const __half2*>(xs_lo + (size_t)r * xstride + gl * 128);
       float s = 0.f;
 #pragma unroll 8
       for (int j = 0; j < 32; j++) {
         const float2 f = __half22float2(p[j]);
         s += f.x + f.y;
+        if (has_lo) {
+          const float2 fl = __half22float2(pl[j]);
+          s += fl.x + fl.y;
+        }
       }
       xsum[gl * RP + r] = s;
     }
@@ -499,7 +511,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
 
   int consumed = 0;
   // consume stages [q0, q0 + n) into y
-  auto consume = [&](int q0, int n, float (&y)[NT][4]) {
+  auto consume = [&](auto lo_tag, int q0, int n, float (&y)[NT][4]) {
+    constexpr bool LO = decltype(lo_tag)::value;
     for (int q = q0; ok && q < q0 + n; q++) {
       const int slot = warp * kStages + q % kStages;
       bool w_ok = mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, a.err, kErrTimeoutGemv);
@@ -544,6 +557,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
             mma_f16(acc1, af[1][0], af[1][1], af[1][2], af[1][3], x01.z, x01.w);
             mma_f16(acc0, af[2][0], af[2][1], af[2][2], af[2][3], x23.x, x23.y);
             mma_f16(acc1, af[3][0], af[3][1], af[3][2], af[3][3], x23.z, x23.w);
+            if constexpr (LO) {   // the same exact weights against the activations' f16 remainder
+              const uint8_t* xl = xs_lo + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+              const uint4 l01 = *reinterpret_cast<const uint4*>(xl);
+              const uint4 l23 = *reinterpret_cast<const uint4*>(xl + 16);
+              mma_f16(acc0, af[0][0], af[0][1], af[0][2], af[0][3], l01.x, l01.y);
+              mma_f16(acc1, af[1][0], af[1][1], af[1][2], af[1][3], l01.z, l01.w);
+              mma_f16(acc0, af[2][0], af[2][1], af[2][2], af[2][3], l23.x, l23.y);
+              mma_f16(acc1, af[3][0], af[3][1], af[3][2], af[3][3], l23.z, l23.w);
+            }
             const float2 xab = *reinterpret_cast<const float2*>(xsum + gl * RP + nt * 8 + 2 * t);
             y[nt][0] = fmaf(s0, acc0[0] + acc1[0], fmaf(b0, xab.x, y[nt][0]));
             y[nt][1] = fmaf(s0, acc0[1] + acc1[1], fmaf(b0, xab.y, y[nt][1]));
@@ -564,6 +586,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
             mma_f16(y[nt], A[1].x, A[1].y, A[1].z, A[1].w, x01.z, x01.w);
             mma_f16(y[nt], A[2].x, A[2].y, A[2].z, A[2].w, x23.x, x23.y);
             mma_f16(y[nt], A[3].x, A[3].y, A[3].z, A[3].w, x23.z, x23.w);
+            if constexpr (LO) {
+              const uint8_t* xl = xs_lo + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+              const uint4 l01 = *reinterpret_cast<const uint4*>(xl);
+              const uint4 l23 = *reinterpret_cast<const uint4*>(xl + 16);
+              mma_f16(y[nt], A[0].x, A[0].y, A[0].z, A[0].w, l01.x, l01.y);
+              mma_f16(y[nt], A[1].x, A[1].y, A[1].z, A[1].w, l01.z, l01.w);
+              mma_f16(y[nt], A[2].x, A[2].y, A[2].z, A[2].w, l23.x, l23.y);
+              mma_f16(y[nt], A[3].x, A[3].y, A[3].z, A[3].w, l23.z, l23.w);
+            }
           }
         }
       }
@@ -592,7 +623,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
       for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    consume(r * sps_full, sps_full, y);
+    if (has_lo) consume(std::true_type{}, r * sps_full, sps_full, y);
+    else consume(std::false_type{}, r * sps_full, sps_full, y);
     if (ok) finish(sbeg + r * kWarps + warp, y);
   }
   ok = __syncthreads_and(ok);
@@ -602,7 +634,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
       for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    consume(n_qa + li * sps_part, sps_part, y);
+    if (has_lo) consume(std::true_type{}, n_qa + li * sps_part, sps_part, y);
+    else consume(std::false_type{}, n_qa + li * sps_part, sps_part, y);
     float* mine = red + ((size_t)((li & 1) * kWarps + warp) * 32 + lane) * NT4;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)

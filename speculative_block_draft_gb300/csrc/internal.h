@@ -60,6 +60,7 @@ struct EpiArgs {
   void* out; int ldo; int out_f32;
   // EPI_RESID: h[r][n] += y; xnext[r][n] = act(h[r][n] * wnext[n]); ssq_out[r*ssq_ld + strip]
   float* h; const float* wnext; void* xnext; float* ssq_out; int ssq_ld;
+  size_t x_lo_off;   // EPI_RESID / EPI_CTX: also write the f16 remainder this many elements on
   // EPI_CTX: x = y; xw[i][r][n] = act(x*ctx_norm*attn_norm_i); ssq_out[(r*ssq_ld+strip)*2+{0,1}]
   const float* ctx_norm; const float* attn_norms; int n_layers; void* xw; int xw_rows;
   // EPI_QKV
@@ -85,6 +86,7 @@ struct GemvArgs {
   int R;                   // activation rows (<= kMaxRows)
   const void* x; int ldx; RowMap xmap;
   int x_bf16;              // tensor-core path: x rows are bf16 (converted to f16 after staging)
+  long long x_lo_off;      // tensor-core path: f16 remainder rows at x + x_lo_off elements (0: none)
   int norm_mode; const float* ssq; int ssq_ld; int ssq_parts; float inv_dim; float eps;
   float* partials; int* tickets;
   unsigned* err;
@@ -131,6 +133,7 @@ struct BlockArgs {
   const float* tokrow;        // [n_req][d] tok_proj(E[anchor]) when d != H
   const float* mask_emb; const float* block_pos; const float* attn_norm0;
   float* h; void* xn; float* ssq; int ssq_ld;
+  size_t xn_lo_off;           // f16 remainder of xn at this element offset (0: none)
   void* emb_out;              // gather mode: [n_req][H] activation rows
 };
 
@@ -158,10 +161,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s);
-size_t gemv_smem_bytes(int fmt, int R, int gps, int k);
+size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t s);
 size_t attn_smem_bytes(int hd);
+cudaError_t launch_attn_merge(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s);

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__
       v = a.mask_emb[(size_t)(k - 1) * a.d + j] + a.block_pos[(size_t)k * a.d + j];
     }
     a.h[(size_t)r * a.d + j] = v;
-    static_cast<XT*>(a.xn)[(size_t)r * a.d + j] = from_f<XT>(v * a.attn_norm0[j]);
+    store_act_split<XT>(a.xn, (size_t)r * a.d + j, a.xn_lo_off, v * a.attn_norm0[j]);
     ss += v * v;
   }
   ss = warp_sum(ss);
