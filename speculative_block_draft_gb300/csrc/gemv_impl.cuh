@@ -425,32 +425,41 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   const int sps_part = (wg1 - wg0 + GS - 1) / GS;   // may be 0
   const int n_qa = rounds * sps_full;
   const int n_q = n_qa + n_left * sps_part;
-  auto stage_of = [&](int q, int& strip_local, int& g0, int& gn) {
-    if (q < n_qa) {
-      const int si = q / sps_full, st = q % sps_full;
-      strip_local = sbeg + si * kWarps + warp;
-      g0 = gbeg + st * GS;
-      gn = min(GS, gend - g0);
-    } else {
-      const int li = (q - n_qa) / sps_part, st = (q - n_qa) % sps_part;
-      strip_local = sbeg + rounds * kWarps + li;
-      g0 = wg0 + st * GS;
-      gn = min(GS, wg1 - g0);
-    }
-  };
+  // issue cursor: stages are issued strictly in order, so (phase, strip, stage) just advance
+  int c_phase = rounds > 0 ? 0 : 1, c_si = 0, c_st = 0;
   int issued = 0;
-  auto issue = [&](int q) {
-    int sl, g0, gn;
-    stage_of(q, sl, g0, gn);
-    const uint8_t* src = a.w + ((size_t)(a.strip0 + sl) * a.groups + g0) * GB;
-    const int slot = warp * kStages + q % kStages;
-    const uint32_t bar = smem_u32(&bars[1 + slot]);
-    mbar_arrive_expect_tx(bar, gn * GB);
-    bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);
+  auto issue_next = [&]() {
+    int strip_local, g0, gn;
+    if (c_phase == 0) {
+      strip_local = sbeg + c_si * kWarps + warp;
+      g0 = gbeg + c_st * GS;
+      gn = min(GS, gend - g0);
+      if (++c_st == sps_full) {
+        c_st = 0;
+        if (++c_si == rounds) {
+          c_phase = 1;
+          c_si = 0;
+        }
+      }
+    } else {
+      strip_local = sbeg + rounds * kWarps + c_si;
+      g0 = wg0 + c_st * GS;
+      gn = min(GS, wg1 - g0);
+      if (++c_st == sps_part) {
+        c_st = 0;
+        c_si++;
+      }
+    }
+    if (lane == 0) {
+      const uint8_t* src = a.w + ((size_t)(a.strip0 + strip_local) * a.groups + g0) * GB;
+      const int slot = warp * kStages + issued % kStages;
+      const uint32_t bar = smem_u32(&bars[1 + slot]);
+      mbar_arrive_expect_tx(bar, gn * GB);
+      bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);
+    }
+    issued++;
   };
-  if (lane == 0)
-    for (int q = 0; q < min(kStages, n_q); q++) issue(q);   // weights never change: no wait needed
-  issued = min(kStages, n_q);
+  for (int q = 0; q < min(kStages, n_q); q++) issue_next();   // weights never change: no wait needed
   pdl_launch_dependents();
   pdl_wait();   // from here on, everything earlier kernels wrote is visible
 
@@ -511,7 +520,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
 
   int consumed = 0;
   // consume stages [q0, q0 + n) into y
-  auto consume = [&](auto lo_tag, int q0, int n, float (&y)[NT][4]) {
+  // consume stages [q0, q0 + n), which cover groups [gfirst, glast) of one strip, into y
+  auto consume = [&](auto lo_tag, int q0, int n, int gfirst, int glast, float (&y)[NT][4]) {
     constexpr bool LO = decltype(lo_tag)::value;
     for (int q = q0; ok && q < q0 + n; q++) {
       const int slot = warp * kStages + q % kStages;
@@ -522,8 +532,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         break;
       }
       consumed = q + 1;
-      int sl_unused, g0, gn;
-      stage_of(q, sl_unused, g0, gn);
+      const int g0 = gfirst + (q - q0) * GS, gn = min(GS, glast - g0);
       const uint8_t* stg = ring + (size_t)slot * kStageBytes;
 #pragma unroll
       for (int gi = 0; gi < GS; gi++) {
@@ -601,8 +610,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       // every lane is done reading this slot before the copy engine refills it
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0 && q + kStages < n_q) issue(q + kStages);
-      if (q + kStages < n_q) issued = q + kStages + 1;
+      if (q + kStages < n_q) issue_next();
     }
   };
   // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
@@ -623,8 +631,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
       for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    if (has_lo) consume(std::true_type{}, r * sps_full, sps_full, y);
-    else consume(std::false_type{}, r * sps_full, sps_full, y);
+    if (has_lo) consume(std::true_type{}, r * sps_full, sps_full, gbeg, gend, y);
+    else consume(std::false_type{}, r * sps_full, sps_full, gbeg, gend, y);
     if (ok) finish(sbeg + r * kWarps + warp, y);
   }
   ok = __syncthreads_and(ok);
@@ -634,8 +642,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
       for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    if (has_lo) consume(std::true_type{}, n_qa + li * sps_part, sps_part, y);
-    else consume(std::false_type{}, n_qa + li * sps_part, sps_part, y);
+    if (has_lo) consume(std::true_type{}, n_qa + li * sps_part, sps_part, wg0, wg1, y);
+    else consume(std::false_type{}, n_qa + li * sps_part, sps_part, wg0, wg1, y);
     float* mine = red + ((size_t)((li & 1) * kWarps + warp) * 32 + lane) * NT4;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
