@@ -450,9 +450,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         c_si++;
       }
     }
+    const uint8_t* src = a.w + ((size_t)(a.strip0 + strip_local) * a.groups + g0) * GB;
+    const int slot = warp * kStages + issued % kStages;
     if (lane == 0) {
-      const uint8_t* src = a.w + ((size_t)(a.strip0 + strip_local) * a.groups + g0) * GB;
-      const int slot = warp * kStages + issued % kStages;
       const uint32_t bar = smem_u32(&bars[1 + slot]);
       mbar_arrive_expect_tx(bar, gn * GB);
       bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);

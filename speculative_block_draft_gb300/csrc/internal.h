@@ -21,10 +21,10 @@ namespace dfl {
 #define DFL_GEMV_WARPS 12
 #endif
 #ifndef DFL_GEMV_STAGES
-#define DFL_GEMV_STAGES 3
+#define DFL_GEMV_STAGES 2
 #endif
 #ifndef DFL_Q4_GROUPS_PER_STAGE
-#define DFL_Q4_GROUPS_PER_STAGE 4
+#define DFL_Q4_GROUPS_PER_STAGE 8
 #endif
 constexpr int kWarps = DFL_GEMV_WARPS;    // consumer warps per tensor-core GEMV CTA
 constexpr int kStages = DFL_GEMV_STAGES;  // ring depth per warp (bulk copies in flight)
