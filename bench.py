@@ -277,6 +277,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--profile-ctx", type=int, default=0,
+                    help="prefill only this many context rows (for short profiler captures; not a bench value)")
     args = ap.parse_args()
     cfg = syn.CONFIGS[args.config]
     if args.impl == "reference":
@@ -303,6 +305,8 @@ def main():
                                                       cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + 8)))
     h, stream = sess.h, sess.stream
     lengths = syn.ctx_lengths(cfg)
+    if args.profile_ctx:
+        lengths = np.minimum(lengths, args.profile_ctx)
     width = cfg.n_taps * cfg.target_hidden
     for b in range(B):
         done = 0
@@ -426,7 +430,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": workload_config(cfg),
+        "config": {**workload_config(cfg), **({"profile_ctx": args.profile_ctx} if args.profile_ctx else {})},
         "round_hbm": {"algorithmic_bytes": rb["total"], "breakdown_mb": {k: round(v / 1e6, 1) for k, v in rb.items()},
                       "achieved_gbs": rb["total"] / (t_max / args.steps) / 1e9,
                       "peak_gbs": peaks["hbm_gbs"],

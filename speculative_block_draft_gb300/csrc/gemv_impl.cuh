@@ -3,12 +3,13 @@
 //
 // Tensor-core path (bf16 / 4-bit weights), one CTA per SM:
 //  * A CTA owns one K slice and a range of 16-row strips. It stages its activation slice
-//    X[R][slice] (bf16) into shared memory with 1-D bulk copies (TMA) once.
+//    X[R][slice] (f16, plus its f16 remainder where the input carries one) into shared memory
+//    with 1-D bulk copies (TMA) once.
 //  * Its warps stream weights through private rings of kStages shared-memory stages filled by
-//    cp.async.bulk. Strips are dealt out in whole rounds (one strip per warp, no
-//    synchronisation); the fewer-than-kWarps leftover strips are shared by all warps, each
-//    taking an equal share of the slice's 64-input groups, and summed through shared memory
-//    (double buffered, in warp order). Work is balanced to within one group.
+//    cp.async.bulk. The CTA's (strip, 64-input group) tiles are cut, in strip-major order, into
+//    one contiguous range per warp, so warps stream without synchronising and are balanced to
+//    within one tile; a strip cut between warps is summed once, after the stream, in warp
+//    order through shared memory.
 //  * 4-bit codes become f16 with one lop3 per register (plus a shift for three of four): the
 //    re-laid-out word of a lane holds rows g and g+8 in alternating nibbles, so row g decodes
 //    to 128 + q (magic 0x5800) and row g+8 to 1024 + 16 q (magic 0x6400, no shift). mma.sync
@@ -70,26 +71,36 @@ __device__ __forceinline__ void store_act(void* base, size_t idx, float v) {
   static_cast<XT*>(base)[idx] = from_f<XT>(v);
 }
 
-// Per-row RMSNorm scale from the producer's per-strip sum-of-squares partials.
+// Per-row RMSNorm scale from the producer's per-strip sum-of-squares partials (one warp per
+// row; eight loads per lane in flight at a time, summed in a fixed order).
 __device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* srow, int nrows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
+  const int two = a.norm_mode == NORM_CTX ? 2 : 1;
   for (int r = warp; r < nrows; r += nw) {
     float s = 1.0f;
     if (r < a.R && a.norm_mode != NORM_NONE) {
-      const int src = map_row(a.xmap, r);
-      if (a.norm_mode == NORM_ONE) {
-        float acc = 0.f;
-        for (int p = lane; p < a.ssq_parts; p += 32) acc += a.ssq[(size_t)src * a.ssq_ld + p];
-        acc = warp_sum(acc);
-        s = rsqrtf(acc * a.inv_dim + a.eps);
-      } else {
-        float sa = 0.f, sb = 0.f;
-        for (int p = lane; p < a.ssq_parts; p += 32) {
-          sa += a.ssq[((size_t)src * a.ssq_ld + p) * 2 + 0];
-          sb += a.ssq[((size_t)src * a.ssq_ld + p) * 2 + 1];
+      const float* base = a.ssq + (size_t)map_row(a.xmap, r) * a.ssq_ld * two;
+      float sa = 0.f, sb = 0.f;
+      for (int p0 = 0; p0 < a.ssq_parts; p0 += 8 * 32) {
+        float va[8], vb[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const int p = p0 + j * 32 + lane;
+          const bool in = p < a.ssq_parts;
+          va[j] = in ? __ldcg(base + (size_t)p * two) : 0.f;
+          vb[j] = in && two == 2 ? __ldcg(base + (size_t)p * 2 + 1) : 0.f;
         }
-        sa = warp_sum(sa);
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          sa += va[j];
+          sb += vb[j];
+        }
+      }
+      sa = warp_sum(sa);
+      if (a.norm_mode == NORM_ONE) {
+        s = rsqrtf(sa * a.inv_dim + a.eps);
+      } else {
         sb = warp_sum(sb);
         const float inv1 = rsqrtf(sa * a.inv_dim + a.eps);
         s = inv1 * rsqrtf(inv1 * inv1 * sb * a.inv_dim + a.eps);
@@ -394,11 +405,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   const int gbeg = slice * a.gps, gend = min(a.groups, gbeg + a.gps), ng = gend - gbeg;
   const int sbeg = (int)((long long)cis * a.n_strips / a.ctas_per_slice);
   const int send = (int)((long long)(cis + 1) * a.n_strips / a.ctas_per_slice);
-  const int n_cta = send - sbeg;                 // strips of this CTA; every warp works on each
+  const int n_cta = send - sbeg;                 // strips of this CTA
   const int xstride = a.gps * 128 + 16;
-  // this warp's share of the slice's 64-input groups (the same share of every strip)
-  const int wg0 = gbeg + (int)((long long)warp * ng / kWarps);
-  const int wg1 = gbeg + (int)((long long)(warp + 1) * ng / kWarps);
 
   const bool has_lo = a.x_lo_off != 0;
   uint8_t* ring = sm;
@@ -417,40 +425,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   }
   __syncthreads();
 
-  // Work of this warp: full rounds first (strip sbeg + r*kWarps + warp, all groups of the slice,
-  // no synchronisation), then the n_cta % kWarps leftover strips shared by all warps (this
-  // warp's groups [wg0, wg1) of each), summed through shared memory.
-  const int rounds = n_cta / kWarps, n_left = n_cta % kWarps;
-  const int sps_full = (ng + GS - 1) / GS;
-  const int sps_part = (wg1 - wg0 + GS - 1) / GS;   // may be 0
-  const int n_qa = rounds * sps_full;
-  const int n_q = n_qa + n_left * sps_part;
-  // issue cursor: stages are issued strictly in order, so (phase, strip, stage) just advance
-  int c_phase = rounds > 0 ? 0 : 1, c_si = 0, c_st = 0;
+  // Work of this warp: one contiguous range [t0, t1) of the CTA's n_cta x ng (strip, group)
+  // tiles in strip-major order, so every warp streams the same number of tiles with no
+  // synchronisation. A range splits at strip boundaries into segments; a segment covering a
+  // whole strip is finished at once, a partial one (at most the first and the last of a range)
+  // is parked in shared memory and summed after the stream, in warp order, by the warp that
+  // owns the strip's last tile.
+  const long long T = (long long)n_cta * ng;
+  const long long t0 = T * warp / kWarps, t1 = T * (warp + 1) / kWarps;
+  const int first_strip = (int)(t0 / ng);
+  // issue cursor: stages never cross a strip boundary
+  long long i_tile = t0;
+  int i_strip = first_strip, i_goff = (int)(t0 % ng);
   int issued = 0;
   auto issue_next = [&]() {
-    int strip_local, g0, gn;
-    if (c_phase == 0) {
-      strip_local = sbeg + c_si * kWarps + warp;
-      g0 = gbeg + c_st * GS;
-      gn = min(GS, gend - g0);
-      if (++c_st == sps_full) {
-        c_st = 0;
-        if (++c_si == rounds) {
-          c_phase = 1;
-          c_si = 0;
-        }
-      }
-    } else {
-      strip_local = sbeg + rounds * kWarps + c_si;
-      g0 = wg0 + c_st * GS;
-      gn = min(GS, wg1 - g0);
-      if (++c_st == sps_part) {
-        c_st = 0;
-        c_si++;
-      }
-    }
-    const uint8_t* src = a.w + ((size_t)(a.strip0 + strip_local) * a.groups + g0) * GB;
+    const int gn = (int)min((long long)min(GS, ng - i_goff), t1 - i_tile);
+    const uint8_t* src = a.w + ((size_t)(a.strip0 + sbeg + i_strip) * a.groups + gbeg + i_goff) * GB;
     const int slot = warp * kStages + issued % kStages;
     if (lane == 0) {
       const uint32_t bar = smem_u32(&bars[1 + slot]);
@@ -458,56 +448,78 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       bulk_g2s(smem_u32(ring + (size_t)slot * kStageBytes), src, gn * GB, bar);
     }
     issued++;
+    i_tile += gn;
+    i_goff += gn;
+    if (i_goff == ng) {
+      i_goff = 0;
+      i_strip++;
+    }
   };
-  for (int q = 0; q < min(kStages, n_q); q++) issue_next();   // weights never change: no wait needed
+  for (int q = 0; q < kStages && i_tile < t1; q++) issue_next();   // weights never change: no wait needed
   pdl_launch_dependents();
   pdl_wait();   // from here on, everything earlier kernels wrote is visible
 
-  // activation slice -> shared (bulk copies), pad rows zeroed
+  // activation slice -> shared (bulk copies of at most 2 KB, started at a different piece in
+  // every CTA so the CTAs do not all read the same L2 lines at once), pad rows zeroed
   const int k0 = gbeg * 64, kbytes = ng * 128;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     const uint32_t bar = smem_u32(&bars[0]);
-    mbar_arrive_expect_tx(bar, a.R * kbytes * (has_lo ? 2 : 1));
-    for (int r = 0; r < a.R; r++) {
-      const int src = map_row(a.xmap, r);
-      const uint8_t* row = static_cast<const uint8_t*>(a.x) + ((size_t)src * a.ldx + k0) * 2;
-      bulk_g2s(smem_u32(xs + (size_t)r * xstride), row, kbytes, bar);
-      if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride), row + a.x_lo_off * 2, kbytes, bar);
+    if (lane == 0) mbar_arrive_expect_tx(bar, a.R * kbytes * (has_lo ? 2 : 1));
+    __syncwarp();
+    const int ppr = (kbytes + 2047) / 2048, n_pc = a.R * ppr;
+    const int rot = blockIdx.x % n_pc;
+    for (int i = lane; i < n_pc; i += 32) {
+      const int j = i + rot < n_pc ? i + rot : i + rot - n_pc;
+      const int r = j / ppr, off = (j - r * ppr) * 2048, len = min(2048, kbytes - off);
+      const uint8_t* row = static_cast<const uint8_t*>(a.x) + ((size_t)map_row(a.xmap, r) * a.ldx + k0) * 2 + off;
+      bulk_g2s(smem_u32(xs + (size_t)r * xstride + off), row, len, bar);
+      if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride + off), row + a.x_lo_off * 2, len, bar);
     }
   }
-  for (int i = threadIdx.x; i < (RP - a.R) * (kbytes / 16); i += blockDim.x) {
-    const int r = a.R + i / (kbytes / 16), c = i % (kbytes / 16);
-    *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
-    if (has_lo) *reinterpret_cast<uint4*>(xs_lo + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
+  for (int r = a.R + warp; r < RP; r += kWarps) {   // pad rows
+    for (int c = lane; c < kbytes / 16; c += 32) {
+      *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
+      if (has_lo) *reinterpret_cast<uint4*>(xs_lo + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
+    }
   }
   compute_row_scales(a, srow, RP);
   bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
   ok = __syncthreads_and(ok);
   if (a.x_bf16 && ok) {  // caller-side bf16 rows (context taps) -> f16 in place
-    for (int i = threadIdx.x; i < a.R * (kbytes / 4); i += blockDim.x) {
-      uint32_t* p = reinterpret_cast<uint32_t*>(xs + (size_t)(i / (kbytes / 4)) * xstride) + i % (kbytes / 4);
-      const uint32_t u = *p;
-      const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
-      *p = pack_f16x2(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
+    for (int r = warp; r < a.R; r += kWarps) {
+      uint32_t* rp = reinterpret_cast<uint32_t*>(xs + (size_t)r * xstride);
+      for (int i = lane; i < kbytes / 4; i += 32) {
+        const uint32_t u = rp[i];
+        const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
+        rp[i] = pack_f16x2(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
+      }
     }
     __syncthreads();
   }
   if (FMT == FMT_Q4 && ok) {
-    for (int i = threadIdx.x; i < RP * ng; i += blockDim.x) {
-      const int r = i / ng, gl = i % ng;
-      const __half2* p = reinterpret_cast<const __half2*>(xs + (size_t)r * xstride + gl * 128);
-      const __half2* pl = reinterpret_cast<const __half2*>(xs_lo + (size_t)r * xstride + gl * 128);
-      float s = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < 32; j++) {
-        const float2 f = __half22float2(p[j]);
-        s += f.x + f.y;
-        if (has_lo) {
-          const float2 fl = __half22float2(pl[j]);
-          s += fl.x + fl.y;
-        }
+    // per (group, activation row) sums of hi + lo: an MMA against an all-ones A operand, with
+    // the B fragments read exactly as the weight MMAs read them
+    const uint32_t one2 = 0x3C003C00u;
+    for (int item = warp; item < ng * NT; item += kWarps) {
+      const int gl = item / NT, nt = item - gl * NT;
+      const uint8_t* xr = xs + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+      const uint4 x01 = *reinterpret_cast<const uint4*>(xr);
+      const uint4 x23 = *reinterpret_cast<const uint4*>(xr + 16);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(acc, one2, one2, one2, one2, x01.x, x01.y);
+      mma_f16(acc, one2, one2, one2, one2, x01.z, x01.w);
+      mma_f16(acc, one2, one2, one2, one2, x23.x, x23.y);
+      mma_f16(acc, one2, one2, one2, one2, x23.z, x23.w);
+      if (has_lo) {
+        const uint8_t* xl = xs_lo + (size_t)(nt * 8 + g) * xstride + (gl * 64 + 16 * t) * 2;
+        const uint4 l01 = *reinterpret_cast<const uint4*>(xl);
+        const uint4 l23 = *reinterpret_cast<const uint4*>(xl + 16);
+        mma_f16(acc, one2, one2, one2, one2, l01.x, l01.y);
+        mma_f16(acc, one2, one2, one2, one2, l01.z, l01.w);
+        mma_f16(acc, one2, one2, one2, one2, l23.x, l23.y);
+        mma_f16(acc, one2, one2, one2, one2, l23.z, l23.w);
       }
-      xsum[gl * RP + r] = s;
+      if (g == 0) *reinterpret_cast<float2*>(xsum + gl * RP + nt * 8 + 2 * t) = make_float2(acc[0], acc[1]);
     }
   }
   __syncthreads();
@@ -518,12 +530,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
 #pragma unroll
     for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
 
+  // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
+  auto finish = [&](int strip_local, float (&y)[NT][4]) {
+    if (a.n_slices > 1) {
+      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * NT4;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+        *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+    } else {
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
+    }
+  };
+  auto piece = [&](int w, int slot) -> float* { return red + ((size_t)(w * 2 + slot) * 32 + lane) * NT4; };
+
   int consumed = 0;
-  // consume stages [q0, q0 + n) into y
-  // consume stages [q0, q0 + n), which cover groups [gfirst, glast) of one strip, into y
-  auto consume = [&](auto lo_tag, int q0, int n, int gfirst, int glast, float (&y)[NT][4]) {
+  // stream this warp's range: stage q covers groups [c_goff, c_goff + gn) of strip c_strip
+  auto stream = [&](auto lo_tag) {
     constexpr bool LO = decltype(lo_tag)::value;
-    for (int q = q0; ok && q < q0 + n; q++) {
+    long long c_tile = t0;
+    int c_strip = first_strip, c_goff = (int)(t0 % ng), seg_start = c_goff;
+    float y[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+    for (int q = 0; ok && c_tile < t1; q++) {
       const int slot = warp * kStages + q % kStages;
       bool w_ok = mbar_wait_bounded(smem_u32(&bars[1 + slot]), (q / kStages) & 1, a.err, kErrTimeoutGemv);
       w_ok = __all_sync(0xffffffffu, w_ok);
@@ -532,12 +563,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         break;
       }
       consumed = q + 1;
-      const int g0 = gfirst + (q - q0) * GS, gn = min(GS, glast - g0);
+      const int gn = (int)min((long long)min(GS, ng - c_goff), t1 - c_tile);
       const uint8_t* stg = ring + (size_t)slot * kStageBytes;
-#pragma unroll
-      for (int gi = 0; gi < GS; gi++) {
-        if (gi >= gn) break;
-        const int gl = g0 - gbeg + gi;
+      auto group = [&](int gi) {
+        const int gl = c_goff + gi;
         if constexpr (FMT == FMT_Q4) {
           const uint8_t* gp = stg + gi * kQ4GroupBytes;
           const uint4 A = *reinterpret_cast<const uint4*>(gp + lane * 16);
@@ -606,66 +635,69 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
             }
           }
         }
+      };
+#pragma unroll
+      for (int gi = 0; gi < GS; gi++) {
+        if (gi >= gn) break;
+        group(gi);
       }
       // every lane is done reading this slot before the copy engine refills it
       fence_proxy_async();
       __syncwarp();
-      if (q + kStages < n_q) issue_next();
-    }
-  };
-  // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
-  auto finish = [&](int strip_local, float (&y)[NT][4]) {
-    if (a.n_slices > 1) {
-      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * NT4;
+      if (i_tile < t1) issue_next();
+      c_tile += gn;
+      c_goff += gn;
+      if (c_goff == ng || c_tile == t1) {   // end of a segment
+        if (seg_start == 0 && c_goff == ng) {
+          finish(sbeg + c_strip, y);
+        } else {
+          float* dst = piece(warp, c_strip == first_strip ? 0 : 1);
 #pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-        *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
-    } else {
-      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
-    }
-  };
-
-  for (int r = 0; r < rounds && ok; r++) {   // whole strips, one per warp
-    float y[NT][4];
+          for (int nt = 0; nt < NT; nt++)
+            *reinterpret_cast<float4*>(dst + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+        }
 #pragma unroll
-    for (int nt = 0; nt < NT; nt++)
+        for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    if (has_lo) consume(std::true_type{}, r * sps_full, sps_full, gbeg, gend, y);
-    else consume(std::false_type{}, r * sps_full, sps_full, gbeg, gend, y);
-    if (ok) finish(sbeg + r * kWarps + warp, y);
-  }
-  ok = __syncthreads_and(ok);
-  for (int li = 0; li < n_left && ok; li++) {   // leftover strips, K shared by all warps
-    float y[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    if (has_lo) consume(std::true_type{}, n_qa + li * sps_part, sps_part, wg0, wg1, y);
-    else consume(std::false_type{}, n_qa + li * sps_part, sps_part, wg0, wg1, y);
-    float* mine = red + ((size_t)((li & 1) * kWarps + warp) * 32 + lane) * NT4;
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-      *reinterpret_cast<float4*>(mine + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
-    ok = __syncthreads_and(ok);
-    if (!ok || warp != li) continue;
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-      for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-    for (int w = 0; w < kWarps; w++) {
-      const float* src = red + ((size_t)((li & 1) * kWarps + w) * 32 + lane) * NT4;
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++) {
-        const float4 v = *reinterpret_cast<const float4*>(src + nt * 4);
-        y[nt][0] += v.x;
-        y[nt][1] += v.y;
-        y[nt][2] += v.z;
-        y[nt][3] += v.w;
+          for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+        if (c_goff == ng) {
+          c_goff = 0;
+          c_strip++;
+        }
+        seg_start = c_goff;
       }
     }
-    finish(sbeg + rounds * kWarps + li, y);
+  };
+  if (has_lo) stream(std::true_type{});
+  else stream(std::false_type{});
+  ok = __syncthreads_and(ok);
+
+  // strips split between warps: the warp owning a strip's last tile sums the pieces in warp order
+  if (ok && t1 > t0) {
+    const long long s_first_tile = (long long)first_strip * ng;
+    if (t0 > s_first_tile && s_first_tile + ng <= t1) {
+      int wa = warp;
+      while (wa > 0 && T * wa / kWarps > s_first_tile) wa--;
+      float y[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
+      for (int w = wa; w <= warp; w++) {
+        const long long w0 = T * w / kWarps, w1 = T * (w + 1) / kWarps;
+        if (w1 == w0) continue;
+        const float* src = piece(w, (int)(w0 / ng) == first_strip ? 0 : 1);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+          const float4 v = *reinterpret_cast<const float4*>(src + nt * 4);
+          y[nt][0] += v.x;
+          y[nt][1] += v.y;
+          y[nt][2] += v.z;
+          y[nt][3] += v.w;
+        }
+      }
+      finish(sbeg + first_strip, y);
+    }
   }
 
   if (!ok && lane == 0) {
@@ -678,26 +710,31 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   }
 
   if (ok && a.n_slices > 1) {
-    // tickets of the strips this warp reduced; the last slice to arrive sums all slices in
-    // slice order and runs the epilogue
+    // every partial of this CTA is written (by whichever warp finished the strip) before any
+    // ticket is taken; the last slice to arrive at a strip sums all slices in slice order and
+    // runs the epilogue
     __threadfence();
-    __syncwarp();
-    for (int si = warp; si < n_cta; si += kWarps) {   // round strips of this warp, then leftover li == warp
-      const int strip_local = sbeg + si;
-      int prev = 0;
-      if (lane == 0) prev = atomicAdd(&a.tickets[strip_local], 1);
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev != a.n_slices - 1) continue;
-      __threadfence();
+    __syncthreads();
+    for (int si0 = warp; si0 < n_cta; si0 += 32 * kWarps) {
+      // one ticket per lane (strips si0 + kWarps * lane), all in flight at once
+      const int my_si = si0 + kWarps * lane;
+      int prev = -1;
+      if (my_si < n_cta) prev = atomicAdd(&a.tickets[sbeg + my_si], 1);
+      unsigned last_mask = __ballot_sync(0xffffffffu, prev == a.n_slices - 1);
+      if (last_mask) __threadfence();
+      while (last_mask) {
+      const int j = __ffs(last_mask) - 1;
+      last_mask &= last_mask - 1;
+      const int strip_local = sbeg + si0 + kWarps * j;
       float y[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
 #pragma unroll
-        for (int j = 0; j < 4; j++) y[nt][j] = 0.f;
-      for (int s0 = 0; s0 < a.n_slices; s0 += 4) {
-        float4 v[4][NT];   // four slices' loads in flight, then summed in slice order
+        for (int jj = 0; jj < 4; jj++) y[nt][jj] = 0.f;
+      for (int s0 = 0; s0 < a.n_slices; s0 += 8) {
+        float4 v[8][NT];   // eight slices' loads in flight, then summed in slice order
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
+        for (int q = 0; q < 8; q++) {
           const float* src = a.partials + (((size_t)strip_local * a.n_slices + s0 + q) * 32 + lane) * NT4;
 #pragma unroll
           for (int nt = 0; nt < NT; nt++)
@@ -705,7 +742,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
+        for (int q = 0; q < 8; q++) {
           if (s0 + q >= a.n_slices) break;
 #pragma unroll
           for (int nt = 0; nt < NT; nt++) {
@@ -718,6 +755,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       }
       if (lane == 0) a.tickets[strip_local] = 0;
       strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
+      }
     }
   }
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
