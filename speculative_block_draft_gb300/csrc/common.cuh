@@ -184,6 +184,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Ticket for "last one to arrive does the follow-up work": an atomic add at GPU scope with
+// acquire-release semantics. Callers pass a CTA barrier first, so the writes of every thread of
+// the CTA are released with it (cumulativity through the barrier), and the thread that sees the
+// final count acquires everything the other CTAs released.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -72,7 +72,7 @@ __device__ __forceinline__ void store_act(void* base, size_t idx, float v) {
 }
 
 // Per-row RMSNorm scale from the producer's per-strip sum-of-squares partials (one warp per
-// row; eight loads per lane in flight at a time, summed in a fixed order).
+// row; sixteen loads per lane in flight at a time, summed in a fixed order).
 __device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* srow, int nrows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
@@ -82,17 +82,17 @@ __device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* sro
     if (r < a.R && a.norm_mode != NORM_NONE) {
       const float* base = a.ssq + (size_t)map_row(a.xmap, r) * a.ssq_ld * two;
       float sa = 0.f, sb = 0.f;
-      for (int p0 = 0; p0 < a.ssq_parts; p0 += 8 * 32) {
-        float va[8], vb[8];
+      for (int p0 = 0; p0 < a.ssq_parts; p0 += 16 * 32) {
+        float va[16], vb[16];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
+        for (int j = 0; j < 16; j++) {
           const int p = p0 + j * 32 + lane;
           const bool in = p < a.ssq_parts;
           va[j] = in ? __ldcg(base + (size_t)p * two) : 0.f;
           vb[j] = in && two == 2 ? __ldcg(base + (size_t)p * 2 + 1) : 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
+        for (int j = 0; j < 16; j++) {
           sa += va[j];
           sb += vb[j];
         }
@@ -217,7 +217,36 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
     }
   }
   if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
-    // residual update / context rows, then this strip's sum-of-squares partial per column
+    // residual update / context rows, then this strip's sum-of-squares partial per column.
+    // Every load is issued before the first store: a load after a store that may alias it
+    // would wait for that store, one L2 round trip per element.
+    float hv[NT][2][2];                       // residual rows (RESID)
+    float wn[2] = {1.f, 1.f};                 // next norm weights of rows nr0, nr1 (RESID)
+    float cn[2], an[DFLASH_MAX_LAYERS][2];    // norm weights of rows nr0, nr1 (CTX)
+    if constexpr (EPI == EPI_RESID) {
+      if (e.wnext) {
+        wn[0] = v0 ? e.wnext[nr0] : 1.f;
+        wn[1] = v1 ? e.wnext[nr1] : 1.f;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int p = 0; p < 2; p++)
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int c = nt * 8 + 2 * t + p;
+            const int nr = h ? nr1 : nr0;
+            hv[nt][p][h] = (c < a.R && (h ? v1 : v0)) ? e.h[(size_t)c * e.ldo + nr] : 0.f;
+          }
+    } else {
+      cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
+      cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
+#pragma unroll
+      for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
+        an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
+        an[i][1] = (i < e.n_layers && v1) ? e.attn_norms[(size_t)i * e.ldo + nr1] : 0.f;
+      }
+    }
     float sq[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
@@ -234,17 +263,18 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
           const float v = y[nt][2 * h + p] * sc;
           if constexpr (EPI == EPI_RESID) {
             const size_t idx = (size_t)c * e.ldo + nr;
-            const float hn = e.h[idx] + v;
+            const float hn = hv[nt][p][h] + v;
             e.h[idx] = hn;
-            store_act_split<XT>(e.xnext, idx, e.x_lo_off, e.wnext ? hn * e.wnext[nr] : hn);
+            store_act_split<XT>(e.xnext, idx, e.x_lo_off, hn * wn[h]);
             s0 += hn * hn;
           } else {
-            const float cn = e.ctx_norm[nr];
-            for (int i = 0; i < e.n_layers; i++)
-              store_act_split<XT>(e.xw, ((size_t)i * e.xw_rows + c) * e.ldo + nr, e.x_lo_off,
-                                  v * cn * e.attn_norms[(size_t)i * e.ldo + nr]);
+#pragma unroll
+            for (int i = 0; i < DFLASH_MAX_LAYERS; i++)
+              if (i < e.n_layers)
+                store_act_split<XT>(e.xw, ((size_t)i * e.xw_rows + c) * e.ldo + nr, e.x_lo_off,
+                                    v * cn[h] * an[i][h]);
             s0 += v * v;
-            s1 += (v * cn) * (v * cn);
+            s1 += (v * cn[h]) * (v * cn[h]);
           }
         }
         sq[nt][p][0] = s0;
@@ -283,13 +313,11 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
 // scratch for blockDim states.
 __device__ __forceinline__ void lm_finish_split(const GemvArgs& a, LmState* sm) {
   const EpiArgs& e = a.e;
-  __threadfence();
   __syncthreads();
   __shared__ int last_split;
-  if (threadIdx.x == 0) last_split = atomicAdd(e.lm_ticket, 1) == (int)gridDim.x - 1;
+  if (threadIdx.x == 0) last_split = atom_add_acq_rel_gpu(e.lm_ticket, 1) == (int)gridDim.x - 1;
   __syncthreads();
   if (!last_split) return;
-  __threadfence();
   for (int c = 0; c < a.R; c++) {
     LmState acc{-INFINITY, 0.f, 0x7fffffff};
     for (int j = threadIdx.x; j < a.n_strips; j += blockDim.x) {
@@ -352,13 +380,11 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
     dst[1] = acc.s;
     dst[2] = __int_as_float(acc.i);
   }
-  __threadfence();
   __syncthreads();
   __shared__ int last;
-  if (threadIdx.x == 0) last = atomicAdd(e.lm_ticket, 1) == (int)gridDim.x - 1;
+  if (threadIdx.x == 0) last = atom_add_acq_rel_gpu(e.lm_ticket, 1) == (int)gridDim.x - 1;
   __syncthreads();
   if (!last) return;
-  __threadfence();
   // last CTA: thread j of row c merges CTAs j, j + P, j + 2P, ... (P threads per row), then a
   // pairwise tree per row; the order is fixed, so the result is reproducible.
   const int P = max(1, (int)blockDim.x / a.R);
@@ -367,11 +393,17 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
   const int c = threadIdx.x / P, j = threadIdx.x % P;
   LmState acc{-INFINITY, 0.f, 0x7fffffff};
   if (c < a.R) {
-#pragma unroll 4
-    for (int b = j; b < (int)gridDim.x; b += P) {
-      const float* src = e.lm_part + ((size_t)b * kMaxRows + c) * 3;
-      LmState o{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))};
-      lm_merge(acc, o);
+    for (int b0 = j; b0 < (int)gridDim.x; b0 += 4 * P) {
+      LmState o[4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const int b = b0 + q * P;
+        const float* src = e.lm_part + ((size_t)b * kMaxRows + c) * 3;
+        o[q] = b < (int)gridDim.x ? LmState{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))}
+                                  : LmState{-INFINITY, 0.f, 0x7fffffff};
+      }
+#pragma unroll
+      for (int q = 0; q < 4; q++) lm_merge(acc, o[q]);
     }
   }
   __syncthreads();
@@ -455,7 +487,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       i_strip++;
     }
   };
-  for (int q = 0; q < kStages && i_tile < t1; q++) issue_next();   // weights never change: no wait needed
+  // Weights never change, so some stages are requested before waiting for the previous kernel;
+  // the rest follow the activation copies, which are on the critical path.
+  for (int q = 0; q < kPrePdlStages && i_tile < t1; q++) issue_next();
   pdl_launch_dependents();
   pdl_wait();   // from here on, everything earlier kernels wrote is visible
 
@@ -476,6 +510,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride + off), row + a.x_lo_off * 2, len, bar);
     }
   }
+  for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
   for (int r = a.R + warp; r < RP; r += kWarps) {   // pad rows
     for (int c = lane; c < kbytes / 16; c += 32) {
       *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
@@ -713,15 +748,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     // every partial of this CTA is written (by whichever warp finished the strip) before any
     // ticket is taken; the last slice to arrive at a strip sums all slices in slice order and
     // runs the epilogue
-    __threadfence();
     __syncthreads();
     for (int si0 = warp; si0 < n_cta; si0 += 32 * kWarps) {
       // one ticket per lane (strips si0 + kWarps * lane), all in flight at once
       const int my_si = si0 + kWarps * lane;
       int prev = -1;
-      if (my_si < n_cta) prev = atomicAdd(&a.tickets[sbeg + my_si], 1);
+      if (my_si < n_cta) prev = atom_add_acq_rel_gpu(&a.tickets[sbeg + my_si], 1);
       unsigned last_mask = __ballot_sync(0xffffffffu, prev == a.n_slices - 1);
-      if (last_mask) __threadfence();
+      __syncwarp();   // the acquiring lane's view extends to the lanes that read the partials
       while (last_mask) {
       const int j = __ffs(last_mask) - 1;
       last_mask &= last_mask - 1;

@@ -28,6 +28,11 @@ namespace dfl {
 #endif
 constexpr int kWarps = DFL_GEMV_WARPS;    // consumer warps per tensor-core GEMV CTA
 constexpr int kStages = DFL_GEMV_STAGES;  // ring depth per warp (bulk copies in flight)
+#ifndef DFL_PRE_PDL_STAGES
+#define DFL_PRE_PDL_STAGES 1
+#endif
+// stages per warp requested before waiting for the previous kernel (the rest after)
+constexpr int kPrePdlStages = DFL_PRE_PDL_STAGES < kStages ? DFL_PRE_PDL_STAGES : kStages;
 constexpr int kQ4GroupBytes = 576;
 constexpr int kBf16GroupBytes = 2048;
 constexpr int kQ4GroupsPerStage = DFL_Q4_GROUPS_PER_STAGE;
