@@ -78,12 +78,12 @@ int nt_for(int R) { return R <= 8 ? 1 : (R <= 16 ? 2 : 4); }
 // Split of one launch over the SMs. Every warp of a CTA works on every strip of that CTA, so the
 // time of a launch is about (strips per CTA) x (groups per K slice); a K split over several
 // CTAs costs a partial tile per strip, counted here as one extra group.
-GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int x_lo) {
+GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int x_lo, int n_sm) {
   GemvPlan p{};
   if (h->fmt == FMT_F32) {
     p.n_slices = 1;
     p.gps = groups;
-    p.ctas_per_slice = std::max(1, std::min((n_strips + kF32Warps - 1) / kF32Warps, 4 * h->n_sm));
+    p.ctas_per_slice = std::max(1, std::min((n_strips + kF32Warps - 1) / kF32Warps, 4 * n_sm));
     p.grid = p.ctas_per_slice;
     return p;
   }
@@ -93,7 +93,7 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int 
     const int gps = (groups + s - 1) / s;
     if (gemv_smem_bytes(h->fmt, R, gps, x_lo) > kSmemLimit) continue;
     const int slices = (groups + gps - 1) / gps;
-    const int ctas = std::max(1, std::min(n_strips, h->n_sm / slices));
+    const int ctas = std::max(1, std::min(n_strips, n_sm / slices));
     const long per_cta = (n_strips + ctas - 1) / ctas;
     const long cost = per_cta * (gps + (slices > 1 ? 1 : 0));
     if (best < 0 || cost < best) {
@@ -108,7 +108,7 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int 
     while (gps > 1 && gemv_smem_bytes(h->fmt, R, gps, x_lo) > kSmemLimit) gps = (gps + 1) / 2;
     p.gps = gps;
     p.n_slices = (groups + gps - 1) / gps;
-    p.ctas_per_slice = std::max(1, std::min(n_strips, h->n_sm / p.n_slices));
+    p.ctas_per_slice = std::max(1, std::min(n_strips, n_sm / p.n_slices));
   }
   p.grid = p.n_slices * p.ctas_per_slice;
   return p;
@@ -207,12 +207,21 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   auto consider = [&](const PackedMat& m, int strips) {
     for (int r : {8, 16, 32})
       for (int lo : {0, 1}) {
-        const GemvPlan p = plan_gemv(h, strips, m.groups, r, lo);
+        const GemvPlan p = plan_gemv(h, strips, m.groups, r, lo, h->n_sm);
         if (p.n_slices > 1) pf = std::max(pf, (size_t)strips * p.n_slices * 32 * nt_for(r) * 4);
         lmg = std::max(lmg, p.grid);
       }
     tk = std::max(tk, strips);
   };
+  // the context K/V of every layer in one grouped launch
+  if (h->L > 1)
+    for (int r : {8, 16, 32})
+      for (int lo : {0, 1}) {
+        const int strips = (2 * h->kvd) / 16;
+        const GemvPlan p = plan_gemv(h, strips, h->qkv[0].groups, r, lo, std::max(1, h->n_sm / h->L));
+        if (p.n_slices > 1) pf = std::max(pf, (size_t)h->L * strips * p.n_slices * 32 * nt_for(r) * 4);
+        tk = std::max(tk, h->L * strips);
+      }
   consider(h->wc, h->wc.n_strips);
   for (int i = 0; i < h->L; i++) {
     consider(h->qkv[i], h->qkv[i].n_strips);
@@ -336,6 +345,8 @@ struct GemvCall {
   float inv_dim = 1.f;
   int epi = EPI_STORE;
   EpiArgs e{};
+  int grp_n = 1;                 // grouped launch of grp_n equally shaped problems
+  long long grp_w_stride = 0, grp_x_stride = 0;
 };
 
 size_t xn_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->r_blk * h->d; }
@@ -356,9 +367,14 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
   const int strips = c.n_strips < 0 ? m.n_strips : c.n_strips;
   if (c.R <= 0 || strips <= 0) return DFLASH_OK;
   if (h->act_f32) c.x_lo_off = 0;
-  const GemvPlan p = plan_gemv(h, strips, m.groups, c.R, c.x_lo_off != 0);
+  const int grp = h->act_f32 ? 1 : std::max(1, c.grp_n);
+  const GemvPlan p = plan_gemv(h, strips, m.groups, c.R, c.x_lo_off != 0, std::max(1, h->n_sm / grp));
   GemvArgs a{};
   a.w = m.w;
+  a.grp_n = grp;
+  a.grp_ctas = p.grid;
+  a.grp_w_stride = c.grp_w_stride;
+  a.grp_x_stride = c.grp_x_stride;
   a.strip0 = c.strip0;
   a.n_strips = strips;
   a.k = m.k;
@@ -388,7 +404,7 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
     a.e.lm_strip = h->lm_strip;
   }
   h->launches++;
-  return status_of(launch_gemv(h->fmt, c.epi, nt_for(c.R), a, p.grid, s));
+  return status_of(launch_gemv(h->fmt, c.epi, nt_for(c.R), a, p.grid * grp, s));
 }
 
 }  // namespace
@@ -427,6 +443,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     return DFLASH_ECAPACITY;
   }
   h->ws_bytes = carve(h, static_cast<uint8_t*>(workspace));
+  for (int i = 2; i < h->L; i++)   // grouped launches rely on equally spaced per-layer matrices
+    if (h->qkv[i].w - h->qkv[0].w != i * (h->qkv[1].w - h->qkv[0].w)) {
+      delete h;
+      return DFLASH_EINVAL;
+    }
 
   const int f = h->fmt;
   bool ok = mat_ok(w->w_c, f) && mat_ok(w->embed, f) && mat_ok(w->lm_head, f) && w->ctx_norm && w->block_pos &&
@@ -550,9 +571,18 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.ssq_ld = h->ssq_ld;
     int st = run_gemv(h, c1, s);
     if (st) return st;
-    // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache
-    for (int i = 0; i < h->L; i++) {
+    // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache; the
+    // tensor-core path runs every layer in one grouped launch (the layers' packed Q/K/V matrices,
+    // context inputs and caches are equally spaced)
+    const bool grouped = !h->act_f32 && h->L > 1;
+    for (int i = 0; i < (grouped ? 1 : h->L); i++) {
       GemvCall c2;
+      if (grouped) {
+        c2.grp_n = h->L;
+        c2.grp_w_stride = h->qkv[1].w - h->qkv[0].w;
+        c2.grp_x_stride = (long long)kMaxCtxChunk * h->d;
+        c2.e.kv_grp_stride = (long long)layer_cache;
+      }
       c2.m = &h->qkv[i];
       c2.strip0 = h->qd / 16;
       c2.n_strips = (2 * h->kvd) / 16;

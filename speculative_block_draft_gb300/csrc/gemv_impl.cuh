@@ -114,7 +114,7 @@ __device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* sro
 // (y[nt][0..1]) and strip*16+g+8 (y[nt][2..3]) at activation columns nt*8+2t and nt*8+2t+1.
 template <int EPI, int NT, typename XT>
 __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, float (&y)[NT][4],
-                                               const float* srow, LmState (&lm)[NT][2]) {
+                                               const float* srow, LmState (&lm)[NT][2], int lyr = 0) {
   const EpiArgs& e = a.e;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
@@ -162,7 +162,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             const int f = nr - half * e.kvd;
             const size_t idx =
                 (((size_t)e.kv_slot[c] * e.n_kv + f / e.hd) * e.cap + e.kv_pos[c]) * e.hd + f % e.hd;
-            store_act<XT>(half ? e.vc : e.kc, idx, v);
+            store_act<XT>(static_cast<uint8_t*>(half ? e.vc : e.kc) + (size_t)lyr * e.kv_grp_stride, idx, v);
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
@@ -433,7 +433,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   extern __shared__ __align__(1024) uint8_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 
-  const int slice = blockIdx.x / a.ctas_per_slice, cis = blockIdx.x % a.ctas_per_slice;
+  const int lyr = a.grp_n > 1 ? (int)blockIdx.x / a.grp_ctas : 0;   // problem of a grouped launch
+  const int bid = (int)blockIdx.x - lyr * a.grp_ctas;
+  const uint8_t* Wb = a.w + (size_t)lyr * a.grp_w_stride;
+  const uint8_t* Xb = static_cast<const uint8_t*>(a.x) + (size_t)lyr * a.grp_x_stride * 2;
+  const int sgl = lyr * a.n_strips;   // this problem's strips in the partials and tickets
+  const int slice = bid / a.ctas_per_slice, cis = bid % a.ctas_per_slice;
   const int gbeg = slice * a.gps, gend = min(a.groups, gbeg + a.gps), ng = gend - gbeg;
   const int sbeg = (int)((long long)cis * a.n_strips / a.ctas_per_slice);
   const int send = (int)((long long)(cis + 1) * a.n_strips / a.ctas_per_slice);
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   int issued = 0;
   auto issue_next = [&]() {
     const int gn = (int)min((long long)min(GS, ng - i_goff), t1 - i_tile);
-    const uint8_t* src = a.w + ((size_t)(a.strip0 + sbeg + i_strip) * a.groups + gbeg + i_goff) * GB;
+    const uint8_t* src = Wb + ((size_t)(a.strip0 + sbeg + i_strip) * a.groups + gbeg + i_goff) * GB;
     const int slot = warp * kStages + issued % kStages;
     if (lane == 0) {
       const uint32_t bar = smem_u32(&bars[1 + slot]);
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
     for (int i = lane; i < n_pc; i += 32) {
       const int j = i + rot < n_pc ? i + rot : i + rot - n_pc;
       const int r = j / ppr, off = (j - r * ppr) * 2048, len = min(2048, kbytes - off);
-      const uint8_t* row = static_cast<const uint8_t*>(a.x) + ((size_t)map_row(a.xmap, r) * a.ldx + k0) * 2 + off;
+      const uint8_t* row = Xb + ((size_t)map_row(a.xmap, r) * a.ldx + k0) * 2 + off;
       bulk_g2s(smem_u32(xs + (size_t)r * xstride + off), row, len, bar);
       if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride + off), row + a.x_lo_off * 2, len, bar);
     }
@@ -568,12 +573,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
   auto finish = [&](int strip_local, float (&y)[NT][4]) {
     if (a.n_slices > 1) {
-      float* part = a.partials + (((size_t)strip_local * a.n_slices + slice) * 32 + lane) * NT4;
+      float* part = a.partials + (((size_t)(sgl + strip_local) * a.n_slices + slice) * 32 + lane) * NT4;
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
         *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
     } else {
-      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr);
     }
   };
   auto piece = [&](int w, int slot) -> float* { return red + ((size_t)(w * 2 + slot) * 32 + lane) * NT4; };
@@ -753,7 +758,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       // one ticket per lane (strips si0 + kWarps * lane), all in flight at once
       const int my_si = si0 + kWarps * lane;
       int prev = -1;
-      if (my_si < n_cta) prev = atom_add_acq_rel_gpu(&a.tickets[sbeg + my_si], 1);
+      if (my_si < n_cta) prev = atom_add_acq_rel_gpu(&a.tickets[sgl + sbeg + my_si], 1);
       unsigned last_mask = __ballot_sync(0xffffffffu, prev == a.n_slices - 1);
       __syncwarp();   // the acquiring lane's view extends to the lanes that read the partials
       while (last_mask) {
@@ -769,7 +774,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         float4 v[8][NT];   // eight slices' loads in flight, then summed in slice order
 #pragma unroll
         for (int q = 0; q < 8; q++) {
-          const float* src = a.partials + (((size_t)strip_local * a.n_slices + s0 + q) * 32 + lane) * NT4;
+          const float* src = a.partials + (((size_t)(sgl + strip_local) * a.n_slices + s0 + q) * 32 + lane) * NT4;
 #pragma unroll
           for (int nt = 0; nt < NT; nt++)
             v[q][nt] = s0 + q < a.n_slices ? __ldcg(reinterpret_cast<const float4*>(src + nt * 4))
@@ -787,8 +792,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
           }
         }
       }
-      if (lane == 0) a.tickets[strip_local] = 0;
-      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm);
+      if (lane == 0) a.tickets[sgl + strip_local] = 0;
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr);
       }
     }
   }

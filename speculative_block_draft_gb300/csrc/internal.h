@@ -72,6 +72,7 @@ struct EpiArgs {
   void* q; void* kb; void* vb; int qd, kvd;
   // EPI_KV (append to a ring of cap rows per (slot, kv head)); cache layout [slot][Hkv][cap][hd]
   void* kc; void* vc; int cap, hd, n_kv;
+  long long kv_grp_stride;   // bytes between the caches of consecutive layers (grouped launches)
   int kv_slot[kMaxRows];
   int kv_pos[kMaxRows];
   // EPI_SWIGLU
@@ -84,6 +85,11 @@ struct EpiArgs {
 
 struct GemvArgs {
   const uint8_t* w;        // packed matrix base
+  // Grouped launch: grp_n equally shaped problems side by side in the grid (grp_ctas CTAs each);
+  // problem j uses w + j * grp_w_stride (bytes) and x + j * grp_x_stride (elements). grp_n = 1:
+  // one problem.
+  int grp_n, grp_ctas;
+  long long grp_w_stride, grp_x_stride;
   int strip0, n_strips;    // strip range of this launch
   int k, groups;           // inputs and 64-input groups
   int n_slices, gps;       // K slices per strip, groups per slice
