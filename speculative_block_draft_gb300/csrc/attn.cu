@@ -192,31 +192,54 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     for (int i = 0; i < min(2, n_tiles); i++) issue(i);
   }
 
-  // Q rows (query row i = head-in-group * gamma + block row), pad rows zero
+  // Q rows (query row i = head-in-group * gamma + block row), pad rows zero; every load of a
+  // thread is issued before its first shared-memory store
+  constexpr int kThreads = kAttnWarps * 32;
+  constexpr int kQPer = 64 * (HD / 8) / kThreads;
   const __half* qg = static_cast<const __half*>(a.q);
-  for (int idx = threadIdx.x; idx < 64 * (HD / 8); idx += blockDim.x) {
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int u = 0; u < kQPer; u++) {
+    const int idx = threadIdx.x + u * kThreads;
     const int i = idx / (HD / 8), c8 = idx % (HD / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
+    qv[u] = make_uint4(0, 0, 0, 0);
     if (i < M) {
       const int h = kvh * grp + i / a.gamma, k = i % a.gamma;
-      v = *reinterpret_cast<const uint4*>(qg + (size_t)(rq.row0 + k) * a.qd + h * HD + c8 * 8);
+      qv[u] = *reinterpret_cast<const uint4*>(qg + (size_t)(rq.row0 + k) * a.qd + h * HD + c8 * 8);
     }
-    *reinterpret_cast<uint4*>(q_s + (c8 / 8) * kSub + swz(i, c8 % 8)) = v;
   }
+  constexpr int kBPer = (16 * (HD / 8) + kThreads - 1) / kThreads;
+  uint4 kv[kBPer], vv[kBPer];
   if (with_block) {
     const __half* kg = static_cast<const __half*>(a.kb);
     const __half* vg = static_cast<const __half*>(a.vb);
-    for (int idx = threadIdx.x; idx < 16 * (HD / 8); idx += blockDim.x) {
+#pragma unroll
+    for (int u = 0; u < kBPer; u++) {
+      const int idx = threadIdx.x + u * kThreads;
       const int k = idx / (HD / 8), c8 = idx % (HD / 8);
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (k < a.gamma) {
+      kv[u] = vv[u] = make_uint4(0, 0, 0, 0);
+      if (idx < 16 * (HD / 8) && k < a.gamma) {
         const size_t off = (size_t)(rq.row0 + k) * a.kvd + kvh * HD + c8 * 8;
-        kv = *reinterpret_cast<const uint4*>(kg + off);
-        vv = *reinterpret_cast<const uint4*>(vg + off);
+        kv[u] = *reinterpret_cast<const uint4*>(kg + off);
+        vv[u] = *reinterpret_cast<const uint4*>(vg + off);
       }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kQPer; u++) {
+    const int idx = threadIdx.x + u * kThreads;
+    const int i = idx / (HD / 8), c8 = idx % (HD / 8);
+    *reinterpret_cast<uint4*>(q_s + (c8 / 8) * kSub + swz(i, c8 % 8)) = qv[u];
+  }
+  if (with_block) {
+#pragma unroll
+    for (int u = 0; u < kBPer; u++) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx >= 16 * (HD / 8)) continue;
+      const int k = idx / (HD / 8), c8 = idx % (HD / 8);
       const uint32_t o = (c8 / 8) * kBlkSub + swz(k, c8 % 8);
-      *reinterpret_cast<uint4*>(bk_s + o) = kv;
-      *reinterpret_cast<uint4*>(bv_s + o) = vv;
+      *reinterpret_cast<uint4*>(bk_s + o) = kv[u];
+      *reinterpret_cast<uint4*>(bv_s + o) = vv[u];
     }
   }
   __syncthreads();
@@ -301,8 +324,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
 }
 
 // Combine the key splits of one query row: grid (request * kv head, query row), one float4 of
-// head_dim per thread. Split weights exp2(m_s - max) are recomputed by every thread (broadcast
-// loads), then O = sum_s w_s O_s / sum_s w_s l_s in split order.
+// head_dim per thread. Splits are taken in order, sixteen at a time with all their loads in
+// flight, and combined online: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M the running
+// maximum.
 template <int HD>
 __global__ void __launch_bounds__(HD / 4) attn_merge_kernel(const __grid_constant__ AttnArgs a) {
   pdl_launch_dependents();
@@ -310,21 +334,32 @@ __global__ void __launch_bounds__(HD / 4) attn_merge_kernel(const __grid_constan
   const int pair = blockIdx.x, i = blockIdx.y, c4 = threadIdx.x;
   const int b = pair / a.hkv, kvh = pair % a.hkv, grp = a.hq / a.hkv;
   const size_t pbase = (size_t)pair * a.n_splits;
-  float mx = -INFINITY;
-#pragma unroll 8
-  for (int s2 = 0; s2 < a.n_splits; s2++) mx = fmaxf(mx, __ldcg(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
-  float L = 0.f;
+  float mx = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s2 = 0; s2 < a.n_splits; s2++) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(&a.part_ml[((pbase + s2) * 64 + i) * 2]));
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + ((pbase + s2) * 64 + i) * HD) + c4);
-    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
-    L = fmaf(w, ml.y, L);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  for (int s0 = 0; s0 < a.n_splits; s0 += 16) {
+    float2 ml[16];
+    float4 v[16];
+#pragma unroll
+    for (int q = 0; q < 16; q++) {
+      const int s2 = s0 + q;
+      const bool in = s2 < a.n_splits;
+      ml[q] = in ? __ldcg(reinterpret_cast<const float2*>(&a.part_ml[((pbase + s2) * 64 + i) * 2]))
+                 : make_float2(-INFINITY, 0.f);
+      v[q] = in ? __ldcg(reinterpret_cast<const float4*>(a.part_o + ((pbase + s2) * 64 + i) * HD) + c4)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 16; q++) {
+      if (ml[q].x == -INFINITY) continue;
+      const float mn = fmaxf(mx, ml[q].x);
+      const float so = mx == -INFINITY ? 0.f : exp2f(mx - mn), w = exp2f(ml[q].x - mn);
+      L = fmaf(w, ml[q].y, L * so);
+      acc.x = fmaf(w, v[q].x, acc.x * so);
+      acc.y = fmaf(w, v[q].y, acc.y * so);
+      acc.z = fmaf(w, v[q].z, acc.z * so);
+      acc.w = fmaf(w, v[q].w, acc.w * so);
+      mx = mn;
+    }
   }
   const float inv = 1.0f / L;
   const int head = kvh * grp + i / a.gamma, k = i % a.gamma;

@@ -101,25 +101,43 @@ __global__ void repack_kernel(const __grid_constant__ RepackArgs a) {
 // residual h, the next input h * attn_norm_0 and one sum-of-squares part per chunk.
 template <typename XT>
 __global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__ BlockArgs a) {
+  // kBlockCols columns of one block row per CTA, four per thread. The constant inputs (mask
+  // embedding, block positions, first norm) are read before waiting for the previous kernel; only
+  // row 0 (the anchor's embedding) needs data of this round.
+  constexpr int kPer = kBlockCols / 256;
   const int r = blockIdx.y, chunk = blockIdx.x, b = r / a.gamma, k = r % a.gamma;
   __shared__ float red[8];
+  const int j0 = chunk * kBlockCols + threadIdx.x;
+  float bp[kPer], an[kPer], base[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; u++) {
+    const int j = j0 + u * 256;
+    const bool in = j < a.d;
+    bp[u] = in ? a.block_pos[(size_t)k * a.d + j] : 0.f;
+    an[u] = in ? a.attn_norm0[j] : 0.f;
+    base[u] = (in && k > 0) ? a.mask_emb[(size_t)(k - 1) * a.d + j] : 0.f;
+  }
   pdl_launch_dependents();
   pdl_wait();
-  int tok = a.anchor[b];
-  tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);  // clamped: no read outside the table
-  float ss = 0.f;
-  const int j0 = chunk * kBlockCols, j1 = min(a.d, j0 + kBlockCols);
-  for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-    float v;
-    if (k == 0) {
-      const float e = a.tokrow ? a.tokrow[(size_t)b * a.d + j]
-                               : load_weight(a.fmt, a.emb, a.emb_scale, a.emb_bias, a.H, tok, j);
-      v = e + a.block_pos[j];
-    } else {
-      v = a.mask_emb[(size_t)(k - 1) * a.d + j] + a.block_pos[(size_t)k * a.d + j];
+  if (k == 0) {
+    int tok = a.anchor[b];
+    tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);  // clamped: no read outside the table
+#pragma unroll
+    for (int u = 0; u < kPer; u++) {
+      const int j = j0 + u * 256;
+      if (j < a.d)
+        base[u] = a.tokrow ? a.tokrow[(size_t)b * a.d + j]
+                           : load_weight(a.fmt, a.emb, a.emb_scale, a.emb_bias, a.H, tok, j);
     }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < kPer; u++) {
+    const int j = j0 + u * 256;
+    if (j >= a.d) continue;
+    const float v = base[u] + bp[u];
     a.h[(size_t)r * a.d + j] = v;
-    store_act_split<XT>(a.xn, (size_t)r * a.d + j, a.xn_lo_off, v * a.attn_norm0[j]);
+    store_act_split<XT>(a.xn, (size_t)r * a.d + j, a.xn_lo_off, v * an[u]);
     ss += v * v;
   }
   ss = warp_sum(ss);
