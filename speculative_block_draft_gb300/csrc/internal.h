@@ -18,13 +18,13 @@ namespace dfl {
 //   bf16 : 2048 B = 4 k16 steps x 32 lanes x 16 B, A-fragment order, values stored as f16
 //   f32  : row-major float rows (CUDA-core path), strips of 16 consecutive logical rows
 #ifndef DFL_GEMV_WARPS
-#define DFL_GEMV_WARPS 12
+#define DFL_GEMV_WARPS 16
 #endif
 #ifndef DFL_GEMV_STAGES
 #define DFL_GEMV_STAGES 2
 #endif
 #ifndef DFL_Q4_GROUPS_PER_STAGE
-#define DFL_Q4_GROUPS_PER_STAGE 8
+#define DFL_Q4_GROUPS_PER_STAGE 6
 #endif
 constexpr int kWarps = DFL_GEMV_WARPS;    // consumer warps per tensor-core GEMV CTA
 constexpr int kStages = DFL_GEMV_STAGES;  // ring depth per warp (bulk copies in flight)
