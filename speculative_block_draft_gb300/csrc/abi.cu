@@ -347,6 +347,8 @@ struct GemvCall {
   EpiArgs e{};
   int grp_n = 1;                 // grouped launch of grp_n equally shaped problems
   long long grp_w_stride = 0, grp_x_stride = 0;
+  const float* x_colscale = nullptr;
+  long long x_colscale_grp_stride = 0;
 };
 
 size_t xn_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->r_blk * h->d; }
@@ -375,6 +377,8 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
   a.grp_ctas = p.grid;
   a.grp_w_stride = c.grp_w_stride;
   a.grp_x_stride = c.grp_x_stride;
+  a.x_colscale = h->act_f32 ? nullptr : c.x_colscale;
+  a.x_colscale_grp_stride = c.x_colscale_grp_stride;
   a.strip0 = c.strip0;
   a.n_strips = strips;
   a.k = m.k;
@@ -562,7 +566,9 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.n_rows = h->d;
     c1.e.ldo = h->d;
     c1.e.ctx_norm = h->ctx_norm;
-    c1.e.attn_norms = h->attn_norm;
+    // tensor-core path: one row x * ctx_norm, the K/V launch applies attn_norm_i to its input;
+    // CUDA-core path: one input row per layer
+    c1.e.attn_norms = h->act_f32 ? h->attn_norm : nullptr;
     c1.e.n_layers = h->L;
     c1.e.xw = h->xw;
     c1.e.xw_rows = kMaxCtxChunk;
@@ -572,22 +578,24 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     int st = run_gemv(h, c1, s);
     if (st) return st;
     // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache; the
-    // tensor-core path runs every layer in one grouped launch (the layers' packed Q/K/V matrices,
-    // context inputs and caches are equally spaced)
-    const bool grouped = !h->act_f32 && h->L > 1;
+    // tensor-core path runs every layer in one grouped launch over the same input rows (the
+    // layers' packed Q/K/V matrices and caches are equally spaced; attn_norm_i scales the input)
+    const bool grouped = !h->act_f32;
     for (int i = 0; i < (grouped ? 1 : h->L); i++) {
       GemvCall c2;
-      if (grouped) {
+      if (!h->act_f32) {
         c2.grp_n = h->L;
-        c2.grp_w_stride = h->qkv[1].w - h->qkv[0].w;
-        c2.grp_x_stride = (long long)kMaxCtxChunk * h->d;
+        c2.grp_w_stride = h->L > 1 ? h->qkv[1].w - h->qkv[0].w : 0;
+        c2.grp_x_stride = 0;   // the same input rows, scaled per layer by attn_norm_i
+        c2.x_colscale = h->attn_norm;
+        c2.x_colscale_grp_stride = h->d;
         c2.e.kv_grp_stride = (long long)layer_cache;
       }
       c2.m = &h->qkv[i];
       c2.strip0 = h->qd / 16;
       c2.n_strips = (2 * h->kvd) / 16;
       c2.R = rc;
-      c2.x = static_cast<const uint8_t*>(h->xw) + (size_t)i * kMaxCtxChunk * h->d * ab;
+      c2.x = static_cast<const uint8_t*>(h->xw) + (grouped ? 0 : (size_t)i * kMaxCtxChunk * h->d * ab);
       c2.ldx = h->d;
       c2.x_lo_off = lo_if(LO_CTXKV, xw_lo(h));
       c2.norm_mode = NORM_CTX;
@@ -910,8 +918,12 @@ int dflash_check_errors(dflash_handle* h, void* stream) {
   unsigned word = 0;
   if (cudaMemcpy(&word, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_ECUDA;
   if (word) {
+    // a kernel gave up part-way: clear the error word and the arrival counters it may have left
     const unsigned zero = 0;
-    if (cudaMemcpy(h->err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) return DFLASH_ECUDA;
+    if (cudaMemcpy(h->err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(h->tickets, 0, (size_t)h->ticket_count * 4) != cudaSuccess ||
+        cudaMemset(h->lm_ticket, 0, 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return DFLASH_ECUDA;
     return DFLASH_ETIMEOUT;
   }
   return DFLASH_OK;

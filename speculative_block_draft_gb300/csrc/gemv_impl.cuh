@@ -110,11 +110,57 @@ __device__ __forceinline__ void compute_row_scales(const GemvArgs& a, float* sro
   }
 }
 
+// Inputs an epilogue reads from global memory (residual rows, norm weights). They are loaded
+// before any store of the epilogue (a load after a store that may alias it would wait for that
+// store, one L2 round trip per element), and on the K-split path together with the partials.
+template <int NT>
+struct EpiPre {
+  float hv[NT][2][2];                 // residual rows (RESID)
+  float wn[2];                        // next norm weights of rows nr0, nr1 (RESID)
+  float cn[2];                        // context norm weights of rows nr0, nr1 (CTX)
+  float an[DFLASH_MAX_LAYERS][2];     // per-layer norm weights of rows nr0, nr1 (CTX, CUDA-core path)
+};
+
+template <int EPI, int NT>
+__device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre<NT>& pre) {
+  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
+    const EpiArgs& e = a.e;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
+    const bool v0 = nr0 >= 0 && nr0 < e.n_rows, v1 = nr1 >= 0 && nr1 < e.n_rows;
+    if constexpr (EPI == EPI_RESID) {
+      pre.wn[0] = (e.wnext && v0) ? e.wnext[nr0] : 1.f;
+      pre.wn[1] = (e.wnext && v1) ? e.wnext[nr1] : 1.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int p = 0; p < 2; p++)
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            const int c = nt * 8 + 2 * t + p;
+            const int nr = h ? nr1 : nr0;
+            pre.hv[nt][p][h] = (c < a.R && (h ? v1 : v0)) ? e.h[(size_t)c * e.ldo + nr] : 0.f;
+          }
+    } else {
+      pre.cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
+      pre.cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
+      if (e.attn_norms) {
+#pragma unroll
+        for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
+          pre.an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
+          pre.an[i][1] = (i < e.n_layers && v1) ? e.attn_norms[(size_t)i * e.ldo + nr1] : 0.f;
+        }
+      }
+    }
+  }
+}
+
 // Epilogue of one complete 16-row strip. Lane (g, t) holds, for n-tile nt, rows strip*16+g
 // (y[nt][0..1]) and strip*16+g+8 (y[nt][2..3]) at activation columns nt*8+2t and nt*8+2t+1.
 template <int EPI, int NT, typename XT>
 __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, float (&y)[NT][4],
-                                               const float* srow, LmState (&lm)[NT][2], int lyr = 0) {
+                                               const float* srow, LmState (&lm)[NT][2], int lyr,
+                                               const EpiPre<NT>& pre) {
   const EpiArgs& e = a.e;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
@@ -217,36 +263,11 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
     }
   }
   if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
-    // residual update / context rows, then this strip's sum-of-squares partial per column.
-    // Every load is issued before the first store: a load after a store that may alias it
-    // would wait for that store, one L2 round trip per element.
-    float hv[NT][2][2];                       // residual rows (RESID)
-    float wn[2] = {1.f, 1.f};                 // next norm weights of rows nr0, nr1 (RESID)
-    float cn[2], an[DFLASH_MAX_LAYERS][2];    // norm weights of rows nr0, nr1 (CTX)
-    if constexpr (EPI == EPI_RESID) {
-      if (e.wnext) {
-        wn[0] = v0 ? e.wnext[nr0] : 1.f;
-        wn[1] = v1 ? e.wnext[nr1] : 1.f;
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int p = 0; p < 2; p++)
-#pragma unroll
-          for (int h = 0; h < 2; h++) {
-            const int c = nt * 8 + 2 * t + p;
-            const int nr = h ? nr1 : nr0;
-            hv[nt][p][h] = (c < a.R && (h ? v1 : v0)) ? e.h[(size_t)c * e.ldo + nr] : 0.f;
-          }
-    } else {
-      cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
-      cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
-#pragma unroll
-      for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
-        an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
-        an[i][1] = (i < e.n_layers && v1) ? e.attn_norms[(size_t)i * e.ldo + nr1] : 0.f;
-      }
-    }
+    // residual update / context rows, then this strip's sum-of-squares partial per column
+    const auto& hv = pre.hv;
+    const auto& wn = pre.wn;
+    const auto& cn = pre.cn;
+    const auto& an = pre.an;
     float sq[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
@@ -267,6 +288,10 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             e.h[idx] = hn;
             store_act_split<XT>(e.xnext, idx, e.x_lo_off, hn * wn[h]);
             s0 += hn * hn;
+          } else if (!e.attn_norms) {   // one row x * ctx_norm; the consumer applies attn_norm_i
+            store_act_split<XT>(e.xw, (size_t)c * e.ldo + nr, e.x_lo_off, v * cn[h]);
+            s0 += v * v;
+            s1 += (v * cn[h]) * (v * cn[h]);
           } else {
 #pragma unroll
             for (int i = 0; i < DFLASH_MAX_LAYERS; i++)
@@ -423,6 +448,10 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
 // ------------------------------------------------------------------------------------------------
 // Tensor-core kernel (bf16 or 4-bit weights, bf16 activations)
 // ------------------------------------------------------------------------------------------------
+#ifndef DFL_RING_AFTER
+#define DFL_RING_AFTER 0   // where the ring's remaining stages are requested (see the kernel)
+#endif
+
 template <int FMT, int NT, int EPI>
 __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_constant__ GemvArgs a) {
   using XT = __half;
@@ -495,8 +524,46 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
   // Weights never change, so some stages are requested before waiting for the previous kernel;
   // the rest follow the activation copies, which are on the critical path.
   for (int q = 0; q < kPrePdlStages && i_tile < t1; q++) issue_next();
+  // per-input scales of the slice (constants), eight columns per thread and chunk: read before
+  // waiting for the previous kernel
+#ifndef DFL_CS_CHUNKS
+#define DFL_CS_CHUNKS 2
+#endif
+  constexpr int kCsChunks = EPI == EPI_KV ? DFL_CS_CHUNKS : 0;   // only the context K/V launch uses them
+  float4 csv[kCsChunks > 0 ? kCsChunks : 1][2];
+  const float* cs = (EPI == EPI_KV && a.x_colscale)
+                        ? a.x_colscale + (size_t)lyr * a.x_colscale_grp_stride + gbeg * 64 : nullptr;
+#pragma unroll
+  for (int u = 0; u < kCsChunks; u++) {
+    const int j = threadIdx.x + u * kGemvThreads;
+    const bool in = cs && 8 * j < ng * 64;
+    csv[u][0] = in ? *reinterpret_cast<const float4*>(cs + 8 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    csv[u][1] = in ? *reinterpret_cast<const float4*>(cs + 8 * j + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (kL2PrefetchTiles > 0 && lane == 0) {
+    // the tiles after the ring's first stages, strip segment by strip segment, into L2: the
+    // previous kernel's tail leaves HBM idle, and these loads then hit L2
+    long long pt = i_tile + (long long)(kStages - kPrePdlStages) * GS;
+    int budget = kL2PrefetchTiles;
+    if (pt < t1) {
+      int ps = (int)(pt / ng), pg = (int)(pt % ng);
+      while (budget > 0 && pt < t1) {
+        const int n = (int)min((long long)min(ng - pg, budget), t1 - pt);
+        prefetch_l2(Wb + ((size_t)(a.strip0 + sbeg + ps) * a.groups + gbeg + pg) * GB, n * GB);
+        pt += n;
+        budget -= n;
+        pg += n;
+        if (pg == ng) {
+          pg = 0;
+          ps++;
+        }
+      }
+    }
+  }
   pdl_launch_dependents();
   pdl_wait();   // from here on, everything earlier kernels wrote is visible
+  if (DFL_RING_AFTER == 0)
+    for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
 
   // activation slice -> shared (bulk copies of at most 2 KB, started at a different piece in
   // every CTA so the CTAs do not all read the same L2 lines at once), pad rows zeroed
@@ -515,14 +582,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       if (has_lo) bulk_g2s(smem_u32(xs_lo + (size_t)r * xstride + off), row + a.x_lo_off * 2, len, bar);
     }
   }
-  for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
   for (int r = a.R + warp; r < RP; r += kWarps) {   // pad rows
     for (int c = lane; c < kbytes / 16; c += 32) {
       *reinterpret_cast<uint4*>(xs + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
       if (has_lo) *reinterpret_cast<uint4*>(xs_lo + (size_t)r * xstride + c * 16) = make_uint4(0, 0, 0, 0);
     }
   }
+  if (DFL_RING_AFTER == 1)
+    for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
   compute_row_scales(a, srow, RP);
+  if (DFL_RING_AFTER == 2)
+    for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
   bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
   ok = __syncthreads_and(ok);
   if (a.x_bf16 && ok) {  // caller-side bf16 rows (context taps) -> f16 in place
@@ -534,6 +604,39 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         rp[i] = pack_f16x2(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
       }
     }
+    __syncthreads();
+  }
+  if (EPI == EPI_KV && cs && ok) {
+    // per-input scale (a layer's norm weights) of the staged slice: x = (hi + lo) * w, split again
+    auto scale_cols = [&](int j, const float4& w0, const float4& w1) {
+      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int r = 0; r < a.R; r++) {
+        uint4* ph = reinterpret_cast<uint4*>(xs + (size_t)r * xstride) + j;
+        uint4* pl = reinterpret_cast<uint4*>(xs_lo + (size_t)r * xstride) + j;
+        const uint4 h4 = *ph;
+        const uint4 l4 = has_lo ? *pl : make_uint4(0, 0, 0, 0);
+        const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, lw[4] = {l4.x, l4.y, l4.z, l4.w};
+        uint32_t oh[4], ol[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hw[q]));
+          const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lw[q]));
+          const float va = (fh.x + fl.x) * w[2 * q], vb = (fh.y + fl.y) * w[2 * q + 1];
+          const __half ha = from_f<__half>(va), hb = from_f<__half>(vb);
+          oh[q] = pack_f16x2(__half2float(ha), __half2float(hb));
+          ol[q] = pack_f16x2(va - __half2float(ha), vb - __half2float(hb));
+        }
+        *ph = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+        if (has_lo) *pl = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < kCsChunks; u++) {
+      const int j = threadIdx.x + u * kGemvThreads;
+      if (8 * j < ng * 64) scale_cols(j, csv[u][0], csv[u][1]);
+    }
+    for (int j = threadIdx.x + kCsChunks * kGemvThreads; 8 * j < ng * 64; j += kGemvThreads)
+      scale_cols(j, *reinterpret_cast<const float4*>(cs + 8 * j), *reinterpret_cast<const float4*>(cs + 8 * j + 4));
     __syncthreads();
   }
   if (FMT == FMT_Q4 && ok) {
@@ -578,7 +681,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       for (int nt = 0; nt < NT; nt++)
         *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
     } else {
-      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr);
+      EpiPre<NT> pre;
+      epi_preload<EPI, NT>(a, a.strip0 + strip_local, pre);
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr, pre);
     }
   };
   auto piece = [&](int w, int slot) -> float* { return red + ((size_t)(w * 2 + slot) * 32 + lane) * NT4; };
@@ -765,6 +870,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       const int j = __ffs(last_mask) - 1;
       last_mask &= last_mask - 1;
       const int strip_local = sbeg + si0 + kWarps * j;
+      EpiPre<NT> pre;   // issued with the partial loads below: one round trip for both
+      epi_preload<EPI, NT>(a, a.strip0 + strip_local, pre);
       float y[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
@@ -793,7 +900,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         }
       }
       if (lane == 0) a.tickets[sgl + strip_local] = 0;
-      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr);
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr, pre);
       }
     }
   }
@@ -846,7 +953,9 @@ __global__ void __launch_bounds__(kF32Warps * 32) gemv_f32_kernel(const __grid_c
         }
       }
     }
-    strip_epilogue<EPI, NT, float>(a, strip, y, srow, lm);
+    EpiPre<NT> pre;
+    epi_preload<EPI, NT>(a, strip, pre);
+    strip_epilogue<EPI, NT, float>(a, strip, y, srow, lm, 0, pre);
   }
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
 }

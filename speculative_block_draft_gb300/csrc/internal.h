@@ -33,6 +33,11 @@ constexpr int kStages = DFL_GEMV_STAGES;  // ring depth per warp (bulk copies in
 #endif
 // stages per warp requested before waiting for the previous kernel (the rest after)
 constexpr int kPrePdlStages = DFL_PRE_PDL_STAGES < kStages ? DFL_PRE_PDL_STAGES : kStages;
+#ifndef DFL_L2_PREFETCH_TILES
+#define DFL_L2_PREFETCH_TILES 0
+#endif
+// weight tiles per warp, beyond its ring, prefetched into L2 before waiting for the previous kernel
+constexpr int kL2PrefetchTiles = DFL_L2_PREFETCH_TILES;
 constexpr int kQ4GroupBytes = 576;
 constexpr int kBf16GroupBytes = 2048;
 constexpr int kQ4GroupsPerStage = DFL_Q4_GROUPS_PER_STAGE;
@@ -97,6 +102,8 @@ struct GemvArgs {
   int R;                   // activation rows (<= kMaxRows)
   const void* x; int ldx; RowMap xmap;
   int x_bf16;              // tensor-core path: x rows are bf16 (converted to f16 after staging)
+  const float* x_colscale; // tensor-core path: optional per-input scale of x (problem j: + j * stride)
+  long long x_colscale_grp_stride;
   long long x_lo_off;      // tensor-core path: f16 remainder rows at x + x_lo_off elements (0: none)
   int norm_mode; const float* ssq; int ssq_ld; int ssq_parts; float inv_dim; float eps;
   float* partials; int* tickets;
