@@ -89,7 +89,7 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int 
   }
   constexpr size_t kSmemLimit = 225 * 1024;
   long best = -1;
-  for (int s = 1; s <= std::max(1, std::min(16, groups / kWarps)); s++) {
+  for (int s = 1; s <= std::max(1, std::min(16, groups / gemv_warps(nt_for(R)))); s++) {
     const int gps = (groups + s - 1) / s;
     if (gemv_smem_bytes(h->fmt, R, gps, x_lo) > kSmemLimit) continue;
     const int slices = (groups + gps - 1) / gps;

@@ -9,13 +9,14 @@ cudaError_t launch_gemv_bf16(int epi, int nt, const GemvArgs& a, int grid, size_
 size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo) {
   if (fmt == FMT_F32) return 0;
   const int rp = R <= 8 ? 8 : (R <= 16 ? 16 : 32);
-  size_t b = (size_t)kWarps * kStages * kStageBytes;   // weight rings
+  const int w = gemv_warps(rp / 8);
+  size_t b = (size_t)w * kStages * kStageBytes;        // weight rings
   b += (size_t)rp * (gps * 128 + 16) * (x_lo ? 2 : 1); // activation slice (and its f16 remainder)
   if (fmt == FMT_Q4) b += (size_t)rp * gps * 4;        // per-group activation sums
   b += kMaxRows * 4;                                   // row scales
-  b += (size_t)kWarps * kMaxRows * sizeof(LmState);    // vocab reduction scratch
-  b += (size_t)2 * kWarps * 32 * (rp / 2) * 4;         // per-strip reduction buffers (2 x warps x 32 x NT*4)
-  b += 16 + (1 + kWarps * kStages) * 8;                // mbarriers
+  b += (size_t)w * kMaxRows * sizeof(LmState);         // vocab reduction scratch
+  b += (size_t)2 * w * 32 * (rp / 2) * 4;              // split-strip pieces (2 per warp x 32 lanes x NT*4)
+  b += 16 + (1 + w * kStages) * 8;                     // mbarriers
   return b;
 }
 

@@ -121,7 +121,8 @@ struct EpiPre {
   float an[DFLASH_MAX_LAYERS][2];     // per-layer norm weights of rows nr0, nr1 (CTX, CUDA-core path)
 };
 
-template <int EPI, int NT>
+// XT = float is the CUDA-core path, which alone writes one context row per layer (EPI_CTX).
+template <int EPI, int NT, typename XT>
 __device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre<NT>& pre) {
   if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
     const EpiArgs& e = a.e;
@@ -144,7 +145,7 @@ __device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre
     } else {
       pre.cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
       pre.cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
-      if (e.attn_norms) {
+      if (std::is_same<XT, float>::value && e.attn_norms) {
 #pragma unroll
         for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
           pre.an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
@@ -288,7 +289,8 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             e.h[idx] = hn;
             store_act_split<XT>(e.xnext, idx, e.x_lo_off, hn * wn[h]);
             s0 += hn * hn;
-          } else if (!e.attn_norms) {   // one row x * ctx_norm; the consumer applies attn_norm_i
+          } else if (!std::is_same<XT, float>::value || !e.attn_norms) {
+            // one row x * ctx_norm; the consumer applies attn_norm_i
             store_act_split<XT>(e.xw, (size_t)c * e.ldo + nr, e.x_lo_off, v * cn[h]);
             s0 += v * v;
             s1 += (v * cn[h]) * (v * cn[h]);
@@ -449,12 +451,14 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
 // Tensor-core kernel (bf16 or 4-bit weights, bf16 activations)
 // ------------------------------------------------------------------------------------------------
 #ifndef DFL_RING_AFTER
-#define DFL_RING_AFTER 0   // where the ring's remaining stages are requested (see the kernel)
+#define DFL_RING_AFTER 1   // where the ring's remaining stages are requested (see the kernel)
 #endif
 
 template <int FMT, int NT, int EPI>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const __grid_constant__ GemvArgs a) {
   using XT = __half;
+  constexpr int kWarps = gemv_warps(NT);   // shadows the NT = 1 default
+  constexpr int kGemvThreads = kWarps * 32;
   constexpr int GS = FMT == FMT_Q4 ? kQ4GroupsPerStage : kBf16GroupsPerStage;
   constexpr int GB = FMT == FMT_Q4 ? kQ4GroupBytes : kBf16GroupBytes;
   constexpr int RP = NT * 8;
@@ -682,7 +686,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
         *reinterpret_cast<float4*>(part + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
     } else {
       EpiPre<NT> pre;
-      epi_preload<EPI, NT>(a, a.strip0 + strip_local, pre);
+      epi_preload<EPI, NT, XT>(a, a.strip0 + strip_local, pre);
       strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr, pre);
     }
   };
@@ -871,7 +875,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_tc_kernel(const __grid_c
       last_mask &= last_mask - 1;
       const int strip_local = sbeg + si0 + kWarps * j;
       EpiPre<NT> pre;   // issued with the partial loads below: one round trip for both
-      epi_preload<EPI, NT>(a, a.strip0 + strip_local, pre);
+      epi_preload<EPI, NT, XT>(a, a.strip0 + strip_local, pre);
       float y[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
@@ -954,7 +958,7 @@ __global__ void __launch_bounds__(kF32Warps * 32) gemv_f32_kernel(const __grid_c
       }
     }
     EpiPre<NT> pre;
-    epi_preload<EPI, NT>(a, strip, pre);
+    epi_preload<EPI, NT, float>(a, strip, pre);
     strip_epilogue<EPI, NT, float>(a, strip, y, srow, lm, 0, pre);
   }
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
@@ -974,7 +978,7 @@ cudaError_t launch_gemv_fmt_nt(int epi, const GemvArgs& a, int grid, size_t smem
         if (err != cudaSuccess) return err;                                                      \
         smem_set = (int)smem;                                                                    \
       }                                                                                          \
-      return launch_pdl(k, dim3(grid), dim3(kGemvThreads), smem, s, a);                          \
+      return launch_pdl(k, dim3(grid), dim3(gemv_warps(NT) * 32), smem, s, a);                   \
     }                                                                                            \
     return cudaGetLastError();                                                                   \
   }

@@ -48,7 +48,9 @@ constexpr int kStageBytes = kQ4GroupsPerStage * kQ4GroupBytes > kBf16GroupsPerSt
 constexpr int kMaxRows = 32;              // activation rows per launch (4 n-tiles of 8)
 constexpr int kXBudget = 112 * 1024;      // shared bytes for the staged activation slice
 constexpr int kMaxCtxChunk = 32;          // context rows per projection chunk
-constexpr int kGemvThreads = kWarps * 32;
+// Warps per tensor-core GEMV CTA by n-tile count: more activation columns need more registers
+// per thread (one CTA per SM, 64K registers).
+__host__ __device__ constexpr int gemv_warps(int nt) { return nt == 1 ? kWarps : (nt == 2 ? 12 : 8); }
 constexpr int kF32Warps = 8;
 
 enum Fmt { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q4 = 2 };
