@@ -48,7 +48,6 @@ struct dflash_handle {
   float* partials = nullptr;
   int* tickets = nullptr;
   float* lm_part = nullptr;
-  int* lm_ticket = nullptr;
   float* lm_strip = nullptr;
   float *att_o = nullptr, *att_ml = nullptr;
   int* att_tickets = nullptr;
@@ -241,7 +240,6 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->partials = cv.take<float>(std::max<size_t>(pf, 4) * 4);
   h->tickets = cv.take<int>((size_t)tk * 4);
   h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4);
-  h->lm_ticket = cv.take<int>(4);
   h->lm_strip = cv.take<float>((size_t)tk * kMaxRows * 3 * 4);
   // attention split partials: n_req * Hkv * splits stays below ~2 waves of CTAs (see draft)
   h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
@@ -358,19 +356,23 @@ size_t xw_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->L * kM
 // projections that feed the attention scores (Q, K, V of the block and of the context rows) is
 // amplified by the softmax; with those and gate-up covered, the rms logit error of the 4-bit
 // 5120-wide drafter drops by 30% at no measured cost. out_proj and the LM head do not need it.
+#ifndef DFL_ATTN_TILES_PER_SPLIT
+#define DFL_ATTN_TILES_PER_SPLIT 2
+#endif
 #ifndef DFL_LO_MASK
 #define DFL_LO_MASK 11
 #endif
 enum { LO_QKV = 1, LO_GU = 2, LO_LM = 4, LO_CTXKV = 8, LO_OUTPROJ = 16 };
 long long lo_if(int bit, size_t off) { return (DFL_LO_MASK & bit) ? (long long)off : 0; }
 
-int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
+int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out = nullptr) {
   const PackedMat& m = *c.m;
   const int strips = c.n_strips < 0 ? m.n_strips : c.n_strips;
   if (c.R <= 0 || strips <= 0) return DFLASH_OK;
   if (h->act_f32) c.x_lo_off = 0;
   const int grp = h->act_f32 ? 1 : std::max(1, c.grp_n);
   const GemvPlan p = plan_gemv(h, strips, m.groups, c.R, c.x_lo_off != 0, std::max(1, h->n_sm / grp));
+  if (plan_out) *plan_out = p;
   GemvArgs a{};
   a.w = m.w;
   a.grp_n = grp;
@@ -404,7 +406,6 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s) {
   a.e = c.e;
   if (c.epi == EPI_LMHEAD) {
     a.e.lm_part = h->lm_part;
-    a.e.lm_ticket = h->lm_ticket;
     a.e.lm_strip = h->lm_strip;
   }
   h->launches++;
@@ -760,10 +761,10 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         h->launches++;
         if ((st = status_of(launch_attn_f32(aa, s)))) return st;
       } else {
-        // about two 64-key tiles per split, up to two CTAs per SM
+        // about DFL_ATTN_TILES_PER_SPLIT 64-key tiles per split, up to two CTAs per SM
         const int pairs = n_req * c.n_kv_heads;
         int splits = std::max(1, (2 * h->n_sm + pairs - 1) / pairs);
-        splits = std::min(splits, std::max(1, (max_tiles + 1) / 2));
+        splits = std::min(splits, std::max(1, (max_tiles + DFL_ATTN_TILES_PER_SPLIT - 1) / DFL_ATTN_TILES_PER_SPLIT));
         splits = std::max(1, std::min(std::min(splits, 64), h->att_pairs_max / pairs));
         aa.n_splits = splits;
         h->launches++;
@@ -879,9 +880,14 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     cl.e.logits = logits ? logits + (size_t)l0 * h->V : nullptr;
     cl.e.vocab = h->V;
     cl.e.rows_per_req = n;
-    cl.e.tok_out = draft + l0;
-    cl.e.conf_out = conf ? conf + l0 : nullptr;
-    if ((st = run_gemv(h, cl, s))) return st;
+    GemvPlan lp{};
+    if ((st = run_gemv(h, cl, s, &lp))) return st;
+    // merge the per-CTA (one K slice) or per-strip (K split) vocab states: token and confidence
+    const bool split = h->fmt != FMT_F32 && lp.n_slices > 1;
+    h->launches++;
+    if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part, split ? h->lm.n_strips : lp.grid, R,
+                                         draft + l0, conf ? conf + l0 : nullptr, s))))
+      return st;
   }
   if (h->probe_stop) cudaEventRecord(h->probe_stop, s);
   h->probe_start = h->probe_stop = nullptr;
@@ -922,7 +928,7 @@ int dflash_check_errors(dflash_handle* h, void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpy(h->err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(h->tickets, 0, (size_t)h->ticket_count * 4) != cudaSuccess ||
-        cudaMemset(h->lm_ticket, 0, 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        cudaDeviceSynchronize() != cudaSuccess)
       return DFLASH_ECUDA;
     return DFLASH_ETIMEOUT;
   }

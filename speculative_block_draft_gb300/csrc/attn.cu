@@ -24,7 +24,8 @@ namespace dfl {
 
 namespace {
 
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 8;   // two groups of four m-tile warps, each taking half of every key tile
+constexpr int kGroupWarps = 4;
 constexpr int kTileKeys = 64;
 constexpr int kSub = 64 * 128;     // one 64-row x 128-byte swizzled sub-tile
 constexpr int kBlkSub = 16 * 128;  // one 16-row x 128-byte swizzled sub-tile
@@ -36,7 +37,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in
 // S[nb] for NKEY keys: Q rows of this warp's m-tile against the key tile.
 template <int HD, int NKEY>
 __device__ __forceinline__ void qk_tile(uint32_t q_base, uint32_t k_base, int sub_bytes, int mt, int lane,
-                                        float (&S)[NKEY / 8][4]) {
+                                        float (&S)[NKEY / 8][4], int key0 = 0) {
 #pragma unroll
   for (int nb = 0; nb < NKEY / 8; nb++)
 #pragma unroll
@@ -52,7 +53,7 @@ __device__ __forceinline__ void qk_tile(uint32_t q_base, uint32_t k_base, int su
     }
 #pragma unroll
     for (int nb = 0; nb < NKEY / 8; nb += 2) {
-      const int key = nb * 8 + (lane & 7) + ((lane >> 4) << 3);
+      const int key = key0 + nb * 8 + (lane & 7) + ((lane >> 4) << 3);
       const int chunk = chunk0 + ((lane >> 3) & 1);
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(k_base + sub * sub_bytes + swz(key, chunk), b0, b1, b2, b3);
@@ -62,10 +63,11 @@ __device__ __forceinline__ void qk_tile(uint32_t q_base, uint32_t k_base, int su
   }
 }
 
+// nvalid counts from key0 (the first of the NKEY keys of this call)
 template <int HD, int NKEY>
 __device__ __forceinline__ void softmax_pv(float (&S)[NKEY / 8][4], int nvalid, float scale_log2, uint32_t v_base,
                                            int sub_bytes, int lane, float (&m_run)[2], float (&l_run)[2],
-                                           float (&O)[HD / 8][4]) {
+                                           float (&O)[HD / 8][4], int key0 = 0) {
   const int t = lane & 3;
   float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -114,7 +116,7 @@ __device__ __forceinline__ void softmax_pv(float (&S)[NKEY / 8][4], int nvalid, 
     const uint32_t a3 = pack_f16x2(S[2 * kb + 1][2], S[2 * kb + 1][3]);
 #pragma unroll
     for (int nd = 0; nd < HD / 8; nd += 2) {
-      const int key = kb * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int key = key0 + kb * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
       const int col8 = nd + (lane >> 4);  // 8-element column block of head_dim
       const int sub = col8 / 8, chunk = col8 % 8;
       uint32_t b0, b1, b2, b3;
@@ -245,7 +247,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
   __syncthreads();
 
   const int n_mt = (M + 15) / 16;
-  const bool active = warp < n_mt;
+  const int mt = warp % kGroupWarps, kg = warp / kGroupWarps;   // m-tile, key half
+  const bool active = mt < n_mt;
   float O[HD / 8][4];
 #pragma unroll
   for (int nd = 0; nd < HD / 8; nd++)
@@ -264,10 +267,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     int slot0, nv;
     tile_info(tb + i, slot0, nv);
     if (active) {
+      constexpr int kHalf = kTileKeys / 2;
       const uint32_t ks = smem_u32(stage_s + (i & 1) * 2 * NSUB * kSub);
-      float S[kTileKeys / 8][4];
-      qk_tile<HD, kTileKeys>(q_base, ks, kSub, warp, lane, S);
-      softmax_pv<HD, kTileKeys>(S, nv, a.scale_log2, ks + NSUB * kSub, kSub, lane, m_run, l_run, O);
+      float S[kHalf / 8][4];
+      qk_tile<HD, kHalf>(q_base, ks, kSub, mt, lane, S, kg * kHalf);
+      softmax_pv<HD, kHalf>(S, nv - kg * kHalf, a.scale_log2, ks + NSUB * kSub, kSub, lane, m_run, l_run, O,
+                            kg * kHalf);
     }
     __syncthreads();
     if (threadIdx.x == 0 && i + 2 < n_tiles) issue(i + 2);
@@ -278,9 +283,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
         mbar_wait_bounded(smem_u32(&bars[i & 1]), (i >> 1) & 1, nullptr, 0);
     return;
   }
-  if (with_block && active) {
+  if (with_block && active && kg == 0) {
     float S[2][4];
-    qk_tile<HD, 16>(q_base, smem_u32(bk_s), kBlkSub, warp, lane, S);
+    qk_tile<HD, 16>(q_base, smem_u32(bk_s), kBlkSub, mt, lane, S);
     softmax_pv<HD, 16>(S, a.gamma, a.scale_log2, smem_u32(bv_s), kBlkSub, lane, m_run, l_run, O);
   }
 #pragma unroll
@@ -288,13 +293,48 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
+  // merge the two key halves: group 1 parks (O, m, l) in the free stage buffers, group 0 folds
+  // them into its own state (the stage buffers hold at least 4 warps x 32 lanes x (HD/2 + 4) floats)
+  {
+    constexpr int kPer = HD / 2 + 4;
+    float* park = reinterpret_cast<float*>(stage_s) + ((size_t)mt * 32 + lane) * kPer;
+    __syncthreads();   // every warp is done with the last tile
+    if (kg == 1 && active) {
+#pragma unroll
+      for (int nd = 0; nd < HD / 8; nd++)
+        *reinterpret_cast<float4*>(park + nd * 4) = make_float4(O[nd][0], O[nd][1], O[nd][2], O[nd][3]);
+      *reinterpret_cast<float4*>(park + HD / 2) = make_float4(m_run[0], m_run[1], l_run[0], l_run[1]);
+    }
+    __syncthreads();
+    if (kg == 0 && active) {
+      const float4 ml = *reinterpret_cast<const float4*>(park + HD / 2);
+      const float mo[2] = {ml.x, ml.y}, lo[2] = {ml.z, ml.w};
+      float sa[2], sb[2];
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        const float mn = fmaxf(m_run[h], mo[h]);
+        sa[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - mn);
+        sb[h] = mo[h] == -INFINITY ? 0.f : exp2f(mo[h] - mn);
+        m_run[h] = mn;
+        l_run[h] = l_run[h] * sa[h] + lo[h] * sb[h];
+      }
+#pragma unroll
+      for (int nd = 0; nd < HD / 8; nd++) {
+        const float4 v = *reinterpret_cast<const float4*>(park + nd * 4);
+        O[nd][0] = O[nd][0] * sa[0] + v.x * sb[0];
+        O[nd][1] = O[nd][1] * sa[0] + v.y * sb[0];
+        O[nd][2] = O[nd][2] * sa[1] + v.z * sb[1];
+        O[nd][3] = O[nd][3] * sa[1] + v.w * sb[1];
+      }
+    }
+  }
 
   __half* out = static_cast<__half*>(a.out);
   if (a.n_splits == 1) {
-    if (active) {
+    if (active && kg == 0) {
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        const int i = warp * 16 + g + 8 * h;
+        const int i = mt * 16 + g + 8 * h;
         if (i >= M) continue;
         const int head = kvh * grp + i / a.gamma, k = i % a.gamma;
         const float inv = 1.0f / l_run[h];
@@ -310,10 +350,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
   // split partials (unnormalised O, running max m and sum l, base 2); attn_merge_kernel combines them
   const int pair = b * a.hkv + kvh;
   const size_t pidx = (size_t)pair * a.n_splits + split;
-  if (active) {
+  if (active && kg == 0) {
 #pragma unroll
     for (int h = 0; h < 2; h++) {
-      const int i = warp * 16 + g + 8 * h;
+      const int i = mt * 16 + g + 8 * h;
       float* po = a.part_o + (pidx * 64 + i) * HD;
 #pragma unroll
       for (int nd = 0; nd < HD / 8; nd++)

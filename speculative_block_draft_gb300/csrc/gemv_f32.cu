@@ -20,6 +20,46 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo) {
   return b;
 }
 
+// Final vocab reduction: one CTA per activation row merges n_parts states (stride kMaxRows rows
+// apart): thread j takes parts j, j + blockDim, ... in order (eight loads in flight), then a
+// pairwise tree; the order is fixed, so the result is reproducible. Writes the greedy token and
+// the softmax probability of that token.
+__global__ void __launch_bounds__(256) lm_reduce_kernel(const float* __restrict__ parts, int n_parts,
+                                                        int32_t* tok_out, float* conf_out) {
+  __shared__ LmState sm[256];
+  const int c = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  LmState acc{-INFINITY, 0.f, 0x7fffffff};
+  for (int b0 = threadIdx.x; b0 < n_parts; b0 += 8 * blockDim.x) {
+    LmState o[8];
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const int b = b0 + q * blockDim.x;
+      const float* src = parts + ((size_t)b * kMaxRows + c) * 3;
+      o[q] = b < n_parts ? LmState{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))}
+                         : LmState{-INFINITY, 0.f, 0x7fffffff};
+    }
+#pragma unroll
+    for (int q = 0; q < 8; q++) lm_merge(acc, o[q]);
+  }
+  sm[threadIdx.x] = acc;
+  __syncthreads();
+  for (int off = blockDim.x / 2; off > 0; off >>= 1) {
+    if ((int)threadIdx.x < off) lm_merge(sm[threadIdx.x], sm[threadIdx.x + off]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    tok_out[c] = sm[0].i;
+    if (conf_out) conf_out[c] = 1.0f / sm[0].s;
+  }
+}
+
+cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t* tok_out, float* conf_out,
+                             cudaStream_t s) {
+  return launch_pdl(lm_reduce_kernel, dim3(rows), dim3(256), 0, s, parts, n_parts, tok_out, conf_out);
+}
+
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s) {
   const size_t smem = gemv_smem_bytes(fmt, a.R, a.gps, a.x_lo_off != 0);
   switch (fmt) {

@@ -335,50 +335,14 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
   }
 }
 
-// Split-K head: the last CTA merges the per-strip states of each column with a fixed order
-// (thread j takes strips j, j + blockDim, ...; then a pairwise tree). Needs blockDim <= 256 and
-// scratch for blockDim states.
-__device__ __forceinline__ void lm_finish_split(const GemvArgs& a, LmState* sm) {
-  const EpiArgs& e = a.e;
-  __syncthreads();
-  __shared__ int last_split;
-  if (threadIdx.x == 0) last_split = atom_add_acq_rel_gpu(e.lm_ticket, 1) == (int)gridDim.x - 1;
-  __syncthreads();
-  if (!last_split) return;
-  for (int c = 0; c < a.R; c++) {
-    LmState acc{-INFINITY, 0.f, 0x7fffffff};
-    for (int j = threadIdx.x; j < a.n_strips; j += blockDim.x) {
-      const float* src = e.lm_strip + ((size_t)j * kMaxRows + c) * 3;
-      LmState o{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))};
-      lm_merge(acc, o);
-    }
-    sm[threadIdx.x] = acc;
-    __syncthreads();
-    int span = 1;
-    while (span < (int)blockDim.x) span <<= 1;
-    for (int off = span / 2; off > 0; off >>= 1) {
-      if ((int)threadIdx.x < off && (int)threadIdx.x + off < (int)blockDim.x)
-        lm_merge(sm[threadIdx.x], sm[threadIdx.x + off]);
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-      e.tok_out[c] = sm[0].i;
-      if (e.conf_out) e.conf_out[c] = 1.0f / sm[0].s;
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) *e.lm_ticket = 0;
-}
-
-// Vocab reduction of the LM-head epilogue: lanes -> warps -> CTA partial -> last CTA.
+// Vocab reduction of the LM-head epilogue, GEMV side: lanes -> warps -> one (max, sum, index)
+// state per CTA and column in e.lm_part (one K slice), or nothing more when K is split (the
+// epilogue already wrote one state per strip to e.lm_strip). lm_reduce_kernel merges them.
 template <int NT>
 __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2], LmState* sm_lm) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int nw = blockDim.x >> 5;
-  if (a.n_slices > 1) {
-    lm_finish_split(a, sm_lm);
-    return;
-  }
+  if (a.n_slices > 1) return;
 #pragma unroll
   for (int nt = 0; nt < NT; nt++)
 #pragma unroll
@@ -407,44 +371,6 @@ __device__ __forceinline__ void lm_finish(const GemvArgs& a, LmState (&lm)[NT][2
     dst[1] = acc.s;
     dst[2] = __int_as_float(acc.i);
   }
-  __syncthreads();
-  __shared__ int last;
-  if (threadIdx.x == 0) last = atom_add_acq_rel_gpu(e.lm_ticket, 1) == (int)gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  // last CTA: thread j of row c merges CTAs j, j + P, j + 2P, ... (P threads per row), then a
-  // pairwise tree per row; the order is fixed, so the result is reproducible.
-  const int P = max(1, (int)blockDim.x / a.R);
-  int span = 1;
-  while (span < P) span <<= 1;
-  const int c = threadIdx.x / P, j = threadIdx.x % P;
-  LmState acc{-INFINITY, 0.f, 0x7fffffff};
-  if (c < a.R) {
-    for (int b0 = j; b0 < (int)gridDim.x; b0 += 4 * P) {
-      LmState o[4];
-#pragma unroll
-      for (int q = 0; q < 4; q++) {
-        const int b = b0 + q * P;
-        const float* src = e.lm_part + ((size_t)b * kMaxRows + c) * 3;
-        o[q] = b < (int)gridDim.x ? LmState{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))}
-                                  : LmState{-INFINITY, 0.f, 0x7fffffff};
-      }
-#pragma unroll
-      for (int q = 0; q < 4; q++) lm_merge(acc, o[q]);
-    }
-  }
-  __syncthreads();
-  sm_lm[threadIdx.x] = acc;
-  __syncthreads();
-  for (int off = span / 2; off > 0; off >>= 1) {
-    if (c < a.R && j < off && j + off < P) lm_merge(sm_lm[threadIdx.x], sm_lm[threadIdx.x + off]);
-    __syncthreads();
-  }
-  if (c < a.R && j == 0) {
-    e.tok_out[c] = sm_lm[threadIdx.x].i;
-    if (e.conf_out) e.conf_out[c] = 1.0f / sm_lm[threadIdx.x].s;
-  }
-  if (threadIdx.x == 0) *e.lm_ticket = 0;
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -85,8 +85,8 @@ struct EpiArgs {
   // EPI_SWIGLU
   void* act; int inter;
   // EPI_LMHEAD
-  float* logits; int vocab; int rows_per_req; int32_t* tok_out; float* conf_out;
-  float* lm_part; int* lm_ticket;
+  float* logits; int vocab; int rows_per_req;
+  float* lm_part;    // one K slice: per-CTA (max, sum, index) per column, merged by lm_reduce_kernel
   float* lm_strip;   // split-K launches: per-strip (max, sum, index) per column, merged in strip order
 };
 
@@ -181,6 +181,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s);
+// Final greedy token + confidence per row from n_parts (max, sum, index) states kMaxRows rows apart.
+cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t* tok_out, float* conf_out,
+                             cudaStream_t s);
 size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t s);
