@@ -153,6 +153,24 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
 int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* target,
                   int32_t* accept_len, int32_t* next_anchor, void* stream);
 
+/* Confidence-scheduled draft-length pruning ("Alg 1", single-user form, in the dflash.ts page's
+ * draft options): draft position k (0-based over the gamma-1 drafts) is dropped, and the block
+ * truncated there, when k >= 1 and conf[k] < thr_k, where thr_k = thresholds[k] if thresholds is
+ * given, else min_conf; position 0 is always kept. conf is dflash_draft_block's confidence (the
+ * softmax probability of the drafted token; the pages' learned acceptance head is not part of
+ * this library). conf: device float [n_req][gamma-1]; thresholds: device float [gamma-1] or NULL;
+ * min_conf: used only when thresholds is NULL (a value <= 0 keeps every position).
+ * Output: keep int32 [n_req] (device), 1 <= keep[i] <= gamma-1, the number of drafts the target
+ * verifies. Pruning never changes what is emitted, only how many positions are verified. */
+int dflash_draft_lengths(dflash_handle* h, int n_req, const float* conf, const float* thresholds,
+                         float min_conf, int32_t* keep, void* stream);
+
+/* Greedy acceptance over pruned blocks: as dflash_accept with accept_len capped at keep[i]
+ * (device int32 [n_req], from dflash_draft_lengths): accept_len = longest prefix with
+ * draft == target within the first keep[i] drafts; next_anchor = target[accept_len]. */
+int dflash_accept_kept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* keep,
+                       const int32_t* target, int32_t* accept_len, int32_t* next_anchor, void* stream);
+
 /* Forget a request slot's context (its length returns to 0). Host-only; no device work. */
 int dflash_reset_request(dflash_handle* h, int req_id);
 

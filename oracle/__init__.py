@@ -83,6 +83,10 @@ def _load():
         lib.orc_argmax_conf.argtypes = [vp, i32, vp, vp, vp]
         lib.orc_accept.restype = i32
         lib.orc_accept.argtypes = [i32, vp, vp, vp]
+        lib.orc_draft_length.restype = i32
+        lib.orc_draft_length.argtypes = [i32, vp, vp, ctypes.c_float]
+        lib.orc_accept_kept.restype = i32
+        lib.orc_accept_kept.argtypes = [i32, i32, vp, vp, vp]
         _lib = lib
     return _lib
 
@@ -162,6 +166,24 @@ def accept(draft, target):
     assert t.shape[0] == d.shape[0] + 1
     nxt = ctypes.c_int()
     a = _load().orc_accept(d.shape[0], _p(d), _p(t), ctypes.byref(nxt))
+    return a, nxt.value
+
+
+def draft_length(conf, thresholds=None, min_conf=0.0):
+    """Drafts kept by confidence-scheduled pruning (position 0 always; the first k >= 1 with
+    conf[k] < threshold ends the block). conf and thresholds are fp32, as the library takes them."""
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    th = None if thresholds is None else np.ascontiguousarray(thresholds, dtype=np.float32)
+    return _load().orc_draft_length(c.shape[0], _p(c), _p(th) if th is not None else None, float(min_conf))
+
+
+def accept_kept(draft, target, keep):
+    """(accepted length, next anchor) when only the first `keep` drafts are verified."""
+    d = np.ascontiguousarray(draft, dtype=np.int32)
+    t = np.ascontiguousarray(target, dtype=np.int32)
+    assert t.shape[0] == d.shape[0] + 1
+    nxt = ctypes.c_int()
+    a = _load().orc_accept_kept(d.shape[0], int(keep), _p(d), _p(t), ctypes.byref(nxt))
     return a, nxt.value
 
 

@@ -11,6 +11,8 @@
  *       and section 3 (bs=8 accepted=7 committed=8; accepted=5 committed=6).
  *  [P2] "A Refusal Is Not A Failure", section "What the port taught, besides that"
  *       (is_causal is false; the drafter borrows the target's embedding and output head).
+ *  [P3] also: DflashDraftOpts.thresholds / minConf and the drafting loop of forwardRows
+ *       (confidence-scheduled draft-length pruning, "Alg 1", single-user form).
  *
  * Readings where the pages leave a step open are stated at each function.
  * Everything is fp64; loops run in the order the definitions are written, each output's sum
@@ -258,6 +260,30 @@ int orc_draft(const orc_cfg* c, const orc_weights* w, int anchor, int n_ctx, con
 int orc_accept(int n, const int* draft, const int* target, int* next_anchor) {
   int a = 0;
   while (a < n && draft[a] == target[a]) a++;
+  *next_anchor = target[a];
+  return a;
+}
+
+/* Confidence-scheduled draft-length pruning ([P3], the draft options and the drafting loop of
+ * forwardRows): walking the drafts in order, position k >= 1 ends the block when its confidence
+ * is below its threshold -- thresholds[k] when a per-position list is given, otherwise min_conf;
+ * position 0 is always drafted. Returns the number of drafts kept (1..n). Reading: the
+ * confidence is the softmax probability of the drafted token (this drafter has no learned
+ * acceptance head), and "below" is the strict comparison the page writes. */
+int orc_draft_length(int n, const float* conf, const float* thresholds, float min_conf) {
+  for (int k = 1; k < n; k++) {
+    const float th = thresholds ? thresholds[k] : min_conf;
+    if (conf[k] < th) return k;
+  }
+  return n;
+}
+
+/* Acceptance over a pruned block: the target verifies only the first keep drafts, so the
+ * accepted length is the longest matching prefix within them and the bonus token is the
+ * target's token right after it. */
+int orc_accept_kept(int n, int keep, const int* draft, const int* target, int* next_anchor) {
+  int a = 0;
+  while (a < keep && a < n && draft[a] == target[a]) a++;
   *next_anchor = target[a];
   return a;
 }

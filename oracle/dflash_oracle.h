@@ -57,5 +57,7 @@ int orc_draft(const orc_cfg* c, const orc_weights* w, int anchor, int n_ctx, con
               double* trace);
 void orc_argmax_conf(const double* logits, int vocab, int* token, double* conf, double* margin);
 int orc_accept(int n, const int* draft, const int* target, int* next_anchor);
+int orc_draft_length(int n, const float* conf, const float* thresholds, float min_conf);
+int orc_accept_kept(int n, int keep, const int* draft, const int* target, int* next_anchor);
 
 #endif

@@ -96,7 +96,8 @@ _lib = None
 SYMBOLS = ["dflash_workspace_bytes", "dflash_create", "dflash_project_ctx", "dflash_draft_block",
            "dflash_accept", "dflash_reset_request", "dflash_ctx_len", "dflash_check_errors",
            "dflash_get_stats", "dflash_set_probe", "dflash_launch_count", "dflash_destroy",
-           "dflash_status_str", "dflash_greedy_from_logits_noalloc"]
+           "dflash_status_str", "dflash_greedy_from_logits_noalloc", "dflash_draft_lengths",
+           "dflash_accept_kept"]
 
 
 def lib():
@@ -136,6 +137,10 @@ def lib():
         L.dflash_status_str.argtypes = [i32]
         L.dflash_greedy_from_logits_noalloc.restype = i32
         L.dflash_greedy_from_logits_noalloc.argtypes = [vp, i32, i32, vp, vp, vp]
+        L.dflash_draft_lengths.restype = i32
+        L.dflash_draft_lengths.argtypes = [vp, i32, vp, vp, f32, vp, vp]
+        L.dflash_accept_kept.restype = i32
+        L.dflash_accept_kept.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -260,6 +265,18 @@ class Handle:
         return _check(lib().dflash_accept(self.h, draft.shape[0], draft.data_ptr(), target.data_ptr(),
                                           accept_len.data_ptr(), next_anchor.data_ptr(), _stream_ptr(stream)),
                       "dflash_accept")
+
+    def draft_lengths(self, conf, keep, thresholds=None, min_conf=0.0, stream=None) -> int:
+        """Confidence-scheduled pruning: keep[i] = drafts of request i the target verifies."""
+        return _check(lib().dflash_draft_lengths(self.h, conf.shape[0], conf.data_ptr(),
+                                                 thresholds.data_ptr() if thresholds is not None else None,
+                                                 float(min_conf), keep.data_ptr(), _stream_ptr(stream)),
+                      "dflash_draft_lengths")
+
+    def accept_kept(self, draft, keep, target, accept_len, next_anchor, stream=None) -> int:
+        return _check(lib().dflash_accept_kept(self.h, draft.shape[0], draft.data_ptr(), keep.data_ptr(),
+                                               target.data_ptr(), accept_len.data_ptr(), next_anchor.data_ptr(),
+                                               _stream_ptr(stream)), "dflash_accept_kept")
 
     def reset_request(self, req_id: int) -> int:
         return _check(lib().dflash_reset_request(self.h, req_id), "dflash_reset_request")

@@ -903,7 +903,28 @@ int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32
   if (!draft || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->G - 1, draft, target, accept_len, next_anchor,
+  return status_of(launch_accept(n_req, h->G - 1, draft, nullptr, target, accept_len, next_anchor,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int dflash_draft_lengths(dflash_handle* h, int n_req, const float* conf, const float* thresholds, float min_conf,
+                         int32_t* keep, void* stream) {
+  if (!h || n_req < 0) return DFLASH_EINVAL;
+  if (n_req == 0) return DFLASH_OK;
+  if (!conf || !keep || min_conf != min_conf) return DFLASH_EINVAL;
+  h->launches++;
+  return status_of(launch_draft_lengths(n_req, h->G - 1, conf, thresholds, min_conf, keep,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int dflash_accept_kept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* keep, const int32_t* target,
+                       int32_t* accept_len, int32_t* next_anchor, void* stream) {
+  if (!h || n_req < 0) return DFLASH_EINVAL;
+  if (n_req == 0) return DFLASH_OK;
+  if (!draft || !keep || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
+  h->launches++;
+  h->stats.accept_calls++;
+  return status_of(launch_accept(n_req, h->G - 1, draft, keep, target, accept_len, next_anchor,
                                  static_cast<cudaStream_t>(stream)));
 }
 

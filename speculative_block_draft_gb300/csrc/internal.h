@@ -193,7 +193,9 @@ cudaError_t launch_attn_f32(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s);
 cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s);
-cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* target,
+cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
                           int32_t* accept_len, int32_t* next_anchor, cudaStream_t s);
+cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
+                                 int32_t* keep, cudaStream_t s);
 
 }  // namespace dfl

@@ -163,21 +163,44 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant
 }
 
 // One warp per request: first mismatch via ballot.
-__global__ void accept_kernel(int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
-                              int32_t* next_anchor) {
+// keep (nullable): per request, only the first keep[b] drafts are verified (pruned blocks).
+__global__ void accept_kernel(int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
+                              int32_t* accept_len, int32_t* next_anchor) {
   const int b = blockIdx.x, lane = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();
-  const bool miss = lane < n && draft[(size_t)b * n + lane] != target[(size_t)b * (n + 1) + lane];
+  const int cap = keep ? min(max(keep[b], 0), n) : n;   // clamped: no read outside target's row
+  const bool miss = lane < cap && draft[(size_t)b * n + lane] != target[(size_t)b * (n + 1) + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
-  const int acc = mask ? __ffs(mask) - 1 : n;
+  const int acc = mask ? __ffs(mask) - 1 : cap;
   if (lane == 0) {
     accept_len[b] = acc;
     next_anchor[b] = target[(size_t)b * (n + 1) + acc];
   }
 }
 
+// Draft-length pruning: one warp per request; the first position k >= 1 whose confidence is
+// below its threshold ends the block.
+__global__ void draft_lengths_kernel(int n, const float* conf, const float* thresholds, float min_conf,
+                                     int32_t* keep) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  bool drop = false;
+  if (lane >= 1 && lane < n) {
+    const float th = thresholds ? thresholds[lane] : min_conf;
+    drop = conf[(size_t)b * n + lane] < th;
+  }
+  const unsigned mask = __ballot_sync(0xffffffffu, drop);
+  if (lane == 0) keep[b] = mask ? __ffs(mask) - 1 : n;
+}
+
 }  // namespace
+
+cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
+                                 int32_t* keep, cudaStream_t s) {
+  return launch_pdl(draft_lengths_kernel, dim3(n_req), dim3(32), 0, s, n, conf, thresholds, min_conf, keep);
+}
 
 cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s) {
   repack_kernel<<<1024, 256, 0, s>>>(a);
@@ -195,9 +218,9 @@ cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
   return launch_pdl(embed_gather_kernel<__half>, dim3(a.n_req), dim3(256), 0, s, a);
 }
 
-cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* target, int32_t* accept_len,
-                          int32_t* next_anchor, cudaStream_t s) {
-  return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, target, accept_len, next_anchor);
+cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
+                          int32_t* accept_len, int32_t* next_anchor, cudaStream_t s) {
+  return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, keep, target, accept_len, next_anchor);
 }
 
 }  // namespace dfl

@@ -68,6 +68,27 @@ class Session:
         self.stream.synchronize()
         return al.cpu().numpy(), na.cpu().numpy()
 
+    def draft_lengths(self, conf: np.ndarray, thresholds: np.ndarray | None = None, min_conf: float = 0.0):
+        c = self.upload(np.asarray(conf, dtype=np.float32))
+        th = self.upload(np.asarray(thresholds, dtype=np.float32)) if thresholds is not None else None
+        keep = torch.empty(c.shape[0], dtype=torch.int32, device=self.device)
+        with torch.cuda.stream(self.stream):
+            self.h.draft_lengths(c, keep, thresholds=th, min_conf=min_conf, stream=self.stream)
+        self.stream.synchronize()
+        return keep.cpu().numpy()
+
+    def accept_kept(self, draft: np.ndarray, keep: np.ndarray, target: np.ndarray):
+        d = self.upload(np.asarray(draft, dtype=np.int32))
+        k = self.upload(np.asarray(keep, dtype=np.int32))
+        t = self.upload(np.asarray(target, dtype=np.int32))
+        nr = d.shape[0]
+        al = torch.empty(nr, dtype=torch.int32, device=self.device)
+        na = torch.empty(nr, dtype=torch.int32, device=self.device)
+        with torch.cuda.stream(self.stream):
+            self.h.accept_kept(d, k, t, al, na, stream=self.stream)
+        self.stream.synchronize()
+        return al.cpu().numpy(), na.cpu().numpy()
+
     def check(self):
         return self.h.check_errors(stream=self.stream)
 

@@ -122,6 +122,51 @@ def test_accept_kernel_exhaustive_vs_oracle():
     s.close()
 
 
+def test_draft_lengths_and_kept_accept_vs_oracle():
+    """Confidence-scheduled pruning and capped acceptance, bit-exact (integer results; the same
+    fp32 confidences and thresholds go to both sides), gamma 8 and 16, per-position thresholds
+    and the uniform minConf, with exact ties."""
+    import oracle
+    from speculative_block_draft_gb300.session import Session
+    rng = np.random.default_rng(11)
+    for gamma in (8, 16):
+        cfg = small(f"s_prune{gamma}", gamma=gamma)
+        s = Session(syn.make_model(cfg), max_batch=1)
+        n, B = gamma - 1, 2048
+        conf = rng.random((B, n)).astype(np.float32)
+        th = (rng.random(n) * 0.5).astype(np.float32)
+        conf[:64, 1] = th[1]                          # ties keep the position
+        for thresholds, min_conf in ((th, 0.0), (None, 0.3), (None, 0.0), (None, 1.5)):
+            keep = s.draft_lengths(conf, thresholds, min_conf)
+            for i in range(B):
+                assert keep[i] == oracle.draft_length(conf[i], thresholds, min_conf)
+        keep = s.draft_lengths(conf, th)
+        d = rng.integers(0, 3, size=(B, n)).astype(np.int32)
+        t = rng.integers(0, 3, size=(B, n + 1)).astype(np.int32)
+        a, nxt = s.accept_kept(d, keep, t)
+        for i in range(B):
+            assert (a[i], nxt[i]) == oracle.accept_kept(d[i], t[i], keep[i])
+        s.close()
+
+
+def test_pruning_on_drafted_confidence():
+    """The pruning step on a real round: confidences from dflash_draft_block decide the kept
+    lengths exactly as the oracle decides them from the same fp32 values."""
+    import oracle
+    from speculative_block_draft_gb300.session import Session
+    cfg = small("s_prune_round", gamma=8, ctx_len=40, batch=4)
+    s = Session(syn.make_model(cfg, norm_jitter=0.1), max_batch=4)
+    for b in range(4):
+        assert s.project([b], [40], syn.taps_rows(cfg, cfg.seed, b, 0, 40)) == 0
+    out = s.draft([0, 1, 2, 3], syn.anchors(cfg.seed, 4, 0, cfg.vocab), logits=False)
+    conf = out["conf"]
+    mid = float(np.median(conf[:, 1:]))
+    keep = s.draft_lengths(conf, None, mid)
+    for i in range(4):
+        assert keep[i] == oracle.draft_length(conf[i], None, mid)
+    s.close()
+
+
 def test_abi_errors_and_decline(monkeypatch):
     import speculative_block_draft_gb300 as pkg
     from speculative_block_draft_gb300.session import Session

@@ -385,3 +385,52 @@ def test_session_window_trim_matches_full_history():
         s.project(0, t[a:b])
     kc, vc = o.ctx_rows(t)
     assert np.array_equal(s.draft(0, 6)["logits"], o.draft(6, kc, vc)["logits"])
+
+
+# ------------------------------------------------------------------------------------------
+# confidence-scheduled draft-length pruning (dflash.ts page: draft options, forwardRows loop)
+# ------------------------------------------------------------------------------------------
+def test_draft_length_page_rules():
+    """Hand cases of the page's rule: position 0 is always drafted; the first later position
+    whose confidence is below its threshold ends the block; a per-position list takes
+    precedence over the uniform minConf; the comparison is strict."""
+    L = oracle.draft_length
+    assert L([0.0, 0.9, 0.9, 0.9], min_conf=0.5) == 4          # position 0 kept even at 0
+    assert L([0.9, 0.9, 0.2, 0.9], min_conf=0.5) == 2          # truncated at the first low one
+    assert L([0.9, 0.1, 0.9, 0.9], min_conf=0.5) == 1
+    assert L([0.9, 0.5, 0.5, 0.5], min_conf=0.5) == 4          # equal is kept (strict <)
+    assert L([0.9, 0.6, 0.3, 0.3], thresholds=[0.99, 0.7, 0.1, 0.1], min_conf=0.0) == 1
+    assert L([0.9, 0.6, 0.3, 0.3], thresholds=[0.99, 0.5, 0.2, 0.4], min_conf=0.95) == 3
+    assert L([0.9, 0.01, 0.0, 0.0], min_conf=0.0) == 4         # minConf 0 keeps everything
+    assert L([0.9], min_conf=0.99) == 1                        # a one-draft block
+
+
+def test_draft_length_invariants():
+    """1 <= keep <= n; raising one threshold never lengthens the block; lowering every
+    threshold to 0 keeps all n; keep is the first drop position of the brute-force scan."""
+    rng = np.random.default_rng(5)
+    for _ in range(2000):
+        n = int(rng.integers(1, 16))
+        conf = rng.random(n).astype(np.float32)
+        th = rng.random(n).astype(np.float32) * 0.6
+        k = oracle.draft_length(conf, th)
+        assert 1 <= k <= n
+        drops = [j for j in range(1, n) if conf[j] < th[j]]
+        assert k == (drops[0] if drops else n)
+        j = int(rng.integers(0, n))
+        th2 = th.copy()
+        th2[j] = min(1.0, th2[j] + 0.3)
+        assert oracle.draft_length(conf, th2) <= k
+        assert oracle.draft_length(conf, np.zeros(n, np.float32)) == n
+
+
+def test_accept_kept_is_capped_acceptance():
+    """Verifying only the first keep drafts: accepted = min(unpruned accepted, keep), and the
+    bonus token is the target's token right after the accepted prefix (exhaustive, n <= 5)."""
+    for n in range(1, 6):
+        for d in itertools.product((0, 1), repeat=n):
+            for t in itertools.product((0, 1), repeat=n + 1):
+                a_full, _ = oracle.accept(np.array(d, dtype=np.int32), np.array(t, dtype=np.int32))
+                for keep in range(1, n + 1):
+                    a, nxt = oracle.accept_kept(np.array(d, dtype=np.int32), np.array(t, dtype=np.int32), keep)
+                    assert a == min(a_full, keep) and nxt == t[a]
