@@ -24,6 +24,7 @@ struct PackedMat {
 
 struct GemvPlan {
   int n_slices, gps, ctas_per_slice, grid;
+  int cluster2 = 0, cpart_cap = 0;   // 2-way K split inside 2-CTA clusters
 };
 
 }  // namespace
@@ -77,7 +78,14 @@ int nt_for(int R) { return R <= 8 ? 1 : (R <= 16 ? 2 : 4); }
 // Split of one launch over the SMs. Every warp of a CTA works on every strip of that CTA, so the
 // time of a launch is about (strips per CTA) x (groups per K slice); a K split over several
 // CTAs costs a partial tile per strip, counted here as one extra group.
-GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int x_lo, int n_sm) {
+#ifndef DFL_CLUSTER_SPLIT
+#define DFL_CLUSTER_SPLIT 1
+#endif
+
+// allow_cluster: the launch may split K in two inside 2-CTA clusters (partials meet in shared
+// memory through the cluster instead of global memory and tickets); lm: the LM-head epilogue.
+GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int x_lo, int n_sm,
+                   int allow_cluster = 0, int lm = 0) {
   GemvPlan p{};
   if (h->fmt == FMT_F32) {
     p.n_slices = 1;
@@ -90,7 +98,7 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int 
   long best = -1;
   for (int s = 1; s <= std::max(1, std::min(16, groups / gemv_warps(nt_for(R)))); s++) {
     const int gps = (groups + s - 1) / s;
-    if (gemv_smem_bytes(h->fmt, R, gps, x_lo) > kSmemLimit) continue;
+    if (gemv_smem_bytes(h->fmt, R, gps, x_lo, lm, 0) > kSmemLimit) continue;
     const int slices = (groups + gps - 1) / gps;
     const int ctas = std::max(1, std::min(n_strips, n_sm / slices));
     const long per_cta = (n_strips + ctas - 1) / ctas;
@@ -104,12 +112,27 @@ GemvPlan plan_gemv(const dflash_handle* h, int n_strips, int groups, int R, int 
   }
   if (best < 0) {  // the activation slice must shrink further: split K until it fits
     int gps = groups;
-    while (gps > 1 && gemv_smem_bytes(h->fmt, R, gps, x_lo) > kSmemLimit) gps = (gps + 1) / 2;
+    while (gps > 1 && gemv_smem_bytes(h->fmt, R, gps, x_lo, lm, 0) > kSmemLimit) gps = (gps + 1) / 2;
     p.gps = gps;
     p.n_slices = (groups + gps - 1) / gps;
     p.ctas_per_slice = std::max(1, std::min(n_strips, n_sm / p.n_slices));
   }
   p.grid = p.n_slices * p.ctas_per_slice;
+  if (DFL_CLUSTER_SPLIT && allow_cluster && groups >= 2 && n_sm >= 2 && n_strips >= 2) {
+    // two slices per 2-CTA cluster: taken when it fits and costs at most a little more streaming
+    // than the best plan (it saves the split-K round trips at the end)
+    const int gps2 = (groups + 1) / 2, pairs = std::min(n_sm / 2, n_strips);
+    const int cap = (n_strips + pairs - 1) / pairs, cap_even = (cap + 1) & ~1;
+    const long cost2 = (long)cap * gps2;
+    if (gemv_smem_bytes(h->fmt, R, gps2, x_lo, lm, cap_even) <= kSmemLimit && (best < 0 || cost2 * 100 <= best * 115)) {
+      p.n_slices = 2;
+      p.gps = gps2;
+      p.ctas_per_slice = pairs;
+      p.grid = 2 * pairs;
+      p.cluster2 = 1;
+      p.cpart_cap = cap_even;
+    }
+  }
   return p;
 }
 
@@ -206,7 +229,7 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   auto consider = [&](const PackedMat& m, int strips) {
     for (int r : {8, 16, 32})
       for (int lo : {0, 1}) {
-        const GemvPlan p = plan_gemv(h, strips, m.groups, r, lo, h->n_sm);
+        const GemvPlan p = plan_gemv(h, strips, m.groups, r, lo, h->n_sm, 0, &m == &h->lm);
         if (p.n_slices > 1) pf = std::max(pf, (size_t)strips * p.n_slices * 32 * nt_for(r) * 4);
         lmg = std::max(lmg, p.grid);
       }
@@ -371,7 +394,8 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out =
   if (c.R <= 0 || strips <= 0) return DFLASH_OK;
   if (h->act_f32) c.x_lo_off = 0;
   const int grp = h->act_f32 ? 1 : std::max(1, c.grp_n);
-  const GemvPlan p = plan_gemv(h, strips, m.groups, c.R, c.x_lo_off != 0, std::max(1, h->n_sm / grp));
+  const GemvPlan p = plan_gemv(h, strips, m.groups, c.R, c.x_lo_off != 0, std::max(1, h->n_sm / grp),
+                               !h->act_f32 && c.epi != EPI_LMHEAD, c.epi == EPI_LMHEAD);
   if (plan_out) *plan_out = p;
   GemvArgs a{};
   a.w = m.w;
@@ -379,6 +403,8 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out =
   a.grp_ctas = p.grid;
   a.grp_w_stride = c.grp_w_stride;
   a.grp_x_stride = c.grp_x_stride;
+  a.cluster2 = p.cluster2;
+  a.cpart_cap = p.cpart_cap;
   a.x_colscale = h->act_f32 ? nullptr : c.x_colscale;
   a.x_colscale_grp_stride = c.x_colscale_grp_stride;
   a.strip0 = c.strip0;

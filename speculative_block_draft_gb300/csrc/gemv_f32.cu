@@ -6,7 +6,7 @@ namespace dfl {
 cudaError_t launch_gemv_q4(int epi, int nt, const GemvArgs& a, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemv_bf16(int epi, int nt, const GemvArgs& a, int grid, size_t smem, cudaStream_t s);
 
-size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo) {
+size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap) {
   if (fmt == FMT_F32) return 0;
   const int rp = R <= 8 ? 8 : (R <= 16 ? 16 : 32);
   const int w = gemv_warps(rp / 8);
@@ -14,8 +14,9 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo) {
   b += (size_t)rp * (gps * 128 + 16) * (x_lo ? 2 : 1); // activation slice (and its f16 remainder)
   if (fmt == FMT_Q4) b += (size_t)rp * gps * 4;        // per-group activation sums
   b += kMaxRows * 4;                                   // row scales
-  b += (size_t)w * kMaxRows * sizeof(LmState);         // vocab reduction scratch
+  if (lm) b += (size_t)w * kMaxRows * sizeof(LmState); // vocab reduction scratch (LM head)
   b += (size_t)2 * w * 32 * (rp / 2) * 4;              // split-strip pieces (2 per warp x 32 lanes x NT*4)
+  b += (size_t)cpart_cap * 32 * (rp / 2) * 4;          // cluster K split: partial tiles
   b += 16 + (1 + w * kStages) * 8;                     // mbarriers
   return b;
 }
@@ -61,7 +62,8 @@ cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t*
 }
 
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s) {
-  const size_t smem = gemv_smem_bytes(fmt, a.R, a.gps, a.x_lo_off != 0);
+  const size_t smem = gemv_smem_bytes(fmt, a.R, a.gps, a.x_lo_off != 0, epi == EPI_LMHEAD,
+                                     a.cluster2 ? a.cpart_cap : 0);
   switch (fmt) {
     case FMT_Q4: return launch_gemv_q4(epi, nt, a, grid, smem, s);
     case FMT_BF16: return launch_gemv_bf16(epi, nt, a, grid, smem, s);

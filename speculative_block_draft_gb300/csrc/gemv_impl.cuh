@@ -397,7 +397,9 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
   const uint8_t* Wb = a.w + (size_t)lyr * a.grp_w_stride;
   const uint8_t* Xb = static_cast<const uint8_t*>(a.x) + (size_t)lyr * a.grp_x_stride * 2;
   const int sgl = lyr * a.n_strips;   // this problem's strips in the partials and tickets
-  const int slice = bid / a.ctas_per_slice, cis = bid % a.ctas_per_slice;
+  // slices of a 2-CTA cluster are neighbouring blocks (slice = rank in the cluster)
+  const int slice = a.cluster2 ? (bid & 1) : bid / a.ctas_per_slice;
+  const int cis = a.cluster2 ? (bid >> 1) : bid % a.ctas_per_slice;
   const int gbeg = slice * a.gps, gend = min(a.groups, gbeg + a.gps), ng = gend - gbeg;
   const int sbeg = (int)((long long)cis * a.n_strips / a.ctas_per_slice);
   const int send = (int)((long long)(cis + 1) * a.n_strips / a.ctas_per_slice);
@@ -412,8 +414,9 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
   float* srow = xsum + (FMT == FMT_Q4 ? RP * a.gps : 0);
   LmState* sm_lm = reinterpret_cast<LmState*>(srow + kMaxRows);
   float* red = reinterpret_cast<float*>(sm_lm + (EPI == EPI_LMHEAD ? kWarps * kMaxRows : 0));
+  float* cpart = red + 2 * kWarps * 32 * NT4;   // cluster K split: [strip pair][slice] partial tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(red + 2 * kWarps * 32 * NT4) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(cpart + (a.cluster2 ? a.cpart_cap * 32 * NT4 : 0)) + 15) & ~uintptr_t(15));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 1 + kWarps * kStages; i++) mbar_init(smem_u32(&bars[i]), 1);
@@ -605,7 +608,21 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
 
   // a finished strip: epilogue now, or publish this CTA's partial of a K-split strip
   auto finish = [&](int strip_local, float (&y)[NT][4]) {
-    if (a.n_slices > 1) {
+    if (a.cluster2) {
+      // strip j of the pair's range is reduced by CTA (j & 1); its two slice partials sit side by
+      // side in that CTA's shared memory, written locally or through the cluster
+      const int j = strip_local - sbeg, owner = j & 1;
+      float* slot = cpart + ((size_t)((j >> 1) * 2 + slice) * 32 + lane) * NT4;
+      if (owner == slice) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+          *reinterpret_cast<float4*>(slot + nt * 4) = make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+      } else {
+        const uint32_t remote = map_shared_rank(smem_u32(slot), (uint32_t)owner);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) st_cluster_v4(remote + nt * 16, make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]));
+      }
+    } else if (a.n_slices > 1) {
       float* part = a.partials + (((size_t)(sgl + strip_local) * a.n_slices + slice) * 32 + lane) * NT4;
 #pragma unroll
       for (int nt = 0; nt < NT; nt++)
@@ -791,7 +808,31 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
     }
   }
 
-  if (ok && a.n_slices > 1) {
+  if (a.cluster2) {
+    // both CTAs of the pair reach this barrier on every path (a CTA that gave up still arrives),
+    // so neither can wait for a partner that left
+    EpiPre<NT> pre;
+    const int o0 = warp;
+    if (2 * o0 + slice < n_cta) epi_preload<EPI, NT, XT>(a, a.strip0 + sbeg + 2 * o0 + slice, pre);
+    cluster_sync();
+    for (int o = o0; ok && 2 * o + slice < n_cta; o += kWarps) {
+      const int strip_local = sbeg + 2 * o + slice;
+      if (o != o0) epi_preload<EPI, NT, XT>(a, a.strip0 + strip_local, pre);
+      const float* p0 = cpart + ((size_t)(o * 2 + 0) * 32 + lane) * NT4;
+      const float* p1 = cpart + ((size_t)(o * 2 + 1) * 32 + lane) * NT4;
+      float y[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; nt++) {   // slice 0 + slice 1, in that order
+        const float4 u = *reinterpret_cast<const float4*>(p0 + nt * 4);
+        const float4 v = *reinterpret_cast<const float4*>(p1 + nt * 4);
+        y[nt][0] = u.x + v.x;
+        y[nt][1] = u.y + v.y;
+        y[nt][2] = u.z + v.z;
+        y[nt][3] = u.w + v.w;
+      }
+      strip_epilogue<EPI, NT, XT>(a, a.strip0 + strip_local, y, srow, lm, lyr, pre);
+    }
+  } else if (ok && a.n_slices > 1) {
     // every partial of this CTA is written (by whichever warp finished the strip) before any
     // ticket is taken; the last slice to arrive at a strip sums all slices in slice order and
     // runs the epilogue
@@ -911,7 +952,7 @@ cudaError_t launch_gemv_fmt_nt(int epi, const GemvArgs& a, int grid, size_t smem
         if (err != cudaSuccess) return err;                                                      \
         smem_set = (int)smem;                                                                    \
       }                                                                                          \
-      return launch_pdl(k, dim3(grid), dim3(gemv_warps(NT) * 32), smem, s, a);                   \
+      return launch_pdl_cluster(k, dim3(grid), dim3(gemv_warps(NT) * 32), smem, s, a.cluster2 ? 2 : 1, a); \
     }                                                                                            \
     return cudaGetLastError();                                                                   \
   }

@@ -97,6 +97,9 @@ struct GemvArgs {
   // one problem.
   int grp_n, grp_ctas;
   long long grp_w_stride, grp_x_stride;
+  // K split over a 2-CTA cluster (n_slices == 2): blockIdx pairs are the two slices of the same
+  // strips; partials meet in the owning CTA's shared memory (cpart_cap strip slots per CTA).
+  int cluster2, cpart_cap;
   int strip0, n_strips;    // strip range of this launch
   int k, groups;           // inputs and 64-input groups
   int n_slices, gps;       // K slices per strip, groups per slice
@@ -160,23 +163,36 @@ struct BlockArgs {
 // Launch with programmatic stream serialization: the kernel may start while the previous kernel
 // of the stream drains; it must call pdl_wait() before reading anything earlier kernels wrote.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args&&... args) {
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t s, int cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-#ifdef DFL_NO_PDL
-  cfg.numAttrs = 0;
-#else
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+#ifndef DFL_NO_PDL
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  n++;
 #endif
+  if (cluster_x > 1) {   // grid.x must be a multiple of cluster_x
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    n++;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, s, 1, std::forward<Args>(args)...);
 }
 
 // ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
@@ -184,7 +200,7 @@ cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, c
 // Final greedy token + confidence per row from n_parts (max, sum, index) states kMaxRows rows apart.
 cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t* tok_out, float* conf_out,
                              cudaStream_t s);
-size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo);
+size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t s);
 size_t attn_smem_bytes(int hd);
