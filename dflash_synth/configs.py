@@ -30,6 +30,7 @@ class DraftConfig:
     adtype: str = "bf16"  # 'f32' | 'bf16'        (taps, context K/V cache, activations)
     eps: float = 1e-6
     agree: float | None = None    # synthetic target agreement rate (None: uniform tokens)
+    ffn: str = "swiglu"           # gated FFN: "swiglu" silu(g)*u, or "gelu" (tanh-form GELU)*u
     append_min: int = 0           # new context rows per request per round (0,0: gamma rows)
     append_max: int = 0
     ctx_min: int = 0              # ragged contexts: P uniform in [ctx_min, ctx_len] (0: fixed)

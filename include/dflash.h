@@ -60,12 +60,13 @@ enum dflash_status {
 };
 
 enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_Q4G64 = 2 };
+enum dflash_ffn { DFLASH_FFN_SWIGLU = 0, DFLASH_FFN_GELU = 1 };
 
 typedef struct {
   int n_layers;       /* drafter layers L (<= DFLASH_MAX_LAYERS) */
   int d;              /* draft width; n_q_heads * head_dim == d */
   int n_q_heads, n_kv_heads, head_dim;   /* head_dim in {64, 128, 256}; n_q_heads % n_kv_heads == 0 */
-  int inter;          /* SwiGLU inner width */
+  int inter;          /* gated FFN inner width */
   int n_taps;         /* m tapped target layers */
   int target_hidden;  /* H; tok_proj / out_proj exist iff d != H */
   int vocab;          /* V */
@@ -81,6 +82,9 @@ typedef struct {
                          wdtype DFLASH_F32). DFLASH_BF16: bf16 taps; internally the tensor-core
                          path runs f16 activations and an f16 context cache with fp32
                          accumulation (bf16 weights are stored as f16 in the workspace). */
+  int ffn_act;        /* FFN gate: DFLASH_FFN_SWIGLU silu(g) * u (the workload's MLP), or
+                         DFLASH_FFN_GELU gelu(g) * u with the tanh approximation of GELU (the
+                         gated-GELU FFN of the dflash.ts page, "geluApprox") */
 } dflash_config;
 
 typedef struct {

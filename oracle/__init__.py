@@ -45,7 +45,7 @@ def build(force: bool = False) -> str:
 class Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter",
                                              "n_taps", "target_hidden", "vocab", "gamma", "window")] + \
-               [("eps", ctypes.c_double), ("causal", ctypes.c_int)]
+               [("eps", ctypes.c_double), ("causal", ctypes.c_int), ("ffn_act", ctypes.c_int)]
 
 
 class Mat(ctypes.Structure):
@@ -83,6 +83,8 @@ def _load():
         lib.orc_argmax_conf.argtypes = [vp, i32, vp, vp, vp]
         lib.orc_accept.restype = i32
         lib.orc_accept.argtypes = [i32, vp, vp, vp]
+        lib.orc_gelu_tanh.restype = ctypes.c_double
+        lib.orc_gelu_tanh.argtypes = [ctypes.c_double]
         lib.orc_draft_length.restype = i32
         lib.orc_draft_length.argtypes = [i32, vp, vp, ctypes.c_float]
         lib.orc_accept_kept.restype = i32
@@ -143,6 +145,12 @@ def silu(x: float) -> float:
     return _load().orc_silu(float(x))
 
 
+def gelu_tanh(x):
+    """GELU in its tanh approximation, elementwise, fp64."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    return np.array([_load().orc_gelu_tanh(float(v)) for v in a.ravel()]).reshape(a.shape)
+
+
 def attention(q, k, v, n_q_heads: int, n_kv_heads: int, head_dim: int, causal_block_start: int = -1):
     q, k, v = _f64(q), _f64(k), _f64(v)
     out = np.empty_like(q)
@@ -200,7 +208,8 @@ class Oracle:
         self.model = model
         self._vecs = {k: np.ascontiguousarray(v, dtype=np.float32) for k, v in model.vecs.items()}
         self.c = Cfg(c.n_layers, c.d, c.n_q_heads, c.n_kv_heads, c.head_dim, c.inter, c.n_taps,
-                     c.target_hidden, c.vocab, c.gamma, c.window, c.eps, 1 if causal else 0)
+                     c.target_hidden, c.vocab, c.gamma, c.window, c.eps, 1 if causal else 0,
+                     1 if getattr(c, "ffn", "swiglu") == "gelu" else 0)
         w = Weights()
         mats = model.mats
         w.w_c = _mat(mats["W_c"])

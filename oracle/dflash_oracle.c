@@ -73,6 +73,13 @@ void orc_rmsnorm(const double* x, const float* w, int n, double eps, double* y) 
 /* SiLU(x) = x / (1 + e^-x): the gate activation of the SwiGLU feed-forward. */
 double orc_silu(double x) { return x / (1.0 + exp(-x)); }
 
+/* The gated-GELU FFN of the dflash.ts page applies "geluApprox" to the gate. Reading: the tanh
+ * approximation of GELU (Hendrycks and Gimpel), 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))). */
+double orc_gelu_tanh(double x) {
+  const double k = sqrt(2.0 / 3.14159265358979323846);
+  return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+}
+
 /* Scaled dot-product attention of [P3] Eq 3 with grouped K/V heads:
  * q [n_q_rows][Hq*hd], k/v [n_keys][Hkv*hd], out [n_q_rows][Hq*hd].
  * Query head h reads key/value head h / (Hq/Hkv) (contiguous groups).
@@ -229,7 +236,8 @@ int orc_draft(const orc_cfg* c, const orc_weights* w, int anchor, int n_ctx, con
       orc_rmsnorm(hd + (int64_t)k * d, L->ff_norm, d, c->eps, nd + (int64_t)k * d);
     orc_linear(&L->w_gate, G, nd, gate);
     orc_linear(&L->w_up, G, nd, up);
-    for (int64_t j = 0; j < (int64_t)G * c->inter; j++) gate[j] = orc_silu(gate[j]) * up[j];
+    for (int64_t j = 0; j < (int64_t)G * c->inter; j++)
+      gate[j] = (c->ffn_act ? orc_gelu_tanh(gate[j]) : orc_silu(gate[j])) * up[j];
     orc_linear(&L->w_down, G, gate, tmp);
     for (int64_t j = 0; j < (int64_t)G * d; j++) hd[j] += tmp[j];
   }

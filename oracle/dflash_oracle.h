@@ -23,6 +23,7 @@ typedef struct {
   double eps;
   int causal;   /* 0 = the method (non-causal block). 1 only for the test that shows the
                    difference a causal mask would make. */
+  int ffn_act;  /* 0 = SwiGLU silu(g) * u; 1 = gated GELU gelu(g) * u (tanh approximation) */
 } orc_cfg;
 
 typedef struct {
@@ -47,6 +48,7 @@ double orc_weight(const orc_mat* m, int n, int k);
 void orc_linear(const orc_mat* m, int rows, const double* x, double* y);
 void orc_rmsnorm(const double* x, const float* w, int n, double eps, double* y);
 double orc_silu(double x);
+double orc_gelu_tanh(double x);
 void orc_attention(int n_q_rows, int n_q_heads, int n_kv_heads, int head_dim, const double* q,
                    int n_keys, const double* k, const double* v, int causal_block_start,
                    double* out);

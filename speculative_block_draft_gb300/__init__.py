@@ -70,7 +70,7 @@ class dflash_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter", "n_taps", "target_hidden", "vocab",
         "gamma", "window", "max_batch", "ctx_capacity")] + \
-        [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int)]
+        [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int), ("ffn_act", ctypes.c_int)]
 
 
 class dflash_matrix(ctypes.Structure):
@@ -178,6 +178,9 @@ def _int_array(xs):
     return arr
 
 
+FFN = {"swiglu": 0, "gelu": 1}
+
+
 def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = None) -> dflash_config:
     """dflash_config for a dflash_synth.DraftConfig."""
     mb = max_batch or cfg.batch
@@ -185,7 +188,7 @@ def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = No
         ctx_capacity = cfg.window if cfg.window > 0 else cfg.ctx_len + 64 * cfg.gamma
     return dflash_config(cfg.n_layers, cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.inter, cfg.n_taps,
                          cfg.target_hidden, cfg.vocab, cfg.gamma, cfg.window, mb, ctx_capacity, cfg.eps,
-                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype])
+                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn])
 
 
 class DeviceModel:

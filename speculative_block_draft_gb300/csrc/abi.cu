@@ -160,6 +160,7 @@ bool valid_config(const dflash_config* c) {
   if (c->window < 0 || c->max_batch < 1 || c->max_batch > DFLASH_MAX_BATCH || c->ctx_capacity < 1) return false;
   if (c->window > 0 && c->ctx_capacity < c->window) return false;
   if (!(c->eps >= 0.f)) return false;
+  if (c->ffn_act != DFLASH_FFN_SWIGLU && c->ffn_act != DFLASH_FFN_GELU) return false;
   if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
   if (c->adtype == DFLASH_F32) {
     if (c->wdtype != DFLASH_F32) return false;
@@ -822,7 +823,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     }
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
-      // a = SiLU(W_gate n2) * (W_up n2), n2 = RMSNorm_ff_i(H_d)
+      // a = act(W_gate n2) * (W_up n2), n2 = RMSNorm_ff_i(H_d); act = SiLU or GELU (tanh form)
       GemvCall cg;
       cg.m = &h->gu[i];
       cg.R = nb * G;
@@ -838,6 +839,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cg.e.n_rows = 2 * h->I;
       cg.e.act = off(h->act, r0, h->I);
       cg.e.inter = h->I;
+      cg.e.ffn_act = c.ffn_act;
       if ((st = run_gemv(h, cg, s))) return st;
     }
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {

@@ -215,8 +215,12 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
       } else if constexpr (EPI == EPI_SWIGLU) {
         const int j = strip * 8 + g;
         if (cv && j < e.inter) {
-          const float silu = ya / (1.0f + __expf(-ya));
-          store_act<XT>(e.act, (size_t)c * e.inter + j, silu * yb);
+          float g_act;
+          if (e.ffn_act == DFLASH_FFN_GELU)   // tanh approximation: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+            g_act = 0.5f * ya * (1.0f + tanhf(0.7978845608028654f * fmaf(0.044715f * ya, ya * ya, ya)));
+          else
+            g_act = ya / (1.0f + __expf(-ya));
+          store_act<XT>(e.act, (size_t)c * e.inter + j, g_act * yb);
         }
       } else if constexpr (EPI == EPI_LMHEAD) {
         // Which CTA finishes a split strip varies between runs, so split launches keep one

@@ -82,8 +82,8 @@ struct EpiArgs {
   long long kv_grp_stride;   // bytes between the caches of consecutive layers (grouped launches)
   int kv_slot[kMaxRows];
   int kv_pos[kMaxRows];
-  // EPI_SWIGLU
-  void* act; int inter;
+  // EPI_SWIGLU (gated FFN: silu(g) * u, or gelu_tanh(g) * u when ffn_act == DFLASH_FFN_GELU)
+  void* act; int inter; int ffn_act;
   // EPI_LMHEAD
   float* logits; int vocab; int rows_per_req;
   float* lm_part;    // one K slice: per-CTA (max, sum, index) per column, merged by lm_reduce_kernel

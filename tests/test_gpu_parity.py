@@ -66,6 +66,19 @@ def test_small_formats_and_head_dims(wdtype, hd):
     run(cfg, rounds=2)
 
 
+@pytest.mark.parametrize("wdtype", ["q4", "bf16", "f32"])
+def test_small_gated_gelu_ffn(wdtype):
+    """The page's gated-GELU FFN (tanh-form GELU on the gate) instead of SwiGLU."""
+    kw = dict(adtype="f32") if wdtype == "f32" else {}
+    run(small(f"s_gelu_{wdtype}", wdtype=wdtype, ffn="gelu", d=512, target_hidden=512, inter=1024,
+              n_q_heads=8, n_kv_heads=2, **kw), rounds=2)
+
+
+def test_small_mha_no_gqa():
+    """Multi-head attention without grouping (one K/V head per query head)."""
+    run(small("s_mha", n_q_heads=8, n_kv_heads=8, head_dim=64, d=512, target_hidden=512, inter=1024), rounds=2)
+
+
 def test_small_d_ne_h_bf16():
     """tok_proj / out_proj present (d != H)."""
     run(small("s_proj", wdtype="bf16", target_hidden=512), rounds=2)

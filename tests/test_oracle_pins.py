@@ -358,6 +358,32 @@ def test_swiglu_ffn_vs_torch():
     assert np.allclose(out["trace"][1], ref.numpy(), atol=1e-13)
 
 
+def test_gelu_tanh_vs_torch():
+    """The gated-GELU gate: GELU in its tanh approximation, against torch's
+    gelu(approximate="tanh")."""
+    x = np.linspace(-8, 8, 4001)
+    ref = torch.nn.functional.gelu(torch.tensor(x, dtype=torch.float64), approximate="tanh").numpy()
+    assert np.allclose(oracle.gelu_tanh(x), ref, rtol=0, atol=1e-14)
+
+
+def test_gated_gelu_ffn_vs_torch():
+    """The page's gated-GELU FFN: with W_o = 0 a layer adds W_down (gelu(W_gate n) * W_up n),
+    n = RMSNorm(H_d; ff_norm), the gate through GELU's tanh form (torch's), the up path linear."""
+    cfg = syn.with_overrides(tiny(L=1), ffn="gelu")
+    m = model(cfg)
+    m.mats["bb.0.o"].data[:] = 0
+    o = oracle.Oracle(m)
+    out = o.draft(1, *o.ctx_rows(taps(cfg, 2)), trace=True)
+    h0 = torch.tensor(out["trace"][0])
+    n = torch.tensor(np.stack([_rms(out["trace"][0][r], m.vecs["bb.0.ff_norm"], cfg.eps) for r in range(cfg.gamma)]))
+    g = n @ torch.tensor(_raw(m.mats["bb.0.gate"])).T
+    u = n @ torch.tensor(_raw(m.mats["bb.0.up"])).T
+    ref = h0 + (torch.nn.functional.gelu(g, approximate="tanh") * u) @ torch.tensor(_raw(m.mats["bb.0.down"])).T
+    assert np.allclose(out["trace"][1], ref.numpy(), atol=1e-13)
+    silu = oracle.Oracle(syn.HostModel(syn.with_overrides(cfg, ffn="swiglu"), m.mats, m.vecs))
+    assert not np.allclose(silu.draft(1, *silu.ctx_rows(taps(cfg, 2)))["logits"], out["logits"], atol=1e-9)
+
+
 @pytest.mark.parametrize("wdtype", ["bf16", "q4"])
 def test_stored_formats_equal_their_dense_f32_copy(wdtype):
     """A drafter stored as bf16 / 4-bit gives the same logits as the f32 drafter holding the
