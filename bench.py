@@ -212,7 +212,7 @@ def oracle_round_seconds(cfg, model, rounds: int = 1, scale_rows: int = 1):
         part = dflash_synth.HostMatrix(hm.fmt, rows, hm.n_in, hm.data[:rows],
                                        None if hm.scale is None else hm.scale[:rows],
                                        None if hm.bias is None else hm.bias[:rows])
-        nrow = n_new if name == "W_c" else (G - 1 if name in ("lm_head", "out_proj") else G)
+        nrow = n_new if name == "W_c" else (cfg.n_draft if name in ("lm_head", "out_proj") else G)
         if name not in xs or xs[name].shape != (nrow, hm.n_in):
             xs[name] = syn.normal(cfg.seed, "bench.x", (nrow, hm.n_in), 1.0).astype(np.float64)
         oracle.linear(part, xs[name])
@@ -300,7 +300,7 @@ def main():
 
     # ---- drafter, context, per-step inputs resident in HBM -----------------------------------
     model = syn.make_model(cfg)
-    B, G, n = cfg.batch, cfg.gamma, cfg.gamma - 1
+    B, G, n = cfg.batch, cfg.gamma, cfg.n_draft
     sess = Session(model, max_batch=B, ctx_capacity=(cfg.window if cfg.window else
                                                       cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + 8)))
     h, stream = sess.h, sess.stream

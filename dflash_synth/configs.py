@@ -31,6 +31,7 @@ class DraftConfig:
     eps: float = 1e-6
     agree: float | None = None    # synthetic target agreement rate (None: uniform tokens)
     ffn: str = "swiglu"           # gated FFN: "swiglu" silu(g)*u, or "gelu" (tanh-form GELU)*u
+    draft_all_rows: bool = False  # draft from all gamma block rows (gamma tokens), not rows 1..gamma-1
     append_min: int = 0           # new context rows per request per round (0,0: gamma rows)
     append_max: int = 0
     ctx_min: int = 0              # ragged contexts: P uniform in [ctx_min, ctx_len] (0: fixed)
@@ -38,7 +39,7 @@ class DraftConfig:
 
     @property
     def n_draft(self) -> int:
-        return self.gamma - 1
+        return self.gamma if self.draft_all_rows else self.gamma - 1
 
     def appends(self) -> tuple[int, int]:
         if self.append_max:

@@ -9,7 +9,7 @@
  *   dflash_draft_block  the block pass: block rows (anchor embedding + block_pos, mask_emb + block_pos),
  *                       the Eq 3 KV-injection layers (non-causal attention of the block over
  *                       [windowed context ++ block], SwiGLU MLP), out_norm, the borrowed target LM head,
- *                       greedy token and softmax confidence for block rows 1..gamma-1.
+ *                       greedy token and softmax confidence of the drafting rows (1..gamma-1).
  *   dflash_accept       greedy acceptance: longest prefix of drafts equal to the target's greedy
  *                       tokens; the bonus token becomes the next anchor ("Inco Hacks Native: DFlash 2
  *                       Speculation", section 3: bs=8 accepted=7 committed=8).
@@ -70,7 +70,7 @@ typedef struct {
   int n_taps;         /* m tapped target layers */
   int target_hidden;  /* H; tok_proj / out_proj exist iff d != H */
   int vocab;          /* V */
-  int gamma;          /* block size (2..DFLASH_MAX_GAMMA); gamma-1 drafts per block */
+  int gamma;          /* block size (2..DFLASH_MAX_GAMMA); n_draft drafts per block (below) */
   int window;         /* sliding window over context rows; 0 = the whole context */
   int max_batch;      /* request slots (<= DFLASH_MAX_BATCH) */
   int ctx_capacity;   /* context rows kept per request and layer. With window > 0 the cache is a
@@ -85,6 +85,9 @@ typedef struct {
   int ffn_act;        /* FFN gate: DFLASH_FFN_SWIGLU silu(g) * u (the workload's MLP), or
                          DFLASH_FFN_GELU gelu(g) * u with the tanh approximation of GELU (the
                          gated-GELU FFN of the dflash.ts page, "geluApprox") */
+  int draft_all_rows; /* 0: drafts from block rows 1..gamma-1 (n_draft = gamma-1, the DFlash2 block:
+                         one verify token + gamma-1 proposals); 1: from all gamma block rows
+                         (n_draft = gamma, the dflash.ts page's forwardRows) */
 } dflash_config;
 
 typedef struct {
@@ -142,29 +145,30 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
                        const void* taps, void* stream);
 
 /* Draft one block per request. req_ids: HOST [n_req]. anchor: device int32 [n_req], the last
- * committed token of each request. Outputs (device): draft int32 [n_req][gamma-1] (greedy tokens of
- * block rows 1..gamma-1), conf float [n_req][gamma-1] (softmax probability of the drafted token;
- * may be NULL), logits float [n_req][gamma-1][V] (may be NULL; written only when given).
+ * committed token of each request. Outputs (device): draft int32 [n_req][n_draft] (greedy tokens of
+ * the drafting rows: block rows 1..gamma-1, or all gamma rows with draft_all_rows), conf float
+ * [n_req][n_draft] (softmax probability of the drafted token; may be NULL), logits float
+ * [n_req][n_draft][V] (may be NULL; written only when given). n_draft = gamma-1+draft_all_rows.
  * Attention of each request reads its context rows [max(0, P - window), P) (all when window == 0)
  * and all gamma block rows, with no causal mask. temperature != 0 -> DFLASH_DECLINED. */
 int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, const int32_t* anchor,
                        float temperature, int32_t* draft, float* conf, float* logits, void* stream);
 
 /* Greedy acceptance for n_req requests (independent of any handle state except gamma).
- * draft int32 [n_req][gamma-1], target int32 [n_req][gamma] (the target's greedy tokens after
- * [anchor, d_1..d_{gamma-1}]). Outputs: accept_len int32 [n_req] = longest prefix with
+ * draft int32 [n_req][n_draft], target int32 [n_req][n_draft+1] (the target's greedy tokens after
+ * [anchor, d_1..d_{n_draft}]). Outputs: accept_len int32 [n_req] = longest prefix with
  * draft == target; next_anchor int32 [n_req] = target[accept_len]; accept_len + 1 tokens commit. */
 int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32_t* target,
                   int32_t* accept_len, int32_t* next_anchor, void* stream);
 
 /* Confidence-scheduled draft-length pruning ("Alg 1", single-user form, in the dflash.ts page's
- * draft options): draft position k (0-based over the gamma-1 drafts) is dropped, and the block
+ * draft options): draft position k (0-based over the n_draft drafts) is dropped, and the block
  * truncated there, when k >= 1 and conf[k] < thr_k, where thr_k = thresholds[k] if thresholds is
  * given, else min_conf; position 0 is always kept. conf is dflash_draft_block's confidence (the
  * softmax probability of the drafted token; the pages' learned acceptance head is not part of
- * this library). conf: device float [n_req][gamma-1]; thresholds: device float [gamma-1] or NULL;
+ * this library). conf: device float [n_req][n_draft]; thresholds: device float [n_draft] or NULL;
  * min_conf: used only when thresholds is NULL (a value <= 0 keeps every position).
- * Output: keep int32 [n_req] (device), 1 <= keep[i] <= gamma-1, the number of drafts the target
+ * Output: keep int32 [n_req] (device), 1 <= keep[i] <= n_draft, the number of drafts the target
  * verifies. Pruning never changes what is emitted, only how many positions are verified. */
 int dflash_draft_lengths(dflash_handle* h, int n_req, const float* conf, const float* thresholds,
                          float min_conf, int32_t* keep, void* stream);

@@ -45,7 +45,8 @@ def build(force: bool = False) -> str:
 class Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter",
                                              "n_taps", "target_hidden", "vocab", "gamma", "window")] + \
-               [("eps", ctypes.c_double), ("causal", ctypes.c_int), ("ffn_act", ctypes.c_int)]
+               [("eps", ctypes.c_double), ("causal", ctypes.c_int), ("ffn_act", ctypes.c_int),
+                ("draft_all_rows", ctypes.c_int)]
 
 
 class Mat(ctypes.Structure):
@@ -209,7 +210,7 @@ class Oracle:
         self._vecs = {k: np.ascontiguousarray(v, dtype=np.float32) for k, v in model.vecs.items()}
         self.c = Cfg(c.n_layers, c.d, c.n_q_heads, c.n_kv_heads, c.head_dim, c.inter, c.n_taps,
                      c.target_hidden, c.vocab, c.gamma, c.window, c.eps, 1 if causal else 0,
-                     1 if getattr(c, "ffn", "swiglu") == "gelu" else 0)
+                     1 if getattr(c, "ffn", "swiglu") == "gelu" else 0, 1 if getattr(c, "draft_all_rows", False) else 0)
         w = Weights()
         mats = model.mats
         w.w_c = _mat(mats["W_c"])
@@ -245,11 +246,11 @@ class Oracle:
         return k, v
 
     def draft(self, anchor: int, k_ctx: np.ndarray, v_ctx: np.ndarray, trace: bool = False):
-        """One block: logits [gamma-1][V], tokens, conf, margin (top1 - top2), optional trace."""
+        """One block: logits [n_draft][V], tokens, conf, margin (top1 - top2), optional trace."""
         c = self.cfg
         n_ctx = k_ctx.shape[1]
         k_ctx, v_ctx = _f64(k_ctx), _f64(v_ctx)
-        n = c.gamma - 1
+        n = c.n_draft
         logits = np.empty((n, c.vocab), dtype=np.float64)
         toks = np.empty(n, dtype=np.int32)
         conf = np.empty(n, dtype=np.float64)

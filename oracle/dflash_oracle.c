@@ -243,18 +243,19 @@ int orc_draft(const orc_cfg* c, const orc_weights* w, int anchor, int n_ctx, con
   }
   if (trace) memcpy(trace + (int64_t)c->n_layers * G * d, hd, sizeof(double) * (size_t)G * d);
 
-  /* rows 1..gamma-1 through the output norm (and out_proj), then the borrowed head */
-  for (int k = 1; k < G; k++)
-    orc_rmsnorm(hd + (int64_t)k * d, w->out_norm, d, c->eps, nd + (int64_t)(k - 1) * d);
+  /* the drafting rows (1..gamma-1, or all gamma rows: the dflash.ts page's forwardRows drafts a
+   * token from every block row) through the output norm (and out_proj), then the borrowed head */
+  const int r0 = c->draft_all_rows ? 0 : 1, nrow = G - r0;
+  for (int k = r0; k < G; k++)
+    orc_rmsnorm(hd + (int64_t)k * d, w->out_norm, d, c->eps, nd + (int64_t)(k - r0) * d);
   if (d != H) {
-    orc_linear(&w->out_proj, G - 1, nd, tmp);
-    orc_linear(&w->lm_head, G - 1, tmp, logits);
+    orc_linear(&w->out_proj, nrow, nd, tmp);
+    orc_linear(&w->lm_head, nrow, tmp, logits);
   } else {
-    orc_linear(&w->lm_head, G - 1, nd, logits);
+    orc_linear(&w->lm_head, nrow, nd, logits);
   }
-  for (int k = 1; k < G; k++)
-    orc_argmax_conf(logits + (int64_t)(k - 1) * V, V, tokens + (k - 1), conf + (k - 1),
-                    margin + (k - 1));
+  for (int k = 0; k < nrow; k++)
+    orc_argmax_conf(logits + (int64_t)k * V, V, tokens + k, conf + k, margin + k);
 
   free(hd); free(nd); free(q); free(keys); free(vals); free(att); free(tmp);
   free(gate); free(up); free(e);

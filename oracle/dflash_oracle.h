@@ -24,6 +24,8 @@ typedef struct {
   int causal;   /* 0 = the method (non-causal block). 1 only for the test that shows the
                    difference a causal mask would make. */
   int ffn_act;  /* 0 = SwiGLU silu(g) * u; 1 = gated GELU gelu(g) * u (tanh approximation) */
+  int draft_all_rows;  /* 0 = drafts from block rows 1..gamma-1 (gamma-1 tokens); 1 = from all
+                          gamma rows (gamma tokens) */
 } orc_cfg;
 
 typedef struct {

@@ -70,7 +70,8 @@ class dflash_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter", "n_taps", "target_hidden", "vocab",
         "gamma", "window", "max_batch", "ctx_capacity")] + \
-        [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int), ("ffn_act", ctypes.c_int)]
+        [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int), ("ffn_act", ctypes.c_int),
+         ("draft_all_rows", ctypes.c_int)]
 
 
 class dflash_matrix(ctypes.Structure):
@@ -188,7 +189,7 @@ def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = No
         ctx_capacity = cfg.window if cfg.window > 0 else cfg.ctx_len + 64 * cfg.gamma
     return dflash_config(cfg.n_layers, cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.inter, cfg.n_taps,
                          cfg.target_hidden, cfg.vocab, cfg.gamma, cfg.window, mb, ctx_capacity, cfg.eps,
-                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn])
+                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn], 1 if cfg.draft_all_rows else 0)
 
 
 class DeviceModel:

@@ -33,6 +33,7 @@ struct dflash_handle {
   dflash_config cfg;
   int fmt = 0, act_f32 = 0, act_bytes = 2;
   int d = 0, H = 0, qd = 0, kvd = 0, I = 0, L = 0, G = 0, V = 0, mH = 0, cap = 0;
+  int nd = 0;   // drafts per block: gamma - 1, or gamma when drafting from every block row
   int n_sm = 148, r_blk = 0, ssq_ld = 0;
   size_t ws_bytes = 0;
 
@@ -161,6 +162,7 @@ bool valid_config(const dflash_config* c) {
   if (c->window > 0 && c->ctx_capacity < c->window) return false;
   if (!(c->eps >= 0.f)) return false;
   if (c->ffn_act != DFLASH_FFN_SWIGLU && c->ffn_act != DFLASH_FFN_GELU) return false;
+  if (c->draft_all_rows != 0 && c->draft_all_rows != 1) return false;
   if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
   if (c->adtype == DFLASH_F32) {
     if (c->wdtype != DFLASH_F32) return false;
@@ -287,6 +289,7 @@ void init_dims(dflash_handle* h, const dflash_config* c) {
   h->I = c->inter;
   h->L = c->n_layers;
   h->G = c->gamma;
+  h->nd = c->gamma - 1 + c->draft_all_rows;
   h->V = c->vocab;
   h->mH = c->n_taps * c->target_hidden;
   // ring rows: at least the requested capacity, a multiple of the 64-row attention tile
@@ -673,7 +676,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dflash_config& c = h->cfg;
   const size_t ab = h->act_bytes;
-  const int G = h->G, n = G - 1, d = h->d;
+  const int G = h->G, n = h->nd, d = h->d;   // n drafting rows per request: the last n block rows
   const int parts = h->ssq_ld;
   const size_t layer_cache = (size_t)c.max_batch * c.n_kv_heads * h->cap * c.head_dim * ab;
   auto off = [&](void* p, size_t rows, size_t width) -> void* {
@@ -863,7 +866,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     }
   }
 
-  // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (rows 1..gamma-1)
+  // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (drafting rows)
   const int lm_req_per_chunk = std::max(1, kMaxRows / n);
   if (h->probe_start) cudaEventRecord(h->probe_start, s);
   for (int b0 = 0; b0 < n_req; b0 += lm_req_per_chunk) {
@@ -879,7 +882,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cp.x = off(h->xn, r0, d);
       cp.ldx = d;
       cp.x_lo_off = lo_if(LO_OUTPROJ, xn_lo(h));
-      cp.xmap = RowMap{n, G, 1};
+      cp.xmap = RowMap{n, G, G - n};
       cp.norm_mode = NORM_ONE;
       cp.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
       cp.ssq_ld = h->ssq_ld;
@@ -896,7 +899,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cl.x = off(h->xn, r0, d);
       cl.ldx = d;
       cl.x_lo_off = lo_if(LO_LM, xn_lo(h));
-      cl.xmap = RowMap{n, G, 1};
+      cl.xmap = RowMap{n, G, G - n};
       cl.norm_mode = NORM_ONE;
       cl.ssq = h->ssq + (size_t)r0 * h->ssq_ld;
       cl.ssq_ld = h->ssq_ld;
@@ -931,7 +934,7 @@ int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32
   if (!draft || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->G - 1, draft, nullptr, target, accept_len, next_anchor,
+  return status_of(launch_accept(n_req, h->nd, draft, nullptr, target, accept_len, next_anchor,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -941,7 +944,7 @@ int dflash_draft_lengths(dflash_handle* h, int n_req, const float* conf, const f
   if (n_req == 0) return DFLASH_OK;
   if (!conf || !keep || min_conf != min_conf) return DFLASH_EINVAL;
   h->launches++;
-  return status_of(launch_draft_lengths(n_req, h->G - 1, conf, thresholds, min_conf, keep,
+  return status_of(launch_draft_lengths(n_req, h->nd, conf, thresholds, min_conf, keep,
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -952,7 +955,7 @@ int dflash_accept_kept(dflash_handle* h, int n_req, const int32_t* draft, const 
   if (!draft || !keep || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->G - 1, draft, keep, target, accept_len, next_anchor,
+  return status_of(launch_accept(n_req, h->nd, draft, keep, target, accept_len, next_anchor,
                                  static_cast<cudaStream_t>(stream)));
 }
 

@@ -55,7 +55,7 @@ class ClosedLoop:
 
     @property
     def n(self) -> int:
-        return self.s.cfg.gamma - 1
+        return self.s.cfg.n_draft
 
     def start(self, req: int, prompt_len: int, anchor: int):
         """A new request: its prompt's prompt_len positions are pending, anchor is its last token."""
@@ -118,7 +118,7 @@ class SyntheticTarget:
         self.p = (cfg.agree or 0.0) if agree is None else agree
 
     def verify(self, rnd: int, req: int, drafts) -> np.ndarray:
-        n = self.cfg.gamma - 1
+        n = self.cfg.n_draft
         d = np.asarray(drafts, dtype=np.int32)
         full = np.concatenate([d, np.zeros(n - d.shape[0], np.int32)]) if d.shape[0] < n else d
         t = self.syn.target_tokens(self.seed, req, rnd, full, self.p, self.cfg.vocab)

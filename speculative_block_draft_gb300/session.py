@@ -43,7 +43,7 @@ class Session:
         return rc
 
     def draft(self, req_ids, anchors: np.ndarray, logits: bool = True, temperature: float = 0.0):
-        n = self.cfg.gamma - 1
+        n = self.cfg.n_draft
         nr = len(req_ids)
         a = self.upload(np.asarray(anchors, dtype=np.int32))
         d = torch.empty((nr, n), dtype=torch.int32, device=self.device)

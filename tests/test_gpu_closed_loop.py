@@ -51,7 +51,7 @@ def loop_pair(cfg, rounds, thresholds=None, min_conf=None, prompt=24):
             outs.append(o)
         res_probe = None
         # the oracle's drafts decide the verification both loops see
-        keep_o = [cfg.gamma - 1] * B
+        keep_o = [cfg.n_draft] * B
         targets = np.stack([tgt.verify(r, b, outs[b]["tokens"]) for b in range(B)])
         res = loop.step(targets=targets)
         gpu = {"tokens": res.drafts, "conf": res.conf}
@@ -100,4 +100,9 @@ def test_closed_loop_matches_oracle():
 def test_closed_loop_windowed_with_pruning():
     c = cfg("loop_win", window=32, gamma=8, agree=0.9, batch=2, wdtype="bf16")
     acc, forced = loop_pair(c, rounds=6, min_conf=0.05)
+    print(f"accepted drafts {acc}, low-margin forced commits {forced}")
+
+
+def test_closed_loop_all_rows():
+    acc, forced = loop_pair(cfg("loop_all", draft_all_rows=True, gamma=5), rounds=5)
     print(f"accepted drafts {acc}, low-margin forced commits {forced}")

@@ -74,6 +74,11 @@ def test_small_gated_gelu_ffn(wdtype):
               n_q_heads=8, n_kv_heads=2, **kw), rounds=2)
 
 
+def test_small_draft_all_rows():
+    """Drafts from all gamma block rows (gamma tokens per block), the page-3 forwardRows form."""
+    run(small("s_allrows", draft_all_rows=True, gamma=6, agree=0.5), rounds=2)
+
+
 def test_small_mha_no_gqa():
     """Multi-head attention without grouping (one K/V head per query head)."""
     run(small("s_mha", n_q_heads=8, n_kv_heads=8, head_dim=64, d=512, target_hidden=512, inter=1024), rounds=2)

@@ -460,3 +460,22 @@ def test_accept_kept_is_capped_acceptance():
                 for keep in range(1, n + 1):
                     a, nxt = oracle.accept_kept(np.array(d, dtype=np.int32), np.array(t, dtype=np.int32), keep)
                     assert a == min(a_full, keep) and nxt == t[a]
+
+
+def test_draft_all_rows_adds_row0_draft():
+    """Drafting from every block row (the page-3 forwardRows): the drafts of rows 1..gamma-1 are
+    exactly the default mode's, and the extra first draft is the borrowed head applied to the
+    output-normed final block row 0 (restated here with a dense head)."""
+    cfg = tiny(gamma=5)
+    m = model(cfg)
+    o1 = oracle.Oracle(m)
+    o2 = oracle.Oracle(syn.HostModel(syn.with_overrides(cfg, draft_all_rows=True), m.mats, m.vecs))
+    k, v = o1.ctx_rows(taps(cfg, 3))
+    a = o1.draft(4, k, v)
+    b = o2.draft(4, k, v, trace=True)
+    assert b["logits"].shape == (cfg.gamma, cfg.vocab) and a["logits"].shape == (cfg.gamma - 1, cfg.vocab)
+    assert np.array_equal(b["logits"][1:], a["logits"]) and np.array_equal(b["tokens"][1:], a["tokens"])
+    h0 = _rms(b["trace"][cfg.n_layers][0], m.vecs["out_norm"], cfg.eps)
+    ref = oracle.dense(m.mats["lm_head"]) @ h0
+    assert np.allclose(b["logits"][0], ref, rtol=0, atol=1e-12)
+    assert b["tokens"][0] == int(np.argmax(ref))

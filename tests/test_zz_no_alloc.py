@@ -32,7 +32,7 @@ def test_noalloc_greedy_matches_draft_block_twice(pkg):
     taps = np.concatenate([syn.taps_rows(cfg, cfg.seed, b, 0, cfg.ctx_len) for b in req])
     assert s.project(req, [cfg.ctx_len] * cfg.batch, taps) == 0
     ref = s.draft(req, syn.anchors(cfg.seed, cfg.batch, 0, cfg.vocab), logits=True)   # the existing entry point
-    rows = cfg.batch * (cfg.gamma - 1)
+    rows = cfg.batch * cfg.n_draft
     logits = torch.from_numpy(ref["logits"].reshape(rows, cfg.vocab)).cuda()
     for call in range(2):                         # two calls in a row share the scratch array
         tok = torch.full((rows,), -1, dtype=torch.int32, device="cuda")
