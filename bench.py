@@ -47,6 +47,8 @@ def round_bytes(cfg, ctx_lens) -> dict:
     act = 4 if cfg.adtype == "f32" else 2
     keys = sum(min(int(P), cfg.window) if cfg.window else int(P) for P in ctx_lens)
     b["kv"] = cfg.n_layers * keys * kvd * 2 * act
+    if cfg.markov_rank:   # W2 of the Markov head streamed once per draft, plus the W1 rows
+        b["markov"] = cfg.n_draft * cfg.vocab * cfg.markov_rank * bpp + cfg.batch * cfg.n_draft * cfg.markov_rank * bpp
     b["total"] = sum(b.values())
     return b
 
@@ -277,10 +279,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--markov-rank", type=int, default=0,
+                    help="add the Markov sequential head of this rank (not part of the headline workload)")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="prefill only this many context rows (for short profiler captures; not a bench value)")
     args = ap.parse_args()
     cfg = syn.CONFIGS[args.config]
+    if args.markov_rank:
+        cfg = syn.with_overrides(cfg, markov_rank=args.markov_rank)
     if args.impl == "reference":
         return run_reference(args, cfg)
 

@@ -218,6 +218,13 @@ def make_model(cfg: DraftConfig, seed: int | None = None, norm_jitter: float = 0
     norm_vec("out_norm")
     mat("embed", c.vocab, c.target_hidden)
     mat("lm_head", c.vocab, c.target_hidden)
+    if c.markov_rank:
+        # Markov sequential head: W1 [V][r] N(0, 0.02) as on the page; W2 (stored transposed,
+        # [V][r]) drawn N(0, 0.5) instead of the page's zero init, so the bias moves the drafts
+        if "markov.w1" not in skip:
+            m.mats["markov.w1"] = make_matrix(seed, "markov.w1", c.vocab, c.markov_rank, fmt)
+        if "markov.w2t" not in skip:
+            m.mats["markov.w2t"] = make_matrix(seed, "markov.w2t", c.vocab, c.markov_rank, fmt, std=0.5)
     return m
 
 

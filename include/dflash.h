@@ -88,6 +88,11 @@ typedef struct {
   int draft_all_rows; /* 0: drafts from block rows 1..gamma-1 (n_draft = gamma-1, the DFlash2 block:
                          one verify token + gamma-1 proposals); 1: from all gamma block rows
                          (n_draft = gamma, the dflash.ts page's forwardRows) */
+  int markov_rank;    /* 0: drafts are the argmax of the head's logits. r > 0 (a multiple of 64,
+                         <= 1024): the Markov sequential head of the dflash.ts page (Eq 5) --
+                         drafts are taken in order and draft k's logits get the bias
+                         W1[prev_k] W2 before its argmax (prev_0 = the anchor, prev_k = draft k-1);
+                         weights markov_w1 [V][r] and markov_w2t [V][r] (= W2 transposed) */
 } dflash_config;
 
 typedef struct {
@@ -114,6 +119,8 @@ typedef struct {
   const float* block_pos;   /* [gamma][d] */
   const float* out_norm;    /* [d] */
   dflash_layer_weights layer[DFLASH_MAX_LAYERS];
+  dflash_matrix markov_w1;  /* [V][r]  Markov head token table (borrowed; markov_rank > 0 only) */
+  dflash_matrix markov_w2t; /* [V][r]  W2 of the Markov head, transposed (copied into the workspace) */
 } dflash_weights;
 
 typedef struct dflash_handle dflash_handle;

@@ -84,6 +84,8 @@ def _load():
         lib.orc_argmax_conf.argtypes = [vp, i32, vp, vp, vp]
         lib.orc_accept.restype = i32
         lib.orc_accept.argtypes = [i32, vp, vp, vp]
+        lib.orc_markov.restype = None
+        lib.orc_markov.argtypes = [ctypes.POINTER(Mat), ctypes.POINTER(Mat), i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.orc_gelu_tanh.restype = ctypes.c_double
         lib.orc_gelu_tanh.argtypes = [ctypes.c_double]
         lib.orc_draft_length.restype = i32
@@ -230,6 +232,22 @@ class Oracle:
             L.ff_norm = _p(self._vecs[f"bb.{i}.ff_norm"])
         self.w = w
 
+    def markov(self, anchor: int, base_logits: np.ndarray, prev_tokens=None):
+        """The Markov head's serial drafts over base logits [n][V]; prev_tokens (n ints) fixes the
+        chain's previous tokens after the first (used to follow another implementation's chain)."""
+        c = self.cfg
+        n, V = base_logits.shape
+        m1, m2 = _mat(self.model.mats["markov.w1"]), _mat(self.model.mats["markov.w2t"])
+        logits = np.empty((n, V), dtype=np.float64)
+        toks = np.empty(n, dtype=np.int32)
+        conf = np.empty(n, dtype=np.float64)
+        margin = np.empty(n, dtype=np.float64)
+        prev = None if prev_tokens is None else np.ascontiguousarray(prev_tokens, dtype=np.int32)
+        base = np.ascontiguousarray(base_logits, dtype=np.float64)
+        _load().orc_markov(ctypes.byref(m1), ctypes.byref(m2), c.markov_rank, V, n, int(anchor), _p(base),
+                           _p(prev) if prev is not None else None, _p(logits), _p(toks), _p(conf), _p(margin))
+        return {"logits": logits, "tokens": toks, "conf": conf, "margin": margin}
+
     @property
     def kvd(self) -> int:
         return self.cfg.n_kv_heads * self.cfg.head_dim
@@ -245,7 +263,7 @@ class Oracle:
             _load().orc_ctx_rows(ctypes.byref(self.c), ctypes.byref(self.w), rows, _p(taps), _p(k), _p(v))
         return k, v
 
-    def draft(self, anchor: int, k_ctx: np.ndarray, v_ctx: np.ndarray, trace: bool = False):
+    def draft(self, anchor: int, k_ctx: np.ndarray, v_ctx: np.ndarray, trace: bool = False, prev_tokens=None):
         """One block: logits [n_draft][V], tokens, conf, margin (top1 - top2), optional trace."""
         c = self.cfg
         n_ctx = k_ctx.shape[1]
@@ -261,6 +279,8 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"orc_draft rejected its inputs (rc={rc})")
         out = {"logits": logits, "tokens": toks, "conf": conf, "margin": margin}
+        if getattr(c, "markov_rank", 0):
+            out = dict(self.markov(anchor, logits, prev_tokens), base_logits=logits)
         if trace:
             out["trace"] = tr
         return out
@@ -297,7 +317,7 @@ class OracleSession:
             self.v[req] = np.ascontiguousarray(self.v[req][:, -c.window:])
             self.first[req] = max(self.first[req], 1)
 
-    def draft(self, req: int, anchor: int, trace: bool = False):
+    def draft(self, req: int, anchor: int, trace: bool = False, prev_tokens=None):
         c = self.o.cfg
         n_pos = self.n_pos.get(req, 0)
         k = self.k.get(req, self._empty)
@@ -306,4 +326,5 @@ class OracleSession:
             assert c.window > 0 and k.shape[1] >= min(c.window, n_pos), "skipped rows would enter the window"
         if c.window > 0 and k.shape[1] > c.window:
             k, v = k[:, -c.window:], v[:, -c.window:]
-        return self.o.draft(anchor, np.ascontiguousarray(k), np.ascontiguousarray(v), trace=trace)
+        return self.o.draft(anchor, np.ascontiguousarray(k), np.ascontiguousarray(v), trace=trace,
+                            prev_tokens=prev_tokens)

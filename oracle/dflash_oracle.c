@@ -296,3 +296,26 @@ int orc_accept_kept(int n, int keep, const int* draft, const int* target, int* n
   *next_anchor = target[a];
   return a;
 }
+
+/* The Markov sequential head ([P3] Eq 5, the markov branch of forwardRows): the drafts are taken
+ * one after another; before the argmax of draft k its logits get the rank-r bias
+ *   b_k = W1[prev_k] W2,  prev_0 = the anchor, prev_k = draft k-1,
+ * W1 [V][r] (a token embedding), W2 [r][V], stored here as W2^T [V][r] so that b_k = W2^T e.
+ * prev_given (NULL for the head's own greedy chain) fixes prev_1.. to given tokens, so that a
+ * caller can follow another implementation's chain past a near-tie. */
+void orc_markov(const orc_mat* w1, const orc_mat* w2t, int rank, int vocab, int n, int anchor,
+                const double* base_logits, const int* prev_given, double* logits, int* tokens,
+                double* conf, double* margin) {
+  double* e = (double*)malloc(sizeof(double) * (size_t)rank);
+  double* bias = (double*)malloc(sizeof(double) * (size_t)vocab);
+  int prev = anchor;
+  for (int k = 0; k < n; k++) {
+    for (int i = 0; i < rank; i++) e[i] = orc_weight(w1, prev, i);
+    orc_linear(w2t, 1, e, bias);
+    for (int j = 0; j < vocab; j++) logits[(int64_t)k * vocab + j] = base_logits[(int64_t)k * vocab + j] + bias[j];
+    orc_argmax_conf(logits + (int64_t)k * vocab, vocab, tokens + k, conf + k, margin + k);
+    prev = prev_given ? prev_given[k] : tokens[k];
+  }
+  free(e);
+  free(bias);
+}

@@ -63,5 +63,8 @@ void orc_argmax_conf(const double* logits, int vocab, int* token, double* conf, 
 int orc_accept(int n, const int* draft, const int* target, int* next_anchor);
 int orc_draft_length(int n, const float* conf, const float* thresholds, float min_conf);
 int orc_accept_kept(int n, int keep, const int* draft, const int* target, int* next_anchor);
+void orc_markov(const orc_mat* w1, const orc_mat* w2t, int rank, int vocab, int n, int anchor,
+                const double* base_logits, const int* prev_given, double* logits, int* tokens,
+                double* conf, double* margin);
 
 #endif

@@ -71,7 +71,7 @@ class dflash_config(ctypes.Structure):
         "n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter", "n_taps", "target_hidden", "vocab",
         "gamma", "window", "max_batch", "ctx_capacity")] + \
         [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int), ("ffn_act", ctypes.c_int),
-         ("draft_all_rows", ctypes.c_int)]
+         ("draft_all_rows", ctypes.c_int), ("markov_rank", ctypes.c_int)]
 
 
 class dflash_matrix(ctypes.Structure):
@@ -86,7 +86,8 @@ class dflash_layer_weights(ctypes.Structure):
 class dflash_weights(ctypes.Structure):
     _fields_ = [(n, dflash_matrix) for n in ("w_c", "tok_proj", "out_proj", "embed", "lm_head")] + \
                [(n, ctypes.c_void_p) for n in ("ctx_norm", "mask_emb", "block_pos", "out_norm")] + \
-               [("layer", dflash_layer_weights * DFLASH_MAX_LAYERS)]
+               [("layer", dflash_layer_weights * DFLASH_MAX_LAYERS)] + \
+               [(n, dflash_matrix) for n in ("markov_w1", "markov_w2t")]
 
 
 class dflash_stats(ctypes.Structure):
@@ -189,7 +190,8 @@ def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = No
         ctx_capacity = cfg.window if cfg.window > 0 else cfg.ctx_len + 64 * cfg.gamma
     return dflash_config(cfg.n_layers, cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.inter, cfg.n_taps,
                          cfg.target_hidden, cfg.vocab, cfg.gamma, cfg.window, mb, ctx_capacity, cfg.eps,
-                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn], 1 if cfg.draft_all_rows else 0)
+                         DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn], 1 if cfg.draft_all_rows else 0,
+                         cfg.markov_rank)
 
 
 class DeviceModel:
@@ -218,6 +220,7 @@ class DeviceModel:
         w = dflash_weights()
         w.w_c, w.tok_proj, w.out_proj = m("W_c"), m("tok_proj"), m("out_proj")
         w.embed, w.lm_head = m("embed"), m("lm_head")
+        w.markov_w1, w.markov_w2t = m("markov.w1"), m("markov.w2t")
         v = host_model.vecs
         w.ctx_norm, w.block_pos, w.out_norm = t("ctx_norm", v["ctx_norm"]), t("block_pos", v["block_pos"]), \
             t("out_norm", v["out_norm"])
@@ -230,9 +233,9 @@ class DeviceModel:
             L.ff_norm = t(f"bb.{i}.ff_norm", v[f"bb.{i}.ff_norm"])
         self.weights = w
 
-    def free(self, keep=("embed",)):
+    def free(self, keep=("embed", "markov.w1")):
         """Drop the device copies the handle no longer needs after dflash_create (the embedding
-        table is borrowed by the handle and must be kept)."""
+        table and the Markov head's W1 are borrowed by the handle and must be kept)."""
         self.tensors = {k: v for k, v in self.tensors.items() if k in keep}
 
 

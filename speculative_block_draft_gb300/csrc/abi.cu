@@ -39,6 +39,10 @@ struct dflash_handle {
 
   PackedMat wc, qkv[DFLASH_MAX_LAYERS], wo[DFLASH_MAX_LAYERS], gu[DFLASH_MAX_LAYERS], down[DFLASH_MAX_LAYERS],
       tok, outp, lm;
+  PackedMat mk;                 // Markov head W2^T [V][r] (markov_rank > 0)
+  dflash_matrix mk_w1{};        // Markov head W1 [V][r], borrowed
+  float* mk_base = nullptr;     // [max_batch][n_draft][V] head logits before the Markov bias
+  void* mk_x = nullptr;         // [max_batch][r] W1 rows (f16 + remainder, or fp32)
   dflash_matrix embed{};
   float *ctx_norm = nullptr, *mask_emb = nullptr, *block_pos = nullptr, *out_norm = nullptr;
   float *attn_norm = nullptr, *ff_norm = nullptr;  // [L][d]
@@ -163,6 +167,7 @@ bool valid_config(const dflash_config* c) {
   if (!(c->eps >= 0.f)) return false;
   if (c->ffn_act != DFLASH_FFN_SWIGLU && c->ffn_act != DFLASH_FFN_GELU) return false;
   if (c->draft_all_rows != 0 && c->draft_all_rows != 1) return false;
+  if (c->markov_rank < 0 || c->markov_rank > 1024 || c->markov_rank % 64) return false;
   if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
   if (c->adtype == DFLASH_F32) {
     if (c->wdtype != DFLASH_F32) return false;
@@ -198,6 +203,7 @@ size_t carve(dflash_handle* h, uint8_t* base) {
     mat(h->outp, h->H, h->d);
   }
   mat(h->lm, h->V, h->H);
+  if (c.markov_rank) mat(h->mk, h->V, c.markov_rank);
 
   const size_t ab = h->act_bytes;
   h->ctx_norm = cv.take<float>(h->d * 4);
@@ -225,6 +231,10 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->ssq = cv.take<float>((size_t)R * h->ssq_ld * 4);
   h->ssq_ctx = cv.take<float>((size_t)kMaxCtxChunk * h->ssq_ld * 2 * 4);
   h->xw = cv.take<void>((size_t)h->L * kMaxCtxChunk * h->d * ab * 2);
+  if (c.markov_rank) {
+    h->mk_base = cv.take<float>((size_t)c.max_batch * h->nd * h->V * 4);
+    h->mk_x = cv.take<void>((size_t)c.max_batch * c.markov_rank * ab * 2);
+  }
 
   // split-K partials / tickets: the largest plan over every matrix and row count
   size_t pf = 0;
@@ -488,6 +498,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   bool ok = mat_ok(w->w_c, f) && mat_ok(w->embed, f) && mat_ok(w->lm_head, f) && w->ctx_norm && w->block_pos &&
             w->out_norm && (h->G < 2 || w->mask_emb);
   if (h->d != h->H) ok = ok && mat_ok(w->tok_proj, f) && mat_ok(w->out_proj, f);
+  if (cfg->markov_rank) ok = ok && mat_ok(w->markov_w1, f) && mat_ok(w->markov_w2t, f);
   for (int i = 0; i < h->L && ok; i++) {
     const dflash_layer_weights& l = w->layer[i];
     ok = mat_ok(l.wq, f) && mat_ok(l.wk, f) && mat_ok(l.wv, f) && mat_ok(l.wo, f) && mat_ok(l.w_gate, f) &&
@@ -529,6 +540,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   {
     RepackSrc l = src_of(w->lm_head, h->V);
     chk(repack(h, h->lm, &l, 1, 0, s));
+  }
+  if (cfg->markov_rank) {
+    RepackSrc mk = src_of(w->markov_w2t, h->V);
+    chk(repack(h, h->mk, &mk, 1, 0, s));
+    h->mk_w1 = w->markov_w1;
   }
   chk(status_of(cudaMemcpyAsync(h->ctx_norm, w->ctx_norm, h->d * 4, cudaMemcpyDefault, s)));
   if (h->G > 1)
@@ -908,17 +924,59 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     }
     cl.epi = EPI_LMHEAD;
     cl.e.n_rows = h->V;
-    cl.e.logits = logits ? logits + (size_t)l0 * h->V : nullptr;
+    // with the Markov head the head's logits are only the base of the serial drafts below
+    const bool markov = c.markov_rank > 0;
+    cl.e.logits = markov ? h->mk_base + (size_t)l0 * h->V : (logits ? logits + (size_t)l0 * h->V : nullptr);
     cl.e.vocab = h->V;
     cl.e.rows_per_req = n;
     GemvPlan lp{};
     if ((st = run_gemv(h, cl, s, &lp))) return st;
+    if (markov) continue;
     // merge the per-CTA (one K slice) or per-strip (K split) vocab states: token and confidence
     const bool split = h->fmt != FMT_F32 && lp.n_slices > 1;
     h->launches++;
     if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part, split ? h->lm.n_strips : lp.grid, R,
-                                         draft + l0, conf ? conf + l0 : nullptr, s))))
+                                         draft + l0, conf ? conf + l0 : nullptr, 1, s))))
       return st;
+  }
+  if (c.markov_rank) {
+    // Markov sequential head (Eq 5 of the dflash.ts page): draft k = argmax(base_k + W1[prev_k] W2),
+    // prev_0 = the anchor, prev_k = draft k-1; one gather, one rank-r GEMV (bias + argmax epilogue)
+    // and one vocab merge per draft, in order
+    const int r = c.markov_rank;
+    const size_t lo_off = h->act_f32 ? 0 : (size_t)c.max_batch * r;
+    for (int k = 0; k < n; k++) {
+      for (int b0 = 0; b0 < n_req; b0 += kMaxRows) {
+        const int nb = std::min(kMaxRows, n_req - b0);
+        h->launches++;
+        if ((st = status_of(launch_markov_gather(nb, k, n, r, h->V, h->fmt, h->mk_w1.data,
+                                                 static_cast<const uint16_t*>(h->mk_w1.scale),
+                                                 static_cast<const uint16_t*>(h->mk_w1.bias), anchor + b0,
+                                                 draft + (size_t)b0 * n, h->mk_x, lo_off, s))))
+          return st;
+        GemvCall cm;
+        cm.m = &h->mk;
+        cm.R = nb;
+        cm.x = h->mk_x;
+        cm.ldx = r;
+        cm.x_lo_off = (long long)lo_off;
+        cm.epi = EPI_LMHEAD;
+        cm.e.n_rows = h->V;
+        cm.e.vocab = h->V;
+        cm.e.rows_per_req = 1;
+        cm.e.logit_bias = h->mk_base + ((size_t)b0 * n + k) * h->V;
+        cm.e.logit_row_stride = (long long)n * h->V;
+        cm.e.logits = logits ? logits + ((size_t)b0 * n + k) * h->V : nullptr;
+        GemvPlan mp{};
+        if ((st = run_gemv(h, cm, s, &mp))) return st;
+        const bool split = h->fmt != FMT_F32 && mp.n_slices > 1;
+        h->launches++;
+        if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part, split ? h->mk.n_strips : mp.grid, nb,
+                                             draft + (size_t)b0 * n + k, conf ? conf + (size_t)b0 * n + k : nullptr,
+                                             n, s))))
+          return st;
+      }
+    }
   }
   if (h->probe_stop) cudaEventRecord(h->probe_stop, s);
   h->probe_start = h->probe_stop = nullptr;

@@ -26,7 +26,7 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap)
 // pairwise tree; the order is fixed, so the result is reproducible. Writes the greedy token and
 // the softmax probability of that token.
 __global__ void __launch_bounds__(256) lm_reduce_kernel(const float* __restrict__ parts, int n_parts,
-                                                        int32_t* tok_out, float* conf_out) {
+                                                        int32_t* tok_out, float* conf_out, int out_stride) {
   __shared__ LmState sm[256];
   const int c = blockIdx.x;
   pdl_launch_dependents();
@@ -51,14 +51,14 @@ __global__ void __launch_bounds__(256) lm_reduce_kernel(const float* __restrict_
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    tok_out[c] = sm[0].i;
-    if (conf_out) conf_out[c] = 1.0f / sm[0].s;
+    tok_out[(size_t)c * out_stride] = sm[0].i;
+    if (conf_out) conf_out[(size_t)c * out_stride] = 1.0f / sm[0].s;
   }
 }
 
 cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t* tok_out, float* conf_out,
-                             cudaStream_t s) {
-  return launch_pdl(lm_reduce_kernel, dim3(rows), dim3(256), 0, s, parts, n_parts, tok_out, conf_out);
+                             int out_stride, cudaStream_t s) {
+  return launch_pdl(lm_reduce_kernel, dim3(rows), dim3(256), 0, s, parts, n_parts, tok_out, conf_out, out_stride);
 }
 
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s) {

@@ -228,13 +228,16 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
         LmState& st = a.n_slices > 1 ? lm_strip_state[nt][p] : lm[nt][p];
         if (a.n_slices > 1) st = LmState{-INFINITY, 0.f, 0x7fffffff};
         if (cv) {
+          const size_t row = (size_t)c * (e.logit_row_stride ? e.logit_row_stride : e.vocab);
           if (v0) {
-            if (e.logits) e.logits[(size_t)c * e.vocab + nr0] = ya;
-            lm_push(st, ya, nr0);
+            const float l = e.logit_bias ? ya + e.logit_bias[row + nr0] : ya;
+            if (e.logits) e.logits[row + nr0] = l;
+            lm_push(st, l, nr0);
           }
           if (v1) {
-            if (e.logits) e.logits[(size_t)c * e.vocab + nr1] = yb;
-            lm_push(st, yb, nr1);
+            const float l = e.logit_bias ? yb + e.logit_bias[row + nr1] : yb;
+            if (e.logits) e.logits[row + nr1] = l;
+            lm_push(st, l, nr1);
           }
         }
       }

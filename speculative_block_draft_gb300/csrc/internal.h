@@ -86,6 +86,8 @@ struct EpiArgs {
   void* act; int inter; int ffn_act;
   // EPI_LMHEAD
   float* logits; int vocab; int rows_per_req;
+  const float* logit_bias;    // added to every logit before the argmax (Markov head), or null
+  long long logit_row_stride; // elements between activation rows in logits / logit_bias (0: vocab)
   float* lm_part;    // one K slice: per-CTA (max, sum, index) per column, merged by lm_reduce_kernel
   float* lm_strip;   // split-K launches: per-strip (max, sum, index) per column, merged in strip order
 };
@@ -197,9 +199,15 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ---- launchers (return cudaGetLastError of the launch) -----------------------------------------
 cudaError_t launch_gemv(int fmt, int epi, int nt, const GemvArgs& a, int grid, cudaStream_t s);
-// Final greedy token + confidence per row from n_parts (max, sum, index) states kMaxRows rows apart.
+// Final greedy token + confidence per row from n_parts (max, sum, index) states kMaxRows rows apart;
+// row c's results go to tok_out[c * out_stride], conf_out[c * out_stride].
 cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t* tok_out, float* conf_out,
-                             cudaStream_t s);
+                             int out_stride, cudaStream_t s);
+// Markov head input of draft k: x[b] = W1[prev] (f16, remainder at x + lo_off), prev = anchor[b] for
+// k == 0, else draft[b * n + k - 1].
+cudaError_t launch_markov_gather(int n_req, int k, int n, int rank, int vocab, int fmt, const void* w1,
+                                 const uint16_t* w1_scale, const uint16_t* w1_bias, const int32_t* anchor,
+                                 const int32_t* draft, void* x, size_t lo_off, cudaStream_t s);
 size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t s);

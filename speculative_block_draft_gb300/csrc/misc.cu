@@ -195,7 +195,33 @@ __global__ void draft_lengths_kernel(int n, const float* conf, const float* thre
   if (lane == 0) keep[b] = mask ? __ffs(mask) - 1 : n;
 }
 
+// Markov head input for draft k of every request: the W1 row of the previous token, as f16 plus
+// its f16 remainder (the row is a stored weight, so hi + lo carries it to ~22 bits).
+template <typename XT>
+__global__ void __launch_bounds__(256) markov_gather_kernel(int k, int n, int rank, int vocab, int fmt,
+                                                            const void* w1, const uint16_t* w1_scale,
+                                                            const uint16_t* w1_bias, const int32_t* anchor,
+                                                            const int32_t* draft, XT* x, size_t lo_off) {
+  const int b = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  int prev = k == 0 ? anchor[b] : draft[(size_t)b * n + k - 1];
+  prev = prev < 0 ? 0 : (prev >= vocab ? vocab - 1 : prev);   // clamped: no read outside the table
+  for (int i = threadIdx.x; i < rank; i += blockDim.x)
+    store_act_split<XT>(x, (size_t)b * rank + i, lo_off, load_weight(fmt, w1, w1_scale, w1_bias, rank, prev, i));
+}
+
 }  // namespace
+
+cudaError_t launch_markov_gather(int n_req, int k, int n, int rank, int vocab, int fmt, const void* w1,
+                                 const uint16_t* w1_scale, const uint16_t* w1_bias, const int32_t* anchor,
+                                 const int32_t* draft, void* x, size_t lo_off, cudaStream_t s) {
+  if (fmt == FMT_F32)   // the CUDA-core path keeps fp32 activations
+    return launch_pdl(markov_gather_kernel<float>, dim3(n_req), dim3(256), 0, s, k, n, rank, vocab, fmt, w1,
+                      w1_scale, w1_bias, anchor, draft, static_cast<float*>(x), (size_t)0);
+  return launch_pdl(markov_gather_kernel<__half>, dim3(n_req), dim3(256), 0, s, k, n, rank, vocab, fmt, w1,
+                    w1_scale, w1_bias, anchor, draft, static_cast<__half*>(x), lo_off);
+}
 
 cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
                                  int32_t* keep, cudaStream_t s) {

@@ -25,7 +25,7 @@ class Session:
         with torch.cuda.stream(self.stream):
             self.h = Handle(self.ccfg, self.dm.weights, stream=self.stream, device=self.device)
         self.stream.synchronize()
-        self.dm.free(keep=("embed",))   # the handle copied the rest into its workspace
+        self.dm.free(keep=("embed", "markov.w1"))   # borrowed by the handle; the rest was copied
 
     def upload(self, arr: np.ndarray, dtype=None) -> torch.Tensor:
         a = np.ascontiguousarray(arr)

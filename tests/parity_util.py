@@ -104,7 +104,10 @@ class Pair:
         assert g["rc"] == 0
         outs = []
         for b in range(B):
-            o = self.os.draft(b, int(anchors[b]))
+            # the Markov head drafts serially: the oracle follows the GPU's chain of previous
+            # tokens, so a near-tie does not make every later row incomparable
+            prev = g["tokens"][b] if c.markov_rank else None
+            o = self.os.draft(b, int(anchors[b]), prev_tokens=prev)
             compare_block(c, g, o, b, report)
             outs.append(o)
         if check_accept:

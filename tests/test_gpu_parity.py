@@ -79,6 +79,19 @@ def test_small_draft_all_rows():
     run(small("s_allrows", draft_all_rows=True, gamma=6, agree=0.5), rounds=2)
 
 
+@pytest.mark.parametrize("wdtype", ["q4", "bf16", "f32"])
+def test_small_markov_head(wdtype):
+    """Markov sequential head (rank 128): serial drafts, each argmax over base logits plus
+    W1[previous token] W2; the oracle follows the GPU's chain of previous tokens."""
+    kw = dict(adtype="f32") if wdtype == "f32" else {}
+    run(small(f"s_markov_{wdtype}", wdtype=wdtype, markov_rank=128, gamma=6, **kw), rounds=2)
+
+
+def test_small_markov_head_batched_all_rows():
+    """Markov head over several requests (one chain each) with drafts from every block row."""
+    run(small("s_markov_b", markov_rank=64, batch=3, ctx_len=50, draft_all_rows=True, agree=0.5), rounds=2)
+
+
 def test_small_mha_no_gqa():
     """Multi-head attention without grouping (one K/V head per query head)."""
     run(small("s_mha", n_q_heads=8, n_kv_heads=8, head_dim=64, d=512, target_hidden=512, inter=1024), rounds=2)

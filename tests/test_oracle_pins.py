@@ -479,3 +479,53 @@ def test_draft_all_rows_adds_row0_draft():
     ref = oracle.dense(m.mats["lm_head"]) @ h0
     assert np.allclose(b["logits"][0], ref, rtol=0, atol=1e-12)
     assert b["tokens"][0] == int(np.argmax(ref))
+
+
+# ------------------------------------------------------------------------------------------
+# Markov sequential head (dflash.ts page, Eq 5: the markov branch of the drafting loop)
+# ------------------------------------------------------------------------------------------
+def _markov_cfg(**kw):
+    return syn.with_overrides(tiny(gamma=5, vocab=97), markov_rank=64, **kw)
+
+
+def test_markov_zero_w2_is_the_parallel_drafter():
+    """W2 = 0 (the page's initialisation) leaves the drafts of the parallel head unchanged."""
+    cfg = _markov_cfg()
+    m = model(cfg)
+    m.mats["markov.w2t"].data[:] = 0
+    o = oracle.Oracle(m)
+    k, v = o.ctx_rows(taps(cfg, 3))
+    out = o.draft(5, k, v)
+    assert np.array_equal(out["logits"], out["base_logits"])
+    base = oracle.Oracle(syn.HostModel(syn.with_overrides(cfg, markov_rank=0), m.mats, m.vecs)).draft(5, k, v)
+    assert np.array_equal(out["tokens"], base["tokens"])
+
+
+def test_markov_bias_chain_and_linearity():
+    """Row k's bias depends only on prev_k (the anchor for row 0, draft k-1 after): changing the
+    anchor moves row 0 only, changing the token fed after row j moves row j+1 only; and the bias
+    is linear in W2 (doubling W2 doubles logits - base)."""
+    cfg = _markov_cfg()
+    m = model(cfg)
+    o = oracle.Oracle(m)
+    rng = np.random.default_rng(3)
+    n, V = cfg.n_draft, cfg.vocab
+    base = rng.normal(size=(n, V))
+    prev = np.array([11, 23, 37, 41], dtype=np.int32)
+    a = o.markov(7, base, prev)["logits"]
+    b = o.markov(8, base, prev)["logits"]
+    assert not np.allclose(a[0], b[0]) and np.array_equal(a[1:], b[1:])
+    for j in range(n - 1):
+        p2 = prev.copy()
+        p2[j] = (p2[j] + 5) % V
+        c = o.markov(7, base, p2)["logits"]
+        changed = [not np.array_equal(a[r], c[r]) for r in range(n)]
+        assert changed == [r == j + 1 for r in range(n)]
+    m2 = syn.HostModel(cfg, dict(m.mats), m.vecs)
+    w2 = m.mats["markov.w2t"]
+    m2.mats["markov.w2t"] = HostMatrix("f32", w2.n_out, w2.n_in, (w2.data * 2).astype(np.float32))
+    d = oracle.Oracle(m2).markov(7, base, prev)["logits"]
+    assert np.allclose(d - base, 2 * (a - base), rtol=0, atol=1e-12)
+    own = o.markov(7, base)                         # its own greedy chain
+    assert np.array_equal(o.markov(7, base, own["tokens"])["logits"], own["logits"])
+    assert own["tokens"][0] == int(np.argmax(own["logits"][0]))
