@@ -56,7 +56,6 @@ struct dflash_handle {
   float* lm_part = nullptr;
   float* lm_strip = nullptr;
   float *att_o = nullptr, *att_ml = nullptr;
-  int* att_tickets = nullptr;
   unsigned* err = nullptr;
   size_t partial_floats = 0;
   int ticket_count = 0, lm_grid_max = 0, att_pairs_max = 0;
@@ -281,7 +280,6 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
   h->att_o = cv.take<float>((size_t)h->att_pairs_max * 64 * c.head_dim * 4);
   h->att_ml = cv.take<float>((size_t)h->att_pairs_max * 64 * 2 * 4);
-  h->att_tickets = cv.take<int>((size_t)c.max_batch * c.n_kv_heads * 4);
   h->err = cv.take<unsigned>(4);
   (void)state_begin;
   return round_up(cv.off, 256);
@@ -793,7 +791,6 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       aa.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
       aa.part_o = h->att_o;
       aa.part_ml = h->att_ml;
-      aa.tickets = h->att_tickets;
       aa.err = h->err;
       int max_tiles = 0;
       for (int b = 0; b < n_req; b++) {
@@ -928,7 +925,6 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     const bool markov = c.markov_rank > 0;
     cl.e.logits = markov ? h->mk_base + (size_t)l0 * h->V : (logits ? logits + (size_t)l0 * h->V : nullptr);
     cl.e.vocab = h->V;
-    cl.e.rows_per_req = n;
     GemvPlan lp{};
     if ((st = run_gemv(h, cl, s, &lp))) return st;
     if (markov) continue;
@@ -963,7 +959,6 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         cm.epi = EPI_LMHEAD;
         cm.e.n_rows = h->V;
         cm.e.vocab = h->V;
-        cm.e.rows_per_req = 1;
         cm.e.logit_bias = h->mk_base + ((size_t)b0 * n + k) * h->V;
         cm.e.logit_row_stride = (long long)n * h->V;
         cm.e.logits = logits ? logits + ((size_t)b0 * n + k) * h->V : nullptr;

@@ -20,9 +20,12 @@
 //      row g+8:  s / 16 * sum (1024 + 16q) x + (b -  64 s) * sum x
 //    so the MMA sees exact integers; the offsets stay small next to q (17x, 8.5x) because the
 //    fp32 group sum loses that factor when they are removed. bf16 weights are stored as f16.
-//  * When a strip's K is split over several CTAs, each writes a partial tile; after its last
-//    strip every CTA settles its tickets, and the last slice to arrive (atomic ticket, no
-//    waiting) sums the partials in slice order and runs the epilogue.
+//  * When a strip's K is split in two, the two slice CTAs form a 2-CTA cluster: partial tiles
+//    are pushed into the owning CTA's shared memory (distributed shared memory), and after one
+//    cluster barrier the owner sums them in slice order and runs the epilogue. Wider K splits
+//    write partial tiles to global memory; after its last strip every CTA settles its tickets,
+//    and the last slice to arrive (acquire-release ticket, no waiting) sums the partials in
+//    slice order and runs the epilogue.
 // CUDA-core path (fp32 weights and activations): one warp per strip, fp32 FMA.
 #pragma once
 

@@ -46,7 +46,6 @@ constexpr int kBf16GroupsPerStage = (kQ4GroupsPerStage * kQ4GroupBytes) / kBf16G
 constexpr int kStageBytes = kQ4GroupsPerStage * kQ4GroupBytes > kBf16GroupsPerStage * kBf16GroupBytes
                                 ? kQ4GroupsPerStage * kQ4GroupBytes : kBf16GroupsPerStage * kBf16GroupBytes;
 constexpr int kMaxRows = 32;              // activation rows per launch (4 n-tiles of 8)
-constexpr int kXBudget = 112 * 1024;      // shared bytes for the staged activation slice
 constexpr int kMaxCtxChunk = 32;          // context rows per projection chunk
 // Warps per tensor-core GEMV CTA by n-tile count: more activation columns need more registers
 // per thread (one CTA per SM, 64K registers).
@@ -85,7 +84,7 @@ struct EpiArgs {
   // EPI_SWIGLU (gated FFN: silu(g) * u, or gelu_tanh(g) * u when ffn_act == DFLASH_FFN_GELU)
   void* act; int inter; int ffn_act;
   // EPI_LMHEAD
-  float* logits; int vocab; int rows_per_req;
+  float* logits; int vocab;
   const float* logit_bias;    // added to every logit before the argmax (Markov head), or null
   long long logit_row_stride; // elements between activation rows in logits / logit_bias (0: vocab)
   float* lm_part;    // one K slice: per-CTA (max, sum, index) per column, merged by lm_reduce_kernel
@@ -132,7 +131,7 @@ struct AttnArgs {
   int plane0;                                                 // layer * max_batch * hkv
   int n_req, n_splits;
   float scale_log2;                                           // log2(e) / sqrt(hd)
-  float* part_o; float* part_ml; int* tickets;
+  float* part_o; float* part_ml;
   unsigned* err;
   AttnReq req[DFLASH_MAX_BATCH];
 };

@@ -65,4 +65,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.dflash_create(ctypes.byref(good), None, None, 0, None, ctypes.byref(h)) == pkg.DFLASH_EINVAL
     assert lib.dflash_draft_block(None, 1, None, None, 0.0, None, None, None, None) == pkg.DFLASH_EINVAL
     assert lib.dflash_ctx_len(None, 0) == -1
+    assert lib.dflash_draft_lengths(None, 1, None, None, 0.0, None, None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_accept_kept(None, 1, None, None, None, None, None, None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_accept(None, 1, None, None, None, None, None) == pkg.DFLASH_EINVAL
     assert b"declined" in lib.dflash_status_str(pkg.DFLASH_DECLINED)
