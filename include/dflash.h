@@ -138,7 +138,10 @@ size_t dflash_workspace_bytes(const dflash_config* cfg);
 
 /* Validate cfg, lay out the workspace (>= dflash_workspace_bytes, 256-byte aligned, device
  * memory owned by the caller), re-lay-out the weights into it and zero all state, all on
- * `stream` (a cudaStream_t; NULL = legacy default stream). *out receives a host-side handle. */
+ * `stream` (a cudaStream_t; NULL = legacy default stream). *out receives a host-side handle.
+ * A handle belongs to the device current at create: make that device current for every call
+ * on it. A handle's calls must be issued in order on one stream (its scratch is shared by all of
+ * them); different handles are independent and may run on different devices and threads. */
 int dflash_create(const dflash_config* cfg, const dflash_weights* weights, void* workspace,
                   size_t workspace_bytes, void* stream, dflash_handle** out);
 

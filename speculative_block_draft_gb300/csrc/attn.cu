@@ -482,12 +482,9 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUt
   cudaError_t err;
 #define DFL_ATTN(HD)                                                                                \
   {                                                                                                 \
-    static int smem_set = 0;                                                                        \
-    if ((int)smem > smem_set) {                                                                     \
-      err = cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-      if (err != cudaSuccess) return err;                                                           \
-      smem_set = (int)smem;                                                                         \
-    }                                                                                               \
+    static std::atomic<int> smem_set[kMaxDevices];                                                  \
+    err = ensure_smem_limit(attn_tc_kernel<HD>, smem, smem_set);                                    \
+    if (err != cudaSuccess) return err;                                                             \
   }                                                                                                 \
   return launch_pdl(attn_tc_kernel<HD>, grid, dim3(kAttnWarps * 32), smem, s, a, kmap, vmap);
   switch (a.hd) {

@@ -956,12 +956,9 @@ cudaError_t launch_gemv_fmt_nt(int epi, const GemvArgs& a, int grid, size_t smem
       gemv_f32_kernel<NT, E><<<grid, kF32Warps * 32, 0, s>>>(a);                                 \
     } else {                                                                                     \
       auto k = gemv_tc_kernel<FMT, NT, E>;                                                       \
-      static int smem_set = 0;                                                                   \
-      if ((int)smem > smem_set) {                                                                \
-        cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        if (err != cudaSuccess) return err;                                                      \
-        smem_set = (int)smem;                                                                    \
-      }                                                                                          \
+      static std::atomic<int> smem_set[kMaxDevices];                                             \
+      cudaError_t err = ensure_smem_limit(k, smem, smem_set);                                    \
+      if (err != cudaSuccess) return err;                                                        \
       return launch_pdl_cluster(k, dim3(grid), dim3(gemv_warps(NT) * 32), smem, s, a.cluster2 ? 2 : 1, a); \
     }                                                                                            \
     return cudaGetLastError();                                                                   \

@@ -4,6 +4,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include <utility>
@@ -160,6 +162,19 @@ struct BlockArgs {
   size_t xn_lo_off;           // f16 remainder of xn at this element offset (0: none)
   void* emb_out;              // gather mode: [n_req][H] activation rows
 };
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the current device (the
+// attribute is per device). `cache` holds the limit set so far, per device ordinal.
+constexpr int kMaxDevices = 64;
+template <typename K>
+inline cudaError_t ensure_smem_limit(K kernel, size_t bytes, std::atomic<int>* cache) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if ((int)bytes <= cache[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cache[dev].store((int)bytes, std::memory_order_relaxed);
+  return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may start while the previous kernel
 // of the stream drains; it must call pdl_wait() before reading anything earlier kernels wrote.
