@@ -78,14 +78,18 @@ def load_traffic(kernel: str):
         return None
 
 
-def kernel_source_hash() -> str:
+# The sources the LM-head launch is compiled from: its GEMV kernel and epilogue, the vocab merge,
+# and the constants and helpers they include. A change to any of them voids a traffic record.
+LM_HEAD_SOURCES = ("common.cuh", "gemv_f32.cu", "gemv_impl.cuh", "gemv_q4.cu", "internal.h")
+
+
+def kernel_source_hash(names=LM_HEAD_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_block_draft_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 

@@ -210,6 +210,51 @@ int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop
 /* Kernel launches issued by this handle since create (all calls), for launch accounting. */
 uint64_t dflash_launch_count(const dflash_handle* h);
 
+/* ---- many-row contraction over a stored drafter matrix (tcgen05 tensor cores) -----------------
+ * y[r][n] = sum_k x[r][k] W[n][k] for r < n_rows, with W one of the drafter's 4-bit matrices as
+ * stored in the handle (the dflash.ts page's linear maps of Eq 2 and Eq 3, the FFN and the
+ * borrowed LM head; each weight is the group-64 affine code w = scale * q + bias). It serves
+ * batches of activation rows (up to DFLASH_ROWS_MATMUL_MAX rows per call) in one pass over the
+ * weights, where the draft round's skinny per-request projections would stream them once per 32
+ * rows. Experimental: not yet covered by the parity tests; the draft round does not call it. */
+#define DFLASH_ROWS_MATMUL_MAX 160
+enum {
+  DFLASH_MAT_CTX = 0,    /* W_c [d][n_taps*H] (Eq 2) */
+  DFLASH_MAT_QKV = 1,    /* layer's [W_q; W_k; W_v] [qd + 2 kvd][d] (Eq 3) */
+  DFLASH_MAT_O = 2,      /* layer's W_o [d][qd] */
+  DFLASH_MAT_GATEUP = 3, /* layer's [W_gate; W_up] [2 inter][d]; y columns gate rows first */
+  DFLASH_MAT_DOWN = 4,   /* layer's W_down [d][inter] */
+  DFLASH_MAT_LM = 5      /* borrowed LM head [vocab][H] */
+};
+
+/* Launch geometry and caller scratch of dflash_rows_matmul for a matrix of n_out rows and k_in
+ * inputs (k_in % 64 == 0), n_rows activation rows, with (x_lo != 0) or without the activations'
+ * f16 remainder, on a device with n_sm SMs. Host only. Returns DFLASH_OK, DFLASH_EINVAL for bad
+ * sizes or a NULL plan, DFLASH_ECAPACITY for n_rows > DFLASH_ROWS_MATMUL_MAX. */
+typedef struct {
+  int n_pad;            /* activation rows padded to a multiple of 16 (the MMA's N) */
+  int m_tiles;          /* 128-row output tiles */
+  int k_slices;         /* K slices per tile (their partial tiles are summed in slice order) */
+  int groups_per_slice; /* 64-input groups per K slice */
+  int grid;             /* CTAs = m_tiles * k_slices */
+  int x_stages;         /* activation ring depth */
+  size_t smem_bytes;    /* dynamic shared memory per CTA */
+  size_t scratch_bytes; /* scratch dflash_rows_matmul needs */
+} dflash_rows_plan;
+int dflash_rows_matmul_plan(int n_out, int k_in, int n_rows, int x_lo, int n_sm, dflash_rows_plan* plan);
+
+/* x: device f16 [n_rows][ldx] (ldx >= k_in, ldx % 8 == 0, 16-byte aligned); x_lo: NULL or the
+ * f16 remainder of x in the same layout (x + x_lo is the activation). y: device fp32
+ * [n_rows][ldy], ldy >= n_out, in the matrix's natural row order. scratch: device, 256-byte
+ * aligned, >= the plan's scratch_bytes, owned by the caller and free for the call's duration.
+ * layer is ignored for DFLASH_MAT_CTX and DFLASH_MAT_LM. Enqueued on `stream`; nothing is
+ * allocated. Returns DFLASH_EINVAL (bad arguments, or a handle whose weights are not 4-bit),
+ * DFLASH_ECAPACITY (n_rows > DFLASH_ROWS_MATMUL_MAX or scratch too small), DFLASH_ECUDA. A bounded
+ * wait that gives up sets the handle's error word (dflash_check_errors -> DFLASH_ETIMEOUT) and
+ * leaves y undefined. */
+int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, const void* x, const void* x_lo,
+                       int ldx, float* y, int ldy, void* scratch, size_t scratch_bytes, void* stream);
+
 void dflash_destroy(dflash_handle* h);
 
 /* Allocation-free greedy token and softmax confidence for logits the caller already holds.

@@ -16,8 +16,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash.so")
-_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu"]
-_HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh"]
+_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu", "gemm_tc05.cu"]
+_HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh", "gemm_tc05.h", "tc05.cuh"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a",
               "-Xcompiler", "-fPIC"]
 
@@ -94,12 +94,22 @@ class dflash_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("rounds", "blocks", "declined", "ctx_rows", "accept_calls")]
 
 
+class dflash_rows_plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_pad", "m_tiles", "k_slices", "groups_per_slice", "grid",
+                                            "x_stages")] + [("smem_bytes", ctypes.c_size_t),
+                                                            ("scratch_bytes", ctypes.c_size_t)]
+
+
+DFLASH_ROWS_MATMUL_MAX = 160
+DFLASH_MAT_CTX, DFLASH_MAT_QKV, DFLASH_MAT_O, DFLASH_MAT_GATEUP, DFLASH_MAT_DOWN, DFLASH_MAT_LM = range(6)
+
+
 _lib = None
 SYMBOLS = ["dflash_workspace_bytes", "dflash_create", "dflash_project_ctx", "dflash_draft_block",
            "dflash_accept", "dflash_reset_request", "dflash_ctx_len", "dflash_check_errors",
            "dflash_get_stats", "dflash_set_probe", "dflash_launch_count", "dflash_destroy",
            "dflash_status_str", "dflash_greedy_from_logits_noalloc", "dflash_draft_lengths",
-           "dflash_accept_kept"]
+           "dflash_accept_kept", "dflash_rows_matmul_plan", "dflash_rows_matmul"]
 
 
 def lib():
@@ -143,6 +153,10 @@ def lib():
         L.dflash_draft_lengths.argtypes = [vp, i32, vp, vp, f32, vp, vp]
         L.dflash_accept_kept.restype = i32
         L.dflash_accept_kept.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+        L.dflash_rows_matmul_plan.restype = i32
+        L.dflash_rows_matmul_plan.argtypes = [i32, i32, i32, i32, i32, P(dflash_rows_plan)]
+        L.dflash_rows_matmul.restype = i32
+        L.dflash_rows_matmul.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp, i32, vp, ctypes.c_size_t, vp]
         _lib = L
     return _lib
 
@@ -154,6 +168,14 @@ def greedy_from_logits_noalloc(logits, token, conf=None, stream=None) -> int:
     return _check(lib().dflash_greedy_from_logits_noalloc(logits.data_ptr(), rows, vocab, token.data_ptr(),
                                                           conf.data_ptr() if conf is not None else None,
                                                           _stream_ptr(stream)), "dflash_greedy_from_logits_noalloc")
+
+
+def rows_matmul_plan(n_out: int, k_in: int, n_rows: int, x_lo: bool, n_sm: int) -> dflash_rows_plan:
+    """dflash_rows_matmul_plan: launch geometry and scratch of a many-row contraction (host only)."""
+    p = dflash_rows_plan()
+    _check(lib().dflash_rows_matmul_plan(n_out, k_in, n_rows, int(bool(x_lo)), n_sm, ctypes.byref(p)),
+           "dflash_rows_matmul_plan")
+    return p
 
 
 class DFlashError(RuntimeError):
@@ -272,6 +294,15 @@ class Handle:
         return _check(lib().dflash_accept(self.h, draft.shape[0], draft.data_ptr(), target.data_ptr(),
                                           accept_len.data_ptr(), next_anchor.data_ptr(), _stream_ptr(stream)),
                       "dflash_accept")
+
+    def rows_matmul(self, matrix, layer, x, y, scratch, x_lo=None, stream=None) -> int:
+        """y[r][n] = sum_k x[r][k] W[n][k] for a stored 4-bit matrix (DFLASH_MAT_*): x f16 [rows][ldx]
+        (int16 bits), x_lo its f16 remainder or None, y fp32 [rows][ldy], scratch a uint8 device
+        tensor of at least the plan's scratch_bytes (256-byte aligned)."""
+        return _check(lib().dflash_rows_matmul(self.h, matrix, layer, x.shape[0], x.data_ptr(),
+                                               x_lo.data_ptr() if x_lo is not None else None, x.stride(0),
+                                               y.data_ptr(), y.stride(0), scratch.data_ptr(), scratch.numel(),
+                                               _stream_ptr(stream)), "dflash_rows_matmul")
 
     def draft_lengths(self, conf, keep, thresholds=None, min_conf=0.0, stream=None) -> int:
         """Confidence-scheduled pruning: keep[i] = drafts of request i the target verifies."""

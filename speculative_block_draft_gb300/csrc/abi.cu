@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <new>
 
+#include "gemm_tc05.h"
 #include "internal.h"
 
 using namespace dfl;
@@ -316,17 +317,40 @@ typedef CUresult (*EncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, v
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
-  static EncodeTiled encode = nullptr;
-  if (!encode) {
+EncodeTiled tensor_map_encoder() {
+  static std::atomic<EncodeTiled> encode{nullptr};
+  EncodeTiled e = encode.load(std::memory_order_acquire);
+  if (!e) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
-      return DFLASH_ECUDA;
-    encode = reinterpret_cast<EncodeTiled>(fn);
+      return nullptr;
+    e = reinterpret_cast<EncodeTiled>(fn);
+    encode.store(e, std::memory_order_release);
   }
+  return e;
+}
+
+// f16 activation rows [rows][ld] as 2-D tiles of 64 inputs x box_rows rows in the 128-byte
+// swizzle (the K-major operand layout of the tcgen05 MMA); rows past `rows` read as zero.
+int make_rows_map(const void* base, int k, int rows, int ld, int box_rows, CUtensorMap* map) {
+  EncodeTiled encode = tensor_map_encoder();
+  if (!encode) return DFLASH_ECUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
+}
+
+int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
+  EncodeTiled encode = tensor_map_encoder();
+  if (!encode) return DFLASH_ECUDA;
   const dflash_config& c = h->cfg;
   const cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)h->cap,
                               (cuuint64_t)h->L * c.max_batch * c.n_kv_heads};
@@ -1054,6 +1078,71 @@ int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop
 }
 
 uint64_t dflash_launch_count(const dflash_handle* h) { return h ? h->launches : 0; }
+
+int dflash_rows_matmul_plan(int n_out, int k_in, int n_rows, int x_lo, int n_sm, dflash_rows_plan* plan) {
+  if (!plan || n_out < 1 || k_in < 64 || k_in % 64 || n_rows < 1 || n_sm < 1) return DFLASH_EINVAL;
+  if (n_rows > DFLASH_ROWS_MATMUL_MAX) return DFLASH_ECAPACITY;
+  const Tc05Plan p = plan_tc05((n_out + 15) / 16, k_in / 64, n_rows, x_lo != 0, n_sm);
+  if (p.npad == 0) return DFLASH_EINVAL;
+  plan->n_pad = p.npad;
+  plan->m_tiles = p.mtiles;
+  plan->k_slices = p.slices;
+  plan->groups_per_slice = p.gps;
+  plan->grid = p.grid;
+  plan->x_stages = p.sx;
+  plan->smem_bytes = p.smem;
+  plan->scratch_bytes = p.scratch;
+  return DFLASH_OK;
+}
+
+int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, const void* x, const void* x_lo,
+                       int ldx, float* y, int ldy, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!h || h->fmt != FMT_Q4 || !x || !y || !scratch || n_rows < 1) return DFLASH_EINVAL;
+  if (n_rows > DFLASH_ROWS_MATMUL_MAX) return DFLASH_ECAPACITY;
+  const bool per_layer = matrix == DFLASH_MAT_QKV || matrix == DFLASH_MAT_O || matrix == DFLASH_MAT_GATEUP ||
+                         matrix == DFLASH_MAT_DOWN;
+  if (per_layer && (layer < 0 || layer >= h->L)) return DFLASH_EINVAL;
+  const PackedMat* m = nullptr;
+  switch (matrix) {
+    case DFLASH_MAT_CTX: m = &h->wc; break;
+    case DFLASH_MAT_QKV: m = &h->qkv[layer]; break;
+    case DFLASH_MAT_O: m = &h->wo[layer]; break;
+    case DFLASH_MAT_GATEUP: m = &h->gu[layer]; break;
+    case DFLASH_MAT_DOWN: m = &h->down[layer]; break;
+    case DFLASH_MAT_LM: m = &h->lm; break;
+    default: return DFLASH_EINVAL;
+  }
+  const uintptr_t misalign = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x_lo);
+  if ((misalign & 15) || (reinterpret_cast<uintptr_t>(scratch) & 255) || ldx < m->k || ldx % 8 || ldy < m->n_rows)
+    return DFLASH_EINVAL;
+  const Tc05Plan p = plan_tc05(m->n_strips, m->groups, n_rows, x_lo != nullptr, h->n_sm);
+  if (p.npad == 0) return DFLASH_EINVAL;
+  if (scratch_bytes < p.scratch) return DFLASH_ECAPACITY;
+  Tc05Args a{};
+  if (make_rows_map(x, m->k, n_rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (x_lo && make_rows_map(x_lo, m->k, n_rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  a.w = m->w;
+  a.xs = reinterpret_cast<float*>(sc);
+  a.part = reinterpret_cast<float*>(sc + p.part_off);
+  a.err = h->err;
+  a.n_strips = m->n_strips;
+  a.groups = m->groups;
+  a.npad = p.npad;
+  a.gps = p.gps;
+  a.mtiles = p.mtiles;
+  a.has_lo = x_lo != nullptr;
+  a.n_out_pad = p.mtiles * 128;
+  a.sx = p.sx;
+  a.tmem_cols = p.tmem_cols;
+  a.x_stage = p.x_stage;
+  a.xs_off = p.xs_off;
+  a.x_tx = p.x_tx;
+  h->launches += 3;
+  const int half = matrix == DFLASH_MAT_GATEUP ? h->I : 0;
+  return status_of(launch_tc05(a, p, static_cast<const __half*>(x), static_cast<const __half*>(x_lo), ldx, n_rows,
+                               m->n_rows, half, y, ldy, static_cast<cudaStream_t>(stream)));
+}
 
 void dflash_destroy(dflash_handle* h) { delete h; }
 

@@ -1,0 +1,42 @@
+// Host-side declarations of the many-row tcgen05 contraction (gemm_tc05.cu), shared with abi.cu.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace dfl {
+
+constexpr unsigned kErrTimeoutTc05 = 4u;  // device error word bit of this kernel's bounded waits
+
+constexpr int kTcWarps = 12;              // copies, MMA issue, 2 decoder warps, 8 fold warps
+constexpr int kTcMaxRows = 160;           // activation rows per call (MMA N <= 160: the fold's sums fit in registers)
+constexpr int kTcSW = 6;                  // raw 4-bit tile stages
+constexpr int kTcSA = 2;                  // decoded f16 A-tile stages
+constexpr int kTcMaxSX = 4;               // activation stages, at most
+constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
+
+struct Tc05Args {
+  CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder: box 64 x npad, 128-byte swizzle
+  const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
+  float* xs;                 // [groups][npad] activation sums per group (scratch)
+  float* part;               // [slices][npad][n_out_pad] partial tiles (scratch)
+  unsigned* err;
+  int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, tmem_cols;
+  uint32_t x_stage, xs_off, x_tx;
+};
+
+struct Tc05Plan {
+  int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, tmem_cols = 0;   // npad == 0: no plan
+  uint32_t x_stage = 0, xs_off = 0, x_tx = 0;
+  size_t smem = 0, xs_bytes = 0, part_off = 0, scratch = 0;
+};
+
+Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
+
+// Group sums, the contraction and the ordered slice reduction into y [rows][ldy] (natural row
+// order of the matrix; half > 0: a gate/up matrix with `half` gate rows).
+cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
+                        int rows, int n_out, int half, float* y, int ldy, cudaStream_t s);
+
+}  // namespace dfl

@@ -37,14 +37,16 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layouts_match_c(tmp_path):
     src = tmp_path / "sz.c"
-    src.write_text('#include "dflash.h"\n#include <stdio.h>\n#include <stddef.h>\nint main(){printf("%zu %zu %zu %zu %zu %zu",'
+    src.write_text('#include "dflash.h"\n#include <stdio.h>\n#include <stddef.h>\nint main(){printf("%zu %zu %zu %zu %zu %zu %zu %zu",'
                    'sizeof(dflash_config), sizeof(dflash_matrix), sizeof(dflash_layer_weights), sizeof(dflash_weights),'
-                   'sizeof(dflash_stats), offsetof(dflash_weights, layer));return 0;}\n')
+                   'sizeof(dflash_stats), offsetof(dflash_weights, layer), sizeof(dflash_rows_plan),'
+                   'offsetof(dflash_rows_plan, smem_bytes));return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
     got = list(map(int, subprocess.check_output([str(exe)]).split()))
     want = [ctypes.sizeof(pkg.dflash_config), ctypes.sizeof(pkg.dflash_matrix), ctypes.sizeof(pkg.dflash_layer_weights),
-            ctypes.sizeof(pkg.dflash_weights), ctypes.sizeof(pkg.dflash_stats), pkg.dflash_weights.layer.offset]
+            ctypes.sizeof(pkg.dflash_weights), ctypes.sizeof(pkg.dflash_stats), pkg.dflash_weights.layer.offset,
+            ctypes.sizeof(pkg.dflash_rows_plan), pkg.dflash_rows_plan.smem_bytes.offset]
     assert got == want
 
 

@@ -1,0 +1,72 @@
+"""Host-side checks of the many-row tcgen05 contraction (dflash_rows_matmul): its launch plan's
+invariants over the drafter's matrix shapes, and argument validation before any launch. No GPU."""
+import ctypes
+
+import pytest
+
+import speculative_block_draft_gb300 as pkg
+
+SMEM_MAX = 232448          # dynamic shared memory a CTA may opt into on sm_103a (227 KB)
+TMEM_COLS = 512            # tensor-memory columns per SM
+
+# (n_out, k_in) of the 5120-wide drafter's stored matrices: W_c, QKV, O, gate/up, down, LM head;
+# plus a one-strip matrix, a matrix whose last 128-row tile is ragged, and one 64-input group
+SHAPES = [(5120, 25600), (7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408), (151936, 5120),
+          (16, 64), (200, 640), (48, 64)]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return pkg.lib()
+
+
+@pytest.mark.parametrize("n_out,k_in", SHAPES)
+@pytest.mark.parametrize("rows", [1, 15, 16, 17, 100, 128, 160])
+@pytest.mark.parametrize("x_lo", [0, 1])
+def test_plan_invariants(lib, n_out, k_in, rows, x_lo):
+    p = pkg.rows_matmul_plan(n_out, k_in, rows, x_lo, 152)
+    groups = k_in // 64
+    assert p.n_pad % 16 == 0 and rows <= p.n_pad < rows + 16            # the MMA's N
+    assert 2 * p.n_pad <= TMEM_COLS                                      # two fp32 accumulators
+    assert p.m_tiles == -(-n_out // 128)
+    assert p.grid == p.m_tiles * p.k_slices
+    # the K slices cover every group once, none empty, each at least 4 groups where K allows
+    assert (p.k_slices - 1) * p.groups_per_slice < groups <= p.k_slices * p.groups_per_slice
+    assert p.groups_per_slice >= min(4, groups)
+    assert 2 <= p.x_stages <= 4 and p.smem_bytes <= SMEM_MAX
+    # activation stage: n_pad rows x 128 B (twice with the remainder) + the group sums, whole KB
+    stage = -(-(p.n_pad * 128 * (2 if x_lo else 1) + 4 * p.n_pad) // 1024) * 1024
+    assert p.smem_bytes >= p.x_stages * stage + 2 * 128 * 128   # + two decoded 16 KB A tiles
+    # scratch: per-group activation sums, then one fp32 partial tile per (K slice, 128-row tile)
+    sums = -(-(groups * p.n_pad * 4) // 256) * 256
+    assert p.scratch_bytes == sums + p.k_slices * p.n_pad * p.m_tiles * 128 * 4
+
+
+def test_plan_fills_the_sms_where_k_allows(lib):
+    lm = pkg.rows_matmul_plan(151936, 5120, 128, 0, 152)        # 1187 tiles: no K split
+    assert (lm.m_tiles, lm.k_slices, lm.grid) == (1187, 1, 1187)
+    qkv = pkg.rows_matmul_plan(7168, 5120, 160, 1, 152)         # 56 tiles: split K three ways
+    assert (qkv.m_tiles, qkv.k_slices, qkv.groups_per_slice) == (56, 3, 27)
+    down = pkg.rows_matmul_plan(5120, 17408, 160, 0, 152)       # 40 tiles over 272 groups
+    assert down.k_slices == 4 and down.grid == 160
+    tiny = pkg.rows_matmul_plan(16, 64, 1, 0, 152)              # one tile, one group
+    assert (tiny.grid, tiny.k_slices, tiny.n_pad) == (1, 1, 16)
+
+
+def test_plan_rejects_bad_sizes(lib):
+    p = pkg.dflash_rows_plan()
+    L = lib
+    assert L.dflash_rows_matmul_plan(5120, 5120, 161, 0, 152, ctypes.byref(p)) == pkg.DFLASH_ECAPACITY
+    for args in ((5120, 5120, 0, 0, 152), (5120, 100, 16, 0, 152), (0, 5120, 16, 0, 152), (5120, 0, 16, 0, 152),
+                 (5120, 5120, 16, 0, 0)):
+        assert L.dflash_rows_matmul_plan(*args, ctypes.byref(p)) == pkg.DFLASH_EINVAL, args
+    assert L.dflash_rows_matmul_plan(5120, 5120, 16, 0, 152, None) == pkg.DFLASH_EINVAL
+
+
+def test_rows_matmul_validates_before_any_launch(lib):
+    # a NULL handle is refused on the host; nothing reaches the device
+    assert lib.dflash_rows_matmul(None, pkg.DFLASH_MAT_LM, 0, 16, None, None, 5120, None, 151936, None, 0,
+                                  None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_rows_matmul(None, pkg.DFLASH_MAT_QKV, 0, 161, None, None, 5120, None, 7168, None, 0,
+                                  None) == pkg.DFLASH_EINVAL
