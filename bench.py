@@ -283,6 +283,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--lat-steps", type=int, default=20,
+                    help="rounds timed one by one after the timed region, for the p10/p50/p90 round latency")
     ap.add_argument("--markov-rank", type=int, default=0,
                     help="add the Markov sequential head of this rank (not part of the headline workload)")
     ap.add_argument("--profile-ctx", type=int, default=0,
@@ -312,7 +314,7 @@ def main():
     model = syn.make_model(cfg)
     B, G, n = cfg.batch, cfg.gamma, cfg.n_draft
     sess = Session(model, max_batch=B, ctx_capacity=(cfg.window if cfg.window else
-                                                      cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + 8)))
+                                                      cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + args.lat_steps + 8)))
     h, stream = sess.h, sess.stream
     lengths = syn.ctx_lengths(cfg)
     if args.profile_ctx:
@@ -425,6 +427,28 @@ def main():
     e2e_t, e2e_blocks = reduce_over_ranks(e0.elapsed_time(e1) / 1e3, float(B * args.e2e_steps))
     e2e_value = e2e_blocks / e2e_t
 
+    # ---- round latency distribution: rounds bracketed one by one (after the timed region, so the
+    # headline is untouched; a bracketed round cannot overlap its neighbours) -------------------
+    latency = None
+    if args.lat_steps > 0:
+        try:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.lat_steps)]
+            with torch.cuda.stream(stream):
+                for i, (a0, a1) in enumerate(evs):
+                    a0.record(stream)
+                    step(args.warmup + i % args.steps)
+                    a1.record(stream)
+            stream.synchronize()
+            assert h.check_errors(stream) == 0
+            ms = np.array([a0.elapsed_time(a1) for a0, a1 in evs])
+            latency = {"rounds": int(ms.size), "p10_ms": float(np.percentile(ms, 10)),
+                       "p50_ms": float(np.percentile(ms, 50)), "p90_ms": float(np.percentile(ms, 90)),
+                       "how": "each round between its own CUDA events on the library's stream, after the "
+                              "timed region; no overlap with neighbouring rounds"}
+        except Exception as exc:   # the distribution is extra; it never costs the headline line
+            latency = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
     if rank != 0:
         sess.close()
         if ws > 1:
@@ -456,6 +480,8 @@ def main():
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
     }
+    if latency is not None:
+        line["round_latency"] = latency
     if not args.no_cpu_baseline and ws >= 1:
         threads = os.cpu_count() or 1
         times = oracle_round_seconds(cfg, model, rounds=2)
