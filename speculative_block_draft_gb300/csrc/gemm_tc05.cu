@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         st_shared_v4(row_8 + c0, r8[0][0], r8[0][1], r8[1][0], r8[1][1]);
         st_shared_v4(row_8 + c1, r8[2][0], r8[2][1], r8[3][0], r8[3][1]);
       }
-      fence_proxy_async();   // these generic-proxy stores are read by the tensor core (async proxy)
+      // the generic-proxy stores are read by the tensor core, and the raw stage is refilled by the
+      // copy engine (both async proxy)
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&full_a[sa]));
@@ -239,6 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         }
       }
       tc05_fence_before();
+      fence_proxy_async();   // these reads of the stages come before the copy engine refills them
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&acc_empty[b]));
