@@ -268,6 +268,7 @@ def workload_config(cfg) -> dict:
                          f"window{cfg.window} ctx{cfg.ctx_len} batch{cfg.batch} weights {cfg.wdtype}"),
             "requests": cfg.batch, "gamma": cfg.gamma, "ctx_len": cfg.ctx_len, "window": cfg.window,
             "new_ctx_rows_per_round": list(cfg.appends()),
+            **({"large_batch_tc05": True} if getattr(cfg, "large_batch_tc05", False) else {}),
             "l2": "no flush: every round streams >1.4 GB of weights, far above the 129 MB L2"}
 
 
@@ -287,12 +288,16 @@ def main():
                     help="rounds timed one by one after the timed region, for the p10/p50/p90 round latency")
     ap.add_argument("--markov-rank", type=int, default=0,
                     help="add the Markov sequential head of this rank (not part of the headline workload)")
+    ap.add_argument("--large-batch-tc05", action="store_true",
+                    help="library option: draft calls of more than 32 block rows on the tcgen05 contraction")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="prefill only this many context rows (for short profiler captures; not a bench value)")
     args = ap.parse_args()
     cfg = syn.CONFIGS[args.config]
     if args.markov_rank:
         cfg = syn.with_overrides(cfg, markov_rank=args.markov_rank)
+    if args.large_batch_tc05:
+        cfg = syn.with_overrides(cfg, large_batch_tc05=True)
     if args.impl == "reference":
         return run_reference(args, cfg)
 

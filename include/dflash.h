@@ -93,6 +93,14 @@ typedef struct {
                          drafts are taken in order and draft k's logits get the bias
                          W1[prev_k] W2 before its argmax (prev_0 = the anchor, prev_k = draft k-1);
                          weights markov_w1 [V][r] and markov_w2t [V][r] (= W2 transposed) */
+  int large_batch_tc05; /* 0 (default): dflash_draft_block runs every projection as the skinny GEMV,
+                         in launches of at most 32 activation rows. 1: a call with more than 32 and
+                         at most DFLASH_ROWS_MATMUL_MAX block rows runs its Q/K/V, O, gate/up, down
+                         and LM-head projections once over all its rows on the tcgen05 contraction
+                         (as dflash_rows_matmul), followed by the same epilogues; it applies to 4-bit
+                         weights with d == H and no Markov head, other calls use the GEMV. The
+                         workspace grows by the contraction's scratch. Experimental: not yet
+                         covered by the parity tests. */
 } dflash_config;
 
 typedef struct {

@@ -60,6 +60,10 @@ struct dflash_handle {
   unsigned* err = nullptr;
   size_t partial_floats = 0;
   int ticket_count = 0, lm_grid_max = 0, att_pairs_max = 0;
+  // many-row draft calls on the tcgen05 contraction (config large_batch_tc05)
+  int tc05_on = 0, tc05_rows = 0;
+  uint8_t* tc05_scratch = nullptr;
+  size_t tc05_scratch_bytes = 0;
   CUtensorMap kmap{}, vmap{};
 
   int64_t ctx_len[DFLASH_MAX_BATCH] = {};
@@ -168,6 +172,7 @@ bool valid_config(const dflash_config* c) {
   if (c->ffn_act != DFLASH_FFN_SWIGLU && c->ffn_act != DFLASH_FFN_GELU) return false;
   if (c->draft_all_rows != 0 && c->draft_all_rows != 1) return false;
   if (c->markov_rank < 0 || c->markov_rank > 1024 || c->markov_rank % 64) return false;
+  if (c->large_batch_tc05 != 0 && c->large_batch_tc05 != 1) return false;
   if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
   if (c->adtype == DFLASH_F32) {
     if (c->wdtype != DFLASH_F32) return false;
@@ -282,6 +287,25 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->att_o = cv.take<float>((size_t)h->att_pairs_max * 64 * c.head_dim * 4);
   h->att_ml = cv.take<float>((size_t)h->att_pairs_max * 64 * 2 * 4);
   h->err = cv.take<unsigned>(4);
+  // the tcgen05 contraction's scratch: the largest plan over the block projections and the head
+  h->tc05_on = 0;
+  h->tc05_rows = std::min(c.max_batch * h->G, kTcMaxRows);
+  if (c.large_batch_tc05 && h->fmt == FMT_Q4 && !h->act_f32 && h->d == h->H && !c.markov_rank &&
+      h->tc05_rows > kMaxRows) {
+    size_t sc = 0;
+    auto need = [&](const PackedMat& m, int lo) {
+      const Tc05Plan p = plan_tc05(m.n_strips, m.groups, h->tc05_rows, lo, h->n_sm);
+      sc = std::max(sc, p.scratch);
+    };
+    need(h->qkv[0], 1);
+    need(h->wo[0], 0);
+    need(h->gu[0], 1);
+    need(h->down[0], 0);
+    need(h->lm, 1);
+    h->tc05_on = sc > 0;
+    h->tc05_scratch_bytes = sc;
+    h->tc05_scratch = cv.take<uint8_t>(sc);
+  }
   (void)state_begin;
   return round_up(cv.off, 256);
 }
@@ -472,6 +496,76 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out =
   }
   h->launches++;
   return status_of(launch_gemv(h->fmt, c.epi, nt_for(c.R), a, p.grid * grp, s));
+}
+
+// Many-row draft calls: one tcgen05 contraction over rows [0, rows) of x (f16 [rows][ldx], the
+// f16 remainder at element offset lo_off when nonzero) into the handle's scratch (partial tiles).
+int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x, int ldx, long long lo_off,
+                   cudaStream_t s, Tc05Plan* out) {
+  const Tc05Plan p = plan_tc05(m.n_strips, m.groups, rows, lo_off != 0, h->n_sm);
+  if (p.npad == 0 || p.scratch > h->tc05_scratch_bytes) return DFLASH_EINVAL;
+  const void* xl = lo_off ? static_cast<const void*>(static_cast<const __half*>(x) + lo_off) : nullptr;
+  Tc05Args a{};
+  if (make_rows_map(x, m.k, rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (xl && make_rows_map(xl, m.k, rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  a.w = m.w;
+  a.xs = reinterpret_cast<float*>(h->tc05_scratch);
+  a.part = reinterpret_cast<float*>(h->tc05_scratch + p.part_off);
+  a.err = h->err;
+  a.n_strips = m.n_strips;
+  a.groups = m.groups;
+  a.npad = p.npad;
+  a.gps = p.gps;
+  a.mtiles = p.mtiles;
+  a.has_lo = xl != nullptr;
+  a.n_out_pad = p.mtiles * 128;
+  a.sx = p.sx;
+  a.tmem_cols = p.tmem_cols;
+  a.x_stage = p.x_stage;
+  a.xs_off = p.xs_off;
+  a.x_tx = p.x_tx;
+  *out = p;
+  h->launches += 2;
+  return status_of(launch_tc05_parts(a, p, static_cast<const __half*>(x), static_cast<const __half*>(xl), ldx,
+                                     rows, s));
+}
+
+// The epilogue of one chunk of a projection (described as for run_gemv) from the contraction's
+// partial tiles; the chunk's row c is contraction row row_base + map_row(c.xmap, c).
+int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row_base, cudaStream_t s,
+                 int* grid_out = nullptr) {
+  const PackedMat& m = *c.m;
+  if (c.R <= 0) return DFLASH_OK;
+  GemvArgs a{};
+  a.w = m.w;
+  a.strip0 = 0;
+  a.n_strips = m.n_strips;
+  a.k = m.k;
+  a.groups = m.groups;
+  a.n_slices = 1;
+  a.gps = m.groups;
+  a.ctas_per_slice = 1;
+  a.R = c.R;
+  a.xmap = c.xmap;
+  a.norm_mode = c.norm_mode;
+  a.ssq = c.ssq;
+  a.ssq_ld = c.ssq_ld;
+  a.ssq_parts = c.ssq_parts;
+  a.inv_dim = c.inv_dim;
+  a.eps = h->cfg.eps;
+  a.err = h->err;
+  a.e = c.e;
+  if (c.epi == EPI_LMHEAD) {
+    a.e.lm_part = h->lm_part;
+    a.e.lm_strip = h->lm_strip;
+  }
+  int grid = (m.n_strips + kF32Warps - 1) / kF32Warps;
+  grid = std::max(1, std::min(grid, c.epi == EPI_LMHEAD ? h->lm_grid_max : 4 * h->n_sm));
+  if (grid_out) *grid_out = grid;
+  h->launches++;
+  return status_of(launch_tc05_epilogue(c.epi, nt_for(c.R), a,
+                                        reinterpret_cast<const float*>(h->tc05_scratch + p.part_off), p.slices,
+                                        p.npad, p.mtiles * 128, row_base, grid, s));
 }
 
 }  // namespace
@@ -767,9 +861,16 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   if ((st = status_of(launch_block_init(ba, s)))) return st;
 
   const int req_per_chunk = std::max(1, kMaxRows / G);
+  // many rows: each projection runs once over all block rows on the tcgen05 contraction, then
+  // its epilogue per chunk (the chunks' row scales, residuals and outputs are those of the GEMV)
+  const int rows_all = n_req * G;
+  const bool tc = h->tc05_on && rows_all > kMaxRows && rows_all <= h->tc05_rows;
+  Tc05Plan tp{};
+  auto project = [&](GemvCall& c, int r0) { return tc ? run_tc05_epi(h, c, tp, r0, s) : run_gemv(h, c, s); };
   for (int i = 0; i < h->L; i++) {
     const int in_parts = i == 0 ? (d + kBlockCols - 1) / kBlockCols : parts;
     // Q, K_d, V_d of RMSNorm_attn_i(H_d)
+    if (tc && (st = run_tc05_parts(h, h->qkv[i], rows_all, h->xn, d, lo_if(LO_QKV, xn_lo(h)), s, &tp))) return st;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       GemvCall cq;
@@ -790,7 +891,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cq.e.vb = off(h->vb, r0, h->kvd);
       cq.e.qd = h->qd;
       cq.e.kvd = h->kvd;
-      if ((st = run_gemv(h, cq, s))) return st;
+      if ((st = project(cq, r0))) return st;
     }
     // attention over [windowed context ++ block], no causal mask
     {
@@ -842,6 +943,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         }
       }
     }
+    if (tc && (st = run_tc05_parts(h, h->wo[i], rows_all, h->attn, h->qd, 0, s, &tp))) return st;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // H_d += W_o attn; next input = H_d * ff_norm_i (+ sums of squares)
@@ -859,8 +961,9 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       co.e.x_lo_off = xn_lo(h);
       co.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       co.e.ssq_ld = h->ssq_ld;
-      if ((st = run_gemv(h, co, s))) return st;
+      if ((st = project(co, r0))) return st;
     }
+    if (tc && (st = run_tc05_parts(h, h->gu[i], rows_all, h->xn, d, lo_if(LO_GU, xn_lo(h)), s, &tp))) return st;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // a = act(W_gate n2) * (W_up n2), n2 = RMSNorm_ff_i(H_d); act = SiLU or GELU (tanh form)
@@ -880,8 +983,9 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cg.e.act = off(h->act, r0, h->I);
       cg.e.inter = h->I;
       cg.e.ffn_act = c.ffn_act;
-      if ((st = run_gemv(h, cg, s))) return st;
+      if ((st = project(cg, r0))) return st;
     }
+    if (tc && (st = run_tc05_parts(h, h->down[i], rows_all, h->act, h->I, 0, s, &tp))) return st;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // H_d += W_down a; next input = H_d * (attn_norm_{i+1} | out_norm)
@@ -899,13 +1003,16 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cd.e.x_lo_off = xn_lo(h);
       cd.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       cd.e.ssq_ld = h->ssq_ld;
-      if ((st = run_gemv(h, cd, s))) return st;
+      if ((st = project(cd, r0))) return st;
     }
   }
 
   // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (drafting rows)
   const int lm_req_per_chunk = std::max(1, kMaxRows / n);
   if (h->probe_start) cudaEventRecord(h->probe_start, s);
+  // many rows (d == H, no Markov head): the head over every block row once; the epilogue reads
+  // the drafting rows through the chunk's row map
+  if (tc && (st = run_tc05_parts(h, h->lm, rows_all, h->xn, d, lo_if(LO_LM, xn_lo(h)), s, &tp))) return st;
   for (int b0 = 0; b0 < n_req; b0 += lm_req_per_chunk) {
     const int nb = std::min(lm_req_per_chunk, n_req - b0);
     const int r0 = b0 * G, l0 = b0 * n, R = nb * n;
@@ -950,13 +1057,15 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     cl.e.logits = markov ? h->mk_base + (size_t)l0 * h->V : (logits ? logits + (size_t)l0 * h->V : nullptr);
     cl.e.vocab = h->V;
     GemvPlan lp{};
-    if ((st = run_gemv(h, cl, s, &lp))) return st;
+    int epi_grid = 0;
+    if ((st = tc ? run_tc05_epi(h, cl, tp, r0, s, &epi_grid) : run_gemv(h, cl, s, &lp))) return st;
     if (markov) continue;
     // merge the per-CTA (one K slice) or per-strip (K split) vocab states: token and confidence
-    const bool split = h->fmt != FMT_F32 && lp.n_slices > 1;
+    const bool split = !tc && h->fmt != FMT_F32 && lp.n_slices > 1;
     h->launches++;
-    if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part, split ? h->lm.n_strips : lp.grid, R,
-                                         draft + l0, conf ? conf + l0 : nullptr, 1, s))))
+    if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part,
+                                         tc ? epi_grid : (split ? h->lm.n_strips : lp.grid), R, draft + l0,
+                                         conf ? conf + l0 : nullptr, 1, s))))
       return st;
   }
   if (c.markov_rank) {

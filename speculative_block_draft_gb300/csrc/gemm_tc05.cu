@@ -339,8 +339,8 @@ Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) {
   return p;
 }
 
-cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
-                        int rows, int n_out, int half, float* y, int ldy, cudaStream_t s) {
+cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
+                              int rows, cudaStream_t s) {
   tc05_xsum_kernel<<<std::min(1024, (a.groups * a.npad + 255) / 256), 256, 0, s>>>(x, xlo, ldx, rows, a.groups,
                                                                                   a.npad, const_cast<float*>(a.xs));
   cudaError_t e = cudaGetLastError();
@@ -349,7 +349,12 @@ cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, c
   e = ensure_smem_limit(tc05_q4_kernel, p.smem, smem_set);
   if (e != cudaSuccess) return e;
   tc05_q4_kernel<<<p.grid, kTcThreads, p.smem, s>>>(a);
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
+                        int rows, int n_out, int half, float* y, int ldy, cudaStream_t s) {
+  const cudaError_t e = launch_tc05_parts(a, p, x, xlo, ldx, rows, s);
   if (e != cudaSuccess) return e;
   const long long total = (long long)rows * n_out;
   const int blocks = (int)std::min<long long>(4096, (total + 255) / 256);

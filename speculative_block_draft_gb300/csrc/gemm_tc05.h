@@ -34,9 +34,20 @@ struct Tc05Plan {
 
 Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
 
-// Group sums, the contraction and the ordered slice reduction into y [rows][ldy] (natural row
-// order of the matrix; half > 0: a gate/up matrix with `half` gate rows).
+// Group sums and the contraction: partial tiles [slices][npad][n_out_pad] in a.part (stored row order).
+cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
+                              int rows, cudaStream_t s);
+
+// launch_tc05_parts, then the ordered slice reduction into y [rows][ldy] (natural row order of
+// the matrix; half > 0: a gate/up matrix with `half` gate rows).
 cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
                         int rows, int n_out, int half, float* y, int ldy, cudaStream_t s);
+
+// A draft-round projection's epilogue (EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
+// partial tiles, through the skinny GEMV's strip epilogues: `a` describes the launch as for the
+// GEMV (a.R <= kMaxRows rows, nt = n-tiles of 8) with a.n_slices == 1; its row c is contraction
+// row row_base + map_row(a.xmap, c). LM head: one vocab state per CTA and row in a.e.lm_part.
+cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
+                                 int n_out_pad, int row_base, int grid, cudaStream_t s);
 
 }  // namespace dfl

@@ -1,0 +1,81 @@
+// Epilogues of the draft round's projections when they run on the many-row tcgen05 contraction:
+// the K slices' partial tiles are summed in slice order and handed, one 16-row strip per warp,
+// to the same strip epilogues the skinny GEMV fuses (row-norm scale, Q/K/V split, residual +
+// next norm input + sums of squares, gated FFN, vocab states). Rows of the contraction are
+// whole block rows; row c of a launch is contraction row row_base + map_row(xmap, c).
+#include "gemm_tc05.h"
+#include "gemv_impl.cuh"
+
+namespace dfl {
+
+namespace {
+
+template <int NT, int EPI>
+__global__ void __launch_bounds__(kF32Warps * 32)
+    tc05_epi_kernel(const __grid_constant__ GemvArgs a, const float* __restrict__ part, int slices, int npad,
+                    int n_out_pad, int row_base) {
+  constexpr int RP = NT * 8;
+  __shared__ float srow[kMaxRows];
+  __shared__ LmState sm_lm[kF32Warps * kMaxRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  compute_row_scales(a, srow, RP);
+  __syncthreads();
+  LmState lm[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+    for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
+  const size_t slice_stride = (size_t)npad * n_out_pad;
+  for (int sl = blockIdx.x * kF32Warps + warp; sl < a.n_strips; sl += gridDim.x * kF32Warps) {
+    const int strip = a.strip0 + sl;
+    float y[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+      for (int p = 0; p < 2; p++) {
+        const int c = nt * 8 + 2 * t + p;
+        float y0 = 0.f, y1 = 0.f;
+        if (c < a.R) {
+          const float* src = part + (size_t)(row_base + map_row(a.xmap, c)) * n_out_pad + strip * 16 + g;
+          for (int s = 0; s < slices; s++) {
+            y0 += __ldcg(src + s * slice_stride);
+            y1 += __ldcg(src + s * slice_stride + 8);
+          }
+        }
+        y[nt][p] = y0;
+        y[nt][2 + p] = y1;
+      }
+    EpiPre<NT> pre;
+    epi_preload<EPI, NT, __half>(a, strip, pre);
+    strip_epilogue<EPI, NT, __half>(a, strip, y, srow, lm, 0, pre);
+  }
+  if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
+}
+
+template <int EPI>
+cudaError_t launch_epi(int nt, const GemvArgs& a, const float* part, int slices, int npad, int n_out_pad,
+                       int row_base, int grid, cudaStream_t s) {
+  switch (nt) {
+    case 1: tc05_epi_kernel<1, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
+    case 2: tc05_epi_kernel<2, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
+    case 3: tc05_epi_kernel<3, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
+    case 4: tc05_epi_kernel<4, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
+                                 int n_out_pad, int row_base, int grid, cudaStream_t s) {
+  switch (epi) {
+    case EPI_QKV: return launch_epi<EPI_QKV>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
+    case EPI_RESID: return launch_epi<EPI_RESID>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
+    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dfl

@@ -57,7 +57,8 @@ def test_host_validation_without_gpu(lib):
     good = pkg.make_config(syn.CONFIGS["c3"])
     assert lib.dflash_workspace_bytes(ctypes.byref(good)) > 1_400_000_000   # repacked drafter + head
     for field, val in (("head_dim", 96), ("gamma", 1), ("gamma", 17), ("max_batch", 65), ("adtype", 7),
-                       ("ffn_act", 2), ("draft_all_rows", 2), ("markov_rank", 96), ("markov_rank", 2048)):
+                       ("ffn_act", 2), ("draft_all_rows", 2), ("markov_rank", 96), ("markov_rank", 2048),
+                       ("large_batch_tc05", 2), ("large_batch_tc05", -1)):
         c = pkg.make_config(syn.CONFIGS["c3"])
         setattr(c, field, val)
         assert lib.dflash_workspace_bytes(ctypes.byref(c)) == 0, field

@@ -70,3 +70,29 @@ def test_rows_matmul_validates_before_any_launch(lib):
                                   None) == pkg.DFLASH_EINVAL
     assert lib.dflash_rows_matmul(None, pkg.DFLASH_MAT_QKV, 0, 161, None, None, 5120, None, 7168, None, 0,
                                   None) == pkg.DFLASH_EINVAL
+
+
+def test_large_batch_option_carves_the_contraction_scratch(lib):
+    """large_batch_tc05 = 1 adds exactly the largest contraction scratch over the block projections
+    and the head (at max_batch * gamma rows, capped at 160) to the workspace; it adds nothing where
+    the option does not apply (one request of 8 rows, 16-bit weights, or a Markov head)."""
+    import dflash_synth as syn
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("the workspace plan uses the device's SM count; checked here with the host default")
+    cfg = syn.CONFIGS["c5"]
+    off = pkg.make_config(cfg)
+    on = pkg.make_config(syn.with_overrides(cfg, large_batch_tc05=True))
+    rows = min(cfg.batch * cfg.gamma, pkg.DFLASH_ROWS_MATMUL_MAX)
+    qkv = cfg.n_q_heads * cfg.head_dim + 2 * cfg.n_kv_heads * cfg.head_dim
+    shapes = [(qkv, cfg.d), (cfg.d, cfg.n_q_heads * cfg.head_dim), (2 * cfg.inter, cfg.d), (cfg.d, cfg.inter),
+              (cfg.vocab, cfg.d)]
+    n_sm = 148   # the library's default when no device is present
+    want = max(pkg.rows_matmul_plan(n, k, rows, 0, n_sm).scratch_bytes for n, k in shapes)
+    want = -(-want // 256) * 256
+    diff = lib.dflash_workspace_bytes(ctypes.byref(on)) - lib.dflash_workspace_bytes(ctypes.byref(off))
+    assert diff == want
+    for over in (dict(batch=1, gamma=8), dict(wdtype="bf16"), dict(markov_rank=64)):
+        a = pkg.make_config(syn.with_overrides(cfg, **over))
+        b = pkg.make_config(syn.with_overrides(cfg, large_batch_tc05=True, **over))
+        assert lib.dflash_workspace_bytes(ctypes.byref(b)) == lib.dflash_workspace_bytes(ctypes.byref(a)), over
