@@ -227,6 +227,42 @@ def oracle_round_seconds(cfg, model, rounds: int = 1, scale_rows: int = 1):
     return [(time.perf_counter() - t0) * scale_rows]
 
 
+def set_oracle_threads(n: int):
+    """OpenMP threads of the oracle's shared library (the process's one OpenMP runtime)."""
+    import ctypes
+    import ctypes.util
+    import oracle
+    oracle._load()
+    gomp = ctypes.CDLL(ctypes.util.find_library("gomp") or "libgomp.so.1")
+    gomp.omp_set_num_threads(int(n))
+
+
+def oracle_table(names=("c1", "c2", "c3", "c5")):
+    """Oracle blocks/s for one round on 1 core and on all cores, per workload. A round of a
+    batched workload is its requests' rounds in sequence (requests are independent, and with the
+    window every request attends to the same number of keys), timed as request 0's round x B.
+    Large drafters on 1 core time a 1/16 row sample of every matrix (attention, <1% of the work,
+    left out), scaled back up."""
+    import platform
+    cores = os.cpu_count() or 1
+    out = []
+    for name in names:
+        cfg = syn.CONFIGS[name]
+        model = syn.make_model(cfg)
+        big = cfg.d * cfg.inter >= 4096 * 4096
+        for threads in sorted({1, cores}):
+            set_oracle_threads(threads)
+            scale = 16 if (big and threads == 1) else 1
+            t_req = oracle_round_seconds(cfg, model, rounds=1, scale_rows=scale)[0]
+            out.append({"config": name, "threads": threads, "round_s": t_req * cfg.batch,
+                        "blocks_per_s": 1.0 / t_req,
+                        "sample": ("full round of request 0" if scale == 1 else
+                                   f"projections on 1/{scale} of every matrix's rows, x{scale}")
+                                  + (f", round = {cfg.batch} x request 0" if cfg.batch > 1 else "")})
+    set_oracle_threads(cores)
+    return {"oracle_table": out, "cores": cores, "host": platform.machine()}
+
+
 def run_reference(args, cfg):
     """The CPU oracle as the reference arm, on this arm's workload and metric."""
     rank, ws, _ = dist_env()
@@ -288,11 +324,16 @@ def main():
                     help="rounds timed one by one after the timed region, for the p10/p50/p90 round latency")
     ap.add_argument("--markov-rank", type=int, default=0,
                     help="add the Markov sequential head of this rank (not part of the headline workload)")
+    ap.add_argument("--oracle-table", default="",
+                    help="comma-separated workloads: print the oracle's 1-core / all-core round times and exit")
     ap.add_argument("--large-batch-tc05", action="store_true",
                     help="library option: draft calls of more than 32 block rows on the tcgen05 contraction")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="prefill only this many context rows (for short profiler captures; not a bench value)")
     args = ap.parse_args()
+    if args.oracle_table:
+        print(json.dumps(oracle_table(tuple(args.oracle_table.split(",")))), flush=True)
+        return 0
     cfg = syn.CONFIGS[args.config]
     if args.markov_rank:
         cfg = syn.with_overrides(cfg, markov_rank=args.markov_rank)

@@ -1,5 +1,5 @@
-"""The bench's multi-GPU host logic (replicas: max elapsed over ranks, units summed) on CPU with
-gloo, world size 2."""
+"""The bench's host logic on CPU: the multi-GPU replicas (max elapsed over ranks, units summed;
+gloo, world size 2) and the oracle timing table."""
 import os
 import sys
 
@@ -41,3 +41,13 @@ def test_round_bytes_match_the_c3_budget():
     b = bench.round_bytes(syn.CONFIGS["c3"], [4096])
     assert abs(b["total"] / 1e6 - 1482.2) < 0.5          # layers 929.0 + head 437.6 + W_c 73.7 + KV 41.9
     assert abs(b["lm_head"] / 1e6 - 437.6) < 0.1
+
+
+def test_oracle_table_one_core_and_all_cores():
+    """The oracle timing table (1 core and all cores per workload) on the tiny fp32 drafter."""
+    import bench
+    t = bench.oracle_table(("c1",))
+    rows = t["oracle_table"]
+    assert {r["threads"] for r in rows} == {1, t["cores"]}
+    for r in rows:
+        assert r["config"] == "c1" and r["round_s"] > 0 and abs(r["blocks_per_s"] * r["round_s"] - 1) < 1e-9
