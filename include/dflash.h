@@ -97,10 +97,12 @@ typedef struct {
                          in launches of at most 32 activation rows. 1: a call with more than 32 and
                          at most DFLASH_ROWS_MATMUL_MAX block rows runs its Q/K/V, O, gate/up, down
                          and LM-head projections once over all its rows on the tcgen05 contraction
-                         (as dflash_rows_matmul), followed by the same epilogues; it applies to 4-bit
-                         weights with d == H and no Markov head, other calls use the GEMV. The
-                         workspace grows by the contraction's scratch. Experimental: not yet
-                         covered by the parity tests. */
+                         (as dflash_rows_matmul), followed by the same epilogues; likewise
+                         dflash_project_ctx runs W_c once per 160 context rows when a call appends
+                         more than 32. It applies to 4-bit weights with d == H and no Markov head;
+                         other calls use the GEMV. The workspace grows by the contraction's scratch
+                         and an f16 copy of 160 tap rows. Experimental: not yet covered by the
+                         parity tests. */
 } dflash_config;
 
 typedef struct {

@@ -64,6 +64,7 @@ struct dflash_handle {
   int tc05_on = 0, tc05_rows = 0;
   uint8_t* tc05_scratch = nullptr;
   size_t tc05_scratch_bytes = 0;
+  void* tc05_taps = nullptr;    // [kTcMaxRows][n_taps * H] f16: context taps converted for TMA
   CUtensorMap kmap{}, vmap{};
 
   int64_t ctx_len[DFLASH_MAX_BATCH] = {};
@@ -302,9 +303,12 @@ size_t carve(dflash_handle* h, uint8_t* base) {
     need(h->gu[0], 1);
     need(h->down[0], 0);
     need(h->lm, 1);
+    const Tc05Plan pc = plan_tc05(h->wc.n_strips, h->wc.groups, kTcMaxRows, 0, h->n_sm);   // context rows
+    sc = std::max(sc, pc.scratch);
     h->tc05_on = sc > 0;
     h->tc05_scratch_bytes = sc;
     h->tc05_scratch = cv.take<uint8_t>(sc);
+    h->tc05_taps = cv.take<void>((size_t)kTcMaxRows * h->mH * 2);
   }
   (void)state_begin;
   return round_up(cv.off, 256);
@@ -705,7 +709,20 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   // rows in call order: (slot, position)
   int req_i = 0, j_in = 0;
   int64_t row = 0;
+  // many rows: W_c runs once per kTcMaxRows rows on the tcgen05 contraction (a whole number of
+  // chunks), then each chunk's epilogue and its context K/V launch as below
+  const bool tc = h->tc05_on && total > kMaxCtxChunk;
+  Tc05Plan wcp{};
+  int64_t tc_row0 = 0;
   while (row < total) {
+    if (tc && (row == 0 || row - tc_row0 >= kTcMaxRows)) {
+      tc_row0 = row;
+      const int rows = (int)std::min<int64_t>(kTcMaxRows, total - row);
+      h->launches++;
+      int st = status_of(launch_bf16_to_f16(tp + (size_t)row * h->mH * ab, (long long)rows * h->mH, h->tc05_taps, s));
+      if (!st) st = run_tc05_parts(h, h->wc, rows, h->tc05_taps, h->mH, 0, s, &wcp);
+      if (st) return st;
+    }
     const int rc = (int)std::min<int64_t>(kMaxCtxChunk, total - row);
     int slots[kMaxCtxChunk], pos[kMaxCtxChunk];
     for (int r = 0; r < rc; r++) {
@@ -738,7 +755,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.x_lo_off = xw_lo(h);
     c1.e.ssq_out = h->ssq_ctx;
     c1.e.ssq_ld = h->ssq_ld;
-    int st = run_gemv(h, c1, s);
+    int st = tc ? run_tc05_epi(h, c1, wcp, (int)(row - tc_row0), s) : run_gemv(h, c1, s);
     if (st) return st;
     // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache; the
     // tensor-core path runs every layer in one grouped launch over the same input rows (the

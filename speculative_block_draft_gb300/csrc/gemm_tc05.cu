@@ -307,7 +307,28 @@ __global__ void __launch_bounds__(256) tc05_reduce_kernel(const float* __restric
   }
 }
 
+// Caller-side bf16 rows (context taps) -> f16, as the skinny GEMV stages them (round to
+// nearest, clamped to the f16 range). n_pairs element pairs.
+__global__ void __launch_bounds__(256) tc05_bf16_to_f16_kernel(const uint32_t* __restrict__ src, long long n_pairs,
+                                                               uint32_t* __restrict__ dst) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_pairs;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t u = src[i];
+    const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xFFFF0000u);
+    dst[i] = pack_f16x2(fminf(fmaxf(lo, -kF16Max), kF16Max), fminf(fmaxf(hi, -kF16Max), kF16Max));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cudaStream_t s) {
+  const long long pairs = n_elems / 2;
+  const int blocks = (int)std::min<long long>(4096, (pairs + 255) / 256);
+  if (blocks < 1) return cudaSuccess;
+  tc05_bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint32_t*>(src), pairs,
+                                                  static_cast<uint32_t*>(dst));
+  return cudaGetLastError();
+}
 
 Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) {
   Tc05Plan p{};

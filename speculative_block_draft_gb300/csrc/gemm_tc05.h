@@ -43,7 +43,10 @@ cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, const __half
 cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
                         int rows, int n_out, int half, float* y, int ldy, cudaStream_t s);
 
-// A draft-round projection's epilogue (EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
+// bf16 -> f16 of n_elems (even) contiguous elements, as the skinny GEMV converts context taps.
+cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cudaStream_t s);
+
+// A draft-round projection's epilogue (EPI_CTX, EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
 // partial tiles, through the skinny GEMV's strip epilogues: `a` describes the launch as for the
 // GEMV (a.R <= kMaxRows rows, nt = n-tiles of 8) with a.n_slices == 1; its row c is contraction
 // row row_base + map_row(a.xmap, c). LM head: one vocab state per CTA and row in a.e.lm_part.

@@ -1,8 +1,8 @@
-// Epilogues of the draft round's projections when they run on the many-row tcgen05 contraction:
-// the K slices' partial tiles are summed in slice order and handed, one 16-row strip per warp,
-// to the same strip epilogues the skinny GEMV fuses (row-norm scale, Q/K/V split, residual +
-// next norm input + sums of squares, gated FFN, vocab states). Rows of the contraction are
-// whole block rows; row c of a launch is contraction row row_base + map_row(xmap, c).
+// Epilogues of the round's projections when they run on the many-row tcgen05 contraction. The K
+// slices' partial tiles are summed in slice order and handed, one 16-row strip per warp, to the
+// same strip epilogues the skinny GEMV fuses: context rows x ctx_norm with sums of squares,
+// row-norm scale, Q/K/V split, residual with next norm input and sums of squares, gated FFN, and
+// vocab states. Row c of a launch is contraction row row_base + map_row(xmap, c).
 #include "gemm_tc05.h"
 #include "gemv_impl.cuh"
 
@@ -70,6 +70,7 @@ cudaError_t launch_epi(int nt, const GemvArgs& a, const float* part, int slices,
 cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
                                  int n_out_pad, int row_base, int grid, cudaStream_t s) {
   switch (epi) {
+    case EPI_CTX: return launch_epi<EPI_CTX>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
     case EPI_QKV: return launch_epi<EPI_QKV>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
     case EPI_RESID: return launch_epi<EPI_RESID>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);

@@ -73,9 +73,10 @@ def test_rows_matmul_validates_before_any_launch(lib):
 
 
 def test_large_batch_option_carves_the_contraction_scratch(lib):
-    """large_batch_tc05 = 1 adds exactly the largest contraction scratch over the block projections
-    and the head (at max_batch * gamma rows, capped at 160) to the workspace; it adds nothing where
-    the option does not apply (one request of 8 rows, 16-bit weights, or a Markov head)."""
+    """large_batch_tc05 = 1 adds exactly the largest contraction scratch (the block projections and
+    the head at max_batch * gamma rows, capped at 160; W_c at 160 context rows) and the f16 copy of
+    160 context-tap rows to the workspace. It adds nothing where the option does not apply (one
+    request of 8 rows, 16-bit weights, or a Markov head)."""
     import dflash_synth as syn
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
@@ -88,8 +89,11 @@ def test_large_batch_option_carves_the_contraction_scratch(lib):
     shapes = [(qkv, cfg.d), (cfg.d, cfg.n_q_heads * cfg.head_dim), (2 * cfg.inter, cfg.d), (cfg.d, cfg.inter),
               (cfg.vocab, cfg.d)]
     n_sm = 148   # the library's default when no device is present
-    want = max(pkg.rows_matmul_plan(n, k, rows, 0, n_sm).scratch_bytes for n, k in shapes)
+    mh = cfg.n_taps * cfg.target_hidden
+    want = max([pkg.rows_matmul_plan(n, k, rows, 0, n_sm).scratch_bytes for n, k in shapes] +
+               [pkg.rows_matmul_plan(cfg.d, mh, pkg.DFLASH_ROWS_MATMUL_MAX, 0, n_sm).scratch_bytes])  # W_c
     want = -(-want // 256) * 256
+    want += -(-(pkg.DFLASH_ROWS_MATMUL_MAX * mh * 2) // 256) * 256   # context taps converted to f16
     diff = lib.dflash_workspace_bytes(ctypes.byref(on)) - lib.dflash_workspace_bytes(ctypes.byref(off))
     assert diff == want
     for over in (dict(batch=1, gamma=8), dict(wdtype="bf16"), dict(markov_rank=64)):
