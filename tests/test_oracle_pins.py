@@ -277,6 +277,41 @@ def test_uniform_attention_pins_key_set(window, n_ctx):
     assert np.allclose(out["trace"][1], h0 + add[None, :], atol=1e-13)
 
 
+@pytest.mark.parametrize("hq,hkv,window,n_ctx", [(4, 4, 0, 5), (4, 4, 3, 6), (4, 2, 4, 7), (4, 1, 0, 0), (2, 2, 0, 3)])
+def test_block_scores_from_live_q_k_v_projections(hq, hkv, window, n_ctx):
+    """Eq 3 of the dflash.ts page with every attention projection live: Q = n W_q^T,
+    K = [K_ctx; n W_k^T], V = [V_ctx; n W_v^T], n = RMSNorm(H_d; attn_norm). W_q and W_k are
+    scaled up so the softmax is far from uniform (the scores decide the output); W_o = I and
+    W_down = 0 make the layer add exactly the attention output. The restatement below builds
+    the projections from the raw matrices and calls torch's scaled_dot_product_attention.
+    Catches K_d built from W_v or W_q, Q built from W_k, a transposed projection, block keys
+    missing from the key set, or a wrong context slice."""
+    cfg = tiny(window=window, L=1, hq=hq, hkv=hkv)
+    m = model(cfg)
+    m.mats["bb.0.q"].data[:] *= 25.0
+    m.mats["bb.0.k"].data[:] *= 25.0
+    m.mats["bb.0.o"].data[:] = np.eye(cfg.d, dtype=np.float32)
+    m.mats["bb.0.down"].data[:] = 0
+    o = oracle.Oracle(m)
+    kc, vc = o.ctx_rows(taps(cfg, n_ctx))
+    out = o.draft(5, kc, vc, trace=True)
+    h0 = out["trace"][0]
+    n = np.stack([_rms(h0[r], m.vecs["bb.0.attn_norm"], cfg.eps) for r in range(cfg.gamma)])
+    lo = max(0, n_ctx - window) if window else 0
+    q = n @ _raw(m.mats["bb.0.q"]).T
+    k = np.concatenate([kc[0, lo:n_ctx], n @ _raw(m.mats["bb.0.k"]).T])
+    v = np.concatenate([vc[0, lo:n_ctx], n @ _raw(m.mats["bb.0.v"]).T])
+    hd, G, nk = cfg.head_dim, cfg.gamma, k.shape[0]
+    tq = torch.tensor(q).view(G, hq, hd).transpose(0, 1)
+    tk = torch.tensor(k).view(nk, hkv, hd).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+    tv = torch.tensor(v).view(nk, hkv, hd).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+    att = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=False)
+    att = att.transpose(0, 1).reshape(G, hq * hd).numpy()
+    p = torch.softmax(tq @ tk.transpose(1, 2) / np.sqrt(hd), dim=-1)
+    assert float(p.max()) > 0.5 or nk == 1          # the scores are far from uniform
+    assert np.allclose(out["trace"][1], h0 + att, rtol=0, atol=1e-12)
+
+
 def test_non_causal_block():
     """is_causal is false: block row 1 (draft 1) depends on block row gamma-1, which only
     mask_emb[gamma-2] feeds. A causal variant of the same oracle shows no such dependence."""
