@@ -273,7 +273,9 @@ void dflash_destroy(dflash_handle* h);
  * forbids the library from calling cudaMalloc) and therefore cannot provide a dflash_create
  * workspace. It runs the same vocab reduction as the LM-head epilogue of dflash_draft_block:
  * token[r] = argmax_j logits[r][j] (lowest index on ties), conf[r] = 1 / sum_j exp(l_rj - max)
- * (conf may be NULL). logits: device fp32 [rows][vocab]; token: device int32 [rows].
+ * (conf may be NULL). logits: device fp32 [rows][vocab], never NaN; an entry of -inf is masked
+ * out (it never wins and adds nothing to the sum), and a row whose every entry is -inf has no
+ * greedy token: token -1, conf 0. token: device int32 [rows].
  * It allocates nothing: its scratch is a fixed ~49 KB array inside the library that every
  * device loading the library keeps until the process exits. Limits: rows <= 64
  * (DFLASH_NOALLOC_MAX_ROWS; more returns DFLASH_ECAPACITY), 2 <= vocab < 2^31.

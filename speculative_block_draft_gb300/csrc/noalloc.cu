@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) greedy_from_logits_kernel(const floa
       st.s = (st.m == -INFINITY) ? 1.f : st.s * __expf(st.m - v) + 1.f;
       st.m = v;
       st.i = (int)j;
-    } else {
+    } else if (v != -INFINITY) {   // a -inf logit is masked out: it adds nothing to the sum
       st.s += __expf(v - st.m);
     }
   }
@@ -88,8 +88,10 @@ __global__ void __launch_bounds__(kThreads) greedy_from_logits_kernel(const floa
     St o{__ldcg(&sc->part[row][k][0]), __ldcg(&sc->part[row][k][1]), __float_as_int(__ldcg(&sc->part[row][k][2]))};
     merge(acc, o);
   }
-  token[row] = acc.i;
-  if (conf) conf[row] = 1.0f / acc.s;
+  // a row whose every logit is -inf has no greedy token
+  const bool none = acc.m == -INFINITY;
+  token[row] = none ? -1 : acc.i;
+  if (conf) conf[row] = none ? 0.f : 1.0f / acc.s;
   sc->ticket[row] = 0;
 }
 

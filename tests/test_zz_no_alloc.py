@@ -49,3 +49,45 @@ def test_noalloc_greedy_matches_draft_block_twice(pkg):
         pkg.greedy_from_logits_noalloc(too_many, out)
     assert e.value.status == pkg.DFLASH_ECAPACITY
     s.close()
+
+
+def _oracle_rows(logits):
+    import oracle
+    out = [oracle.argmax_conf(row) for row in logits.astype(np.float64)]
+    return np.array([o[0] for o in out]), np.array([o[1] for o in out])
+
+
+@pytest.mark.parametrize("vocab", [2, 17, 63, 64, 65, 5000])
+def test_noalloc_small_vocab_ties_and_masked_entries(pkg, vocab):
+    """Against the oracle's argmax / confidence: vocabularies below the 64 CTAs of a row (some
+    CTAs get no entries), exact ties (the lowest index wins), -inf entries at the start of CTA
+    ranges (masked out, no NaN), and a fully masked row (token -1, confidence 0)."""
+    rng = np.random.default_rng(vocab)
+    rows = 12
+    lg = rng.normal(size=(rows, vocab)).astype(np.float32)
+    lg[1, :] = 0.5                                                # all equal: token 0, conf 1/V
+    top = lg[2].max() + 1.0
+    lg[2, [vocab - 1, vocab // 2, min(1, vocab - 1)]] = top      # exact tie at three indices
+    starts = sorted({c * vocab // 64 for c in range(64)})
+    if len(starts) == vocab:                                      # vocab <= 64: every entry starts a range
+        starts = starts[::2]
+    lg[3, starts] = -np.inf                                       # masked CTA starts
+    lg[4, 0] = -np.inf                                            # masked first entry
+    lg[5, :] = -np.inf
+    lg[5, vocab - 1] = 2.0                                        # one live entry, the last
+    lg[6, :] = -np.inf                                            # nothing live
+    d_lg = torch.from_numpy(lg).cuda()
+    for call in range(2):
+        tok = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
+        conf = torch.full((rows,), -1.0, dtype=torch.float32, device="cuda")
+        assert pkg.greedy_from_logits_noalloc(d_lg, tok, conf) == 0
+        torch.cuda.synchronize()
+        t, c = tok.cpu().numpy(), conf.cpu().numpy().astype(np.float64)
+        live = [r for r in range(rows) if r != 6]
+        ot, oc = _oracle_rows(lg[live])
+        assert np.array_equal(t[live], ot), (call, t, ot)
+        assert np.all(np.isfinite(c[live]))
+        assert np.max(np.abs(np.log(c[live]) - np.log(oc))) <= 1e-5, call
+        assert t[6] == -1 and c[6] == 0.0
+        assert t[2] == min(1, vocab - 1)
+        assert abs(c[1] - 1.0 / vocab) <= 1e-5 / vocab
