@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     // ---- copies: raw 4-bit tiles, activation tiles and group sums --------------------------------
     if (lane == 0 && ng > 0) {
       bool ok = true;
+      int nw = 0, nx = 0;   // stages whose copies were issued
       for (int i = 0; i < ng && ok; i++) {
         const int g = g0 + i, sw = i % kTcSW, sx = i % a.sx;
         if (i >= kTcSW)
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         for (int s = 0; s < strips_in_tile; s++)
           bulk_g2s(smem_u32(wring + sw * kTcWStage + s * kQ4GroupBytes),
                    a.w + ((size_t)(mt * kTcStrips + s) * a.groups + g) * kQ4GroupBytes, kQ4GroupBytes, fw);
+        nw = i + 1;
         if (i >= a.sx) ok = mbar_wait_bounded(smem_u32(&empty_x[sx]), ((i / a.sx) + 1) & 1, a.err, kErrTimeoutTc05);
         if (!ok) break;
         const uint32_t fx = smem_u32(&full_x[sx]);
@@ -114,7 +116,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
         if (a.has_lo) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
         bulk_g2s(smem_u32(xst + a.xs_off), a.xs + (size_t)g * a.npad, (uint32_t)(a.npad * 4), fx);
+        nx = i + 1;
       }
+      // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
+      // the last fill of every stage has completed (earlier fills of a stage completed before
+      // its refill was issued); after a normal run these waits return at once
+      for (int j = nw > kTcSW ? nw - kTcSW : 0; j < nw; j++)
+        mbar_wait_bounded(smem_u32(&full_w[j % kTcSW]), (j / kTcSW) & 1, nullptr, 0);
+      for (int j = nx > a.sx ? nx - a.sx : 0; j < nx; j++)
+        mbar_wait_bounded(smem_u32(&full_x[j % a.sx]), (j / a.sx) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
     // ---- MMA issue ----------------------------------------------------------------------------

@@ -120,3 +120,15 @@ class Pair:
                 if int(ga[b]) == a_o:
                     assert int(gn[b]) == int(targets[b][a_o])
         return g, outs
+
+
+_MODELS = {}
+
+
+def cached_model(cfg, norm_jitter=0.0):
+    """make_model(cfg) drawn once per process and shared by the test files (the 4-bit 5120-wide
+    drafter takes tens of seconds to draw)."""
+    key = (cfg, norm_jitter)
+    if key not in _MODELS:
+        _MODELS[key] = syn.make_model(cfg, norm_jitter=norm_jitter)
+    return _MODELS[key]
