@@ -209,8 +209,36 @@ int64_t dflash_ctx_len(const dflash_handle* h, int req_id);
  * bounded device wait gave up since the last check, DFLASH_ECUDA on a CUDA error, else DFLASH_OK. */
 int dflash_check_errors(dflash_handle* h, void* stream);
 
+/* ---- failure-handling test hooks ---------------------------------------------------------------
+ * The pages' rule that an acceleration path may decline a request but must never fail one (the
+ * "A Refusal Is Not A Failure" page, its closing rule) is kept on the device by bounded waits:
+ * every wait of a kernel on an mbarrier gives up after a limit, sets a bit of the handle's error
+ * word, waits for the CTA's own copies in flight and returns. These two calls let a test make such
+ * a wait run out; neither is needed in production.
+ *
+ * dflash_set_wait_limit: the limit of the kernels' waits from the next launch on, in microseconds
+ * (0 restores the default of 1 s). Waits that only drain a CTA's own copies before it leaves
+ * always allow 1 s. Enqueued on `stream` (a 4-byte host-to-device copy). Returns DFLASH_EINVAL for
+ * a NULL handle, DFLASH_ECUDA on a CUDA error.
+ *
+ * dflash_debug_stall: in the next dflash_draft_block call only, CTA `cta` of every tensor-core
+ * projection launch also waits on an mbarrier that no copy and no thread completes, so that wait
+ * runs out after the limit and the launch gives up; the round's outputs are then undefined and
+ * dflash_check_errors returns DFLASH_ETIMEOUT (clearing the error word and the split-K tickets
+ * the launches left). cta < 0 disarms it. Host-only. Returns DFLASH_EINVAL for a NULL handle. */
+int dflash_set_wait_limit(dflash_handle* h, unsigned limit_us, void* stream);
+int dflash_debug_stall(dflash_handle* h, int cta);
+
 /* Host-side counters. */
 int dflash_get_stats(const dflash_handle* h, dflash_stats* out);
+
+/* Accepted-length histogram of every dflash_accept / dflash_accept_kept call since create (the
+ * "Inco Hacks Native" page, section 3, logs each round as bs= accepted= committed=; here
+ * counts[a] = blocks whose accepted length was a, and such a block committed a + 1 tokens).
+ * Kept on the device by the accept kernel; this call synchronises `stream` and copies
+ * counts[0 .. n_counts-1], 1 <= n_counts <= DFLASH_MAX_GAMMA + 1. Returns DFLASH_EINVAL for a
+ * NULL handle or counts or a bad n_counts, DFLASH_ECUDA on a CUDA error. */
+int dflash_accept_histogram(dflash_handle* h, uint64_t* counts, int n_counts, void* stream);
 
 /* Record two caller-created CUDA events (cudaEvent_t) around the launch of one kernel of the
  * next dflash_draft_block call, for live per-kernel timing. kernel: 0 = the LM head (the largest

@@ -109,7 +109,8 @@ SYMBOLS = ["dflash_workspace_bytes", "dflash_create", "dflash_project_ctx", "dfl
            "dflash_accept", "dflash_reset_request", "dflash_ctx_len", "dflash_check_errors",
            "dflash_get_stats", "dflash_set_probe", "dflash_launch_count", "dflash_destroy",
            "dflash_status_str", "dflash_greedy_from_logits_noalloc", "dflash_draft_lengths",
-           "dflash_accept_kept", "dflash_rows_matmul_plan", "dflash_rows_matmul"]
+           "dflash_accept_kept", "dflash_rows_matmul_plan", "dflash_rows_matmul", "dflash_set_wait_limit",
+           "dflash_debug_stall", "dflash_accept_histogram"]
 
 
 def lib():
@@ -157,6 +158,12 @@ def lib():
         L.dflash_rows_matmul_plan.argtypes = [i32, i32, i32, i32, i32, P(dflash_rows_plan)]
         L.dflash_rows_matmul.restype = i32
         L.dflash_rows_matmul.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp, i32, vp, ctypes.c_size_t, vp]
+        L.dflash_set_wait_limit.restype = i32
+        L.dflash_set_wait_limit.argtypes = [vp, ctypes.c_uint, vp]
+        L.dflash_debug_stall.restype = i32
+        L.dflash_debug_stall.argtypes = [vp, i32]
+        L.dflash_accept_histogram.restype = i32
+        L.dflash_accept_histogram.argtypes = [vp, P(ctypes.c_uint64), i32, vp]
         _lib = L
     return _lib
 
@@ -336,6 +343,22 @@ class Handle:
 
     def launch_count(self) -> int:
         return lib().dflash_launch_count(self.h)
+
+    def accept_histogram(self, stream=None) -> list:
+        """counts[a] = accepted blocks whose accepted length was a, for a = 0 .. n_draft."""
+        n = self.cfg.gamma - 1 + self.cfg.draft_all_rows + 1
+        buf = (ctypes.c_uint64 * n)()
+        _check(lib().dflash_accept_histogram(self.h, buf, n, _stream_ptr(stream)), "dflash_accept_histogram")
+        return list(buf)
+
+    def set_wait_limit(self, limit_us: int, stream=None) -> int:
+        """Test hook: limit of the kernels' bounded waits in microseconds (0: the 1 s default)."""
+        return _check(lib().dflash_set_wait_limit(self.h, limit_us, _stream_ptr(stream)), "dflash_set_wait_limit")
+
+    def debug_stall(self, cta: int) -> int:
+        """Test hook: CTA `cta` of every projection launch of the next draft call waits on a barrier
+        nothing completes (cta < 0 disarms)."""
+        return _check(lib().dflash_debug_stall(self.h, cta), "dflash_debug_stall")
 
     def close(self):
         if getattr(self, "h", None):

@@ -58,6 +58,7 @@ struct dflash_handle {
   float* lm_strip = nullptr;
   float *att_o = nullptr, *att_ml = nullptr;
   unsigned* err = nullptr;
+  unsigned long long* acc_hist = nullptr;   // [DFLASH_MAX_GAMMA + 1] blocks per accepted length
   size_t partial_floats = 0;
   int ticket_count = 0, lm_grid_max = 0, att_pairs_max = 0;
   // many-row draft calls on the tcgen05 contraction (config large_batch_tc05)
@@ -71,6 +72,7 @@ struct dflash_handle {
   dflash_stats stats{};
   uint64_t launches = 0;
   cudaEvent_t probe_start = nullptr, probe_stop = nullptr;
+  int stall_armed = 0, stall_active = 0;   // test hook: CTA + 1 that stalls in the next / this draft call
 };
 
 namespace {
@@ -287,7 +289,8 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
   h->att_o = cv.take<float>((size_t)h->att_pairs_max * 64 * c.head_dim * 4);
   h->att_ml = cv.take<float>((size_t)h->att_pairs_max * 64 * 2 * 4);
-  h->err = cv.take<unsigned>(4);
+  h->err = cv.take<unsigned>(8);   // [0] error bits, [1] wait limit in us (0: 1 s)
+  h->acc_hist = cv.take<unsigned long long>((DFLASH_MAX_GAMMA + 1) * 8);
   // the tcgen05 contraction's scratch: the largest plan over the block projections and the head
   h->tc05_on = 0;
   h->tc05_rows = std::min(c.max_batch * h->G, kTcMaxRows);
@@ -493,6 +496,7 @@ int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out =
   a.partials = h->partials;
   a.tickets = h->tickets;
   a.err = h->err;
+  a.stall_cta1 = h->fmt == FMT_F32 ? 0 : h->stall_active;
   a.e = c.e;
   if (c.epi == EPI_LMHEAD) {
     a.e.lm_part = h->lm_part;
@@ -822,6 +826,15 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     if (r < 0 || r >= h->cfg.max_batch || seen[r]) return DFLASH_EINVAL;
     seen[r] = true;
   }
+  // an armed stall (test hook) applies to this call's projection launches only
+  struct StallScope {
+    dflash_handle* h;
+    explicit StallScope(dflash_handle* hh) : h(hh) {
+      h->stall_active = h->stall_armed;
+      h->stall_armed = 0;
+    }
+    ~StallScope() { h->stall_active = 0; }
+  } stall_scope(h);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dflash_config& c = h->cfg;
   const size_t ab = h->act_bytes;
@@ -1137,7 +1150,7 @@ int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32
   if (!draft || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->nd, draft, nullptr, target, accept_len, next_anchor,
+  return status_of(launch_accept(n_req, h->nd, draft, nullptr, target, accept_len, next_anchor, h->acc_hist,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -1158,7 +1171,7 @@ int dflash_accept_kept(dflash_handle* h, int n_req, const int32_t* draft, const 
   if (!draft || !keep || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->nd, draft, keep, target, accept_len, next_anchor,
+  return status_of(launch_accept(n_req, h->nd, draft, keep, target, accept_len, next_anchor, h->acc_hist,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -1204,6 +1217,26 @@ int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop
 }
 
 uint64_t dflash_launch_count(const dflash_handle* h) { return h ? h->launches : 0; }
+
+int dflash_accept_histogram(dflash_handle* h, uint64_t* counts, int n_counts, void* stream) {
+  if (!h || !counts || n_counts < 1 || n_counts > DFLASH_MAX_GAMMA + 1) return DFLASH_EINVAL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DFLASH_ECUDA;
+  unsigned long long v[DFLASH_MAX_GAMMA + 1];
+  if (cudaMemcpy(v, h->acc_hist, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_ECUDA;
+  for (int a = 0; a < n_counts; a++) counts[a] = (uint64_t)v[a];
+  return DFLASH_OK;
+}
+
+int dflash_set_wait_limit(dflash_handle* h, unsigned limit_us, void* stream) {
+  if (!h) return DFLASH_EINVAL;
+  return status_of(cudaMemcpyAsync(h->err + 1, &limit_us, 4, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+}
+
+int dflash_debug_stall(dflash_handle* h, int cta) {
+  if (!h) return DFLASH_EINVAL;
+  h->stall_armed = cta < 0 ? 0 : cta + 1;
+  return DFLASH_OK;
+}
 
 int dflash_rows_matmul_plan(int n_out, int k_in, int n_rows, int x_lo, int n_sm, dflash_rows_plan* plan) {
   if (!plan || n_out < 1 || k_in < 64 || k_in % 64 || n_rows < 1 || n_sm < 1) return DFLASH_EINVAL;

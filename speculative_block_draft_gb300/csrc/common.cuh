@@ -53,15 +53,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait for phase `parity` of an mbarrier for at most ~1 s. On timeout, set `code` in the device
-// error word and return false: the caller stops issuing work and leaves.
+// Wait for phase `parity` of an mbarrier for a bounded time. On timeout, set `code` in the device
+// error word err[0] and return false: the caller stops issuing work and leaves. The limit is
+// err[1] microseconds when that word is nonzero (a test setting), else 1 s; a wait without an
+// error word (err == nullptr: draining a CTA's own copies before it leaves) always allows 1 s.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned* err,
                                                   unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const unsigned limit_us = err ? *reinterpret_cast<volatile unsigned*>(err + 1) : 0u;
+  const uint64_t limit_ns = limit_us ? (uint64_t)limit_us * 1000ull : 1000000000ull;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > 1000000000ull) {
+    if (global_timer_ns() - t0 > limit_ns) {
       if (err) atomicOr(err, code);
       return false;
     }

@@ -17,7 +17,7 @@ size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap)
   if (lm) b += (size_t)w * kMaxRows * sizeof(LmState); // vocab reduction scratch (LM head)
   b += (size_t)2 * w * 32 * (rp / 2) * 4;              // split-strip pieces (2 per warp x 32 lanes x NT*4)
   b += (size_t)cpart_cap * 32 * (rp / 2) * 4;          // cluster K split: partial tiles
-  b += 16 + (1 + w * kStages) * 8;                     // mbarriers
+  b += 16 + (2 + w * kStages) * 8;                     // mbarriers
   return b;
 }
 

@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
       (reinterpret_cast<uintptr_t>(cpart + (a.cluster2 ? a.cpart_cap * 32 * NT4 : 0)) + 15) & ~uintptr_t(15));
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 1 + kWarps * kStages; i++) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 2 + kWarps * kStages; i++) mbar_init(smem_u32(&bars[i]), 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -537,6 +537,8 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
   if (DFL_RING_AFTER == 2)
     for (int q = kPrePdlStages; q < kStages && i_tile < t1; q++) issue_next();
   bool ok = mbar_wait_bounded(smem_u32(&bars[0]), 0, a.err, kErrTimeoutGemv);
+  if (a.stall_cta1 == (int)blockIdx.x + 1 && threadIdx.x == 0)   // test hook: no copy or thread ends this wait
+    ok = mbar_wait_bounded(smem_u32(&bars[1 + kWarps * kStages]), 0, a.err, kErrTimeoutGemv) && ok;
   ok = __syncthreads_and(ok);
   if (a.x_bf16 && ok) {  // caller-side bf16 rows (context taps) -> f16 in place
     for (int r = warp; r < a.R; r += kWarps) {

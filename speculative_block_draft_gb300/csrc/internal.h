@@ -116,6 +116,7 @@ struct GemvArgs {
   int norm_mode; const float* ssq; int ssq_ld; int ssq_parts; float inv_dim; float eps;
   float* partials; int* tickets;
   unsigned* err;
+  int stall_cta1;          // test hook: CTA stall_cta1 - 1 also waits on a barrier nothing completes (0: none)
   EpiArgs e;
 };
 
@@ -232,7 +233,7 @@ cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s);
 cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s);
 cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                          int32_t* accept_len, int32_t* next_anchor, cudaStream_t s);
+                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, cudaStream_t s);
 cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
                                  int32_t* keep, cudaStream_t s);
 

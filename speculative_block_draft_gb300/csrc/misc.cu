@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant
 
 // One warp per request: first mismatch via ballot.
 // keep (nullable): per request, only the first keep[b] drafts are verified (pruned blocks).
+// hist (nullable): hist[a] counts the blocks whose accepted length is a (0 <= a <= n).
 __global__ void accept_kernel(int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                              int32_t* accept_len, int32_t* next_anchor) {
+                              int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist) {
   const int b = blockIdx.x, lane = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();
@@ -176,6 +177,7 @@ __global__ void accept_kernel(int n, const int32_t* draft, const int32_t* keep, 
   if (lane == 0) {
     accept_len[b] = acc;
     next_anchor[b] = target[(size_t)b * (n + 1) + acc];
+    if (hist) atomicAdd(hist + acc, 1ull);
   }
 }
 
@@ -245,8 +247,9 @@ cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                          int32_t* accept_len, int32_t* next_anchor, cudaStream_t s) {
-  return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, keep, target, accept_len, next_anchor);
+                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, cudaStream_t s) {
+  return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, keep, target, accept_len, next_anchor,
+                    hist);
 }
 
 }  // namespace dfl

@@ -71,4 +71,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.dflash_draft_lengths(None, 1, None, None, 0.0, None, None) == pkg.DFLASH_EINVAL
     assert lib.dflash_accept_kept(None, 1, None, None, None, None, None, None) == pkg.DFLASH_EINVAL
     assert lib.dflash_accept(None, 1, None, None, None, None, None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_set_wait_limit(None, 1000, None) == pkg.DFLASH_EINVAL
+    assert lib.dflash_debug_stall(None, 0) == pkg.DFLASH_EINVAL
+    assert lib.dflash_accept_histogram(None, None, 1, None) == pkg.DFLASH_EINVAL
     assert b"declined" in lib.dflash_status_str(pkg.DFLASH_DECLINED)

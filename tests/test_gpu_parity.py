@@ -148,8 +148,15 @@ def test_accept_kernel_exhaustive_vs_oracle():
     d = rng.integers(0, 3, size=(4096, 7)).astype(np.int32)
     t = rng.integers(0, 3, size=(4096, 8)).astype(np.int32)
     a, nxt = s.accept(d, t)
+    want = np.zeros(8, dtype=np.int64)
     for i in range(4096):
         assert (a[i], nxt[i]) == oracle.accept(d[i], t[i])
+        want[oracle.accept(d[i], t[i])[0]] += 1
+    # the device histogram of accepted lengths counts every block once, at its length
+    assert s.h.accept_histogram(stream=s.stream) == list(want)
+    s.accept(d[:100], t[:100])
+    want += np.bincount(a[:100], minlength=8)
+    assert s.h.accept_histogram(stream=s.stream) == list(want)
     s.close()
 
 
@@ -229,6 +236,42 @@ def test_abi_errors_and_decline(monkeypatch):
     assert h.draft_block([], anchor, draft) == 0
     assert h.reset_request(1) == 0 and h.ctx_len(1) == 0
     assert s.check() == 0
+    s.close()
+
+
+def test_bounded_wait_runs_out_reports_and_recovers():
+    """A device wait that runs out is reported, never a hang, and the next round is exact again
+    (the "A Refusal Is Not A Failure" page's closing rule: an acceleration path declines, never
+    fails). With the wait limit shortened to 20 ms, CTA 0 of every projection launch of one draft
+    call waits on an mbarrier that nothing completes. The down projection here (K = 4096 over
+    16 strips) splits K four ways over global partials and tickets, so the stalled CTA leaves a
+    strip's ticket short of its count: the following round is only right if dflash_check_errors
+    cleared the tickets."""
+    import time
+
+    import speculative_block_draft_gb300 as pkg
+    from parity_util import Pair
+    cfg = small("s_stall", inter=4096, ctx_len=40)
+    pair = Pair(cfg, syn.make_model(cfg, norm_jitter=0.1), ctx_capacity=64)
+    pair.prefill(syn.ctx_lengths(cfg))
+    report = {}
+    pair.round(0, report)
+    s = pair.gpu
+    s.h.set_wait_limit(20000, stream=s.stream)
+    s.h.debug_stall(0)
+    t0 = time.time()
+    g = s.draft([0], syn.anchors(cfg.seed, 1, 1, cfg.vocab), logits=False)
+    assert g["rc"] == 0
+    with pytest.raises(pkg.DFlashError) as e:
+        s.check()
+    assert e.value.status == pkg.DFLASH_ETIMEOUT
+    assert time.time() - t0 < 30.0
+    assert s.check() == 0                       # the word was cleared
+    s.h.set_wait_limit(0, stream=s.stream)
+    pair.round(1, report)                       # the hook was one-shot; tickets were cleared
+    pair.round(2, report)
+    assert s.check() == 0
+    print(f"\n[s_stall] {report}, stalled call {time.time() - t0:.2f} s")
     s.close()
 
 

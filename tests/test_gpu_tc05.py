@@ -190,7 +190,7 @@ _FULL = {}
 def _full_session(m):
     from speculative_block_draft_gb300.session import Session
     if "s" not in _FULL:
-        _FULL["s"] = Session(m, max_batch=1, ctx_capacity=64)
+        _FULL["s"] = Session(m, max_batch=1, ctx_capacity=CONFIGS["c3"].window)
     return _FULL["s"]
 
 
