@@ -53,15 +53,33 @@ def round_bytes(cfg, ctx_lens) -> dict:
     return b
 
 
+def round_flops(cfg, ctx_lens, ctx_rows: float) -> dict:
+    """Algorithmic multiply-add work of one round (2 FLOP per weight and activation row):
+    projections of every block row, the head over the drafting rows, W_c and each layer's context
+    K/V over the round's new context rows, and the block attention (QK^T and PV)."""
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    p = round_params(cfg)
+    rows_b, rows_d = cfg.batch * cfg.gamma, cfg.batch * cfg.n_draft
+    f = {"layers": 2.0 * rows_b * p["layers"], "lm_head": 2.0 * rows_d * p["lm_head"],
+         "W_c": 2.0 * ctx_rows * p["W_c"], "ctx_kv": 2.0 * ctx_rows * cfg.n_layers * 2 * kvd * cfg.d}
+    if "tok_out_proj" in p:
+        f["tok_out_proj"] = 2.0 * (cfg.batch + rows_d) * p["tok_out_proj"] / 2
+    keys = sum((min(int(P), cfg.window) if cfg.window else int(P)) + cfg.gamma for P in ctx_lens)
+    f["attention"] = 4.0 * cfg.n_layers * cfg.n_q_heads * cfg.gamma * keys * cfg.head_dim
+    f["total"] = sum(f.values())
+    return f
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d.get("bf16_tflops", 1700.0))),
                 "source": "measured"}
     except (OSError, KeyError, ValueError):
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
 def load_traffic(kernel: str):
@@ -305,6 +323,7 @@ def workload_config(cfg) -> dict:
             "requests": cfg.batch, "gamma": cfg.gamma, "ctx_len": cfg.ctx_len, "window": cfg.window,
             "new_ctx_rows_per_round": list(cfg.appends()),
             **({"large_batch_tc05": True} if getattr(cfg, "large_batch_tc05", False) else {}),
+            **({"skinny_tc05": True} if getattr(cfg, "skinny_tc05", False) else {}),
             "l2": "no flush: every round streams >1.4 GB of weights, far above the 129 MB L2"}
 
 
@@ -328,6 +347,8 @@ def main():
                     help="comma-separated workloads: print the oracle's 1-core / all-core round times and exit")
     ap.add_argument("--large-batch-tc05", action="store_true",
                     help="library option: draft calls of more than 32 block rows on the tcgen05 contraction")
+    ap.add_argument("--skinny-tc05", action="store_true",
+                    help="draft calls of at most 32 block rows run their projections on the tcgen05 projection kernel")
     ap.add_argument("--profile-ctx", type=int, default=0,
                     help="prefill only this many context rows (for short profiler captures; not a bench value)")
     args = ap.parse_args()
@@ -339,6 +360,8 @@ def main():
         cfg = syn.with_overrides(cfg, markov_rank=args.markov_rank)
     if args.large_batch_tc05:
         cfg = syn.with_overrides(cfg, large_batch_tc05=True)
+    if args.skinny_tc05:
+        cfg = syn.with_overrides(cfg, skinny_tc05=True)
     if args.impl == "reference":
         return run_reference(args, cfg)
 
@@ -503,6 +526,9 @@ def main():
 
     peaks = load_peaks()
     rb = round_bytes(cfg, lengths)
+    ctx_rows = float(np.mean([np.sum(counts[args.warmup + i]) for i in range(args.steps)]))
+    rf = round_flops(cfg, lengths, ctx_rows)
+    t_round = t_max / args.steps
     lm_bytes = round_bytes(cfg, lengths)["lm_head"]
     lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
     traffic = load_traffic("lm_head")
@@ -516,6 +542,13 @@ def main():
                       "peak_gbs": peaks["hbm_gbs"],
                       "frac": rb["total"] / (t_max / args.steps) / 1e9 / peaks["hbm_gbs"],
                       "peak_source": peaks["source"]},
+        "round_tensor": {"algorithmic_flop": rf["total"],
+                         "breakdown_gflop": {k: round(v / 1e9, 2) for k, v in rf.items()},
+                         "achieved_tflops": rf["total"] / t_round / 1e12,
+                         "peak_tflops": peaks["bf16_tflops_sustained"],
+                         "frac": rf["total"] / t_round / 1e12 / peaks["bf16_tflops_sustained"],
+                         "peak_source": f"{peaks['source']} (cuBLAS bf16, sustained; the projections run f16 "
+                                        f"operands on the same tensor-core rate)"},
         "roofline": {"kernel": "LM head (4-bit GEMV + fused argmax/softmax confidence), 1 launch per round",
                      "bound": "hbm", "achieved": lm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": lm_gbs / peaks["hbm_gbs"], "traffic": traffic,

@@ -34,6 +34,7 @@ class DraftConfig:
     draft_all_rows: bool = False  # draft from all gamma block rows (gamma tokens), not rows 1..gamma-1
     markov_rank: int = 0          # Markov sequential head rank r (0: none), a multiple of 64
     large_batch_tc05: bool = False  # many-row draft calls on the tcgen05 contraction (library option)
+    skinny_tc05: bool = False     # draft calls of <= 32 rows on the tcgen05 projection kernel (library option)
     append_min: int = 0           # new context rows per request per round (0,0: gamma rows)
     append_max: int = 0
     ctx_min: int = 0              # ragged contexts: P uniform in [ctx_min, ctx_len] (0: fixed)

@@ -101,8 +101,13 @@ typedef struct {
                          dflash_project_ctx runs W_c once per 160 context rows when a call appends
                          more than 32. It applies to 4-bit weights with d == H and no Markov head;
                          other calls use the GEMV. The workspace grows by the contraction's scratch
-                         and an f16 copy of 160 tap rows. Experimental: not yet covered by the
-                         parity tests. */
+                         and an f16 copy of 160 tap rows. */
+  int skinny_tc05;    /* 0: calls of at most 32 block rows run every projection as the mma.sync
+                         GEMV. 1: with 4-bit weights and f16 activations, a dflash_draft_block call
+                         of at most 32 block rows runs its Q/K/V, O, gate/up and down projections
+                         and (d == H) the LM head each as one tcgen05 launch with the same fused
+                         epilogues: weights dequantised to f16 (one rounding) in shared memory,
+                         fp32 accumulators in tensor memory. */
 } dflash_config;
 
 typedef struct {

@@ -16,7 +16,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash.so")
-_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu", "gemm_tc05.cu", "tc05_epi.cu"]
+_SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu", "gemm_tc05.cu", "tc05_epi.cu",
+            "proj_tc05.cu"]
 _HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh", "gemm_tc05.h", "tc05.cuh"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a",
               "-Xcompiler", "-fPIC"]
@@ -71,7 +72,8 @@ class dflash_config(ctypes.Structure):
         "n_layers", "d", "n_q_heads", "n_kv_heads", "head_dim", "inter", "n_taps", "target_hidden", "vocab",
         "gamma", "window", "max_batch", "ctx_capacity")] + \
         [("eps", ctypes.c_float), ("wdtype", ctypes.c_int), ("adtype", ctypes.c_int), ("ffn_act", ctypes.c_int),
-         ("draft_all_rows", ctypes.c_int), ("markov_rank", ctypes.c_int), ("large_batch_tc05", ctypes.c_int)]
+         ("draft_all_rows", ctypes.c_int), ("markov_rank", ctypes.c_int), ("large_batch_tc05", ctypes.c_int),
+         ("skinny_tc05", ctypes.c_int)]
 
 
 class dflash_matrix(ctypes.Structure):
@@ -220,7 +222,8 @@ def make_config(cfg, max_batch: int | None = None, ctx_capacity: int | None = No
     return dflash_config(cfg.n_layers, cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.inter, cfg.n_taps,
                          cfg.target_hidden, cfg.vocab, cfg.gamma, cfg.window, mb, ctx_capacity, cfg.eps,
                          DTYPE[cfg.wdtype], DTYPE[cfg.adtype], FFN[cfg.ffn], 1 if cfg.draft_all_rows else 0,
-                         cfg.markov_rank, 1 if getattr(cfg, "large_batch_tc05", False) else 0)
+                         cfg.markov_rank, 1 if getattr(cfg, "large_batch_tc05", False) else 0,
+                         1 if getattr(cfg, "skinny_tc05", False) else 0)
 
 
 class DeviceModel:

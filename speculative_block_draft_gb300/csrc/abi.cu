@@ -66,6 +66,9 @@ struct dflash_handle {
   uint8_t* tc05_scratch = nullptr;
   size_t tc05_scratch_bytes = 0;
   void* tc05_taps = nullptr;    // [kTcMaxRows][n_taps * H] f16: context taps converted for TMA
+  // draft calls of <= 32 rows on the tcgen05 projection kernel (config skinny_tc05)
+  int pj_on = 0;
+  float* pj_partials = nullptr;  // [n_sm][2][32][128] pieces of tiles cut between CTAs
   CUtensorMap kmap{}, vmap{};
 
   int64_t ctx_len[DFLASH_MAX_BATCH] = {};
@@ -176,6 +179,7 @@ bool valid_config(const dflash_config* c) {
   if (c->draft_all_rows != 0 && c->draft_all_rows != 1) return false;
   if (c->markov_rank < 0 || c->markov_rank > 1024 || c->markov_rank % 64) return false;
   if (c->large_batch_tc05 != 0 && c->large_batch_tc05 != 1) return false;
+  if (c->skinny_tc05 != 0 && c->skinny_tc05 != 1) return false;
   if (c->wdtype < DFLASH_F32 || c->wdtype > DFLASH_Q4G64) return false;
   if (c->adtype == DFLASH_F32) {
     if (c->wdtype != DFLASH_F32) return false;
@@ -313,6 +317,8 @@ size_t carve(dflash_handle* h, uint8_t* base) {
     h->tc05_scratch = cv.take<uint8_t>(sc);
     h->tc05_taps = cv.take<void>((size_t)kTcMaxRows * h->mH * 2);
   }
+  h->pj_on = c.skinny_tc05 && h->fmt == FMT_Q4 && !h->act_f32;
+  if (h->pj_on) h->pj_partials = cv.take<float>((size_t)h->n_sm * 2 * kProjMaxRows * 128 * 4);
   (void)state_begin;
   return round_up(cv.off, 256);
 }
@@ -517,7 +523,6 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   if (make_rows_map(x, m.k, rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
   if (xl && make_rows_map(xl, m.k, rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
   a.w = m.w;
-  a.xs = reinterpret_cast<float*>(h->tc05_scratch);
   a.part = reinterpret_cast<float*>(h->tc05_scratch + p.part_off);
   a.err = h->err;
   a.n_strips = m.n_strips;
@@ -530,12 +535,10 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   a.sx = p.sx;
   a.tmem_cols = p.tmem_cols;
   a.x_stage = p.x_stage;
-  a.xs_off = p.xs_off;
   a.x_tx = p.x_tx;
   *out = p;
-  h->launches += 2;
-  return status_of(launch_tc05_parts(a, p, static_cast<const __half*>(x), static_cast<const __half*>(xl), ldx,
-                                     rows, s));
+  h->launches += 1;
+  return status_of(launch_tc05_parts(a, p, s));
 }
 
 // The epilogue of one chunk of a projection (described as for run_gemv) from the contraction's
@@ -574,6 +577,61 @@ int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row
   return status_of(launch_tc05_epilogue(c.epi, nt_for(c.R), a,
                                         reinterpret_cast<const float*>(h->tc05_scratch + p.part_off), p.slices,
                                         p.npad, p.mtiles * 128, row_base, grid, s));
+}
+
+// One projection of a draft call of at most kProjMaxRows block rows on the tcgen05 projection
+// kernel: the contraction runs over rows [0, rows) of x (f16 [rows][ldx], the f16 remainder at
+// element offset lo_off when nonzero); the epilogue (described as for run_gemv) reads contraction
+// row row_base + map_row(c.xmap, r) for its row r.
+int run_proj(dflash_handle* h, const GemvCall& c, int rows, const void* x, int ldx, long long lo_off, int row_base,
+             cudaStream_t s) {
+  const PackedMat& m = *c.m;
+  if (c.R <= 0) return DFLASH_OK;
+  const ProjPlan p = plan_proj_tc05(m.n_strips, m.groups, rows, lo_off != 0, h->n_sm);
+  if (p.npad == 0 || p.grid > h->n_sm || p.mtiles > h->ticket_count) return DFLASH_EINVAL;
+  ProjArgs pa{};
+  const void* xl = lo_off ? static_cast<const void*>(static_cast<const __half*>(x) + lo_off) : nullptr;
+  if (make_rows_map(x, m.k, rows, ldx, p.npad, &pa.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (xl && make_rows_map(xl, m.k, rows, ldx, p.npad, &pa.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  GemvArgs& a = pa.g;
+  a.w = m.w;
+  a.strip0 = 0;
+  a.n_strips = m.n_strips;
+  a.k = m.k;
+  a.groups = m.groups;
+  a.n_slices = c.epi == EPI_LMHEAD ? 2 : 1;   // LM head: one vocab state per strip, merged in strip order
+  a.gps = m.groups;
+  a.ctas_per_slice = 1;
+  a.R = c.R;
+  a.xmap = c.xmap;
+  a.norm_mode = c.norm_mode;
+  a.ssq = c.ssq;
+  a.ssq_ld = c.ssq_ld;
+  a.ssq_parts = c.ssq_parts;
+  a.inv_dim = c.inv_dim;
+  a.eps = h->cfg.eps;
+  a.err = h->err;
+  a.e = c.e;
+  if (c.epi == EPI_LMHEAD) {
+    a.e.lm_part = h->lm_part;
+    a.e.lm_strip = h->lm_strip;
+  }
+  pa.w = m.w;
+  pa.partials = h->pj_partials;
+  pa.tickets = h->tickets;
+  pa.n_strips = m.n_strips;
+  pa.groups = m.groups;
+  pa.mtiles = p.mtiles;
+  pa.npad = p.npad;
+  pa.has_lo = xl != nullptr;
+  pa.sa = p.sa;
+  pa.sx = p.sx;
+  pa.sw = p.sw;
+  pa.tmem_cols = p.tmem_cols;
+  pa.row_base = row_base;
+  pa.x_stage = p.x_stage;
+  h->launches++;
+  return status_of(launch_proj_tc05(c.epi, nt_for(c.R), pa, p, s));
 }
 
 }  // namespace
@@ -895,12 +953,22 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   // its epilogue per chunk (the chunks' row scales, residuals and outputs are those of the GEMV)
   const int rows_all = n_req * G;
   const bool tc = h->tc05_on && rows_all > kMaxRows && rows_all <= h->tc05_rows;
+  // at most 32 rows: each projection is one launch of the tcgen05 projection kernel (config
+  // skinny_tc05), its contraction over all block rows, its epilogue over the chunk's rows
+  const bool pj = h->pj_on && rows_all <= kProjMaxRows;
   Tc05Plan tp{};
-  auto project = [&](GemvCall& c, int r0) { return tc ? run_tc05_epi(h, c, tp, r0, s) : run_gemv(h, c, s); };
+  const void* px = nullptr;   // the projection's input rows and remainder offset (pj)
+  int pldx = 0;
+  long long plo = 0;
+  auto project = [&](GemvCall& c, int r0) {
+    if (pj) return run_proj(h, c, rows_all, px, pldx, plo, r0, s);
+    return tc ? run_tc05_epi(h, c, tp, r0, s) : run_gemv(h, c, s);
+  };
   for (int i = 0; i < h->L; i++) {
     const int in_parts = i == 0 ? (d + kBlockCols - 1) / kBlockCols : parts;
     // Q, K_d, V_d of RMSNorm_attn_i(H_d)
     if (tc && (st = run_tc05_parts(h, h->qkv[i], rows_all, h->xn, d, lo_if(LO_QKV, xn_lo(h)), s, &tp))) return st;
+    px = h->xn, pldx = d, plo = lo_if(LO_QKV, xn_lo(h));
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       GemvCall cq;
@@ -974,6 +1042,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       }
     }
     if (tc && (st = run_tc05_parts(h, h->wo[i], rows_all, h->attn, h->qd, 0, s, &tp))) return st;
+    px = h->attn, pldx = h->qd, plo = 0;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // H_d += W_o attn; next input = H_d * ff_norm_i (+ sums of squares)
@@ -994,6 +1063,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       if ((st = project(co, r0))) return st;
     }
     if (tc && (st = run_tc05_parts(h, h->gu[i], rows_all, h->xn, d, lo_if(LO_GU, xn_lo(h)), s, &tp))) return st;
+    px = h->xn, pldx = d, plo = lo_if(LO_GU, xn_lo(h));
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // a = act(W_gate n2) * (W_up n2), n2 = RMSNorm_ff_i(H_d); act = SiLU or GELU (tanh form)
@@ -1016,6 +1086,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       if ((st = project(cg, r0))) return st;
     }
     if (tc && (st = run_tc05_parts(h, h->down[i], rows_all, h->act, h->I, 0, s, &tp))) return st;
+    px = h->act, pldx = h->I, plo = 0;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
       const int nb = std::min(req_per_chunk, n_req - b0), r0 = b0 * G;
       // H_d += W_down a; next input = H_d * (attn_norm_{i+1} | out_norm)
@@ -1088,13 +1159,18 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     cl.e.vocab = h->V;
     GemvPlan lp{};
     int epi_grid = 0;
-    if ((st = tc ? run_tc05_epi(h, cl, tp, r0, s, &epi_grid) : run_gemv(h, cl, s, &lp))) return st;
+    const bool pj_lm = pj && d == h->H;
+    if (pj_lm) {
+      if ((st = run_proj(h, cl, rows_all, h->xn, d, lo_if(LO_LM, xn_lo(h)), r0, s))) return st;
+    } else if ((st = tc ? run_tc05_epi(h, cl, tp, r0, s, &epi_grid) : run_gemv(h, cl, s, &lp))) {
+      return st;
+    }
     if (markov) continue;
-    // merge the per-CTA (one K slice) or per-strip (K split) vocab states: token and confidence
-    const bool split = !tc && h->fmt != FMT_F32 && lp.n_slices > 1;
+    // merge the per-CTA (one K slice) or per-strip (K split, projection kernel) vocab states
+    const bool split = pj_lm || (!tc && h->fmt != FMT_F32 && lp.n_slices > 1);
     h->launches++;
     if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part,
-                                         tc ? epi_grid : (split ? h->lm.n_strips : lp.grid), R, draft + l0,
+                                         split ? h->lm.n_strips : (tc ? epi_grid : lp.grid), R, draft + l0,
                                          conf ? conf + l0 : nullptr, 1, s))))
       return st;
   }
@@ -1282,7 +1358,6 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   if (x_lo && make_rows_map(x_lo, m->k, n_rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   a.w = m->w;
-  a.xs = reinterpret_cast<float*>(sc);
   a.part = reinterpret_cast<float*>(sc + p.part_off);
   a.err = h->err;
   a.n_strips = m->n_strips;
@@ -1295,12 +1370,10 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   a.sx = p.sx;
   a.tmem_cols = p.tmem_cols;
   a.x_stage = p.x_stage;
-  a.xs_off = p.xs_off;
   a.x_tx = p.x_tx;
-  h->launches += 3;
+  h->launches += 2;
   const int half = matrix == DFLASH_MAT_GATEUP ? h->I : 0;
-  return status_of(launch_tc05(a, p, static_cast<const __half*>(x), static_cast<const __half*>(x_lo), ldx, n_rows,
-                               m->n_rows, half, y, ldy, static_cast<cudaStream_t>(stream)));
+  return status_of(launch_tc05(a, p, n_rows, m->n_rows, half, y, ldy, static_cast<cudaStream_t>(stream)));
 }
 
 void dflash_destroy(dflash_handle* h) { delete h; }

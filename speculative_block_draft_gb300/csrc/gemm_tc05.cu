@@ -2,20 +2,20 @@
 // fifth-generation tensor cores (tcgen05), for batches of activation rows (up to 160) where the
 // skinny mma.sync GEMV runs into the legacy tensor path's ceiling.
 //
-// One CTA per (128-row output tile, K slice), twelve warps:
+// One CTA per (128-row output tile, K slice), ten warps:
 //  * warp 0 (one thread) streams the tile's 4-bit (strip, group) tiles with bulk copies, and the
 //    activation rows of each 64-input group (f16, plus the f16 remainder where given) with 2-D
-//    tensor copies in the 128-byte swizzle, together with the group's activation sums;
-//  * warps 2-3 decode the codes to exact f16 integers -- 128 + q for rows 0-7 of a strip (magic
-//    0x5800), 64 + q for rows 8-15 (magic 0x5400) -- and store them as the MMA's K-major A tile in
-//    the same swizzle (the stored word order of a lane covers whole 16-byte chunks of a row);
+//    tensor copies in the 128-byte swizzle;
+//  * warps 2-9 (one 16-row strip each) dequantise the codes to f16 weights, w = s q + b with one
+//    rounding (the code q is made exact in f16 from its nibble with a magic-number lop3 and one
+//    exact subtraction, then one fused f16 multiply-add with the row's scale and bias), and store
+//    them as the MMA's K-major A tile in the same swizzle (the stored word order of a lane covers
+//    whole 16-byte chunks of a row);
 //  * warp 1 allocates tensor memory and one of its threads issues tcgen05.mma kind::f16
-//    (M = 128 output rows, N = the activation rows padded to 16, K = 16) into one of two fp32
-//    accumulators per group, then commits to the stages' and the accumulator's mbarriers;
-//  * warps 4-11 (two warpgroups, each one half of the columns) read the group's accumulator from
-//    tensor memory and fold the group-64 affine code in fp32:
-//      y += s * sum (c + q) x + (b - c s) * sum x,   c = 128 or 64,
-//    which equals sum (s q + b) x exactly in real arithmetic; the MMA only sees exact integers.
+//    (M = 128 output rows, N = the activation rows padded to 16, K = 16), accumulating the whole K
+//    slice in one fp32 accumulator, then commits to the stages' mbarriers;
+//  * warps 4-7 (tensor-memory lane quarters 0-3) finally read the accumulator and store the
+//    slice's partial tile.
 // Every mbarrier wait is bounded (error word + early exit); tensor memory is freed at the end.
 // The K slices' partial tiles are summed in slice order by a separate kernel.
 #include <cuda.h>
@@ -33,13 +33,17 @@ constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcStrips = 8;                              // 16-row strips per 128-row tile
 constexpr int kTcWStage = kTcStrips * kQ4GroupBytes;      // 4608 B: one group of one tile, raw
 constexpr int kTcAStage = 128 * 128;                      // 16 KB: one group of one tile, f16
-constexpr int kTcFoldChunks = kTcMaxRows / 32;            // 16-column chunks per fold warpgroup
-
-// codes at bits 4-7 / 20-23 -> 64 + q (0x5400 is 64.0 with ulp 1/16)
-__device__ __forceinline__ uint32_t nib_hi_to_f16x2_64(uint32_t u) { return lop3_and_or(u, 0x00F000F0u, 0x54005400u); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// (c + q0, c + q1) -> s * (q0, q1) + b in f16 with one rounding; q exact after the subtraction
+__device__ __forceinline__ uint32_t dequant2(uint32_t v, __half2 c, __half2 s, __half2 b) {
+  return h2_bits(__hfma2(__hsub2(bits_h2(v), c), s, b));
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_constant__ Tc05Args a) {
@@ -55,9 +59,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   uint64_t* empty_x = full_x + kTcMaxSX;
   uint64_t* full_a = empty_x + kTcMaxSX;
   uint64_t* empty_a = full_a + kTcSA;
-  uint64_t* acc_full = empty_a + kTcSA;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_done = empty_a + kTcSA;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x % a.mtiles, slice = blockIdx.x / a.mtiles;
@@ -67,20 +70,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcSW; i++) {
       mbar_init(smem_u32(&full_w[i]), 1);
-      mbar_init(smem_u32(&empty_w[i]), 2 + 8);   // two decoder warps + eight fold warps
+      mbar_init(smem_u32(&empty_w[i]), kTcStrips);   // the eight decoder warps
     }
     for (int i = 0; i < a.sx; i++) {
       mbar_init(smem_u32(&full_x[i]), 1);
-      mbar_init(smem_u32(&empty_x[i]), 1 + 8);   // the MMA commit + eight fold warps
+      mbar_init(smem_u32(&empty_x[i]), 1);            // the MMA commit
     }
     for (int i = 0; i < kTcSA; i++) {
-      mbar_init(smem_u32(&full_a[i]), 2);        // two decoder warps
-      mbar_init(smem_u32(&empty_a[i]), 1);       // the MMA commit
+      mbar_init(smem_u32(&full_a[i]), kTcStrips);     // the eight decoder warps
+      mbar_init(smem_u32(&empty_a[i]), 1);            // the MMA commit
     }
-    for (int b = 0; b < 2; b++) {
-      mbar_init(smem_u32(&acc_full[b]), 1);      // the MMA commit
-      mbar_init(smem_u32(&acc_empty[b]), 8);     // eight fold warps
-    }
+    mbar_init(smem_u32(acc_done), 1);                 // the last MMA commit
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- copies: raw 4-bit tiles, activation tiles and group sums --------------------------------
+    // ---- copies: raw 4-bit tiles and activation tiles --------------------------------------------
     if (lane == 0 && ng > 0) {
       bool ok = true;
       int nw = 0, nx = 0;   // stages whose copies were issued
@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         mbar_arrive_expect_tx(fx, a.x_tx);
         tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
         if (a.has_lo) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
-        bulk_g2s(smem_u32(xst + a.xs_off), a.xs + (size_t)g * a.npad, (uint32_t)(a.npad * 4), fx);
         nx = i + 1;
       }
       // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
@@ -133,33 +132,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
       bool ok = true;
       int issued = 0;
       for (int i = 0; i < ng && ok; i++) {
-        const int sa = i % kTcSA, sx = i % a.sx, b = i & 1;
+        const int sa = i % kTcSA, sx = i % a.sx;
         ok = mbar_wait_bounded(smem_u32(&full_a[sa]), (i / kTcSA) & 1, a.err, kErrTimeoutTc05) &&
-             mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05) &&
-             (i < 2 || mbar_wait_bounded(smem_u32(&acc_empty[b]), ((i >> 1) + 1) & 1, a.err, kErrTimeoutTc05));
+             mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05);
         if (!ok) break;
         tc05_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * a.npad);
         const uint32_t abase = smem_u32(aring + sa * kTcAStage);
         const uint32_t xbase = smem_u32(xring + (size_t)sx * a.x_stage);
 #pragma unroll
         for (int kk = 0; kk < 4; kk++) {
           const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
-          umma_f16_ss(d, ad, umma_desc_sw128(xbase + 32 * kk), idesc, kk > 0 ? 1u : 0u);
-          if (a.has_lo) umma_f16_ss(d, ad, umma_desc_sw128(xbase + a.npad * 128 + 32 * kk), idesc, 1u);
+          umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          if (a.has_lo) umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + a.npad * 128 + 32 * kk), idesc, 1u);
         }
         umma_commit(smem_u32(&empty_a[sa]));
         umma_commit(smem_u32(&empty_x[sx]));
-        umma_commit(smem_u32(&acc_full[b]));
         issued = i + 1;
       }
+      if (ok) umma_commit(smem_u32(acc_done));
       // nothing of this CTA may still be running on the tensor core when its memory is freed
-      if (issued > 0)
-        mbar_wait_bounded(smem_u32(&acc_full[(issued - 1) & 1]), ((issued - 1) >> 1) & 1, a.err, kErrTimeoutTc05);
+      if (issued > 0) mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % kTcSA]), ((issued - 1) / kTcSA) & 1, a.err,
+                                        kErrTimeoutTc05);
     }
-  } else if (warp < 4) {
-    // ---- decode: 4-bit codes -> exact f16 integers, swizzled K-major A tile ---------------------
-    const int dw = warp - 2, g8 = lane >> 2, t = lane & 3;
+  } else {
+    // ---- dequantise: 4-bit codes -> f16 weights, swizzled K-major A tile -------------------------
+    const int s = warp - 2, g8 = lane >> 2, t = lane & 3;
+    const __half2 c1024 = __float2half2_rn(1024.f), c64 = __float2half2_rn(64.f);
     bool ok = true;
     for (int i = 0; i < ng && ok; i++) {
       const int sw = i % kTcSW, sa = i % kTcSA;
@@ -167,35 +165,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
            (i < kTcSA || mbar_wait_bounded(smem_u32(&empty_a[sa]), ((i / kTcSA) + 1) & 1, a.err, kErrTimeoutTc05));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const uint8_t* wst = wring + sw * kTcWStage;
+      const uint8_t* gp = wring + sw * kTcWStage + s * kQ4GroupBytes;
       const uint32_t ast = smem_u32(aring + sa * kTcAStage);
+      uint32_t rg[4][2], r8[4][2];
+      if (s < strips_in_tile) {
+        const uint4 W = *reinterpret_cast<const uint4*>(gp + lane * 16);
+        const uint32_t sbg = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * g8);
+        const uint32_t sb8 = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g8 + 8));
+        const __half2 sg = __float2half2_rn(__uint_as_float(sbg << 16));
+        const __half2 bg = __float2half2_rn(__uint_as_float(sbg & 0xFFFF0000u));
+        const __half2 s8 = __float2half2_rn(__uint_as_float(sb8 << 16));
+        const __half2 b8 = __float2half2_rn(__uint_as_float(sb8 & 0xFFFF0000u));
+        const uint32_t w4[4] = {W.x, W.y, W.z, W.w};
 #pragma unroll
-      for (int u = 0; u < kTcStrips / 2; u++) {
-        const int s = dw * (kTcStrips / 2) + u;
-        uint32_t rg[4][2], r8[4][2];
-        if (s < strips_in_tile) {
-          const uint4 W = *reinterpret_cast<const uint4*>(wst + s * kQ4GroupBytes + lane * 16);
-          const uint32_t w4[4] = {W.x, W.y, W.z, W.w};
-#pragma unroll
-          for (int j = 0; j < 4; j++) {
-            // word j of lane (g, t): inputs k0 = 16 t + 4 j .. k0 + 3 of rows g and g + 8
-            rg[j][0] = nib128_to_f16x2(w4[j] << 3);      // row g,     k0, k0 + 1
-            rg[j][1] = nib128_to_f16x2(w4[j] >> 5);      // row g,     k0 + 2, k0 + 3
-            r8[j][0] = nib_hi_to_f16x2_64(w4[j]);        // row g + 8, k0, k0 + 1
-            r8[j][1] = nib_hi_to_f16x2_64(w4[j] >> 8);   // row g + 8, k0 + 2, k0 + 3
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; j++) rg[j][0] = rg[j][1] = r8[j][0] = r8[j][1] = 0u;
+        for (int j = 0; j < 4; j++) {
+          // word j of lane (g, t): inputs k0 = 16 t + 4 j .. k0 + 3 of rows g and g + 8, nibbles
+          // (g,k0) (g+8,k0) (g,k0+2) (g+8,k0+2) (g,k0+1) (g+8,k0+1) (g,k0+3) (g+8,k0+3) from bit 0
+          const uint32_t w = w4[j], w8 = w >> 8;
+          rg[j][0] = dequant2(lop3_and_or(w, 0x000F000Fu, 0x64006400u), c1024, sg, bg);    // 1024 + q
+          rg[j][1] = dequant2(lop3_and_or(w8, 0x000F000Fu, 0x64006400u), c1024, sg, bg);
+          r8[j][0] = dequant2(lop3_and_or(w, 0x00F000F0u, 0x54005400u), c64, s8, b8);      // 64 + q
+          r8[j][1] = dequant2(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), c64, s8, b8);
         }
-        // 16-byte chunk c of row r lives at r * 128 + ((c ^ (r % 8)) * 16); r % 8 == g here
-        const uint32_t row_g = ast + (uint32_t)(s * 16 + g8) * 128, row_8 = row_g + 8 * 128;
-        const uint32_t c0 = (uint32_t)(((2 * t) ^ g8) << 4), c1 = (uint32_t)(((2 * t + 1) ^ g8) << 4);
-        st_shared_v4(row_g + c0, rg[0][0], rg[0][1], rg[1][0], rg[1][1]);
-        st_shared_v4(row_g + c1, rg[2][0], rg[2][1], rg[3][0], rg[3][1]);
-        st_shared_v4(row_8 + c0, r8[0][0], r8[0][1], r8[1][0], r8[1][1]);
-        st_shared_v4(row_8 + c1, r8[2][0], r8[2][1], r8[3][0], r8[3][1]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) rg[j][0] = rg[j][1] = r8[j][0] = r8[j][1] = 0u;
       }
+      // 16-byte chunk c of row r lives at r * 128 + ((c ^ (r % 8)) * 16); r % 8 == g here
+      const uint32_t row_g = ast + (uint32_t)(s * 16 + g8) * 128, row_8 = row_g + 8 * 128;
+      const uint32_t c0 = (uint32_t)(((2 * t) ^ g8) << 4), c1 = (uint32_t)(((2 * t + 1) ^ g8) << 4);
+      st_shared_v4(row_g + c0, rg[0][0], rg[0][1], rg[1][0], rg[1][1]);
+      st_shared_v4(row_g + c1, rg[2][0], rg[2][1], rg[3][0], rg[3][1]);
+      st_shared_v4(row_8 + c0, r8[0][0], r8[0][1], r8[1][0], r8[1][1]);
+      st_shared_v4(row_8 + c1, r8[2][0], r8[2][1], r8[3][0], r8[3][1]);
       // the generic-proxy stores are read by the tensor core, and the raw stage is refilled by the
       // copy engine (both async proxy)
       fence_proxy_async();
@@ -205,70 +207,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         mbar_arrive(smem_u32(&empty_w[sw]));
       }
     }
-  } else {
-    // ---- fold: per-group affine code, fp32 ---------------------------------------------------------
-    const int fw = warp - 4, wg = fw >> 2, quarter = warp & 3;
-    const int n = quarter * 32 + lane;                       // tile row = tensor-memory lane
-    const int nch = a.npad / 16, half = (nch + 1) / 2;
-    const int ch0 = wg == 0 ? 0 : half, ch1 = wg == 0 ? half : nch;
-    const bool row_in = n < strips_in_tile * 16;
-    const float off = (n & 15) < 8 ? -128.f : -64.f;
-    float y[kTcFoldChunks * 16];
-#pragma unroll
-    for (int j = 0; j < kTcFoldChunks * 16; j++) y[j] = 0.f;
-    bool ok = true;
-    for (int i = 0; i < ng && ok; i++) {
-      const int sw = i % kTcSW, sx = i % a.sx, b = i & 1;
-      ok = mbar_wait_bounded(smem_u32(&acc_full[b]), (i >> 1) & 1, a.err, kErrTimeoutTc05) &&
-           mbar_wait_bounded(smem_u32(&full_w[sw]), (i / kTcSW) & 1, a.err, kErrTimeoutTc05) &&
-           mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05);
+    if (warp >= 4 && warp < 8 && ok && ng > 0) {
+      // ---- the slice's partial tile: tensor memory -> part[slice][column][tile row] -----------
+      const int quarter = warp & 3, n = quarter * 32 + lane;   // tile row = tensor-memory lane
+      ok = mbar_wait_bounded(smem_u32(acc_done), 0, a.err, kErrTimeoutTc05);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc05_fence_after();
-      float s = 0.f, bb = 0.f;
-      if (row_in) {
-        const uint32_t sbw =
-            *reinterpret_cast<const uint32_t*>(wring + sw * kTcWStage + (n >> 4) * kQ4GroupBytes + 512 + (n & 15) * 4);
-        s = __uint_as_float(sbw << 16);
-        bb = fmaf(off, s, __uint_as_float(sbw & 0xFFFF0000u));
-      }
-      const float* xs = reinterpret_cast<const float*>(xring + (size_t)sx * a.x_stage + a.xs_off);
-      const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * a.npad);
-#pragma unroll
-      for (int c = 0; c < kTcFoldChunks; c++) {
-        const int ch = ch0 + c;
-        if (ch < ch1) {   // uniform across the warp
+      if (ok) {
+        tc05_fence_after();
+        float* out = a.part + (size_t)slice * a.npad * a.n_out_pad + (size_t)mt * 128 + n;
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+        for (int ch = 0; ch < a.npad / 16; ch++) {
           float v[16];
           tmem_ld16(tb + (uint32_t)(ch * 16), v);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 x4 = *reinterpret_cast<const float4*>(xs + ch * 16 + e);
-            y[c * 16 + e + 0] = fmaf(s, v[e + 0], fmaf(bb, x4.x, y[c * 16 + e + 0]));
-            y[c * 16 + e + 1] = fmaf(s, v[e + 1], fmaf(bb, x4.y, y[c * 16 + e + 1]));
-            y[c * 16 + e + 2] = fmaf(s, v[e + 2], fmaf(bb, x4.z, y[c * 16 + e + 2]));
-            y[c * 16 + e + 3] = fmaf(s, v[e + 3], fmaf(bb, x4.w, y[c * 16 + e + 3]));
-          }
+          for (int e = 0; e < 16; e++) out[(size_t)(ch * 16 + e) * a.n_out_pad] = v[e];
         }
-      }
-      tc05_fence_before();
-      fence_proxy_async();   // these reads of the stages come before the copy engine refills them
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&acc_empty[b]));
-        mbar_arrive(smem_u32(&empty_x[sx]));
-        mbar_arrive(smem_u32(&empty_w[sw]));
-      }
-    }
-    if (ok) {
-      // partial tile of this K slice: part[slice][column][tile row], rows of a warp contiguous
-      float* out = a.part + (size_t)slice * a.npad * a.n_out_pad + (size_t)mt * 128 + n;
-#pragma unroll
-      for (int c = 0; c < kTcFoldChunks; c++) {
-        const int ch = ch0 + c;
-        if (ch < ch1) {
-#pragma unroll
-          for (int e = 0; e < 16; e++) out[(size_t)(ch * 16 + e) * a.n_out_pad] = y[c * 16 + e];
-        }
+        tc05_fence_before();
       }
     }
   }
@@ -277,26 +231,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   if (warp == 1) {
     tc05_fence_after();
     tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
-  }
-}
-
-// Per (group, padded row) sums of the activations over the group's 64 inputs (f16 + remainder),
-// zero for padding rows.
-__global__ void __launch_bounds__(256) tc05_xsum_kernel(const __half* __restrict__ x, const __half* __restrict__ xlo,
-                                                        int ldx, int rows, int groups, int npad, float* xs) {
-  const int total = groups * npad;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
-    const int g = idx / npad, r = idx - g * npad;
-    float acc = 0.f;
-    if (r < rows) {
-      const __half* p = x + (size_t)r * ldx + g * 64;
-      for (int k = 0; k < 64; k++) acc += __half2float(p[k]);
-      if (xlo) {
-        const __half* q = xlo + (size_t)r * ldx + g * 64;
-        for (int k = 0; k < 64; k++) acc += __half2float(q[k]);
-      }
-    }
-    xs[idx] = acc;
   }
 }
 
@@ -351,41 +285,34 @@ Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) {
   p.gps = (groups + s - 1) / s;
   p.slices = (groups + p.gps - 1) / p.gps;
   p.grid = p.mtiles * p.slices;
-  const uint32_t xb = (uint32_t)p.npad * 128u * (x_lo ? 2u : 1u);
-  p.xs_off = xb;
-  p.x_tx = xb + (uint32_t)p.npad * 4u;
-  p.x_stage = (p.x_tx + 1023u) / 1024u * 1024u;
+  p.x_stage = (uint32_t)p.npad * 128u * (x_lo ? 2u : 1u);   // a multiple of 2048 B
+  p.x_tx = p.x_stage;
   const size_t fixed = 1024 /* alignment slack */ + (size_t)kTcSA * kTcAStage + (size_t)kTcSW * kTcWStage +
-                       (size_t)(2 * kTcSW + 2 * kTcMaxSX + 2 * kTcSA + 4) * 8 + 16;
+                       (size_t)(2 * kTcSW + 2 * kTcMaxSX + 2 * kTcSA + 1) * 8 + 16;
   const size_t room = kTcSmemMax > fixed ? kTcSmemMax - fixed : 0;
   p.sx = (int)std::min<size_t>(kTcMaxSX, room / p.x_stage);
   if (p.sx < 2) return Tc05Plan{};
   p.smem = fixed + (size_t)p.sx * p.x_stage;
   int cols = 32;
-  while (cols < 2 * p.npad) cols *= 2;
+  while (cols < p.npad) cols *= 2;
   p.tmem_cols = cols;
-  p.xs_bytes = ((size_t)groups * p.npad * 4 + 255) / 256 * 256;
-  p.part_off = p.xs_bytes;
-  p.scratch = p.part_off + (size_t)p.slices * p.npad * p.mtiles * 128 * 4;
+  p.part_off = 0;
+  p.scratch = (size_t)p.slices * p.npad * p.mtiles * 128 * 4;
   return p;
 }
 
-cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
-                              int rows, cudaStream_t s) {
-  tc05_xsum_kernel<<<std::min(1024, (a.groups * a.npad + 255) / 256), 256, 0, s>>>(x, xlo, ldx, rows, a.groups,
-                                                                                  a.npad, const_cast<float*>(a.xs));
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t s) {
   static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e;
   e = ensure_smem_limit(tc05_q4_kernel, p.smem, smem_set);
   if (e != cudaSuccess) return e;
   tc05_q4_kernel<<<p.grid, kTcThreads, p.smem, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
-                        int rows, int n_out, int half, float* y, int ldy, cudaStream_t s) {
-  const cudaError_t e = launch_tc05_parts(a, p, x, xlo, ldx, rows, s);
+cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_out, int half, float* y, int ldy,
+                        cudaStream_t s) {
+  const cudaError_t e = launch_tc05_parts(a, p, s);
   if (e != cudaSuccess) return e;
   const long long total = (long long)rows * n_out;
   const int blocks = (int)std::min<long long>(4096, (total + 255) / 256);

@@ -9,39 +9,37 @@ namespace dfl {
 
 constexpr unsigned kErrTimeoutTc05 = 4u;  // device error word bit of this kernel's bounded waits
 
-constexpr int kTcWarps = 12;              // copies, MMA issue, 2 decoder warps, 8 fold warps
-constexpr int kTcMaxRows = 160;           // activation rows per call (MMA N <= 160: the fold's sums fit in registers)
-constexpr int kTcSW = 6;                  // raw 4-bit tile stages
-constexpr int kTcSA = 2;                  // decoded f16 A-tile stages
+constexpr int kTcWarps = 10;              // copies, MMA issue, 8 dequantising warps (4 of them also the epilogue)
+constexpr int kTcMaxRows = 160;           // activation rows per call (the MMA's N, padded to 16)
+constexpr int kTcSW = 8;                  // raw 4-bit tile stages
+constexpr int kTcSA = 4;                  // dequantised f16 A-tile stages
 constexpr int kTcMaxSX = 4;               // activation stages, at most
 constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
 
 struct Tc05Args {
   CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder: box 64 x npad, 128-byte swizzle
   const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
-  float* xs;                 // [groups][npad] activation sums per group (scratch)
   float* part;               // [slices][npad][n_out_pad] partial tiles (scratch)
   unsigned* err;
   int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, tmem_cols;
-  uint32_t x_stage, xs_off, x_tx;
+  uint32_t x_stage, x_tx;
 };
 
 struct Tc05Plan {
   int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, tmem_cols = 0;   // npad == 0: no plan
-  uint32_t x_stage = 0, xs_off = 0, x_tx = 0;
-  size_t smem = 0, xs_bytes = 0, part_off = 0, scratch = 0;
+  uint32_t x_stage = 0, x_tx = 0;
+  size_t smem = 0, part_off = 0, scratch = 0;
 };
 
 Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
 
-// Group sums and the contraction: partial tiles [slices][npad][n_out_pad] in a.part (stored row order).
-cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
-                              int rows, cudaStream_t s);
+// The contraction: partial tiles [slices][npad][n_out_pad] in a.part (stored row order).
+cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t s);
 
 // launch_tc05_parts, then the ordered slice reduction into y [rows][ldy] (natural row order of
 // the matrix; half > 0: a gate/up matrix with `half` gate rows).
-cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, const __half* x, const __half* xlo, int ldx,
-                        int rows, int n_out, int half, float* y, int ldy, cudaStream_t s);
+cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_out, int half, float* y, int ldy,
+                        cudaStream_t s);
 
 // bf16 -> f16 of n_elems (even) contiguous elements, as the skinny GEMV converts context taps.
 cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cudaStream_t s);
@@ -52,5 +50,31 @@ cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cu
 // row row_base + map_row(a.xmap, c). LM head: one vocab state per CTA and row in a.e.lm_part.
 cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
                                  int n_out_pad, int row_base, int grid, cudaStream_t s);
+
+// ---- skinny projections of the draft round on tcgen05 (proj_tc05.cu) ---------------------------
+constexpr unsigned kErrTimeoutProj = 8u;  // device error word bit of its bounded waits
+constexpr int kProjMaxRows = 32;          // contraction rows (the MMA's N: 16 or 32)
+
+struct ProjArgs {
+  CUtensorMap xmap, xlmap;   // contraction rows (f16) and their f16 remainder: box 64 x npad, 128-byte swizzle
+  GemvArgs g;                // the epilogue (rows, row map, norms, outputs) as for the GEMV
+  const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
+  float* partials;           // [grid][2][npad][128] pieces of tiles cut between CTAs
+  int* tickets;              // [mtiles] arrivals, zero between launches
+  int n_strips, groups, mtiles, npad, has_lo, sa, sx, sw, tmem_cols;
+  int row_base;              // contraction row of the epilogue's row map origin
+  uint32_t x_stage;
+};
+
+struct ProjPlan {
+  int npad = 0, mtiles = 0, grid = 0, sa = 0, sx = 0, sw = 0, tmem_cols = 0;   // npad == 0: no plan
+  uint32_t x_stage = 0;
+  size_t smem = 0, partial_floats = 0;
+};
+
+ProjPlan plan_proj_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
+
+// One projection: EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD (nt = n-tiles of 8 epilogue rows).
+cudaError_t launch_proj_tc05(int epi, int nt, const ProjArgs& pa, const ProjPlan& p, cudaStream_t s);
 
 }  // namespace dfl

@@ -43,6 +43,25 @@ def test_round_bytes_match_the_c3_budget():
     assert abs(b["lm_head"] / 1e6 - 437.6) < 0.1
 
 
+def test_round_flops_c5_hand_count():
+    """The batched workload's algorithmic FLOP per round, counted by hand: 160 block rows through
+    five layers of (Q/K/V 5120x7168, O 5120x5120, gate/up/down 3x5120x17408), 128 drafting rows
+    through the 151936x5120 head, 144 new context rows through W_c (5120x25600) and each layer's
+    context K/V (2x1024x5120), and the block attention over a 2048-key window plus the 5 block keys."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    cfg = syn.CONFIGS["c5"]
+    f = bench.round_flops(cfg, [4096] * 32, 144.0)
+    layer = 5120 * 7168 + 5120 * 5120 + 3 * 5120 * 17408
+    assert f["layers"] == 2 * 160 * 5 * layer
+    assert f["lm_head"] == 2 * 128 * 151936 * 5120
+    assert f["W_c"] == 2 * 144 * 5120 * 25600
+    assert f["ctx_kv"] == 2 * 144 * 5 * 2048 * 5120
+    assert f["attention"] == 4 * 5 * 40 * 5 * (32 * (2048 + 5)) * 128
+    assert abs(f["total"] - sum(v for k, v in f.items() if k != "total")) < 1
+
+
 def test_oracle_table_one_core_and_all_cores():
     """The oracle timing table (1 core and all cores per workload) on the tiny fp32 drafter."""
     import bench

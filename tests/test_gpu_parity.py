@@ -124,6 +124,23 @@ def test_batch_ragged_and_row_chunks():
     run(cfg, rounds=3, ctx_capacity=160)
 
 
+@pytest.mark.parametrize("case", ["hd64", "hd128_gelu", "allrows_b3", "b4_g8_32rows", "g16", "markov", "d_ne_h"])
+def test_small_skinny_tc05(case):
+    """Draft calls of at most 32 block rows on the tcgen05 projection kernel (config skinny_tc05):
+    several 128-row tiles cut between CTAs (ragged last tiles: vocab 1000, d 256 / 512), 16 and 32
+    contraction rows, drafting-row maps of one to four requests, the gated-GELU FFN, the Markov
+    head's base logits, and d != H (the head then stays on the GEMV)."""
+    kw = {"hd64": dict(),
+          "hd128_gelu": dict(ffn="gelu", d=512, target_hidden=512, inter=1024, n_q_heads=4, n_kv_heads=2,
+                             head_dim=128),
+          "allrows_b3": dict(draft_all_rows=True, batch=3, ctx_len=50, agree=0.5),
+          "b4_g8_32rows": dict(batch=4, gamma=8, ctx_len=60, ctx_min=5, window=48, agree=0.6),
+          "g16": dict(gamma=16, n_kv_heads=4),
+          "markov": dict(markov_rank=128, gamma=6),
+          "d_ne_h": dict(target_hidden=512)}[case]
+    run(small(f"s_pj_{case}", skinny_tc05=True, **kw), rounds=2, ctx_capacity=64 if case == "b4_g8_32rows" else None)
+
+
 def test_deterministic_repeat():
     """Same inputs, two handles: bit-identical logits, tokens and confidence."""
     from speculative_block_draft_gb300.session import Session
@@ -294,10 +311,14 @@ def c3_model():
     return cached_model(CONFIGS["c3"], norm_jitter=0.1)
 
 
-def test_c3_dflash2_q4_full():
-    """The bench workload: 4-bit 5120-wide drafter, block 8, window 2048 over context 4096."""
-    rep = run(CONFIGS["c3"], rounds=2, model=c3_model())
-    print("c3", rep)
+@pytest.mark.parametrize("skinny", [False, True], ids=["gemv", "tc05"])
+def test_c3_dflash2_q4_full(skinny):
+    """The bench workload: 4-bit 5120-wide drafter, block 8, window 2048 over context 4096; on the
+    mma.sync GEMV and on the tcgen05 projection kernel (config skinny_tc05)."""
+    cfg = syn.with_overrides(CONFIGS["c3"], skinny_tc05=skinny)
+    m = c3_model()
+    rep = run(cfg, rounds=2, model=syn.HostModel(cfg, m.mats, dict(m.vecs)))
+    print("c3", skinny, rep)
 
 
 def _c4_oracle_ctx(cfg, model):
@@ -334,12 +355,15 @@ def test_c4_full_context_window0():
     print(cfg.name, rep)
 
 
-def test_c5_batched_sampled_requests():
+@pytest.mark.parametrize("tc05", [False, True], ids=["gemv", "tc05"])
+def test_c5_batched_sampled_requests(tc05):
     """32 requests, gamma 5, ragged contexts in [512, 16384], U{1..8} appends, agreement 0.6.
-    The GPU runs all 32; the oracle recomputes requests 0 and 17 (requests are independent)."""
+    The GPU runs all 32; the oracle recomputes requests 0 and 17 (requests are independent).
+    tc05: the 160 block rows run every projection and the head once on the tcgen05 contraction,
+    and context appends over 32 rows run W_c on it too."""
     from parity_util import MARGIN, Pair, accept_checked, compare_block
     import oracle
-    cfg = CONFIGS["c5"]
+    cfg = syn.with_overrides(CONFIGS["c5"], large_batch_tc05=tc05)
     m = c3_model()
     model = syn.HostModel(cfg, m.mats, dict(m.vecs))
     model.vecs["block_pos"] = syn.normal(cfg.seed, "block_pos", (32, cfg.d), 0.02)[: cfg.gamma].copy()

@@ -2,21 +2,20 @@
 fp64 linear map, element by element, and of the draft round when it runs its projections on
 that contraction (config large_batch_tc05).
 
-Error model of the contraction (it reads each weight as the group-64 affine code
-w = s q + b and computes, per group g of 64 inputs, v_g = sum (c + q_k) x_k on the tensor cores
-with c = 128 or 64, then y += s v_g + (b - c s) sum x_k in fp32):
-  * the products (c + q) x are exact in fp32 (8-bit integers times f16 values);
-  * the group sums v_g and sum x_k carry fp32 accumulation error, at most 2^-23 per addition
-    relative to the running magnitude (allowing truncating accumulation): over 64 inputs, or
-    128 with the f16 remainder, at most 128 * 2^-23 * sum (c + q)|x|;
-  * the fold's two fused multiply-adds and the ordered sum of the K slices add at most
-    2^-23 relative to the running sum per step, over K/64 groups.
-So |y - y_exact| <= (2^-16 + (K/64 + 2) 2^-22) * sum_g (|s| sum q|x| + (256|s| + |b|) sum |x|),
-a deterministic bound that is loose because the offsets c make the intermediate terms large.
-Two checks are tight: (1) with inputs on a 1/8 (remainder 1/64) grid every group sum is exact
-in fp32, so only the fold's roundings remain (bounded by 2^-22 times the running magnitudes,
-computed here from the exact group terms); (2) with N(0, 1) inputs the rms error stays below
-1e-4 of the rms output (random rounding grows like sqrt(K) * 2^-24 times the terms)."""
+Error model of the contraction. It dequantises each stored weight, the group-64 affine code
+w = s q + b, to f16 with one rounding (q made exact, then one fused f16 multiply-add), and
+accumulates y = sum_k f16(w_k) (hi_k + lo_k) on the tensor cores in fp32 over a K slice, then sums
+the slices in fp32:
+  * |f16(w) - w| <= 2^-11 |w| + 2^-25 (round to nearest; the second term covers f16 subnormals);
+  * f16 x f16 products are exact in fp32;
+  * the accumulation of n = K (2K with the remainder) terms plus the slice sum adds at most
+    (n + slices) 2^-22 times sum |f16(w) x| (a crude bound that allows truncating additions).
+So |y - y_exact| <= (2^-11 + 1.001 (n + slices) 2^-22) sum_k |w_k| |x_k| + 2^-25 sum_k |x_k|, a
+deterministic bound. The tight check is statistical: the rounding errors of the weights are
+independent and at most 2^-11 relative (most synthetic weights, |w| < 1/16 on the 2^-15 grid that
+bf16 scales and biases give them, are exact in f16), so the rms error stays below 2e-4 of the rms
+output for both the N(0, 1) inputs and the inputs on an exact 1/8 (remainder 1/64) grid; an fp32
+emulation of the same arithmetic gives about 2.5e-5."""
 import numpy as np
 import pytest
 
@@ -66,37 +65,22 @@ def _rows_of(blocks, sel):
                           np.ascontiguousarray(bias))
 
 
-def _codes(hm):
-    """q [n][G][64] float64, s, b [n][G] float64 of a q4 HostMatrix."""
+def _weights(hm):
+    """The exact stored weights w = s q + b [n][k] (float64) of a q4 HostMatrix."""
     n, k = hm.n_out, hm.n_in
     shifts = (4 * np.arange(8, dtype=np.uint32))[None, None, :]
     q = ((hm.data[:, :, None] >> shifts) & 15).reshape(n, k // 64, 64).astype(np.float64)
-    s = syn.bf16_bits_to_f32(hm.scale).astype(np.float64)
-    b = syn.bf16_bits_to_f32(hm.bias).astype(np.float64)
-    return q, s, b
+    sc = syn.bf16_bits_to_f32(hm.scale).astype(np.float64)[:, :, None]
+    bi = syn.bf16_bits_to_f32(hm.bias).astype(np.float64)[:, :, None]
+    return (sc * q + bi).reshape(n, k)
 
 
-def _bounds(hm, xh, xl, gps):
-    """(deterministic bound, fold-only bound) per [row][output] for inputs x = xh + xl."""
-    q, s, b = _codes(hm)
-    G = q.shape[1]
-    x = (xh + xl).reshape(xh.shape[0], G, 64)
-    ax = (np.abs(xh) + np.abs(xl)).reshape(xh.shape[0], G, 64)
-    X = ax.sum(axis=2)                                            # [r][G]
-    P = np.matmul(ax.transpose(1, 0, 2), q.transpose(1, 2, 0)).transpose(1, 2, 0)   # sum q |x|, [r][n][G]
-    inner = np.abs(s)[None] * P + (256 * np.abs(s) + np.abs(b))[None] * X[:, None, :]
-    det = (2.0 ** -16 + (G + 2) * 2.0 ** -22) * inner.sum(axis=2)
-    # fold only (exact group sums): running sums within each K slice, from the exact terms
-    v = np.matmul(x.transpose(1, 0, 2), (q + 128.0).transpose(1, 2, 0)).transpose(1, 2, 0)
-    xs = x.sum(axis=2)
-    t_s = np.abs(s)[None] * np.abs(v)
-    t_b = (np.abs(b) + 128 * np.abs(s))[None] * np.abs(xs)[:, None, :]
-    contrib = s[None] * (v - 128.0 * xs[:, None, :]) + b[None] * xs[:, None, :]
-    fold = np.zeros(det.shape)
-    for g0 in range(0, G, gps):
-        run = np.cumsum(contrib[:, :, g0:g0 + gps], axis=2)
-        fold += (np.abs(run) + t_s[:, :, g0:g0 + gps] + t_b[:, :, g0:g0 + gps]).sum(axis=2)
-    return det, 4 * U * (fold + np.abs(contrib).sum(axis=2))
+def _bound(hm, xh, xl, slices):
+    """Deterministic error bound per [row][output] for inputs x = xh + xl."""
+    aw = np.abs(_weights(hm))
+    ax = np.abs(xh) + np.abs(xl)
+    n_terms = xh.shape[1] * (2 if np.any(xl) else 1)
+    return (2.0 ** -11 + 1.001 * (n_terms + slices) * 2.0 ** -22) * (ax @ aw.T) + 2.0 ** -25 * ax.sum(axis=1)[:, None]
 
 
 def _check(h, which, blocks_map, rows, lo, exact, n_sample=None, seed=0):
@@ -128,14 +112,11 @@ def _check(h, which, blocks_map, rows, lo, exact, n_sample=None, seed=0):
     got = y.cpu().numpy().astype(np.float64)[:, sel]
     assert np.all(np.isfinite(got))
     err = np.abs(got - ref)
-    det, fold = _bounds(sub, xh, xl, plan.groups_per_slice)
+    det = _bound(sub, xh, xl, plan.k_slices)
     assert np.all(err <= det), f"{which}: max err {err.max()} above the deterministic bound"
-    if exact:
-        assert np.all(err <= fold), f"{which}: max err {err.max()}, fold bound {fold[err > fold].min()}"
-    else:
-        rms = np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(ref ** 2))
-        assert rms <= 1e-4, f"{which}: relative rms error {rms}"
-    return float(err.max())
+    rms = np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(ref ** 2))
+    assert rms <= 2e-4, f"{which}: relative rms error {rms}"
+    return float(err.max()), float(rms)
 
 
 SMALL = DraftConfig("tc05_small", n_layers=1, d=256, n_q_heads=4, n_kv_heads=2, head_dim=64, inter=1024, n_taps=4,
@@ -179,9 +160,9 @@ def test_rows_matmul_full_shapes_160_rows(which, lo):
     m = cached_model(CONFIGS["c3"], norm_jitter=0.1)
     s = _full_session(m)
     mats = _mats(m)
-    e1 = _check(s.h, which, mats, 160, lo, exact=False, n_sample=128, seed=5)
-    e2 = _check(s.h, which, mats, 160, lo, exact=True, n_sample=128, seed=6)
-    print(f"\n{which} lo={lo}: max err normal {e1:.3g}, grid {e2:.3g}")
+    e1, r1 = _check(s.h, which, mats, 160, lo, exact=False, n_sample=128, seed=5)
+    e2, r2 = _check(s.h, which, mats, 160, lo, exact=True, n_sample=128, seed=6)
+    print(f"\n{which} lo={lo}: max err normal {e1:.3g} (rms {r1:.2g}), grid {e2:.3g} (rms {r2:.2g})")
 
 
 _FULL = {}

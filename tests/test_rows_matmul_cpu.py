@@ -28,19 +28,19 @@ def test_plan_invariants(lib, n_out, k_in, rows, x_lo):
     p = pkg.rows_matmul_plan(n_out, k_in, rows, x_lo, 152)
     groups = k_in // 64
     assert p.n_pad % 16 == 0 and rows <= p.n_pad < rows + 16            # the MMA's N
-    assert 2 * p.n_pad <= TMEM_COLS                                      # two fp32 accumulators
+    assert p.n_pad <= TMEM_COLS // 2                                     # one fp32 accumulator, two CTAs per SM
     assert p.m_tiles == -(-n_out // 128)
     assert p.grid == p.m_tiles * p.k_slices
     # the K slices cover every group once, none empty, each at least 4 groups where K allows
     assert (p.k_slices - 1) * p.groups_per_slice < groups <= p.k_slices * p.groups_per_slice
     assert p.groups_per_slice >= min(4, groups)
     assert 2 <= p.x_stages <= 4 and p.smem_bytes <= SMEM_MAX
-    # activation stage: n_pad rows x 128 B (twice with the remainder) + the group sums, whole KB
-    stage = -(-(p.n_pad * 128 * (2 if x_lo else 1) + 4 * p.n_pad) // 1024) * 1024
-    assert p.smem_bytes >= p.x_stages * stage + 2 * 128 * 128   # + two decoded 16 KB A tiles
-    # scratch: per-group activation sums, then one fp32 partial tile per (K slice, 128-row tile)
-    sums = -(-(groups * p.n_pad * 4) // 256) * 256
-    assert p.scratch_bytes == sums + p.k_slices * p.n_pad * p.m_tiles * 128 * 4
+    # activation stage: n_pad rows x 128 B (twice with the remainder), a multiple of 1024 B
+    stage = p.n_pad * 128 * (2 if x_lo else 1)
+    assert stage % 1024 == 0
+    assert p.smem_bytes >= p.x_stages * stage + 4 * 128 * 128 + 8 * 4608   # + four f16 A tiles, eight raw stages
+    # scratch: one fp32 partial tile per (K slice, 128-row tile)
+    assert p.scratch_bytes == p.k_slices * p.n_pad * p.m_tiles * 128 * 4
 
 
 def test_plan_fills_the_sms_where_k_allows(lib):
