@@ -127,6 +127,19 @@ __device__ __forceinline__ void softmax_pv(float (&S)[NKEY / 8][4], int nvalid, 
   }
 }
 
+// Online combination of one key split (m, l, unnormalised O) into the running (M, L, O).
+__device__ __forceinline__ void merge_split(float2 ml, float4 v, float& mx, float& L, float4& acc) {
+  if (ml.x == -INFINITY) return;
+  const float mn = fmaxf(mx, ml.x);
+  const float so = mx == -INFINITY ? 0.f : exp2f(mx - mn), w = exp2f(ml.x - mn);
+  L = fmaf(w, ml.y, L * so);
+  acc.x = fmaf(w, v.x, acc.x * so);
+  acc.y = fmaf(w, v.y, acc.y * so);
+  acc.z = fmaf(w, v.z, acc.z * so);
+  acc.w = fmaf(w, v.w, acc.w * so);
+  mx = mn;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_constant__ AttnArgs a,
                                                                   const __grid_constant__ CUtensorMap kmap,
@@ -389,17 +402,7 @@ __global__ void __launch_bounds__(HD / 4) attn_merge_kernel(const __grid_constan
                 : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int q = 0; q < 16; q++) {
-      if (ml[q].x == -INFINITY) continue;
-      const float mn = fmaxf(mx, ml[q].x);
-      const float so = mx == -INFINITY ? 0.f : exp2f(mx - mn), w = exp2f(ml[q].x - mn);
-      L = fmaf(w, ml[q].y, L * so);
-      acc.x = fmaf(w, v[q].x, acc.x * so);
-      acc.y = fmaf(w, v[q].y, acc.y * so);
-      acc.z = fmaf(w, v[q].z, acc.z * so);
-      acc.w = fmaf(w, v[q].w, acc.w * so);
-      mx = mn;
-    }
+    for (int q = 0; q < 16; q++) merge_split(ml[q], v[q], mx, L, acc);
   }
   const float inv = 1.0f / L;
   const int head = kvh * grp + i / a.gamma, k = i % a.gamma;

@@ -92,29 +92,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   tc05_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The copy and MMA warps run their loops with all 32 lanes (one lane issues): a lone lane whose
+  // warp-mates wait at a block barrier is scheduled far too rarely for an issue loop.
   if (warp == 0) {
     // ---- copies: raw 4-bit tiles and activation tiles --------------------------------------------
-    if (lane == 0 && ng > 0) {
+    if (ng > 0) {
       bool ok = true;
       int nw = 0, nx = 0;   // stages whose copies were issued
       for (int i = 0; i < ng && ok; i++) {
         const int g = g0 + i, sw = i % kTcSW, sx = i % a.sx;
         if (i >= kTcSW)
-          ok = mbar_wait_bounded(smem_u32(&empty_w[sw]), ((i / kTcSW) + 1) & 1, a.err, kErrTimeoutTc05);
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[sw]), ((i / kTcSW) + 1) & 1, a.err,
+                                                         kErrTimeoutTc05));
         if (!ok) break;
-        const uint32_t fw = smem_u32(&full_w[sw]);
-        mbar_arrive_expect_tx(fw, (uint32_t)(strips_in_tile * kQ4GroupBytes));
-        for (int s = 0; s < strips_in_tile; s++)
-          bulk_g2s(smem_u32(wring + sw * kTcWStage + s * kQ4GroupBytes),
-                   a.w + ((size_t)(mt * kTcStrips + s) * a.groups + g) * kQ4GroupBytes, kQ4GroupBytes, fw);
+        if (lane == 0) {
+          const uint32_t fw = smem_u32(&full_w[sw]);
+          mbar_arrive_expect_tx(fw, (uint32_t)(strips_in_tile * kQ4GroupBytes));
+          for (int s = 0; s < strips_in_tile; s++)
+            bulk_g2s(smem_u32(wring + sw * kTcWStage + s * kQ4GroupBytes),
+                     a.w + ((size_t)(mt * kTcStrips + s) * a.groups + g) * kQ4GroupBytes, kQ4GroupBytes, fw);
+        }
+        __syncwarp();
         nw = i + 1;
-        if (i >= a.sx) ok = mbar_wait_bounded(smem_u32(&empty_x[sx]), ((i / a.sx) + 1) & 1, a.err, kErrTimeoutTc05);
+        if (i >= a.sx)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_x[sx]), ((i / a.sx) + 1) & 1, a.err,
+                                                         kErrTimeoutTc05));
         if (!ok) break;
-        const uint32_t fx = smem_u32(&full_x[sx]);
-        uint8_t* xst = xring + (size_t)sx * a.x_stage;
-        mbar_arrive_expect_tx(fx, a.x_tx);
-        tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
-        if (a.has_lo) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
+        if (lane == 0) {
+          const uint32_t fx = smem_u32(&full_x[sx]);
+          uint8_t* xst = xring + (size_t)sx * a.x_stage;
+          mbar_arrive_expect_tx(fx, a.x_tx);
+          tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
+          if (a.has_lo) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
+        }
+        __syncwarp();
         nx = i + 1;
       }
       // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
@@ -127,29 +138,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     }
   } else if (warp == 1) {
     // ---- MMA issue ----------------------------------------------------------------------------
-    if (lane == 0 && ng > 0) {
+    if (ng > 0) {
       const uint32_t idesc = umma_idesc_f16_f32(128, a.npad);
       bool ok = true;
       int issued = 0;
       for (int i = 0; i < ng && ok; i++) {
         const int sa = i % kTcSA, sx = i % a.sx;
-        ok = mbar_wait_bounded(smem_u32(&full_a[sa]), (i / kTcSA) & 1, a.err, kErrTimeoutTc05) &&
-             mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full_a[sa]), (i / kTcSA) & 1, a.err, kErrTimeoutTc05) &&
+                                     mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05));
         if (!ok) break;
         tc05_fence_after();
-        const uint32_t abase = smem_u32(aring + sa * kTcAStage);
-        const uint32_t xbase = smem_u32(xring + (size_t)sx * a.x_stage);
+        if (lane == 0) {
+          const uint32_t abase = smem_u32(aring + sa * kTcAStage);
+          const uint32_t xbase = smem_u32(xring + (size_t)sx * a.x_stage);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
-          umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
-          if (a.has_lo) umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + a.npad * 128 + 32 * kk), idesc, 1u);
+          for (int kk = 0; kk < 4; kk++) {
+            const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
+            umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            if (a.has_lo) umma_f16_ss(tmem, ad, umma_desc_sw128(xbase + a.npad * 128 + 32 * kk), idesc, 1u);
+          }
+          umma_commit(smem_u32(&empty_a[sa]));
+          umma_commit(smem_u32(&empty_x[sx]));
+          if (i + 1 == ng) umma_commit(smem_u32(acc_done));
         }
-        umma_commit(smem_u32(&empty_a[sa]));
-        umma_commit(smem_u32(&empty_x[sx]));
+        __syncwarp();
         issued = i + 1;
       }
-      if (ok) umma_commit(smem_u32(acc_done));
       // nothing of this CTA may still be running on the tensor core when its memory is freed
       if (issued > 0) mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % kTcSA]), ((issued - 1) / kTcSA) & 1, a.err,
                                         kErrTimeoutTc05);

@@ -34,9 +34,10 @@ namespace {
 constexpr int kPjWarps = 14;
 constexpr int kPjThreads = kPjWarps * 32;
 constexpr int kPjEpiWarp0 = 10;                           // epilogue warps 10-13
+constexpr int kPjChains = 4;                              // independent accumulators per segment (one per K step)
 constexpr int kPjStrips = 8;                              // 16-row strips per 128-row tile
 constexpr int kPjKG = 4;                                  // groups per raw stage (per-strip copies of 2304 B)
-constexpr int kPjWStage = kPjStrips * kPjKG * kQ4GroupBytes;   // 18 KB: one raw stage
+constexpr int kPjWStage = kPjStrips * kPjKG * kQ4GroupBytes;   // 18 KB: a raw stage's weights
 constexpr int kPjAStage = 128 * 128;                      // 16 KB: one unit, f16
 constexpr uint32_t kPjEpiBar = 1;                         // named barrier of the epilogue warps
 
@@ -90,19 +91,19 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
   const GemvArgs& a = pa.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // A stages (pa.sa): dequantised weights of one unit. Raw stages (pa.sw): the 4-bit tiles of up to
+  // kPjKG units and, after them, those units' activation tiles, so both share one lookahead.
+  const uint32_t raw_bytes = kPjWStage + kPjKG * pa.x_stage;   // a multiple of 1024
   uint8_t* aring = sm;                                          // pa.sa x 16 KB (1024-aligned)
-  uint8_t* xring = aring + pa.sa * kPjAStage;                   // pa.sx x pa.x_stage (1024-aligned)
-  uint8_t* wring = xring + (size_t)pa.sx * pa.x_stage;          // pa.sw x kPjWStage
-  float* tile = reinterpret_cast<float*>(wring + (size_t)pa.sw * kPjWStage);   // [128][NP] fp32
+  uint8_t* wring = aring + pa.sa * kPjAStage;                   // pa.sw x raw_bytes (1024-aligned)
+  float* tile = reinterpret_cast<float*>(wring + (size_t)pa.sw * raw_bytes);   // [128][NP] fp32
   float* srow = tile + 128 * NP;                                // kMaxRows row scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(srow + kMaxRows);
-  uint64_t* full_w = bars;
-  uint64_t* empty_w = full_w + pa.sw;
-  uint64_t* full_x = empty_w + pa.sw;
-  uint64_t* empty_x = full_x + pa.sx;
-  uint64_t* full_a = empty_x + pa.sx;
-  uint64_t* empty_a = full_a + pa.sa;
-  uint64_t* acc_full = empty_a + pa.sa;
+  uint64_t* full_w = bars;                                      // weights and activations landed
+  uint64_t* empty_w = full_w + pa.sw;                           // decoders and MMAs done with a raw stage
+  uint64_t* full_a = empty_w + pa.sw;                           // an A stage written
+  uint64_t* freed = full_a + pa.sa;                             // an A stage's MMAs completed
+  uint64_t* acc_full = freed + pa.sa;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   int* flag = reinterpret_cast<int*>(tmem_slot + 1);           // last-arriver decision, broadcast
@@ -116,19 +117,15 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int i = 0; i < pa.sw; i++) {
       mbar_init(smem_u32(&full_w[i]), 1);
-      mbar_init(smem_u32(&empty_w[i]), kPjStrips);   // the eight dequantising warps
-    }
-    for (int i = 0; i < pa.sx; i++) {
-      mbar_init(smem_u32(&full_x[i]), 1);
-      mbar_init(smem_u32(&empty_x[i]), 1);            // the MMA commit
+      mbar_init(smem_u32(&empty_w[i]), kPjStrips + 1);   // eight dequantising warps + the MMA commit
     }
     for (int i = 0; i < pa.sa; i++) {
       mbar_init(smem_u32(&full_a[i]), kPjStrips);
-      mbar_init(smem_u32(&empty_a[i]), 1);            // the MMA commit
+      mbar_init(smem_u32(&freed[i]), 1);                  // the MMA commit
     }
     for (int b = 0; b < 2; b++) {
-      mbar_init(smem_u32(&acc_full[b]), 1);           // the MMA commit
-      mbar_init(smem_u32(&acc_empty[b]), 4);          // the four epilogue warps
+      mbar_init(smem_u32(&acc_full[b]), 1);               // the MMA commit
+      mbar_init(smem_u32(&acc_empty[b]), 4);              // the four epilogue warps
     }
     fence_barrier_init();
   }
@@ -142,85 +139,106 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
 
+  // The copy and MMA warps run their loops with all 32 lanes (one lane issues): a lone lane whose
+  // warp-mates wait at a block barrier is scheduled far too rarely for an issue loop.
   if (warp == 0) {
-    if (lane == 0 && n_units > 0) {
-      // ---- weight copies: never depend on earlier kernels, so they start at once -----------------
+    // ---- copies ------------------------------------------------------------------------------------
+    if (n_units > 0) {
       bool ok = true;
-      int nw = 0;   // stages issued
-      StageWalk st{u0, 0, 0};
-      st.set(u1, pa.groups);
-      for (; st.v < u1 && ok; st.next(u1, pa.groups)) {
-        const int sw = st.j % pa.sw;
-        if (st.j >= pa.sw)
-          ok = mbar_wait_bounded(smem_u32(&empty_w[sw]), ((st.j / pa.sw) + 1) & 1, a.err, kErrTimeoutProj);
-        if (!ok) break;
+      int nw = 0;   // stages whose copies were issued
+      auto weights = [&](const StageWalk& st, int sw) {
+        if (lane != 0) return;
         const int strips = min(kPjStrips, pa.n_strips - st.mt * kPjStrips);
         const uint32_t fw = smem_u32(&full_w[sw]);
-        mbar_arrive_expect_tx(fw, (uint32_t)(strips * st.n * kQ4GroupBytes));
+        mbar_arrive_expect_tx(fw, (uint32_t)(strips * st.n * kQ4GroupBytes + st.n * pa.x_stage));
         for (int s = 0; s < strips; s++)
-          bulk_g2s(smem_u32(wring + sw * kPjWStage + s * (kPjKG * kQ4GroupBytes)),
+          bulk_g2s(smem_u32(wring + (size_t)sw * raw_bytes + s * (kPjKG * kQ4GroupBytes)),
                    pa.w + ((size_t)(st.mt * kPjStrips + s) * pa.groups + st.g) * kQ4GroupBytes,
                    (uint32_t)(st.n * kQ4GroupBytes), fw);
+      };
+      auto acts = [&](const StageWalk& st, int sw) {
+        if (lane != 0) return;
+        const uint32_t fw = smem_u32(&full_w[sw]);
+        for (int gi = 0; gi < st.n; gi++) {
+          const uint32_t xst = smem_u32(wring + (size_t)sw * raw_bytes + kPjWStage + gi * pa.x_stage);
+          tma_load_2d(xst, &pa.xmap, (st.g + gi) * 64, 0, fw);
+          if (pa.has_lo) tma_load_2d(xst + NP * 128, &pa.xlmap, (st.g + gi) * 64, 0, fw);
+        }
+      };
+      // weights never change: the first stages' weights go out before waiting for the previous
+      // kernel, their activations after it
+      StageWalk st{u0, 0, 0};
+      st.set(u1, pa.groups);
+      StageWalk first = st;
+      for (; st.v < u1 && st.j < pa.sw; st.next(u1, pa.groups)) {
+        weights(st, st.j);
+        nw = st.j + 1;
+      }
+      pdl_wait();
+      for (StageWalk q = first; q.v < u1 && q.j < pa.sw; q.next(u1, pa.groups)) acts(q, q.j);
+      __syncwarp();
+      for (; st.v < u1 && ok; st.next(u1, pa.groups)) {
+        const int sw = st.j % pa.sw;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[sw]), ((st.j / pa.sw) + 1) & 1, a.err,
+                                                       kErrTimeoutProj));
+        if (!ok) break;
+        weights(st, sw);
+        acts(st, sw);
+        __syncwarp();
         nw = st.j + 1;
       }
       // leave no copy in flight into this CTA's shared memory, also when a consumer gave up
       for (int j = nw > pa.sw ? nw - pa.sw : 0; j < nw; j++)
         mbar_wait_bounded(smem_u32(&full_w[j % pa.sw]), (j / pa.sw) & 1, nullptr, 0);
-    } else if (lane == 1 && n_units > 0) {
-      // ---- activation copies, once the previous kernel's outputs are visible ---------------------
-      pdl_wait();
-      bool ok = true;
-      int nx = 0;
-      for (int i = 0; i < n_units && ok; i++) {
-        const int g = (int)((u0 + i) % pa.groups), sx = i % pa.sx;
-        if (i >= pa.sx) ok = mbar_wait_bounded(smem_u32(&empty_x[sx]), ((i / pa.sx) + 1) & 1, a.err, kErrTimeoutProj);
-        if (!ok) break;
-        const uint32_t fx = smem_u32(&full_x[sx]);
-        uint8_t* xst = xring + (size_t)sx * pa.x_stage;
-        mbar_arrive_expect_tx(fx, pa.x_stage);
-        tma_load_2d(smem_u32(xst), &pa.xmap, g * 64, 0, fx);
-        if (pa.has_lo) tma_load_2d(smem_u32(xst + NP * 128), &pa.xlmap, g * 64, 0, fx);
-        nx = i + 1;
-      }
-      for (int j = nx > pa.sx ? nx - pa.sx : 0; j < nx; j++)
-        mbar_wait_bounded(smem_u32(&full_x[j % pa.sx]), (j / pa.sx) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
-    // ---- MMA issue: one accumulator per segment (the range's units of one tile) -------------------
-    if (lane == 0 && n_units > 0) {
+    // ---- MMA issue: per segment (the range's units of one tile) kPjChains accumulators, K step kk
+    // of every unit into chain kk, so consecutive MMAs do not wait for each other's results
+    if (n_units > 0) {
       const uint32_t idesc = umma_idesc_f16_f32(128, NP);
       bool ok = true;
       int issued = 0, seg = -1, first_of_seg = 1;
-      for (int i = 0; i < n_units && ok; i++) {
-        const int g = (int)((u0 + i) % pa.groups), sa = i % pa.sa, sx = i % pa.sx;
-        if (i == 0 || g == 0) {   // a new segment
-          seg++;
-          first_of_seg = 1;
-          if (seg >= 2)
-            ok = mbar_wait_bounded(smem_u32(&acc_empty[seg & 1]), ((seg >> 1) + 1) & 1, a.err, kErrTimeoutProj);
-        }
-        ok = ok && mbar_wait_bounded(smem_u32(&full_a[sa]), (i / pa.sa) & 1, a.err, kErrTimeoutProj) &&
-             mbar_wait_bounded(smem_u32(&full_x[sx]), (i / pa.sx) & 1, a.err, kErrTimeoutProj);
-        if (!ok) break;
-        tc05_fence_after();
-        const uint32_t d = tmem + (uint32_t)((seg & 1) * NP);
-        const uint32_t abase = smem_u32(aring + sa * kPjAStage);
-        const uint32_t xbase = smem_u32(xring + (size_t)sx * pa.x_stage);
+      StageWalk st{u0, 0, 0};
+      st.set(u1, pa.groups);
+      for (; st.v < u1 && ok; st.next(u1, pa.groups)) {
+        const int sw = st.j % pa.sw;
+        for (int gi = 0; gi < st.n && ok; gi++) {
+          const int i = st.i + gi, g = st.g + gi, sa = i % pa.sa;
+          if (i == 0 || g == 0) {   // a new segment
+            seg++;
+            first_of_seg = 1;
+            if (seg >= 2)
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&acc_empty[seg & 1]), ((seg >> 1) + 1) & 1,
+                                                             a.err, kErrTimeoutProj));
+          }
+          // the decoders wrote this A stage after the raw stage (weights and activations) landed
+          ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full_a[sa]), (i / pa.sa) & 1, a.err,
+                                                               kErrTimeoutProj));
+          if (!ok) break;
+          tc05_fence_after();
+          if (lane == 0) {
+            const uint32_t d = tmem + (uint32_t)((seg & 1) * kPjChains * NP);
+            const uint32_t abase = smem_u32(aring + sa * kPjAStage);
+            const uint32_t xbase = smem_u32(wring + (size_t)sw * raw_bytes + kPjWStage + gi * pa.x_stage);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
-          umma_f16_ss(d, ad, umma_desc_sw128(xbase + 32 * kk), idesc, (first_of_seg && kk == 0) ? 0u : 1u);
-          if (pa.has_lo) umma_f16_ss(d, ad, umma_desc_sw128(xbase + NP * 128 + 32 * kk), idesc, 1u);
+            for (int kk = 0; kk < 4; kk++) {
+              const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
+              const uint32_t dk = d + (uint32_t)(kk * NP);
+              umma_f16_ss(dk, ad, umma_desc_sw128(xbase + 32 * kk), idesc, first_of_seg ? 0u : 1u);
+              if (pa.has_lo) umma_f16_ss(dk, ad, umma_desc_sw128(xbase + NP * 128 + 32 * kk), idesc, 1u);
+            }
+            umma_commit(smem_u32(&freed[sa]));
+            if (gi + 1 == st.n) umma_commit(smem_u32(&empty_w[sw]));   // its activations were read
+            if (i + 1 == n_units || g + 1 == pa.groups) umma_commit(smem_u32(&acc_full[seg & 1]));
+          }
+          __syncwarp();
+          first_of_seg = 0;
+          issued = i + 1;
         }
-        first_of_seg = 0;
-        umma_commit(smem_u32(&empty_a[sa]));
-        umma_commit(smem_u32(&empty_x[sx]));
-        if (i + 1 == n_units || g + 1 == pa.groups) umma_commit(smem_u32(&acc_full[seg & 1]));
-        issued = i + 1;
       }
       // nothing of this CTA may still be running on the tensor core when its memory is freed
       if (issued > 0)
-        mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % pa.sa]), ((issued - 1) / pa.sa) & 1, a.err,
+        mbar_wait_bounded(smem_u32(&freed[(issued - 1) % pa.sa]), ((issued - 1) / pa.sa) & 1, a.err,
                           kErrTimeoutProj);
     }
   } else if (warp < kPjEpiWarp0) {
@@ -235,12 +253,12 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
       const int strips = min(kPjStrips, pa.n_strips - st.mt * kPjStrips);
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full_w[sw]), (st.j / pa.sw) & 1, a.err, kErrTimeoutProj));
       if (!ok) break;
-      const uint8_t* sp = wring + sw * kPjWStage + s * (kPjKG * kQ4GroupBytes);
+      const uint8_t* sp = wring + (size_t)sw * raw_bytes + s * (kPjKG * kQ4GroupBytes);
       __half2 sg, bg, s8, b8;
       for (int gi = 0; gi < st.n && ok; gi++) {
         const int i = st.i + gi, sa = i % pa.sa;
         if (i >= pa.sa)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_a[sa]), ((i / pa.sa) + 1) & 1, a.err,
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&freed[sa]), ((i / pa.sa) + 1) & 1, a.err,
                                                          kErrTimeoutProj));
         if (!ok) break;
         const uint8_t* gp = sp + gi * kQ4GroupBytes;
@@ -353,17 +371,33 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
       const long long su1 = min(u1, te);
       const bool whole = u == tb && su1 == te;
       const int b = seg & 1;
-      // one thread waits and the barrier hands the result to all four warps, so that they take
-      // the same number of named barriers whatever happens
-      if (et == 0) *okflag = mbar_wait_bounded(smem_u32(&acc_full[b]), (seg >> 1) & 1, a.err, kErrTimeoutProj);
+      // one warp waits and the barrier hands the result to all four warps, so that they take the
+      // same number of named barriers whatever happens
+      if (ew == 0) {
+        const bool w_ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&acc_full[b]), (seg >> 1) & 1, a.err,
+                                                                    kErrTimeoutProj));
+        if (lane == 0) *okflag = w_ok;
+      }
       epi_bar();
       ok = *okflag != 0;
       if (!ok) break;
       tc05_fence_after();
+      // the segment's result: its chains summed in chain order
       float v[NP];
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * NP);
-      tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&v[0]));
-      if constexpr (NP > 16) tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kPjChains * NP);
+#pragma unroll
+      for (int h = 0; h < NP; h += 16) {
+        float w[16];
+        tmem_ld16(taddr + h, w);
+#pragma unroll
+        for (int e = 0; e < 16; e++) v[h + e] = w[e];
+#pragma unroll
+        for (int ch = 1; ch < kPjChains; ch++) {
+          tmem_ld16(taddr + (uint32_t)(ch * NP + h), w);
+#pragma unroll
+          for (int e = 0; e < 16; e++) v[h + e] += w[e];
+        }
+      }
       tc05_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
@@ -447,12 +481,12 @@ ProjPlan plan_proj_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) 
   const long long T = (long long)p.mtiles * groups;
   p.grid = (int)std::min<long long>(n_sm, T);
   p.x_stage = (uint32_t)p.npad * 128u * (x_lo ? 2u : 1u);
-  p.sa = 3;
-  p.sx = p.x_stage <= 4096 ? 8 : 6;
-  p.tmem_cols = 2 * p.npad < 32 ? 32 : 2 * p.npad;
-  const size_t fixed = 1024 /* alignment slack */ + (size_t)p.sa * kPjAStage + (size_t)p.sx * p.x_stage +
-                       (size_t)128 * p.npad * 4 + kMaxRows * 4 + (size_t)(2 * p.sx + 2 * p.sa + 4) * 8 + 16;
-  const size_t per_stage = kPjWStage + 16;   // a raw stage and its two barriers
+  p.sa = 4;                                // dequantised A stages
+  p.sx = 0;
+  p.tmem_cols = 2 * kPjChains * p.npad;    // two segments in flight, kPjChains accumulators each
+  const size_t fixed = 1024 /* alignment slack */ + (size_t)p.sa * kPjAStage + (size_t)128 * p.npad * 4 +
+                       kMaxRows * 4 + (size_t)(2 * p.sa + 4) * 8 + 16;
+  const size_t per_stage = kPjWStage + (size_t)kPjKG * p.x_stage + 16;   // a raw stage and its two barriers
   const size_t room = kTcSmemMax > fixed ? kTcSmemMax - fixed : 0;
   p.sw = (int)std::min<size_t>(8, room / per_stage);
   if (p.sw < 2) return ProjPlan{};
