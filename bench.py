@@ -83,22 +83,42 @@ def load_peaks() -> dict:
 
 
 def load_traffic(kernel: str):
-    """ncu DRAM bytes per launch of `kernel`, if captured on the current kernel sources."""
+    """ncu DRAM bytes per launch of `kernel` (a PROBES name), if captured on the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         ent = d[kernel]
-        if ent.get("source_hash") != kernel_source_hash():
+        if ent.get("source_hash") != kernel_source_hash(tuple(ent.get("sources", LM_HEAD_SOURCES))):
             return None
         return float(ent["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 
 
-# The sources the LM-head launch is compiled from: its GEMV kernel and epilogue, the vocab merge,
-# and the constants and helpers they include. A change to any of them voids a traffic record.
+# The sources the projection launches are compiled from: the GEMV kernel and its epilogues, the
+# vocab merge, and the constants and helpers they include. A change to any of them voids a record.
 LM_HEAD_SOURCES = ("common.cuh", "gemv_f32.cu", "gemv_impl.cuh", "gemv_q4.cu", "internal.h")
+ATTN_SOURCES = ("attn.cu", "common.cuh", "internal.h")
+
+# Kernel classes of a round that bench.py times live (dflash_set_probe kinds): name, probe kind,
+# launches per round, algorithmic bytes per launch (weights at their stored size; attention: the
+# window's context K and V rows of one layer).
+def probe_classes(cfg, ctx_lens, ctx_rows_per_round):
+    bpp = BYTES_PER_PARAM[cfg.wdtype]
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    act = 4 if cfg.adtype == "f32" else 2
+    keys = sum(min(int(P), cfg.window) if cfg.window else int(P) for P in ctx_lens)
+    L, d, I = cfg.n_layers, cfg.d, cfg.inter
+    chunks = max(1, -(-int(round(ctx_rows_per_round)) // 32))
+    return [("lm_head", 0, 1, cfg.vocab * cfg.target_hidden * bpp),
+            ("qkv", 1, L, (qd + 2 * kvd) * d * bpp),
+            ("attention", 2, L, keys * kvd * 2 * act),
+            ("o", 3, L, d * qd * bpp),
+            ("gate_up", 4, L, 2 * I * d * bpp),
+            ("down", 5, L, d * I * bpp),
+            ("w_c", 6, chunks, d * cfg.n_taps * cfg.target_hidden * bpp),
+            ("ctx_kv", 7, chunks, L * 2 * kvd * d * bpp)]
 
 
 def kernel_source_hash(names=LM_HEAD_SOURCES) -> str:
@@ -347,6 +367,8 @@ def main():
                     help="comma-separated workloads: print the oracle's 1-core / all-core round times and exit")
     ap.add_argument("--large-batch-tc05", action="store_true",
                     help="library option: draft calls of more than 32 block rows on the tcgen05 contraction")
+    ap.add_argument("--probe-rounds", type=int, default=5,
+                    help="rounds per kernel class timed live after the timed region (one launch each)")
     ap.add_argument("--skinny-tc05", action="store_true",
                     help="draft calls of at most 32 block rows run their projections on the tcgen05 projection kernel")
     ap.add_argument("--profile-ctx", type=int, default=0,
@@ -383,7 +405,7 @@ def main():
     model = syn.make_model(cfg)
     B, G, n = cfg.batch, cfg.gamma, cfg.n_draft
     sess = Session(model, max_batch=B, ctx_capacity=(cfg.window if cfg.window else
-                                                      cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + args.lat_steps + 8)))
+                                                      cfg.ctx_len + 8 * (args.steps + args.warmup + args.e2e_steps + args.lat_steps + 8 * args.probe_rounds + 8)))
     h, stream = sess.h, sess.stream
     lengths = syn.ctx_lengths(cfg)
     if args.profile_ctx:
@@ -420,7 +442,7 @@ def main():
         c = [int(x) for x in counts[s]]
         h.project_ctx(req, c, dev_taps[s], stream=stream)
         if probe is not None:
-            h.set_probe(*probe)
+            h.set_probe(*probe, kernel=0)
         rc = h.draft_block(req, dev_anchor[s], draft, conf, None, stream=stream)
         assert rc == 0
         h.accept(draft, dev_target[s], acc_len, nxt, stream=stream)
@@ -458,6 +480,23 @@ def main():
     lm_ms = float(np.mean([a.elapsed_time(b) for a, b in probes]))
     t_max, blocks = reduce_over_ranks(elapsed, float(B * args.steps))
     value = blocks / t_max
+
+    # ---- every kernel class of the round timed live: events around one launch per probe round ----
+    ctx_rows = float(np.mean([np.sum(counts[args.warmup + i]) for i in range(args.steps)]))
+    classes = probe_classes(cfg, lengths, ctx_rows)
+    class_ms = {}
+    for name, kind, _, _ in classes:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.probe_rounds)]
+        with torch.cuda.stream(stream):
+            for j, (a0, a1) in enumerate(evs):
+                a0.record(stream)   # torch creates the events on first record; the library re-records them
+                a1.record(stream)
+                h.set_probe(a0, a1, kernel=kind)
+                step(args.warmup + j % args.steps)
+        stream.synchronize()
+        class_ms[name] = float(np.mean([a0.elapsed_time(a1) for a0, a1 in evs]))
+    assert h.check_errors(stream) == 0
 
     # ---- end to end through the C ABI with host buffers --------------------------------------
     pin_taps = [torch.from_numpy(t.view(np.int16) if t.dtype == np.uint16 else t).pin_memory()
@@ -526,12 +565,31 @@ def main():
 
     peaks = load_peaks()
     rb = round_bytes(cfg, lengths)
-    ctx_rows = float(np.mean([np.sum(counts[args.warmup + i]) for i in range(args.steps)]))
     rf = round_flops(cfg, lengths, ctx_rows)
     t_round = t_max / args.steps
-    lm_bytes = round_bytes(cfg, lengths)["lm_head"]
-    lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
-    traffic = load_traffic("lm_head")
+    # per kernel class: live achieved GB/s against its algorithmic bytes; the roofline object is
+    # the class that takes the largest share of the round (launch time x launches per round)
+    class_ms["lm_head"] = lm_ms
+    t_round_ms = 1e3 * t_max / args.steps
+    by_kernel = {}
+    for name, kind, per_round, nbytes in classes:
+        ms = class_ms[name]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        by_kernel[name] = {"avg_launch_us": 1e3 * ms, "launches_per_round": per_round,
+                           "share_of_round": ms * per_round / t_round_ms, "algorithmic_bytes_per_launch": nbytes,
+                           "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["share_of_round"])
+    dk = by_kernel[dom]
+    roof = {"kernel": f"{dom}: " + {"lm_head": "4-bit GEMV + fused argmax/softmax confidence, then the vocab merge",
+                                    "attention": "block attention over the window (+ split merge)",
+                                    "w_c": "4-bit GEMV, context projection (Eq 2) + ctx norm sums",
+                                    "ctx_kv": "4-bit GEMV, context K/V of every layer, one grouped launch"}.get(
+                dom, "4-bit GEMV with fused epilogue, layer 0 (the layers are identical)"),
+            "bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": dk["frac"], "traffic": load_traffic(dom),
+            "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"],
+            "avg_launch_ms": dk["avg_launch_us"] / 1e3, "share_of_round": dk["share_of_round"],
+            "peak_source": f"{peaks['source']} (burst copy, MEASURED_PEAKS.json hbm_gbs)"}
     line = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
@@ -549,11 +607,8 @@ def main():
                          "frac": rf["total"] / t_round / 1e12 / peaks["bf16_tflops_sustained"],
                          "peak_source": f"{peaks['source']} (cuBLAS bf16, sustained; the projections run f16 "
                                         f"operands on the same tensor-core rate)"},
-        "roofline": {"kernel": "LM head (4-bit GEMV + fused argmax/softmax confidence), 1 launch per round",
-                     "bound": "hbm", "achieved": lm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": lm_gbs / peaks["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes_per_launch": lm_bytes, "avg_launch_ms": lm_ms,
-                     "peak_source": f"{peaks['source']} (burst copy, MEASURED_PEAKS.json hbm_gbs)"},
+        "roofline": roof,
+        "roofline_by_kernel": by_kernel,
         "e2e": {"value": e2e_value, "unit": "blocks/s", "h2d_bytes_per_step": h2d // max(1, args.e2e_steps),
                 "d2h_bytes_per_step": d2h // max(1, args.e2e_steps), "steps": args.e2e_steps},
         "gpu_launches": int(launches),

@@ -245,9 +245,22 @@ int dflash_get_stats(const dflash_handle* h, dflash_stats* out);
  * NULL handle or counts or a bad n_counts, DFLASH_ECUDA on a CUDA error. */
 int dflash_accept_histogram(dflash_handle* h, uint64_t* counts, int n_counts, void* stream);
 
-/* Record two caller-created CUDA events (cudaEvent_t) around the launch of one kernel of the
- * next dflash_draft_block call, for live per-kernel timing. kernel: 0 = the LM head (the largest
- * launch of the round). Events are used once, then forgotten. */
+/* Record two caller-created CUDA events (cudaEvent_t) around the first launch (or launch pair) of
+ * one kind in the next dflash_draft_block or dflash_project_ctx call that runs it, for live
+ * per-kernel timing: the LM head with its vocab merge; layer 0's Q/K/V projection, attention
+ * (with its split merge), O projection, gate/up projection, down projection; the context
+ * projection W_c and the context K/V append of the first 32-row chunk. Events are used once,
+ * then forgotten. Returns DFLASH_EINVAL for a NULL handle or an unknown kind. */
+enum {
+  DFLASH_PROBE_LM_HEAD = 0,
+  DFLASH_PROBE_QKV = 1,
+  DFLASH_PROBE_ATTN = 2,
+  DFLASH_PROBE_O = 3,
+  DFLASH_PROBE_GATE_UP = 4,
+  DFLASH_PROBE_DOWN = 5,
+  DFLASH_PROBE_WC = 6,
+  DFLASH_PROBE_CTX_KV = 7
+};
 int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop_event);
 
 /* Kernel launches issued by this handle since create (all calls), for launch accounting. */

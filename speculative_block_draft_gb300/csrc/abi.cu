@@ -75,6 +75,7 @@ struct dflash_handle {
   dflash_stats stats{};
   uint64_t launches = 0;
   cudaEvent_t probe_start = nullptr, probe_stop = nullptr;
+  int probe_kernel = 0;         // DFLASH_PROBE_* the events go around (used once)
   int stall_armed = 0, stall_active = 0;   // test hook: CTA + 1 that stalls in the next / this draft call
 };
 
@@ -444,6 +445,17 @@ struct GemvCall {
   const float* x_colscale = nullptr;
   long long x_colscale_grp_stride = 0;
 };
+
+// Live per-kernel timing (dflash_set_probe): events around the first launch of the chosen kind.
+void probe_begin(dflash_handle* h, int kind, cudaStream_t s) {
+  if (h->probe_start && h->probe_kernel == kind) cudaEventRecord(h->probe_start, s);
+}
+void probe_end(dflash_handle* h, int kind, cudaStream_t s) {
+  if (h->probe_stop && h->probe_kernel == kind) {
+    cudaEventRecord(h->probe_stop, s);
+    h->probe_start = h->probe_stop = nullptr;
+  }
+}
 
 size_t xn_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->r_blk * h->d; }
 size_t xw_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->L * kMaxCtxChunk * h->d; }
@@ -817,8 +829,10 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.x_lo_off = xw_lo(h);
     c1.e.ssq_out = h->ssq_ctx;
     c1.e.ssq_ld = h->ssq_ld;
+    probe_begin(h, DFLASH_PROBE_WC, s);
     int st = tc ? run_tc05_epi(h, c1, wcp, (int)(row - tc_row0), s) : run_gemv(h, c1, s);
     if (st) return st;
+    probe_end(h, DFLASH_PROBE_WC, s);
     // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache; the
     // tensor-core path runs every layer in one grouped launch over the same input rows (the
     // layers' packed Q/K/V matrices and caches are equally spaced; attn_norm_i scales the input)
@@ -858,8 +872,10 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         c2.e.kv_slot[r] = slots[r];
         c2.e.kv_pos[r] = pos[r];
       }
+      probe_begin(h, DFLASH_PROBE_CTX_KV, s);
       st = run_gemv(h, c2, s);
       if (st) return st;
+      probe_end(h, DFLASH_PROBE_CTX_KV, s);
     }
     row += rc;
   }
@@ -989,7 +1005,9 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cq.e.vb = off(h->vb, r0, h->kvd);
       cq.e.qd = h->qd;
       cq.e.kvd = h->kvd;
+      if (i == 0) probe_begin(h, DFLASH_PROBE_QKV, s);
       if ((st = project(cq, r0))) return st;
+      if (i == 0) probe_end(h, DFLASH_PROBE_QKV, s);
     }
     // attention over [windowed context ++ block], no causal mask
     {
@@ -1033,12 +1051,14 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         splits = std::min(splits, std::max(1, (max_tiles + DFL_ATTN_TILES_PER_SPLIT - 1) / DFL_ATTN_TILES_PER_SPLIT));
         splits = std::max(1, std::min(std::min(splits, 64), h->att_pairs_max / pairs));
         aa.n_splits = splits;
+        if (i == 0) probe_begin(h, DFLASH_PROBE_ATTN, s);
         h->launches++;
         if ((st = status_of(launch_attn_tc(aa, h->kmap, h->vmap, s)))) return st;
         if (splits > 1) {
           h->launches++;
           if ((st = status_of(launch_attn_merge(aa, s)))) return st;
         }
+        if (i == 0) probe_end(h, DFLASH_PROBE_ATTN, s);
       }
     }
     if (tc && (st = run_tc05_parts(h, h->wo[i], rows_all, h->attn, h->qd, 0, s, &tp))) return st;
@@ -1060,7 +1080,9 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       co.e.x_lo_off = xn_lo(h);
       co.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       co.e.ssq_ld = h->ssq_ld;
+      if (i == 0) probe_begin(h, DFLASH_PROBE_O, s);
       if ((st = project(co, r0))) return st;
+      if (i == 0) probe_end(h, DFLASH_PROBE_O, s);
     }
     if (tc && (st = run_tc05_parts(h, h->gu[i], rows_all, h->xn, d, lo_if(LO_GU, xn_lo(h)), s, &tp))) return st;
     px = h->xn, pldx = d, plo = lo_if(LO_GU, xn_lo(h));
@@ -1083,7 +1105,9 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cg.e.act = off(h->act, r0, h->I);
       cg.e.inter = h->I;
       cg.e.ffn_act = c.ffn_act;
+      if (i == 0) probe_begin(h, DFLASH_PROBE_GATE_UP, s);
       if ((st = project(cg, r0))) return st;
+      if (i == 0) probe_end(h, DFLASH_PROBE_GATE_UP, s);
     }
     if (tc && (st = run_tc05_parts(h, h->down[i], rows_all, h->act, h->I, 0, s, &tp))) return st;
     px = h->act, pldx = h->I, plo = 0;
@@ -1104,13 +1128,15 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cd.e.x_lo_off = xn_lo(h);
       cd.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       cd.e.ssq_ld = h->ssq_ld;
+      if (i == 0) probe_begin(h, DFLASH_PROBE_DOWN, s);
       if ((st = project(cd, r0))) return st;
+      if (i == 0) probe_end(h, DFLASH_PROBE_DOWN, s);
     }
   }
 
   // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (drafting rows)
   const int lm_req_per_chunk = std::max(1, kMaxRows / n);
-  if (h->probe_start) cudaEventRecord(h->probe_start, s);
+  probe_begin(h, DFLASH_PROBE_LM_HEAD, s);
   // many rows (d == H, no Markov head): the head over every block row once; the epilogue reads
   // the drafting rows through the chunk's row map
   if (tc && (st = run_tc05_parts(h, h->lm, rows_all, h->xn, d, lo_if(LO_LM, xn_lo(h)), s, &tp))) return st;
@@ -1212,8 +1238,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       }
     }
   }
-  if (h->probe_stop) cudaEventRecord(h->probe_stop, s);
-  h->probe_start = h->probe_stop = nullptr;
+  probe_end(h, DFLASH_PROBE_LM_HEAD, s);
   h->stats.rounds++;
   h->stats.blocks += (uint64_t)n_req;
   return DFLASH_OK;
@@ -1286,7 +1311,8 @@ int dflash_get_stats(const dflash_handle* h, dflash_stats* out) {
 }
 
 int dflash_set_probe(dflash_handle* h, int kernel, void* start_event, void* stop_event) {
-  if (!h || kernel != 0) return DFLASH_EINVAL;
+  if (!h || kernel < DFLASH_PROBE_LM_HEAD || kernel > DFLASH_PROBE_CTX_KV) return DFLASH_EINVAL;
+  h->probe_kernel = kernel;
   h->probe_start = static_cast<cudaEvent_t>(start_event);
   h->probe_stop = static_cast<cudaEvent_t>(stop_event);
   return DFLASH_OK;

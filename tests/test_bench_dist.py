@@ -62,6 +62,23 @@ def test_round_flops_c5_hand_count():
     assert abs(f["total"] - sum(v for k, v in f.items() if k != "total")) < 1
 
 
+def test_probe_classes_cover_the_round_bytes():
+    """The live per-kernel roofline classes: the layer classes (x L) add up to the round's layer
+    bytes, the head and W_c to theirs, attention to the window's K/V bytes; the context K/V launch
+    re-streams W_k and W_v of every layer."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    cfg = syn.CONFIGS["c3"]
+    rb = bench.round_bytes(cfg, [4096])
+    cls = {name: (kind, n, b) for name, kind, n, b in bench.probe_classes(cfg, [4096], 8.0)}
+    assert sorted(k for k, _, _ in cls.values()) == list(range(8))
+    layer = sum(n * b for name, (_, n, b) in cls.items() if name in ("qkv", "o", "gate_up", "down"))
+    assert abs(layer - rb["layers"]) < 1 and abs(cls["lm_head"][2] - rb["lm_head"]) < 1
+    assert abs(cls["w_c"][2] - rb["W_c"]) < 1 and abs(cls["attention"][1] * cls["attention"][2] - rb["kv"]) < 1
+    assert abs(cls["ctx_kv"][2] - 5 * 2 * 1024 * 5120 * bench.Q4_BYTES_PER_PARAM) < 1
+
+
 def test_oracle_table_one_core_and_all_cores():
     """The oracle timing table (1 core and all cores per workload) on the tiny fp32 drafter."""
     import bench
