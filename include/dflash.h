@@ -57,6 +57,7 @@ enum dflash_status {
   DFLASH_ECAPACITY = -2,  /* context cache or batch capacity exceeded */
   DFLASH_ECUDA = -3,      /* a CUDA runtime call failed */
   DFLASH_ETIMEOUT = -4,   /* a bounded device-side wait gave up (reported by dflash_check_errors) */
+  DFLASH_EBOUNDS = -5,    /* a device bounds check failed (builds with DFL_DEBUG_CHECKS; see below) */
 };
 
 enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_Q4G64 = 2 };
@@ -210,8 +211,12 @@ int dflash_reset_request(dflash_handle* h, int req_id);
 /* Current context length of a request slot (host mirror), or -1 for a bad slot. */
 int64_t dflash_ctx_len(const dflash_handle* h, int req_id);
 
-/* Synchronise `stream`, then read and clear the device error word. Returns DFLASH_ETIMEOUT if a
- * bounded device wait gave up since the last check, DFLASH_ECUDA on a CUDA error, else DFLASH_OK. */
+/* Synchronise `stream`, then read and clear the device error word. Returns DFLASH_EBOUNDS if a
+ * device bounds check failed since the last check (only libraries compiled with DFL_DEBUG_CHECKS
+ * check: out-of-range anchors, previous Markov tokens and kept-draft counts, which every build
+ * clamps; cache slots and ring positions of context appends, which every build skips when out of
+ * range; and the weight-tile and cache-plane ranges the kernels compute), DFLASH_ETIMEOUT if a
+ * bounded device wait gave up, DFLASH_ECUDA on a CUDA error, else DFLASH_OK. */
 int dflash_check_errors(dflash_handle* h, void* stream);
 
 /* ---- failure-handling test hooks ---------------------------------------------------------------

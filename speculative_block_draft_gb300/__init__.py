@@ -16,6 +16,15 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash.so")
+# Debug build (DFLASH_DEBUG_CHECKS=1 in the environment selects it): the same kernels compiled with
+# device bounds checks that report through dflash_check_errors (DFLASH_EBOUNDS) instead of silently
+# clamping or skipping; a stand-in for a memory checker.
+_BUILD_DEBUG = os.path.join(_HERE, "_build_debug")
+LIB_PATH_DEBUG = os.path.join(_BUILD_DEBUG, "libdflash.so")
+
+
+def _debug_selected() -> bool:
+    return os.environ.get("DFLASH_DEBUG_CHECKS") == "1"
 _SOURCES = ["abi.cu", "gemv_q4.cu", "gemv_bf16.cu", "gemv_f32.cu", "attn.cu", "misc.cu", "noalloc.cu", "gemm_tc05.cu", "tc05_epi.cu",
             "proj_tc05.cu"]
 _HEADERS = ["internal.h", "common.cuh", "gemv_impl.cuh", "gemm_tc05.h", "tc05.cuh"]
@@ -23,6 +32,7 @@ NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,c
               "-Xcompiler", "-fPIC"]
 
 DFLASH_OK, DFLASH_DECLINED, DFLASH_EINVAL, DFLASH_ECAPACITY, DFLASH_ECUDA, DFLASH_ETIMEOUT = 0, 1, -1, -2, -3, -4
+DFLASH_EBOUNDS = -5
 DFLASH_F32, DFLASH_BF16, DFLASH_Q4G64 = 0, 1, 2
 DFLASH_MAX_LAYERS = 8
 DFLASH_MAX_BATCH = 64
@@ -35,18 +45,24 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a (one -gencode) into _build/libdflash.so, in parallel."""
-    os.makedirs(_BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool | None = None) -> str:
+    """Compile csrc/*.cu for sm_103a (one -gencode) into _build/libdflash.so, in parallel; with
+    debug (default: DFLASH_DEBUG_CHECKS=1 in the environment) the bounds-checking build into
+    _build_debug/libdflash.so."""
+    if debug is None:
+        debug = _debug_selected()
+    out_dir, lib_path = (_BUILD_DEBUG, LIB_PATH_DEBUG) if debug else (_BUILD, LIB_PATH)
+    flags = NVCC_FLAGS + (["-DDFL_DEBUG_CHECKS"] if debug else [])
+    os.makedirs(out_dir, exist_ok=True)
     deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS] + [os.path.join(_INCLUDE, "dflash.h")]
     newest = max(os.path.getmtime(p) for p in deps)
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
-        return LIB_PATH
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= newest:
+        return lib_path
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(_BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(_CSRC, src), "-o", obj]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *flags, "-c", os.path.join(_CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -56,12 +72,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(_SOURCES)) as ex:
         objs = list(ex.map(compile_one, _SOURCES))
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = lib_path + f".{os.getpid()}.tmp"
     r = subprocess.run([nvcc, "-shared", "-cudart", "shared", *objs, "-o", tmp], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 # ---------------------------------------------------------------------------------------------
@@ -119,9 +135,10 @@ def lib():
     """Load libdflash.so (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libdflash.so is not built ({LIB_PATH}); run speculative_block_draft_gb300.build()")
-        L = ctypes.CDLL(LIB_PATH)
+        path = LIB_PATH_DEBUG if _debug_selected() else LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"libdflash.so is not built ({path}); run speculative_block_draft_gb300.build()")
+        L = ctypes.CDLL(path)
         vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         P = ctypes.POINTER
         L.dflash_workspace_bytes.restype = ctypes.c_size_t

@@ -942,6 +942,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   ba.ssq_ld = h->ssq_ld;
   ba.xn_lo_off = xn_lo(h);
   ba.emb_out = h->emb;
+  ba.err = h->err;
   if (d != h->H) {
     h->launches++;
     if ((st = status_of(launch_embed_gather(ba, s)))) return st;
@@ -1213,7 +1214,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         if ((st = status_of(launch_markov_gather(nb, k, n, r, h->V, h->fmt, h->mk_w1.data,
                                                  static_cast<const uint16_t*>(h->mk_w1.scale),
                                                  static_cast<const uint16_t*>(h->mk_w1.bias), anchor + b0,
-                                                 draft + (size_t)b0 * n, h->mk_x, lo_off, s))))
+                                                 draft + (size_t)b0 * n, h->mk_x, lo_off, h->err, s))))
           return st;
         GemvCall cm;
         cm.m = &h->mk;
@@ -1251,7 +1252,7 @@ int dflash_accept(dflash_handle* h, int n_req, const int32_t* draft, const int32
   if (!draft || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->nd, draft, nullptr, target, accept_len, next_anchor, h->acc_hist,
+  return status_of(launch_accept(n_req, h->nd, draft, nullptr, target, accept_len, next_anchor, h->acc_hist, h->err,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -1272,7 +1273,7 @@ int dflash_accept_kept(dflash_handle* h, int n_req, const int32_t* draft, const 
   if (!draft || !keep || !target || !accept_len || !next_anchor) return DFLASH_EINVAL;
   h->launches++;
   h->stats.accept_calls++;
-  return status_of(launch_accept(n_req, h->nd, draft, keep, target, accept_len, next_anchor, h->acc_hist,
+  return status_of(launch_accept(n_req, h->nd, draft, keep, target, accept_len, next_anchor, h->acc_hist, h->err,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -1293,13 +1294,14 @@ int dflash_check_errors(dflash_handle* h, void* stream) {
   unsigned word = 0;
   if (cudaMemcpy(&word, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DFLASH_ECUDA;
   if (word) {
-    // a kernel gave up part-way: clear the error word and the arrival counters it may have left
+    // a kernel gave up part-way (or, in a debug build, a bounds check failed): clear the error word
+    // and the arrival counters it may have left
     const unsigned zero = 0;
     if (cudaMemcpy(h->err, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(h->tickets, 0, (size_t)h->ticket_count * 4) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return DFLASH_ECUDA;
-    return DFLASH_ETIMEOUT;
+    return (word & kErrBounds) ? DFLASH_EBOUNDS : DFLASH_ETIMEOUT;
   }
   return DFLASH_OK;
 }
@@ -1412,6 +1414,7 @@ const char* dflash_status_str(int s) {
     case DFLASH_ECAPACITY: return "capacity exceeded";
     case DFLASH_ECUDA: return "CUDA error";
     case DFLASH_ETIMEOUT: return "a bounded device wait timed out";
+    case DFLASH_EBOUNDS: return "a device bounds check failed (debug build)";
     default: return "unknown status";
   }
 }

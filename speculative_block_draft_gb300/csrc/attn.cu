@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
   const int tb = (int)((long long)split * T / a.n_splits), te = (int)((long long)(split + 1) * T / a.n_splits);
   const int n_tiles = te - tb;
   const bool with_block = split == a.n_splits - 1;
+  in_bounds(rq.slot >= 0 && rq.slot < a.max_batch && s_lo + len1 <= a.cap, threadIdx.x == 0 ? a.err : nullptr);
   const int plane = a.plane0 + rq.slot * a.hkv + kvh;
 
   auto tile_info = [&](int ti, int& slot0, int& nvalid) {

@@ -72,6 +72,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Device bounds checks of debug builds (compiled with -DDFL_DEBUG_CHECKS): in_bounds(cond, err)
+// returns cond, and a false cond also sets kErrBounds in the error word, which dflash_check_errors
+// reports as DFLASH_EBOUNDS. Release builds compile the report away and keep only the caller's own
+// guard (a clamp or a skipped access), so both builds compute the same results on valid inputs.
+__device__ __forceinline__ bool in_bounds(bool cond, unsigned* err) {
+#ifdef DFL_DEBUG_CHECKS
+  if (!cond && err) atomicOr(err, kErrBounds);
+#else
+  (void)err;
+#endif
+  return cond;
+}
+
 // 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(

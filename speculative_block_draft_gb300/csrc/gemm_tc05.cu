@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
                                                          kErrTimeoutTc05));
         if (!ok) break;
         if (lane == 0) {
+          in_bounds(mt < a.mtiles && g < a.groups && strips_in_tile > 0, a.err);
           const uint32_t fw = smem_u32(&full_w[sw]);
           mbar_arrive_expect_tx(fw, (uint32_t)(strips_in_tile * kQ4GroupBytes));
           for (int s = 0; s < strips_in_tile; s++)

@@ -210,6 +210,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             const float v = h ? yb : ya;
             const int half = nr >= e.kvd;
             const int f = nr - half * e.kvd;
+            if (!in_bounds(e.kv_slot[c] >= 0 && e.kv_pos[c] >= 0 && e.kv_pos[c] < e.cap, a.err)) continue;
             const size_t idx =
                 (((size_t)e.kv_slot[c] * e.n_kv + f / e.hd) * e.cap + e.kv_pos[c]) * e.hd + f % e.hd;
             store_act<XT>(static_cast<uint8_t*>(half ? e.vc : e.kc) + (size_t)lyr * e.kv_grp_stride, idx, v);
@@ -449,6 +450,7 @@ __global__ void __launch_bounds__(gemv_warps(NT) * 32, 1) gemv_tc_kernel(const _
   int issued = 0;
   auto issue_next = [&]() {
     const int gn = (int)min((long long)min(GS, ng - i_goff), t1 - i_tile);
+    in_bounds(sbeg + i_strip < a.n_strips && gbeg + i_goff + gn <= a.groups && gn > 0, lane == 0 ? a.err : nullptr);
     const uint8_t* src = Wb + ((size_t)(a.strip0 + sbeg + i_strip) * a.groups + gbeg + i_goff) * GB;
     const int slot = warp * kStages + issued % kStages;
     if (lane == 0) {

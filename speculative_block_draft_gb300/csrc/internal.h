@@ -61,6 +61,7 @@ enum NormMode { NORM_NONE = 0, NORM_ONE = 1, NORM_CTX = 2 };
 // Device error word bits.
 constexpr unsigned kErrTimeoutGemv = 1u;
 constexpr unsigned kErrTimeoutAttn = 2u;
+constexpr unsigned kErrBounds = 16u;   // a device bounds check failed (builds with DFL_DEBUG_CHECKS)
 
 struct RowMap {      // activation row r of a launch reads source row (r/per)*stride + off + r%per
   int per, stride, off;
@@ -162,6 +163,7 @@ struct BlockArgs {
   float* h; void* xn; float* ssq; int ssq_ld;
   size_t xn_lo_off;           // f16 remainder of xn at this element offset (0: none)
   void* emb_out;              // gather mode: [n_req][H] activation rows
+  unsigned* err;              // device error word (bounds checks of debug builds)
 };
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the current device (the
@@ -222,7 +224,7 @@ cudaError_t launch_lm_reduce(const float* parts, int n_parts, int rows, int32_t*
 // k == 0, else draft[b * n + k - 1].
 cudaError_t launch_markov_gather(int n_req, int k, int n, int rank, int vocab, int fmt, const void* w1,
                                  const uint16_t* w1_scale, const uint16_t* w1_bias, const int32_t* anchor,
-                                 const int32_t* draft, void* x, size_t lo_off, cudaStream_t s);
+                                 const int32_t* draft, void* x, size_t lo_off, unsigned* err, cudaStream_t s);
 size_t gemv_smem_bytes(int fmt, int R, int gps, int x_lo, int lm, int cpart_cap);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            cudaStream_t s);
@@ -233,7 +235,8 @@ cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
 cudaError_t launch_block_init(const BlockArgs& a, cudaStream_t s);
 cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s);
 cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, cudaStream_t s);
+                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, unsigned* err,
+                          cudaStream_t s);
 cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
                                  int32_t* keep, cudaStream_t s);
 

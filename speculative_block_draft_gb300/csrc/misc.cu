@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(256) block_init_kernel(const __grid_constant__
   pdl_wait();
   if (k == 0) {
     int tok = a.anchor[b];
-    tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);  // clamped: no read outside the table
+    if (!in_bounds(tok >= 0 && tok < a.vocab, threadIdx.x == 0 && chunk == 0 ? a.err : nullptr))
+      tok = tok < 0 ? 0 : a.vocab - 1;   // clamped: no read outside the table
 #pragma unroll
     for (int u = 0; u < kPer; u++) {
       const int j = j0 + u * 256;
@@ -156,7 +157,8 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant
   pdl_launch_dependents();
   pdl_wait();
   int tok = a.anchor[b];
-  tok = tok < 0 ? 0 : (tok >= a.vocab ? a.vocab - 1 : tok);
+  if (!in_bounds(tok >= 0 && tok < a.vocab, threadIdx.x == 0 ? a.err : nullptr))
+    tok = tok < 0 ? 0 : a.vocab - 1;   // clamped: no read outside the table
   for (int j = threadIdx.x; j < a.H; j += blockDim.x)
     static_cast<XT*>(a.emb_out)[(size_t)b * a.H + j] =
         from_f<XT>(load_weight(a.fmt, a.emb, a.emb_scale, a.emb_bias, a.H, tok, j));
@@ -166,11 +168,16 @@ __global__ void __launch_bounds__(256) embed_gather_kernel(const __grid_constant
 // keep (nullable): per request, only the first keep[b] drafts are verified (pruned blocks).
 // hist (nullable): hist[a] counts the blocks whose accepted length is a (0 <= a <= n).
 __global__ void accept_kernel(int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                              int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist) {
+                              int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, unsigned* err) {
   const int b = blockIdx.x, lane = threadIdx.x;
   pdl_launch_dependents();
   pdl_wait();
-  const int cap = keep ? min(max(keep[b], 0), n) : n;   // clamped: no read outside target's row
+  int cap = n;
+  if (keep) {
+    cap = keep[b];
+    if (!in_bounds(cap >= 0 && cap <= n, lane == 0 ? err : nullptr))
+      cap = cap < 0 ? 0 : n;   // clamped: no read outside target's row
+  }
   const bool miss = lane < cap && draft[(size_t)b * n + lane] != target[(size_t)b * (n + 1) + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
   const int acc = mask ? __ffs(mask) - 1 : cap;
@@ -203,12 +210,14 @@ template <typename XT>
 __global__ void __launch_bounds__(256) markov_gather_kernel(int k, int n, int rank, int vocab, int fmt,
                                                             const void* w1, const uint16_t* w1_scale,
                                                             const uint16_t* w1_bias, const int32_t* anchor,
-                                                            const int32_t* draft, XT* x, size_t lo_off) {
+                                                            const int32_t* draft, XT* x, size_t lo_off,
+                                                            unsigned* err) {
   const int b = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();
   int prev = k == 0 ? anchor[b] : draft[(size_t)b * n + k - 1];
-  prev = prev < 0 ? 0 : (prev >= vocab ? vocab - 1 : prev);   // clamped: no read outside the table
+  if (!in_bounds(prev >= 0 && prev < vocab, threadIdx.x == 0 ? err : nullptr))
+    prev = prev < 0 ? 0 : vocab - 1;   // clamped: no read outside the table
   for (int i = threadIdx.x; i < rank; i += blockDim.x)
     store_act_split<XT>(x, (size_t)b * rank + i, lo_off, load_weight(fmt, w1, w1_scale, w1_bias, rank, prev, i));
 }
@@ -217,12 +226,12 @@ __global__ void __launch_bounds__(256) markov_gather_kernel(int k, int n, int ra
 
 cudaError_t launch_markov_gather(int n_req, int k, int n, int rank, int vocab, int fmt, const void* w1,
                                  const uint16_t* w1_scale, const uint16_t* w1_bias, const int32_t* anchor,
-                                 const int32_t* draft, void* x, size_t lo_off, cudaStream_t s) {
+                                 const int32_t* draft, void* x, size_t lo_off, unsigned* err, cudaStream_t s) {
   if (fmt == FMT_F32)   // the CUDA-core path keeps fp32 activations
     return launch_pdl(markov_gather_kernel<float>, dim3(n_req), dim3(256), 0, s, k, n, rank, vocab, fmt, w1,
-                      w1_scale, w1_bias, anchor, draft, static_cast<float*>(x), (size_t)0);
+                      w1_scale, w1_bias, anchor, draft, static_cast<float*>(x), (size_t)0, err);
   return launch_pdl(markov_gather_kernel<__half>, dim3(n_req), dim3(256), 0, s, k, n, rank, vocab, fmt, w1,
-                    w1_scale, w1_bias, anchor, draft, static_cast<__half*>(x), lo_off);
+                    w1_scale, w1_bias, anchor, draft, static_cast<__half*>(x), lo_off, err);
 }
 
 cudaError_t launch_draft_lengths(int n_req, int n, const float* conf, const float* thresholds, float min_conf,
@@ -247,9 +256,10 @@ cudaError_t launch_embed_gather(const BlockArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_accept(int n_req, int n, const int32_t* draft, const int32_t* keep, const int32_t* target,
-                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, cudaStream_t s) {
+                          int32_t* accept_len, int32_t* next_anchor, unsigned long long* hist, unsigned* err,
+                          cudaStream_t s) {
   return launch_pdl(accept_kernel, dim3(n_req), dim3(32), 0, s, n, draft, keep, target, accept_len, next_anchor,
-                    hist);
+                    hist, err);
 }
 
 }  // namespace dfl

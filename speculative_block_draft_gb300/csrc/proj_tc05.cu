@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kPjThreads, 1) proj_tc05_kernel(const __grid_c
       int nw = 0;   // stages whose copies were issued
       auto weights = [&](const StageWalk& st, int sw) {
         if (lane != 0) return;
+        in_bounds(st.mt < pa.mtiles && st.g + st.n <= pa.groups && st.n > 0, a.err);
         const int strips = min(kPjStrips, pa.n_strips - st.mt * kPjStrips);
         const uint32_t fw = smem_u32(&full_w[sw]);
         mbar_arrive_expect_tx(fw, (uint32_t)(strips * st.n * kQ4GroupBytes + st.n * pa.x_stage));

@@ -75,3 +75,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.dflash_debug_stall(None, 0) == pkg.DFLASH_EINVAL
     assert lib.dflash_accept_histogram(None, None, 1, None) == pkg.DFLASH_EINVAL
     assert b"declined" in lib.dflash_status_str(pkg.DFLASH_DECLINED)
+
+
+def test_debug_build_exports_the_same_symbols():
+    """The bounds-checking build compiles for sm_103a and exports every declared entry point."""
+    path = pkg.build(debug=True)
+    assert path == pkg.LIB_PATH_DEBUG
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    assert set(declared()) <= set(re.findall(r" T (dflash_\w+)", out))
