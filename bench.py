@@ -275,6 +275,51 @@ def set_oracle_threads(n: int):
     gomp.omp_set_num_threads(int(n))
 
 
+def rows_matmul_bench(which: str, rows_list, iters: int = 5) -> dict:
+    """Time dflash_rows_matmul (the many-row tcgen05 contraction) on one stored matrix of the
+    4-bit 5120-wide drafter (a one-layer drafter with the full head, so the model stays small):
+    per row count, the call's time (contraction + slice reduction) and its algorithmic rates."""
+    import torch
+
+    import speculative_block_draft_gb300 as pkg
+    from speculative_block_draft_gb300.session import Session
+    pkg.build()
+    c3 = syn.CONFIGS["c3"]
+    cfg = syn.with_overrides(c3, name="rows_matmul_l1", n_layers=1, window=0, ctx_len=16)
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    shapes = {"lm": (pkg.DFLASH_MAT_LM, cfg.vocab, cfg.target_hidden), "ctx": (pkg.DFLASH_MAT_CTX, cfg.d, cfg.n_taps * cfg.target_hidden),
+              "qkv": (pkg.DFLASH_MAT_QKV, qd + 2 * kvd, cfg.d), "o": (pkg.DFLASH_MAT_O, cfg.d, qd),
+              "gateup": (pkg.DFLASH_MAT_GATEUP, 2 * cfg.inter, cfg.d), "down": (pkg.DFLASH_MAT_DOWN, cfg.d, cfg.inter)}
+    mat, n_out, k = shapes[which]
+    s = Session(syn.make_model(cfg), max_batch=1, ctx_capacity=64)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    peaks = load_peaks()
+    out = []
+    for rows in rows_list:
+        plan = pkg.rows_matmul_plan(n_out, k, rows, 0, nsm)
+        sc = torch.empty(plan.scratch_bytes + 256, dtype=torch.uint8, device="cuda")
+        sc = sc[(256 - sc.data_ptr() % 256) % 256:]
+        x = torch.randn(rows, k, device="cuda").half().view(torch.int16)
+        y = torch.empty(rows, n_out, dtype=torch.float32, device="cuda")
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ms = []
+        for _ in range(iters):
+            ev[0].record()
+            s.h.rows_matmul(mat, 0, x, y, sc)
+            ev[1].record()
+            torch.cuda.synchronize()
+            ms.append(ev[0].elapsed_time(ev[1]))
+        t = float(np.median(ms)) / 1e3
+        wbytes = n_out * k * Q4_BYTES_PER_PARAM
+        out.append({"rows": rows, "us": 1e6 * t, "grid": plan.grid, "k_slices": plan.k_slices,
+                    "weights_gbs": wbytes / t / 1e9, "hbm_frac": wbytes / t / 1e9 / peaks["hbm_gbs"],
+                    "tflops": 2 * rows * n_out * k / t / 1e12,
+                    "tensor_frac": 2 * rows * n_out * k / t / 1e12 / peaks["bf16_tflops_sustained"]})
+    assert s.check() == 0
+    s.close()
+    return {"rows_matmul": which, "shape": [n_out, k], "results": out}
+
+
 def oracle_table(names=("c1", "c2", "c3", "c5")):
     """Oracle blocks/s for one round on 1 core and on all cores, per workload. A round of a
     batched workload is its requests' rounds in sequence (requests are independent, and with the
@@ -367,6 +412,9 @@ def main():
                     help="comma-separated workloads: print the oracle's 1-core / all-core round times and exit")
     ap.add_argument("--large-batch-tc05", action="store_true",
                     help="library option: draft calls of more than 32 block rows on the tcgen05 contraction")
+    ap.add_argument("--rows-matmul", default="", choices=["", "lm", "ctx", "qkv", "o", "gateup", "down"],
+                    help="time dflash_rows_matmul on one matrix of the 4-bit drafter instead of the round")
+    ap.add_argument("--rows", default="16,32,64,160", help="activation row counts for --rows-matmul")
     ap.add_argument("--probe-rounds", type=int, default=5,
                     help="rounds per kernel class timed live after the timed region (one launch each)")
     ap.add_argument("--skinny-tc05", action="store_true",
@@ -376,6 +424,10 @@ def main():
     args = ap.parse_args()
     if args.oracle_table:
         print(json.dumps(oracle_table(tuple(args.oracle_table.split(",")))), flush=True)
+        return 0
+    if args.rows_matmul:
+        print(json.dumps(rows_matmul_bench(args.rows_matmul, [int(v) for v in args.rows.split(",")], args.steps)),
+              flush=True)
         return 0
     cfg = syn.CONFIGS[args.config]
     if args.markov_rank:
