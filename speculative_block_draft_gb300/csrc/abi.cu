@@ -288,7 +288,12 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->lm_grid_max = lmg;
   h->partials = cv.take<float>(std::max<size_t>(pf, 4) * 4);
   h->tickets = cv.take<int>((size_t)tk * 4);
-  h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4);
+  // vocab states per CTA and row; a many-row draft call on the tcgen05 contraction keeps one slice
+  // per row chunk
+  const bool tc_possible = c.large_batch_tc05 && h->fmt == FMT_Q4 && !h->act_f32 && h->d == h->H && !c.markov_rank &&
+                           std::min(c.max_batch * h->G, kTcMaxRows) > kMaxRows;
+  const int lm_slices = tc_possible ? kTcMaxChunks : 1;
+  h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4 * lm_slices);
   h->lm_strip = cv.take<float>((size_t)tk * kMaxRows * 3 * 4);
   // attention split partials: n_req * Hkv * splits stays below ~2 waves of CTAs (see draft)
   h->att_pairs_max = std::max(4 * h->n_sm, c.max_batch * c.n_kv_heads);
@@ -299,8 +304,7 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   // the tcgen05 contraction's scratch: the largest plan over the block projections and the head
   h->tc05_on = 0;
   h->tc05_rows = std::min(c.max_batch * h->G, kTcMaxRows);
-  if (c.large_batch_tc05 && h->fmt == FMT_Q4 && !h->act_f32 && h->d == h->H && !c.markov_rank &&
-      h->tc05_rows > kMaxRows) {
+  if (tc_possible) {
     size_t sc = 0;
     auto need = [&](const PackedMat& m, int lo) {
       const Tc05Plan p = plan_tc05(m.n_strips, m.groups, h->tc05_rows, lo, h->n_sm);
@@ -553,12 +557,10 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   return status_of(launch_tc05_parts(a, p, s));
 }
 
-// The epilogue of one chunk of a projection (described as for run_gemv) from the contraction's
-// partial tiles; the chunk's row c is contraction row row_base + map_row(c.xmap, c).
-int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row_base, cudaStream_t s,
-                 int* grid_out = nullptr) {
+// The epilogue arguments of one row chunk of a projection (described as for run_gemv) on the
+// contraction's partial tiles; an LM-head chunk's vocab states go to its own slice of lm_part.
+GemvArgs tc05_epi_args(dflash_handle* h, const GemvCall& c, int chunk, int grid) {
   const PackedMat& m = *c.m;
-  if (c.R <= 0) return DFLASH_OK;
   GemvArgs a{};
   a.w = m.w;
   a.strip0 = 0;
@@ -579,16 +581,43 @@ int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row
   a.err = h->err;
   a.e = c.e;
   if (c.epi == EPI_LMHEAD) {
-    a.e.lm_part = h->lm_part;
+    a.e.lm_part = h->lm_part + (size_t)chunk * grid * kMaxRows * 3;
     a.e.lm_strip = h->lm_strip;
   }
-  int grid = (m.n_strips + kF32Warps - 1) / kF32Warps;
-  grid = std::max(1, std::min(grid, c.epi == EPI_LMHEAD ? h->lm_grid_max : 4 * h->n_sm));
+  return a;
+}
+
+int tc05_epi_grid(const dflash_handle* h, const GemvCall& c) {
+  const int grid = (c.m->n_strips + kF32Warps - 1) / kF32Warps;
+  return std::max(1, std::min(grid, c.epi == EPI_LMHEAD ? h->lm_grid_max : 4 * h->n_sm));
+}
+
+// The epilogues of n row chunks of one projection from the contraction's partial tiles, one launch;
+// chunk j's row c is contraction row r0[j] + map_row(calls[j].xmap, c).
+int run_tc05_epi_chunks(dflash_handle* h, const GemvCall* calls, const int* r0, int n, const Tc05Plan& p,
+                        cudaStream_t s, int* grid_out = nullptr) {
+  if (n <= 0) return DFLASH_OK;
+  if (n > kTcMaxChunks) return DFLASH_EINVAL;
+  static thread_local Tc05EpiChunks ch;   // ~6 KB of launch arguments
+  const int grid = tc05_epi_grid(h, calls[0]);
+  int nt = 1;
+  for (int j = 0; j < n; j++) {
+    ch.a[j] = tc05_epi_args(h, calls[j], j, grid);
+    ch.row_base[j] = r0[j];
+    nt = std::max(nt, nt_for(calls[j].R));
+  }
+  ch.n = n;
   if (grid_out) *grid_out = grid;
   h->launches++;
-  return status_of(launch_tc05_epilogue(c.epi, nt_for(c.R), a,
+  return status_of(launch_tc05_epilogue(calls[0].epi, nt, ch,
                                         reinterpret_cast<const float*>(h->tc05_scratch + p.part_off), p.slices,
-                                        p.npad, p.mtiles * 128, row_base, grid, s));
+                                        p.npad, p.mtiles * 128, grid, s));
+}
+
+// The epilogue of one chunk of a projection (the context projection's chunks).
+int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row_base, cudaStream_t s) {
+  if (c.R <= 0) return DFLASH_OK;
+  return run_tc05_epi_chunks(h, &c, &row_base, 1, p, s);
 }
 
 // One projection of a draft call of at most kProjMaxRows block rows on the tcgen05 projection
@@ -977,13 +1006,26 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   const void* px = nullptr;   // the projection's input rows and remainder offset (pj)
   int pldx = 0;
   long long plo = 0;
+  // tcgen05 contraction: a projection's row chunks are collected and get one epilogue launch
+  GemvCall tc_calls[kTcMaxChunks];
+  int tc_r0[kTcMaxChunks], tc_n = 0;
   auto project = [&](GemvCall& c, int r0) {
     if (pj) return run_proj(h, c, rows_all, px, pldx, plo, r0, s);
-    return tc ? run_tc05_epi(h, c, tp, r0, s) : run_gemv(h, c, s);
+    if (!tc) return run_gemv(h, c, s);
+    if (tc_n == kTcMaxChunks) return (int)DFLASH_EINVAL;
+    tc_calls[tc_n] = c;
+    tc_r0[tc_n++] = r0;
+    return (int)DFLASH_OK;
+  };
+  auto flush = [&](int* grid_out = nullptr) {
+    const int n_chunks = tc_n;
+    tc_n = 0;
+    return tc ? run_tc05_epi_chunks(h, tc_calls, tc_r0, n_chunks, tp, s, grid_out) : (int)DFLASH_OK;
   };
   for (int i = 0; i < h->L; i++) {
     const int in_parts = i == 0 ? (d + kBlockCols - 1) / kBlockCols : parts;
     // Q, K_d, V_d of RMSNorm_attn_i(H_d)
+    if (i == 0) probe_begin(h, DFLASH_PROBE_QKV, s);
     if (tc && (st = run_tc05_parts(h, h->qkv[i], rows_all, h->xn, d, lo_if(LO_QKV, xn_lo(h)), s, &tp))) return st;
     px = h->xn, pldx = d, plo = lo_if(LO_QKV, xn_lo(h));
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
@@ -1006,10 +1048,10 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cq.e.vb = off(h->vb, r0, h->kvd);
       cq.e.qd = h->qd;
       cq.e.kvd = h->kvd;
-      if (i == 0) probe_begin(h, DFLASH_PROBE_QKV, s);
       if ((st = project(cq, r0))) return st;
-      if (i == 0) probe_end(h, DFLASH_PROBE_QKV, s);
     }
+    if ((st = flush())) return st;
+    if (i == 0) probe_end(h, DFLASH_PROBE_QKV, s);
     // attention over [windowed context ++ block], no causal mask
     {
       AttnArgs aa{};
@@ -1062,6 +1104,7 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         if (i == 0) probe_end(h, DFLASH_PROBE_ATTN, s);
       }
     }
+    if (i == 0) probe_begin(h, DFLASH_PROBE_O, s);
     if (tc && (st = run_tc05_parts(h, h->wo[i], rows_all, h->attn, h->qd, 0, s, &tp))) return st;
     px = h->attn, pldx = h->qd, plo = 0;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
@@ -1081,10 +1124,11 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       co.e.x_lo_off = xn_lo(h);
       co.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       co.e.ssq_ld = h->ssq_ld;
-      if (i == 0) probe_begin(h, DFLASH_PROBE_O, s);
       if ((st = project(co, r0))) return st;
-      if (i == 0) probe_end(h, DFLASH_PROBE_O, s);
     }
+    if ((st = flush())) return st;
+    if (i == 0) probe_end(h, DFLASH_PROBE_O, s);
+    if (i == 0) probe_begin(h, DFLASH_PROBE_GATE_UP, s);
     if (tc && (st = run_tc05_parts(h, h->gu[i], rows_all, h->xn, d, lo_if(LO_GU, xn_lo(h)), s, &tp))) return st;
     px = h->xn, pldx = d, plo = lo_if(LO_GU, xn_lo(h));
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
@@ -1106,10 +1150,11 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cg.e.act = off(h->act, r0, h->I);
       cg.e.inter = h->I;
       cg.e.ffn_act = c.ffn_act;
-      if (i == 0) probe_begin(h, DFLASH_PROBE_GATE_UP, s);
       if ((st = project(cg, r0))) return st;
-      if (i == 0) probe_end(h, DFLASH_PROBE_GATE_UP, s);
     }
+    if ((st = flush())) return st;
+    if (i == 0) probe_end(h, DFLASH_PROBE_GATE_UP, s);
+    if (i == 0) probe_begin(h, DFLASH_PROBE_DOWN, s);
     if (tc && (st = run_tc05_parts(h, h->down[i], rows_all, h->act, h->I, 0, s, &tp))) return st;
     px = h->act, pldx = h->I, plo = 0;
     for (int b0 = 0; b0 < n_req; b0 += req_per_chunk) {
@@ -1129,10 +1174,10 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       cd.e.x_lo_off = xn_lo(h);
       cd.e.ssq_out = h->ssq + (size_t)r0 * h->ssq_ld;
       cd.e.ssq_ld = h->ssq_ld;
-      if (i == 0) probe_begin(h, DFLASH_PROBE_DOWN, s);
       if ((st = project(cd, r0))) return st;
-      if (i == 0) probe_end(h, DFLASH_PROBE_DOWN, s);
     }
+    if ((st = flush())) return st;
+    if (i == 0) probe_end(h, DFLASH_PROBE_DOWN, s);
   }
 
   // out_norm (+ out_proj), borrowed LM head, greedy token and softmax confidence (drafting rows)
@@ -1184,22 +1229,36 @@ int dflash_draft_block(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     const bool markov = c.markov_rank > 0;
     cl.e.logits = markov ? h->mk_base + (size_t)l0 * h->V : (logits ? logits + (size_t)l0 * h->V : nullptr);
     cl.e.vocab = h->V;
+    if (tc) {   // collected: one epilogue launch for every chunk, then one vocab merge per chunk
+      if ((st = project(cl, r0))) return st;
+      continue;
+    }
     GemvPlan lp{};
-    int epi_grid = 0;
     const bool pj_lm = pj && d == h->H;
     if (pj_lm) {
       if ((st = run_proj(h, cl, rows_all, h->xn, d, lo_if(LO_LM, xn_lo(h)), r0, s))) return st;
-    } else if ((st = tc ? run_tc05_epi(h, cl, tp, r0, s, &epi_grid) : run_gemv(h, cl, s, &lp))) {
+    } else if ((st = run_gemv(h, cl, s, &lp))) {
       return st;
     }
     if (markov) continue;
     // merge the per-CTA (one K slice) or per-strip (K split, projection kernel) vocab states
-    const bool split = pj_lm || (!tc && h->fmt != FMT_F32 && lp.n_slices > 1);
+    const bool split = pj_lm || (h->fmt != FMT_F32 && lp.n_slices > 1);
     h->launches++;
-    if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part,
-                                         split ? h->lm.n_strips : (tc ? epi_grid : lp.grid), R, draft + l0,
-                                         conf ? conf + l0 : nullptr, 1, s))))
+    if ((st = status_of(launch_lm_reduce(split ? h->lm_strip : h->lm_part, split ? h->lm.n_strips : lp.grid, R,
+                                         draft + l0, conf ? conf + l0 : nullptr, 1, s))))
       return st;
+  }
+  if (tc) {
+    const int n_chunks = tc_n;
+    int epi_grid = 0;
+    if ((st = flush(&epi_grid))) return st;
+    for (int j = 0; j < n_chunks && !c.markov_rank; j++) {
+      const int l0 = (tc_r0[j] / G) * n;
+      h->launches++;
+      if ((st = status_of(launch_lm_reduce(h->lm_part + (size_t)j * epi_grid * kMaxRows * 3, epi_grid,
+                                           tc_calls[j].R, draft + l0, conf ? conf + l0 : nullptr, 1, s))))
+        return st;
+    }
   }
   if (c.markov_rank) {
     // Markov sequential head (Eq 5 of the dflash.ts page): draft k = argmax(base_k + W1[prev_k] W2),

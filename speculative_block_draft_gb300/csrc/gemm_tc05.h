@@ -45,11 +45,19 @@ cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_ou
 cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cudaStream_t s);
 
 // A draft-round projection's epilogue (EPI_CTX, EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
-// partial tiles, through the skinny GEMV's strip epilogues: `a` describes the launch as for the
-// GEMV (a.R <= kMaxRows rows, nt = n-tiles of 8) with a.n_slices == 1; its row c is contraction
-// row row_base + map_row(a.xmap, c). LM head: one vocab state per CTA and row in a.e.lm_part.
-cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
-                                 int n_out_pad, int row_base, int grid, cudaStream_t s);
+// partial tiles, through the skinny GEMV's strip epilogues, for up to kTcMaxChunks row chunks in
+// one launch (grid.y = chunk): ch.a[j] describes chunk j as for the GEMV (a.R <= kMaxRows rows,
+// nt = n-tiles of 8 for the largest chunk) with a.n_slices == 1; its row c is contraction row
+// ch.row_base[j] + map_row(ch.a[j].xmap, c). LM head: one vocab state per CTA and row in each
+// chunk's a.e.lm_part.
+constexpr int kTcMaxChunks = 8;   // ceil(160 / (gamma * floor(32 / gamma))) for gamma in 2..16
+struct Tc05EpiChunks {
+  GemvArgs a[kTcMaxChunks];
+  int row_base[kTcMaxChunks];
+  int n;
+};
+cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
+                                 int n_out_pad, int grid, cudaStream_t s);
 
 // ---- skinny projections of the draft round on tcgen05 (proj_tc05.cu) ---------------------------
 constexpr unsigned kErrTimeoutProj = 8u;  // device error word bit of its bounded waits

@@ -2,7 +2,8 @@
 // slices' partial tiles are summed in slice order and handed, one 16-row strip per warp, to the
 // same strip epilogues the skinny GEMV fuses: context rows x ctx_norm with sums of squares,
 // row-norm scale, Q/K/V split, residual with next norm input and sums of squares, gated FFN, and
-// vocab states. Row c of a launch is contraction row row_base + map_row(xmap, c).
+// vocab states. One launch covers every row chunk of a projection (grid.y = chunk); row c of
+// chunk j is contraction row row_base[j] + map_row(xmap_j, c).
 #include "gemm_tc05.h"
 #include "gemv_impl.cuh"
 
@@ -12,9 +13,11 @@ namespace {
 
 template <int NT, int EPI>
 __global__ void __launch_bounds__(kF32Warps * 32)
-    tc05_epi_kernel(const __grid_constant__ GemvArgs a, const float* __restrict__ part, int slices, int npad,
-                    int n_out_pad, int row_base) {
+    tc05_epi_kernel(const __grid_constant__ Tc05EpiChunks ch, const float* __restrict__ part, int slices, int npad,
+                    int n_out_pad) {
   constexpr int RP = NT * 8;
+  const GemvArgs& a = ch.a[blockIdx.y];   // this CTA's row chunk
+  const int row_base = ch.row_base[blockIdx.y];
   __shared__ float srow[kMaxRows];
   __shared__ LmState sm_lm[kF32Warps * kMaxRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -53,13 +56,14 @@ __global__ void __launch_bounds__(kF32Warps * 32)
 }
 
 template <int EPI>
-cudaError_t launch_epi(int nt, const GemvArgs& a, const float* part, int slices, int npad, int n_out_pad,
-                       int row_base, int grid, cudaStream_t s) {
+cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad, int n_out_pad,
+                       int grid, cudaStream_t s) {
+  const dim3 g(grid, ch.n);
   switch (nt) {
-    case 1: tc05_epi_kernel<1, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
-    case 2: tc05_epi_kernel<2, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
-    case 3: tc05_epi_kernel<3, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
-    case 4: tc05_epi_kernel<4, EPI><<<grid, kF32Warps * 32, 0, s>>>(a, part, slices, npad, n_out_pad, row_base); break;
+    case 1: tc05_epi_kernel<1, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
+    case 2: tc05_epi_kernel<2, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
+    case 3: tc05_epi_kernel<3, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
+    case 4: tc05_epi_kernel<4, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -67,14 +71,15 @@ cudaError_t launch_epi(int nt, const GemvArgs& a, const float* part, int slices,
 
 }  // namespace
 
-cudaError_t launch_tc05_epilogue(int epi, int nt, const GemvArgs& a, const float* part, int slices, int npad,
-                                 int n_out_pad, int row_base, int grid, cudaStream_t s) {
+cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
+                                 int n_out_pad, int grid, cudaStream_t s) {
+  if (ch.n < 1 || ch.n > kTcMaxChunks) return cudaErrorInvalidValue;
   switch (epi) {
-    case EPI_CTX: return launch_epi<EPI_CTX>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
-    case EPI_QKV: return launch_epi<EPI_QKV>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
-    case EPI_RESID: return launch_epi<EPI_RESID>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
-    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, a, part, slices, npad, n_out_pad, row_base, grid, s);
+    case EPI_CTX: return launch_epi<EPI_CTX>(nt, ch, part, slices, npad, n_out_pad, grid, s);
+    case EPI_QKV: return launch_epi<EPI_QKV>(nt, ch, part, slices, npad, n_out_pad, grid, s);
+    case EPI_RESID: return launch_epi<EPI_RESID>(nt, ch, part, slices, npad, n_out_pad, grid, s);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, ch, part, slices, npad, n_out_pad, grid, s);
+    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, ch, part, slices, npad, n_out_pad, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

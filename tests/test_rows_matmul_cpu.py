@@ -94,6 +94,8 @@ def test_large_batch_option_carves_the_contraction_scratch(lib):
                [pkg.rows_matmul_plan(cfg.d, mh, pkg.DFLASH_ROWS_MATMUL_MAX, 0, n_sm).scratch_bytes])  # W_c
     want = -(-want // 256) * 256
     want += -(-(pkg.DFLASH_ROWS_MATMUL_MAX * mh * 2) // 256) * 256   # context taps converted to f16
+    # the head's vocab states: one slice per row chunk (up to 8) of n_sm CTAs x 32 rows x (max, sum, index)
+    want += (8 - 1) * n_sm * 32 * 3 * 4
     diff = lib.dflash_workspace_bytes(ctypes.byref(on)) - lib.dflash_workspace_bytes(ctypes.byref(off))
     assert diff == want
     for over in (dict(batch=1, gamma=8), dict(wdtype="bf16"), dict(markov_rank=64)):
