@@ -277,7 +277,7 @@ uint64_t dflash_launch_count(const dflash_handle* h);
  * borrowed LM head; each weight is the group-64 affine code w = scale * q + bias). It serves
  * batches of activation rows (up to DFLASH_ROWS_MATMUL_MAX rows per call) in one pass over the
  * weights, where the draft round's skinny per-request projections would stream them once per 32
- * rows. Experimental: not yet covered by the parity tests; the draft round does not call it. */
+ * rows; the draft round's large_batch_tc05 option runs its projections on it. */
 #define DFLASH_ROWS_MATMUL_MAX 160
 enum {
   DFLASH_MAT_CTX = 0,    /* W_c [d][n_taps*H] (Eq 2) */
@@ -297,7 +297,7 @@ typedef struct {
   int m_tiles;          /* 128-row output tiles */
   int k_slices;         /* K slices per tile (their partial tiles are summed in slice order) */
   int groups_per_slice; /* 64-input groups per K slice */
-  int grid;             /* CTAs = m_tiles * k_slices */
+  int grid;             /* CTAs = ceil(m_tiles / 3) * k_slices (three output tiles per CTA) */
   int x_stages;         /* activation ring depth */
   size_t smem_bytes;    /* dynamic shared memory per CTA */
   size_t scratch_bytes; /* scratch dflash_rows_matmul needs */

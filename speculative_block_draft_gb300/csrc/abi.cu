@@ -390,6 +390,22 @@ int make_rows_map(const void* base, int k, int rows, int ld, int box_rows, CUten
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
 }
 
+// A stored 4-bit matrix ([strip][group] tiles of 576 B) as a 3-D map of 32-bit words
+// [n_strips][groups][144], box 144 x 1 x 8: one group of a 128-row output tile per copy; strips past
+// the matrix read as zero.
+int make_q4_tile_map(const PackedMat& m, CUtensorMap* map) {
+  EncodeTiled encode = tensor_map_encoder();
+  if (!encode) return DFLASH_ECUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)(kQ4GroupBytes / 4), (cuuint64_t)m.groups, (cuuint64_t)m.n_strips};
+  const cuuint64_t strides[2] = {(cuuint64_t)kQ4GroupBytes, (cuuint64_t)m.groups * kQ4GroupBytes};
+  const cuuint32_t box[3] = {kQ4GroupBytes / 4, 1, 8};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(m.w), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
+}
+
 int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return DFLASH_ECUDA;
@@ -538,6 +554,7 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   Tc05Args a{};
   if (make_rows_map(x, m.k, rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
   if (xl && make_rows_map(xl, m.k, rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_q4_tile_map(m, &a.wmap) != DFLASH_OK) return DFLASH_ECUDA;
   a.w = m.w;
   a.part = reinterpret_cast<float*>(h->tc05_scratch + p.part_off);
   a.err = h->err;
@@ -546,6 +563,7 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   a.npad = p.npad;
   a.gps = p.gps;
   a.mtiles = p.mtiles;
+  a.tgroups = p.tgroups;
   a.has_lo = xl != nullptr;
   a.n_out_pad = p.mtiles * 128;
   a.sx = p.sx;
@@ -1443,6 +1461,7 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   Tc05Args a{};
   if (make_rows_map(x, m->k, n_rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
   if (x_lo && make_rows_map(x_lo, m->k, n_rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_q4_tile_map(*m, &a.wmap) != DFLASH_OK) return DFLASH_ECUDA;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   a.w = m->w;
   a.part = reinterpret_cast<float*>(sc + p.part_off);
@@ -1452,6 +1471,7 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   a.npad = p.npad;
   a.gps = p.gps;
   a.mtiles = p.mtiles;
+  a.tgroups = p.tgroups;
   a.has_lo = x_lo != nullptr;
   a.n_out_pad = p.mtiles * 128;
   a.sx = p.sx;

@@ -11,22 +11,25 @@ constexpr unsigned kErrTimeoutTc05 = 4u;  // device error word bit of this kerne
 
 constexpr int kTcWarps = 10;              // copies, MMA issue, 8 dequantising warps (4 of them also the epilogue)
 constexpr int kTcMaxRows = 160;           // activation rows per call (the MMA's N, padded to 16)
-constexpr int kTcSW = 8;                  // raw 4-bit tile stages
-constexpr int kTcSA = 4;                  // dequantised f16 A-tile stages
+constexpr int kTcTiles = 3;               // 128-row output tiles per CTA (3 x 160 accumulator columns <= 512)
+constexpr int kTcSW = 3;                  // raw 4-bit stages (one 64-input group of a CTA's tiles each)
+constexpr int kTcSA = 2;                  // dequantised f16 A stages
 constexpr int kTcMaxSX = 4;               // activation stages, at most
 constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
 
 struct Tc05Args {
   CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder: box 64 x npad, 128-byte swizzle
+  CUtensorMap wmap;          // the stored 4-bit matrix as [strip][group][144 words]: box 144 x 1 x 8 (one
+                             // group of a 128-row tile, 4608 B), rows past the matrix read as zero
   const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
   float* part;               // [slices][npad][n_out_pad] partial tiles (scratch)
   unsigned* err;
-  int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, tmem_cols;
+  int n_strips, groups, npad, gps, mtiles, tgroups, has_lo, n_out_pad, sx, tmem_cols;
   uint32_t x_stage, x_tx;
 };
 
 struct Tc05Plan {
-  int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, tmem_cols = 0;   // npad == 0: no plan
+  int npad = 0, mtiles = 0, tgroups = 0, slices = 0, gps = 0, grid = 0, sx = 0, tmem_cols = 0;   // npad == 0: no plan
   uint32_t x_stage = 0, x_tx = 0;
   size_t smem = 0, part_off = 0, scratch = 0;
 };

@@ -28,9 +28,9 @@ def test_plan_invariants(lib, n_out, k_in, rows, x_lo):
     p = pkg.rows_matmul_plan(n_out, k_in, rows, x_lo, 152)
     groups = k_in // 64
     assert p.n_pad % 16 == 0 and rows <= p.n_pad < rows + 16            # the MMA's N
-    assert p.n_pad <= TMEM_COLS // 2                                     # one fp32 accumulator, two CTAs per SM
+    assert 3 * p.n_pad <= TMEM_COLS                                      # one fp32 accumulator per tile, 3 tiles
     assert p.m_tiles == -(-n_out // 128)
-    assert p.grid == p.m_tiles * p.k_slices
+    assert p.grid == -(-p.m_tiles // 3) * p.k_slices                      # CTAs: groups of 3 tiles x K slices
     # the K slices cover every group once, none empty, each at least 4 groups where K allows
     assert (p.k_slices - 1) * p.groups_per_slice < groups <= p.k_slices * p.groups_per_slice
     assert p.groups_per_slice >= min(4, groups)
@@ -38,18 +38,18 @@ def test_plan_invariants(lib, n_out, k_in, rows, x_lo):
     # activation stage: n_pad rows x 128 B (twice with the remainder), a multiple of 1024 B
     stage = p.n_pad * 128 * (2 if x_lo else 1)
     assert stage % 1024 == 0
-    assert p.smem_bytes >= p.x_stages * stage + 4 * 128 * 128 + 8 * 4608   # + four f16 A tiles, eight raw stages
+    assert p.smem_bytes >= p.x_stages * stage + 2 * 3 * 128 * 128 + 3 * 3 * 4608   # + two A stages, three raw stages
     # scratch: one fp32 partial tile per (K slice, 128-row tile)
     assert p.scratch_bytes == p.k_slices * p.n_pad * p.m_tiles * 128 * 4
 
 
 def test_plan_fills_the_sms_where_k_allows(lib):
-    lm = pkg.rows_matmul_plan(151936, 5120, 128, 0, 152)        # 1187 tiles: no K split
-    assert (lm.m_tiles, lm.k_slices, lm.grid) == (1187, 1, 1187)
-    qkv = pkg.rows_matmul_plan(7168, 5120, 160, 1, 152)         # 56 tiles: split K three ways
-    assert (qkv.m_tiles, qkv.k_slices, qkv.groups_per_slice) == (56, 3, 27)
-    down = pkg.rows_matmul_plan(5120, 17408, 160, 0, 152)       # 40 tiles over 272 groups
-    assert down.k_slices == 4 and down.grid == 160
+    lm = pkg.rows_matmul_plan(151936, 5120, 128, 0, 152)        # 1187 tiles in 396 groups of 3: no K split
+    assert (lm.m_tiles, lm.k_slices, lm.grid) == (1187, 1, 396)
+    qkv = pkg.rows_matmul_plan(7168, 5120, 160, 1, 152)         # 56 tiles (19 groups): split K 8 ways
+    assert (qkv.m_tiles, qkv.k_slices, qkv.groups_per_slice, qkv.grid) == (56, 8, 10, 152)
+    down = pkg.rows_matmul_plan(5120, 17408, 160, 0, 152)       # 40 tiles (14 groups) over 272 groups
+    assert down.k_slices == 11 and down.grid == 154
     tiny = pkg.rows_matmul_plan(16, 64, 1, 0, 152)              # one tile, one group
     assert (tiny.grid, tiny.k_slices, tiny.n_pad) == (1, 1, 16)
 
