@@ -290,15 +290,21 @@ enum {
 
 /* Launch geometry and caller scratch of dflash_rows_matmul for a matrix of n_out rows and k_in
  * inputs (k_in % 64 == 0), n_rows activation rows, with (x_lo != 0) or without the activations'
- * f16 remainder, on a device with n_sm SMs. Host only. Returns DFLASH_OK, DFLASH_EINVAL for bad
+ * f16 remainder, on a device with n_sm SMs: the shape (tiles per CTA, K slices) with the shortest
+ * modelled time, CTAs dispatched in index order to the SM that frees first. Host only. Returns DFLASH_OK, DFLASH_EINVAL for bad
  * sizes or a NULL plan, DFLASH_ECAPACITY for n_rows > DFLASH_ROWS_MATMUL_MAX. */
 typedef struct {
   int n_pad;            /* activation rows padded to a multiple of 16 (the MMA's N) */
   int m_tiles;          /* 128-row output tiles */
   int k_slices;         /* K slices per tile (their partial tiles are summed in slice order) */
   int groups_per_slice; /* 64-input groups per K slice */
-  int grid;             /* CTAs = ceil(m_tiles / 3) * k_slices (three output tiles per CTA) */
+  int grid;             /* CTAs = tile_groups * k_slices */
   int x_stages;         /* activation ring depth */
+  int tile_groups;      /* groups of consecutive output tiles, one per CTA and K slice: */
+  int tiles_big;        /*   the first big_groups hold tiles_big tiles (1-3), */
+  int big_groups;
+  int tiles_small;      /*   the others tiles_small (the last possibly fewer) */
+  int w_stages;         /* ring depth of the raw 4-bit tiles */
   size_t smem_bytes;    /* dynamic shared memory per CTA */
   size_t scratch_bytes; /* scratch dflash_rows_matmul needs */
 } dflash_rows_plan;

@@ -306,17 +306,23 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->tc05_rows = std::min(c.max_batch * h->G, kTcMaxRows);
   if (tc_possible) {
     size_t sc = 0;
+    // every row count a many-row call can have (33 .. tc05_rows): the plan's K slices may grow as
+    // the rows shrink
     auto need = [&](const PackedMat& m, int lo) {
-      const Tc05Plan p = plan_tc05(m.n_strips, m.groups, h->tc05_rows, lo, h->n_sm);
-      sc = std::max(sc, p.scratch);
+      for (int r = kMaxRows + 1; r <= h->tc05_rows + 15; r += 16) {
+        const Tc05Plan p = plan_tc05(m.n_strips, m.groups, std::min(r, h->tc05_rows), lo, h->n_sm);
+        sc = std::max(sc, p.scratch);
+      }
     };
     need(h->qkv[0], 1);
     need(h->wo[0], 0);
     need(h->gu[0], 1);
     need(h->down[0], 0);
     need(h->lm, 1);
-    const Tc05Plan pc = plan_tc05(h->wc.n_strips, h->wc.groups, kTcMaxRows, 0, h->n_sm);   // context rows
-    sc = std::max(sc, pc.scratch);
+    for (int r = kMaxRows + 1; r <= kTcMaxRows + 15; r += 16) {   // context rows, in chunks of up to 160
+      const Tc05Plan pc = plan_tc05(h->wc.n_strips, h->wc.groups, std::min(r, kTcMaxRows), 0, h->n_sm);
+      sc = std::max(sc, pc.scratch);
+    }
     h->tc05_on = sc > 0;
     h->tc05_scratch_bytes = sc;
     h->tc05_scratch = cv.take<uint8_t>(sc);
@@ -560,16 +566,7 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   a.err = h->err;
   a.n_strips = m.n_strips;
   a.groups = m.groups;
-  a.npad = p.npad;
-  a.gps = p.gps;
-  a.mtiles = p.mtiles;
-  a.tgroups = p.tgroups;
-  a.has_lo = xl != nullptr;
-  a.n_out_pad = p.mtiles * 128;
-  a.sx = p.sx;
-  a.tmem_cols = p.tmem_cols;
-  a.x_stage = p.x_stage;
-  a.x_tx = p.x_tx;
+  tc05_fill_args(p, xl != nullptr, a);
   *out = p;
   h->launches += 1;
   return status_of(launch_tc05_parts(a, p, s));
@@ -1430,6 +1427,11 @@ int dflash_rows_matmul_plan(int n_out, int k_in, int n_rows, int x_lo, int n_sm,
   plan->groups_per_slice = p.gps;
   plan->grid = p.grid;
   plan->x_stages = p.sx;
+  plan->tile_groups = p.tgroups;
+  plan->tiles_big = p.tiles_big;
+  plan->big_groups = p.groups_big;
+  plan->tiles_small = p.tiles_small;
+  plan->w_stages = p.sw;
   plan->smem_bytes = p.smem;
   plan->scratch_bytes = p.scratch;
   return DFLASH_OK;
@@ -1468,16 +1470,7 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   a.err = h->err;
   a.n_strips = m->n_strips;
   a.groups = m->groups;
-  a.npad = p.npad;
-  a.gps = p.gps;
-  a.mtiles = p.mtiles;
-  a.tgroups = p.tgroups;
-  a.has_lo = x_lo != nullptr;
-  a.n_out_pad = p.mtiles * 128;
-  a.sx = p.sx;
-  a.tmem_cols = p.tmem_cols;
-  a.x_stage = p.x_stage;
-  a.x_tx = p.x_tx;
+  tc05_fill_args(p, x_lo != nullptr, a);
   h->launches += 2;
   const int half = matrix == DFLASH_MAT_GATEUP ? h->I : 0;
   return status_of(launch_tc05(a, p, n_rows, m->n_rows, half, y, ldy, static_cast<cudaStream_t>(stream)));

@@ -24,6 +24,12 @@
 // wait is bounded (error word + early exit); tensor memory is freed at the end. The K slices'
 // partial tiles are summed in slice order by a separate kernel.
 #include <cuda.h>
+
+#include <algorithm>
+#include <array>
+#include <map>
+#include <mutex>
+#include <vector>
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -37,9 +43,7 @@ namespace {
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcStrips = 8;                                      // 16-row strips per 128-row tile
 constexpr int kTcTileW = kTcStrips * kQ4GroupBytes;               // 4608 B: one group of one tile, raw
-constexpr int kTcWStage = kTcTiles * kTcTileW;                    // one group of a CTA's tiles, raw
 constexpr int kTcTileA = 128 * 128;                               // 16 KB: one group of one tile, f16
-constexpr int kTcAStage = kTcTiles * kTcTileA;
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -53,16 +57,31 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t v, __half2 c, __half2 s, _
   return h2_bits(__hfma2(__hsub2(bits_h2(v), c), s, b));
 }
 
+// Ring position: stage index and the parity of its current fill.
+struct RingPos {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++stage == n) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+template <bool LO>
 __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_constant__ Tc05Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* aring = sm;                                          // kTcSA x kTcAStage (1024-aligned)
-  uint8_t* xring = aring + kTcSA * kTcAStage;                   // a.sx x a.x_stage (1024-aligned)
-  uint8_t* wring = xring + (size_t)a.sx * a.x_stage;            // kTcSW x kTcWStage
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wring + kTcSW * kTcWStage);
+  const int cb = a.tiles_big;                                   // tiles of the largest CTA: ring strides
+  const uint32_t a_stage = (uint32_t)cb * kTcTileA, w_stage = (uint32_t)cb * kTcTileW;
+  uint8_t* aring = sm;                                          // kTcSA x a_stage (1024-aligned)
+  uint8_t* xring = aring + kTcSA * a_stage;                     // a.sx x a.x_stage (1024-aligned)
+  uint8_t* wring = xring + (size_t)a.sx * a.x_stage;            // a.sw x w_stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wring + (size_t)a.sw * w_stage);
   uint64_t* full_w = bars;
-  uint64_t* empty_w = full_w + kTcSW;
-  uint64_t* full_x = empty_w + kTcSW;
+  uint64_t* empty_w = full_w + kTcMaxSW;
+  uint64_t* full_x = empty_w + kTcMaxSW;
   uint64_t* empty_x = full_x + kTcMaxSX;
   uint64_t* full_a = empty_x + kTcMaxSX;
   uint64_t* empty_a = full_a + kTcSA;
@@ -70,13 +89,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA -> (tile group, K slice); the first a.groups_big tile groups hold tiles_big tiles, the
+  // rest tiles_small (the last one possibly fewer)
   const int tg = blockIdx.x % a.tgroups, slice = blockIdx.x / a.tgroups;
-  const int mt0 = tg * kTcTiles, n_tiles = min(kTcTiles, a.mtiles - mt0);
+  const int mt0 = tg < a.groups_big ? tg * cb : a.groups_big * cb + (tg - a.groups_big) * a.tiles_small;
+  const int n_tiles = min(tg < a.groups_big ? cb : a.tiles_small, a.mtiles - mt0);
   const int g0 = slice * a.gps, ng = min(a.groups, g0 + a.gps) - g0;
-  auto strips_of = [&](int t) { return min(kTcStrips, a.n_strips - (mt0 + t) * kTcStrips); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kTcSW; i++) {
+    for (int i = 0; i < a.sw; i++) {
       mbar_init(smem_u32(&full_w[i]), 1);
       mbar_init(smem_u32(&empty_w[i]), kTcStrips);   // the eight decoder warps
     }
@@ -105,75 +126,87 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     if (ng > 0) {
       const uint32_t w_bytes = (uint32_t)(n_tiles * kTcTileW);   // whole boxes, zero-filled rows included
       bool ok = true;
-      int nw = 0, nx = 0;   // stages whose copies were issued
+      RingPos pw, px;
+      int nw = 0, nx = 0;   // fills issued
       for (int i = 0; i < ng && ok; i++) {
-        const int g = g0 + i, sw = i % kTcSW, sx = i % a.sx;
-        if (i >= kTcSW)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[sw]), ((i / kTcSW) + 1) & 1, a.err,
+        const int g = g0 + i;
+        if (i >= a.sw)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[pw.stage]), pw.phase ^ 1u, a.err,
                                                          kErrTimeoutTc05));
         if (!ok) break;
         if (lane == 0) {
           in_bounds(mt0 < a.mtiles && g < a.groups, a.err);
-          const uint32_t fw = smem_u32(&full_w[sw]);
+          const uint32_t fw = smem_u32(&full_w[pw.stage]);
           mbar_arrive_expect_tx(fw, w_bytes);
           // one tensor copy per tile: its 8 strips' tiles of group g (strips past the matrix: zeros)
           for (int t = 0; t < n_tiles; t++)
-            tma_load_3d(smem_u32(wring + sw * kTcWStage + t * kTcTileW), &a.wmap, 0, g, (mt0 + t) * kTcStrips, fw);
+            tma_load_3d(smem_u32(wring + pw.stage * w_stage + t * kTcTileW), &a.wmap, 0, g, (mt0 + t) * kTcStrips,
+                        fw);
         }
         __syncwarp();
         nw = i + 1;
+        pw.next(a.sw);
         if (i >= a.sx)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_x[sx]), ((i / a.sx) + 1) & 1, a.err,
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_x[px.stage]), px.phase ^ 1u, a.err,
                                                          kErrTimeoutTc05));
         if (!ok) break;
         if (lane == 0) {
-          const uint32_t fx = smem_u32(&full_x[sx]);
-          uint8_t* xst = xring + (size_t)sx * a.x_stage;
+          const uint32_t fx = smem_u32(&full_x[px.stage]);
+          uint8_t* xst = xring + (size_t)px.stage * a.x_stage;
           mbar_arrive_expect_tx(fx, a.x_tx);
           tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
-          if (a.has_lo) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
+          if (LO) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
         }
         __syncwarp();
         nx = i + 1;
+        px.next(a.sx);
       }
       // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
       // the last fill of every stage has completed (earlier fills of a stage completed before
       // its refill was issued); after a normal run these waits return at once
-      for (int j = nw > kTcSW ? nw - kTcSW : 0; j < nw; j++)
-        mbar_wait_bounded(smem_u32(&full_w[j % kTcSW]), (j / kTcSW) & 1, nullptr, 0);
+      for (int j = nw > a.sw ? nw - a.sw : 0; j < nw; j++)
+        mbar_wait_bounded(smem_u32(&full_w[j % a.sw]), (j / a.sw) & 1, nullptr, 0);
       for (int j = nx > a.sx ? nx - a.sx : 0; j < nx; j++)
         mbar_wait_bounded(smem_u32(&full_x[j % a.sx]), (j / a.sx) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
     // ---- MMA issue: accumulator t (tensor-memory columns t * npad ...) for tile t ----------------
+    // The whole warp runs the loop; one elected lane issues each MMA and commit. Descriptors are
+    // the rings' base descriptors plus start-address offsets (16-byte units in the low field;
+    // shared-memory addresses stay below 2^18, so the field never carries).
     if (ng > 0) {
       const uint32_t idesc = umma_idesc_f16_f32(128, a.npad);
+      const uint64_t a_base = umma_desc_sw128(smem_u32(aring)), x_base = umma_desc_sw128(smem_u32(xring));
+      const uint32_t a_step = a_stage >> 4, x_step = a.x_stage >> 4, lo_off = (uint32_t)a.npad * 8u;
       bool ok = true;
+      RingPos pa, px;
       int issued = 0;
       for (int i = 0; i < ng && ok; i++) {
-        const int sa = i % kTcSA, sx = i % a.sx;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&full_a[sa]), (i / kTcSA) & 1, a.err, kErrTimeoutTc05) &&
-                                     mbar_wait_bounded(smem_u32(&full_x[sx]), (i / a.sx) & 1, a.err, kErrTimeoutTc05));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(smem_u32(&full_a[pa.stage]), pa.phase, a.err, kErrTimeoutTc05) &&
+                            mbar_wait_bounded(smem_u32(&full_x[px.stage]), px.phase, a.err, kErrTimeoutTc05));
         if (!ok) break;
         tc05_fence_after();
-        if (lane == 0) {
-          const uint32_t xbase = smem_u32(xring + (size_t)sx * a.x_stage);
-          for (int t = 0; t < n_tiles; t++) {
-            const uint32_t abase = smem_u32(aring + sa * kTcAStage + t * kTcTileA);
+        const uint64_t ad = a_base + (uint64_t)(pa.stage * a_step);
+        const uint64_t xd = x_base + (uint64_t)(px.stage * x_step);
+#pragma unroll
+        for (int t = 0; t < kTcTiles; t++) {
+          if (t < n_tiles) {
             const uint32_t d = tmem + (uint32_t)(t * a.npad);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
-              const uint64_t ad = umma_desc_sw128(abase + 32 * kk);
-              umma_f16_ss(d, ad, umma_desc_sw128(xbase + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
-              if (a.has_lo) umma_f16_ss(d, ad, umma_desc_sw128(xbase + a.npad * 128 + 32 * kk), idesc, 1u);
+              const uint64_t adk = ad + (uint64_t)(t * (kTcTileA >> 4) + 2 * kk);
+              umma_f16_ss_warp(d, adk, xd + (uint64_t)(2 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+              if (LO) umma_f16_ss_warp(d, adk, xd + (uint64_t)(lo_off + 2 * kk), idesc, 1u);
             }
           }
-          umma_commit(smem_u32(&empty_a[sa]));
-          umma_commit(smem_u32(&empty_x[sx]));
-          if (i + 1 == ng) umma_commit(smem_u32(acc_done));
         }
-        __syncwarp();
+        umma_commit_warp(smem_u32(&empty_a[pa.stage]));
+        umma_commit_warp(smem_u32(&empty_x[px.stage]));
+        if (i + 1 == ng) umma_commit_warp(smem_u32(acc_done));
         issued = i + 1;
+        pa.next(kTcSA);
+        px.next(a.sx);
       }
       // nothing of this CTA may still be running on the tensor core when its memory is freed
       if (issued > 0) mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % kTcSA]), ((issued - 1) / kTcSA) & 1, a.err,
@@ -181,28 +214,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     }
   } else {
     // ---- dequantise: 4-bit codes -> f16 weights, swizzled K-major A tiles -------------------------
+    // Warp s (0-7) takes strip s of every tile. All of a group's words are read first, then
+    // converted and stored, so the tiles' shared-memory latencies overlap.
     const int s = warp - 2, g8 = lane >> 2, t4 = lane & 3;
     const __half2 c1024 = __float2half2_rn(1024.f), c64 = __float2half2_rn(64.f);
     bool ok = true;
+    RingPos pw, pa;
     for (int i = 0; i < ng && ok; i++) {
-      const int sw = i % kTcSW, sa = i % kTcSA;
-      ok = mbar_wait_bounded(smem_u32(&full_w[sw]), (i / kTcSW) & 1, a.err, kErrTimeoutTc05) &&
-           (i < kTcSA || mbar_wait_bounded(smem_u32(&empty_a[sa]), ((i / kTcSA) + 1) & 1, a.err, kErrTimeoutTc05));
+      ok = mbar_wait_bounded(smem_u32(&full_w[pw.stage]), pw.phase, a.err, kErrTimeoutTc05) &&
+           (i < kTcSA || mbar_wait_bounded(smem_u32(&empty_a[pa.stage]), pa.phase ^ 1u, a.err, kErrTimeoutTc05));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      for (int t = 0; t < n_tiles; t++) {
-        const uint8_t* gp = wring + sw * kTcWStage + (t * kTcStrips + s) * kQ4GroupBytes;
-        const uint32_t ast = smem_u32(aring + sa * kTcAStage + t * kTcTileA);
-        uint32_t rg[4][2], r8[4][2];
-        if (s < strips_of(t)) {
-          const uint4 W = *reinterpret_cast<const uint4*>(gp + lane * 16);
-          const uint32_t sbg = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * g8);
-          const uint32_t sb8 = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g8 + 8));
-          const __half2 sg = __float2half2_rn(__uint_as_float(sbg << 16));
-          const __half2 bg = __float2half2_rn(__uint_as_float(sbg & 0xFFFF0000u));
-          const __half2 s8 = __float2half2_rn(__uint_as_float(sb8 << 16));
-          const __half2 b8 = __float2half2_rn(__uint_as_float(sb8 & 0xFFFF0000u));
-          const uint32_t w4[4] = {W.x, W.y, W.z, W.w};
+      uint4 W[kTcTiles];
+      uint32_t sbg[kTcTiles], sb8[kTcTiles];
+#pragma unroll
+      for (int t = 0; t < kTcTiles; t++) {
+        if (t < n_tiles) {
+          const uint8_t* gp = wring + pw.stage * w_stage + (t * kTcStrips + s) * kQ4GroupBytes;
+          W[t] = *reinterpret_cast<const uint4*>(gp + lane * 16);
+          sbg[t] = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * g8);
+          sb8[t] = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g8 + 8));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTcTiles; t++) {
+        if (t < n_tiles) {
+          const uint32_t ast = smem_u32(aring + pa.stage * a_stage + t * kTcTileA);
+          const __half2 sg = __float2half2_rn(__uint_as_float(sbg[t] << 16));
+          const __half2 bg = __float2half2_rn(__uint_as_float(sbg[t] & 0xFFFF0000u));
+          const __half2 s8 = __float2half2_rn(__uint_as_float(sb8[t] << 16));
+          const __half2 b8 = __float2half2_rn(__uint_as_float(sb8[t] & 0xFFFF0000u));
+          const uint32_t w4[4] = {W[t].x, W[t].y, W[t].z, W[t].w};
+          uint32_t rg[4][2], r8[4][2];
 #pragma unroll
           for (int j = 0; j < 4; j++) {
             // word j of lane (g, t): inputs k0 = 16 t + 4 j .. k0 + 3 of rows g and g + 8, nibbles
@@ -213,26 +256,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
             r8[j][0] = dequant2(lop3_and_or(w, 0x00F000F0u, 0x54005400u), c64, s8, b8);      // 64 + q
             r8[j][1] = dequant2(lop3_and_or(w8, 0x00F000F0u, 0x54005400u), c64, s8, b8);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; j++) rg[j][0] = rg[j][1] = r8[j][0] = r8[j][1] = 0u;
+          // 16-byte chunk c of row r lives at r * 128 + ((c ^ (r % 8)) * 16); r % 8 == g here
+          const uint32_t row_g = ast + (uint32_t)(s * 16 + g8) * 128, row_8 = row_g + 8 * 128;
+          const uint32_t c0 = (uint32_t)(((2 * t4) ^ g8) << 4), c1 = (uint32_t)(((2 * t4 + 1) ^ g8) << 4);
+          st_shared_v4(row_g + c0, rg[0][0], rg[0][1], rg[1][0], rg[1][1]);
+          st_shared_v4(row_g + c1, rg[2][0], rg[2][1], rg[3][0], rg[3][1]);
+          st_shared_v4(row_8 + c0, r8[0][0], r8[0][1], r8[1][0], r8[1][1]);
+          st_shared_v4(row_8 + c1, r8[2][0], r8[2][1], r8[3][0], r8[3][1]);
         }
-        // 16-byte chunk c of row r lives at r * 128 + ((c ^ (r % 8)) * 16); r % 8 == g here
-        const uint32_t row_g = ast + (uint32_t)(s * 16 + g8) * 128, row_8 = row_g + 8 * 128;
-        const uint32_t c0 = (uint32_t)(((2 * t4) ^ g8) << 4), c1 = (uint32_t)(((2 * t4 + 1) ^ g8) << 4);
-        st_shared_v4(row_g + c0, rg[0][0], rg[0][1], rg[1][0], rg[1][1]);
-        st_shared_v4(row_g + c1, rg[2][0], rg[2][1], rg[3][0], rg[3][1]);
-        st_shared_v4(row_8 + c0, r8[0][0], r8[0][1], r8[1][0], r8[1][1]);
-        st_shared_v4(row_8 + c1, r8[2][0], r8[2][1], r8[3][0], r8[3][1]);
       }
       // the generic-proxy stores are read by the tensor core, and the raw stage is refilled by the
       // copy engine (both async proxy)
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&full_a[sa]));
-        mbar_arrive(smem_u32(&empty_w[sw]));
+        mbar_arrive(smem_u32(&full_a[pa.stage]));
+        mbar_arrive(smem_u32(&empty_w[pw.stage]));
       }
+      pw.next(a.sw);
+      pa.next(kTcSA);
     }
     if (warp >= 4 && warp < 8 && ok && ng > 0) {
       // ---- the slice's partial tiles: tensor memory -> part[slice][column][output row] ----------
@@ -303,40 +345,168 @@ cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cu
   return cudaGetLastError();
 }
 
-Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) {
+namespace {
+
+// Cost model of one launch, in SM cycles, for choosing a plan: per 64-input group a fixed ~150
+// cycles of waits and commits plus, per tile, the larger of its MMAs' issue time (measured on this
+// kernel's issue loop: ~50 + 0.19 N cycles per M = 128, K = 16 instruction) and its 4.6 KB share
+// of HBM; per CTA ~3000 cycles of start-up and the store of its partial tiles; per extra K slice
+// the partial tiles written and read once more. The CTAs are dispatched in index order to the SM
+// that frees first (one CTA per SM fits), which is what the makespan below simulates.
+struct CostModel {
+  double per_group, per_tile_group, per_cta, per_tile_out, hbm_bytes_per_cycle;
+};
+
+CostModel cost_model(int npad, int x_lo, int n_sm) {
+  CostModel c{};
+  const double mma = 50.0 + 0.19 * npad;
+  const double hbm = 6.6e12 / 2.07e9;   // bytes per SM cycle, whole GPU
+  c.per_group = 150.0;
+  c.per_tile_group = std::max(4.0 * (x_lo ? 2.0 : 1.0) * mma, kTcTileW / (hbm / n_sm));
+  c.per_cta = 3000.0;
+  c.per_tile_out = 128.0 * npad * 4.0 / 40.0;
+  c.hbm_bytes_per_cycle = hbm;
+  return c;
+}
+
+double makespan(const CostModel& c, int n_sm, int mtiles, int cb, int nb, int cs, int groups, int gps) {
+  const int slices = (groups + gps - 1) / gps;
+  const int rest = mtiles - nb * cb;
+  const int tgroups = nb + (rest > 0 ? (rest + cs - 1) / cs : 0);
+  std::vector<double> sm(n_sm, 0.0);   // a binary heap of SM free times
+  auto cmp = [](double x, double y) { return x > y; };
+  double end = 0.0;
+  for (int b = 0; b < tgroups * slices; b++) {
+    const int tg = b % tgroups, sl = b / tgroups;
+    const int mt0 = tg < nb ? tg * cb : nb * cb + (tg - nb) * cs;
+    const int nt = std::min(tg < nb ? cb : cs, mtiles - mt0);
+    const int ng = std::min(groups, (sl + 1) * gps) - sl * gps;
+    const double cost = c.per_cta + ng * (c.per_group + nt * c.per_tile_group) + nt * c.per_tile_out;
+    std::pop_heap(sm.begin(), sm.end(), cmp);
+    sm.back() += cost;
+    end = std::max(end, sm.back());
+    std::push_heap(sm.begin(), sm.end(), cmp);
+  }
+  return end;
+}
+
+// Shared memory of a CTA with cb tiles, sw raw stages and sx activation stages.
+size_t tc05_smem(int cb, int sw, int sx, uint32_t x_stage) {
+  return 1024 /* alignment slack */ + (size_t)kTcSA * cb * kTcTileA + (size_t)sw * cb * kTcTileW +
+         (size_t)sx * x_stage + (size_t)(2 * kTcMaxSW + 2 * kTcMaxSX + 2 * kTcSA + 1) * 8 + 16;
+}
+
+}  // namespace
+
+Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_sm) {
   Tc05Plan p{};
-  if (n_strips < 1 || groups < 1 || rows < 1 || rows > kTcMaxRows || n_sm < 1) return p;
-  p.npad = (rows + 15) / 16 * 16;
-  p.mtiles = (n_strips + kTcStrips - 1) / kTcStrips;
-  p.tgroups = (p.mtiles + kTcTiles - 1) / kTcTiles;
-  // K slices: enough CTAs to cover the SMs, each slice at least 4 groups long
-  const int want = (n_sm + p.tgroups - 1) / p.tgroups;
-  const int s = std::max(1, std::min(want, groups / 4));
-  p.gps = (groups + s - 1) / s;
+  const int mtiles = (n_strips + kTcStrips - 1) / kTcStrips;
+  const CostModel cm = cost_model(npad, x_lo, n_sm);
+  // Candidates: every CTA with c tiles (c = 3, 2, 1) and s K slices (each >= 4 groups long), or,
+  // with one slice, k x n_sm CTAs of three tiles followed by CTAs of two.
+  struct Cand {
+    int cb, nb, cs, gps;
+    double t;
+  } best{0, 0, 0, 0, 0.0};
+  auto consider = [&](int cb, int nb, int cs, int gps) {
+    double t = makespan(cm, n_sm, mtiles, cb, nb, cs, groups, gps);
+    const int slices = (groups + gps - 1) / gps;
+    t += (slices - 1) * (double)npad * mtiles * 128 * 8.0 / cm.hbm_bytes_per_cycle;   // partials re-read
+    if (best.cb == 0 || t < best.t * 0.99) best = Cand{cb, nb, cs, gps, t};
+  };
+  for (int c = kTcTiles; c >= 1; c--) {
+    if (c * npad > 512 || (c > 1 && c > mtiles)) continue;   // accumulators must fit tensor memory
+    const int tg = (mtiles + c - 1) / c;
+    for (int s = 1; s <= std::max(1, std::min(groups / 4, 64)); s++) {
+      const int gps = (groups + s - 1) / s;
+      if (s > 1 && (groups + gps - 1) / gps != s) continue;   // same slicing as a smaller s
+      if (s > 1 && (long long)tg * s > 3LL * n_sm) break;   // beyond ~3 waves more slices only add work
+      consider(c, tg, c, gps);
+    }
+  }
+  if (kTcTiles * npad <= 512)
+    for (int k = 1; (long long)k * n_sm * kTcTiles < mtiles; k++) consider(kTcTiles, k * n_sm, 2, groups);
+  p.npad = npad;
+  p.mtiles = mtiles;
+  p.tiles_big = best.cb;
+  p.groups_big = best.nb;
+  p.tiles_small = best.cs;
+  p.gps = best.gps;
   p.slices = (groups + p.gps - 1) / p.gps;
+  const int rest = mtiles - p.groups_big * p.tiles_big;
+  p.tgroups = p.groups_big + (rest > 0 ? (rest + p.tiles_small - 1) / p.tiles_small : 0);
   p.grid = p.tgroups * p.slices;
-  p.x_stage = (uint32_t)p.npad * 128u * (x_lo ? 2u : 1u);   // a multiple of 2048 B
+  p.x_stage = (uint32_t)npad * 128u * (x_lo ? 2u : 1u);   // a multiple of 2048 B
   p.x_tx = p.x_stage;
-  const size_t fixed = 1024 /* alignment slack */ + (size_t)kTcSA * kTcAStage + (size_t)kTcSW * kTcWStage +
-                       (size_t)(2 * kTcSW + 2 * kTcMaxSX + 2 * kTcSA + 1) * 8 + 16;
-  const size_t room = kTcSmemMax > fixed ? kTcSmemMax - fixed : 0;
-  p.sx = (int)std::min<size_t>(kTcMaxSX, room / p.x_stage);
-  if (p.sx < 2) return Tc05Plan{};
-  p.smem = fixed + (size_t)p.sx * p.x_stage;
+  // raw stages: four when three activation stages still fit, else three (two activation stages
+  // at least)
+  p.sw = 0;
+  for (int sw = kTcMaxSW; sw >= 2 && p.sw == 0; sw--) {
+    const size_t base = tc05_smem(p.tiles_big, sw, 0, p.x_stage);
+    const int sx = base < kTcSmemMax ? (int)std::min<size_t>(kTcMaxSX, (kTcSmemMax - base) / p.x_stage) : 0;
+    if (sx >= 3 || (sw == 3 && sx >= 2) || (sw == 2 && sx >= 2)) {
+      p.sw = sw;
+      p.sx = sx;
+    }
+  }
+  if (p.sw == 0) return Tc05Plan{};
+  p.smem = tc05_smem(p.tiles_big, p.sw, p.sx, p.x_stage);
   int cols = 32;
-  while (cols < kTcTiles * p.npad) cols *= 2;
+  while (cols < p.tiles_big * npad) cols *= 2;
   p.tmem_cols = cols;
   p.part_off = 0;
-  p.scratch = (size_t)p.slices * p.npad * p.mtiles * 128 * 4;
+  p.scratch = (size_t)p.slices * npad * mtiles * 128 * 4;
   return p;
 }
 
+// Plans depend on the activation rows only through npad; a launch asks for one per projection, so
+// they are kept (a few dozen shapes per drafter).
+Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm) {
+  if (n_strips < 1 || groups < 1 || rows < 1 || rows > kTcMaxRows || n_sm < 1) return Tc05Plan{};
+  const int npad = (rows + 15) / 16 * 16;
+  static std::mutex mu;
+  static std::map<std::array<int, 5>, Tc05Plan> cache;
+  const std::array<int, 5> key{n_strips, groups, npad, x_lo ? 1 : 0, n_sm};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const Tc05Plan p = plan_tc05_uncached(n_strips, groups, npad, x_lo, n_sm);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() < 4096) cache.emplace(key, p);
+  return p;
+}
+
+void tc05_fill_args(const Tc05Plan& p, int has_lo, Tc05Args& a) {
+  a.npad = p.npad;
+  a.gps = p.gps;
+  a.mtiles = p.mtiles;
+  a.tgroups = p.tgroups;
+  a.tiles_big = p.tiles_big;
+  a.groups_big = p.groups_big;
+  a.tiles_small = p.tiles_small;
+  a.has_lo = has_lo;
+  a.n_out_pad = p.mtiles * 128;
+  a.sx = p.sx;
+  a.sw = p.sw;
+  a.tmem_cols = p.tmem_cols;
+  a.x_stage = p.x_stage;
+  a.x_tx = p.x_tx;
+}
+
 cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t s) {
-  static std::atomic<int> smem_set[kMaxDevices];
+  static std::atomic<int> smem_set[2][kMaxDevices];
   cudaError_t e;
-  e = ensure_smem_limit(tc05_q4_kernel, p.smem, smem_set);
-  if (e != cudaSuccess) return e;
-  tc05_q4_kernel<<<p.grid, kTcThreads, p.smem, s>>>(a);
+  if (a.has_lo) {
+    e = ensure_smem_limit(tc05_q4_kernel<true>, p.smem, smem_set[1]);
+    if (e != cudaSuccess) return e;
+    tc05_q4_kernel<true><<<p.grid, kTcThreads, p.smem, s>>>(a);
+  } else {
+    e = ensure_smem_limit(tc05_q4_kernel<false>, p.smem, smem_set[0]);
+    if (e != cudaSuccess) return e;
+    tc05_q4_kernel<false><<<p.grid, kTcThreads, p.smem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

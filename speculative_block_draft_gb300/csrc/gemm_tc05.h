@@ -11,8 +11,8 @@ constexpr unsigned kErrTimeoutTc05 = 4u;  // device error word bit of this kerne
 
 constexpr int kTcWarps = 10;              // copies, MMA issue, 8 dequantising warps (4 of them also the epilogue)
 constexpr int kTcMaxRows = 160;           // activation rows per call (the MMA's N, padded to 16)
-constexpr int kTcTiles = 3;               // 128-row output tiles per CTA (3 x 160 accumulator columns <= 512)
-constexpr int kTcSW = 3;                  // raw 4-bit stages (one 64-input group of a CTA's tiles each)
+constexpr int kTcTiles = 3;               // 128-row output tiles per CTA, at most (3 x 160 accumulator columns <= 512)
+constexpr int kTcMaxSW = 4;               // raw 4-bit stages (one 64-input group of a CTA's tiles each), at most
 constexpr int kTcSA = 2;                  // dequantised f16 A stages
 constexpr int kTcMaxSX = 4;               // activation stages, at most
 constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
@@ -24,17 +24,25 @@ struct Tc05Args {
   const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
   float* part;               // [slices][npad][n_out_pad] partial tiles (scratch)
   unsigned* err;
-  int n_strips, groups, npad, gps, mtiles, tgroups, has_lo, n_out_pad, sx, tmem_cols;
+  int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, sw, tmem_cols;
+  // CTA b covers tile group b % tgroups and K slice b / tgroups; the first groups_big tile groups
+  // hold tiles_big consecutive 128-row tiles, the others tiles_small (the last possibly fewer)
+  int tgroups, tiles_big, groups_big, tiles_small;
   uint32_t x_stage, x_tx;
 };
 
 struct Tc05Plan {
-  int npad = 0, mtiles = 0, tgroups = 0, slices = 0, gps = 0, grid = 0, sx = 0, tmem_cols = 0;   // npad == 0: no plan
+  int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, sw = 0, tmem_cols = 0;   // npad == 0: no plan
+  int tgroups = 0, tiles_big = 0, groups_big = 0, tiles_small = 0;
   uint32_t x_stage = 0, x_tx = 0;
   size_t smem = 0, part_off = 0, scratch = 0;
 };
 
+// The launch shape with the shortest modelled time: tiles per CTA, K slices, ring depths.
 Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
+
+// Copies the plan's shape into the kernel arguments (maps, pointers and sizes are the caller's).
+void tc05_fill_args(const Tc05Plan& p, int has_lo, Tc05Args& a);
 
 // The contraction: partial tiles [slices][npad][n_out_pad] in a.part (stored row order).
 cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t s);

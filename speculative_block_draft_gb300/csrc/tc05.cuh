@@ -75,6 +75,27 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// The same two operations executed by a whole converged warp: elect.sync picks one lane, which
+// issues. Keeping the issuing loop warp-uniform lets the operands stay in uniform registers (a
+// lane-0 branch around the MMA costs ~30 cycles per instruction more, measured).
+__device__ __forceinline__ void umma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp receives lane (taddr's lane + i).
 // The wait is in the same statement, so no use of the registers can move above it.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {

@@ -28,30 +28,41 @@ def test_plan_invariants(lib, n_out, k_in, rows, x_lo):
     p = pkg.rows_matmul_plan(n_out, k_in, rows, x_lo, 152)
     groups = k_in // 64
     assert p.n_pad % 16 == 0 and rows <= p.n_pad < rows + 16            # the MMA's N
-    assert 3 * p.n_pad <= TMEM_COLS                                      # one fp32 accumulator per tile, 3 tiles
+    assert 1 <= p.tiles_small <= p.tiles_big <= 3
+    assert p.tiles_big * p.n_pad <= TMEM_COLS                            # one fp32 accumulator per tile
     assert p.m_tiles == -(-n_out // 128)
-    assert p.grid == -(-p.m_tiles // 3) * p.k_slices                      # CTAs: groups of 3 tiles x K slices
+    # the tile groups cover every 128-row tile once: big groups first, the last group may be short
+    assert 1 <= p.big_groups <= p.tile_groups and (p.big_groups - 1) * p.tiles_big < p.m_tiles
+    covered = p.big_groups * p.tiles_big + (p.tile_groups - p.big_groups) * p.tiles_small
+    last = p.tiles_big if p.tile_groups == p.big_groups else p.tiles_small
+    assert covered - last < p.m_tiles <= covered
+    assert p.tiles_big == 1 or p.tiles_big <= p.m_tiles
+    assert p.grid == p.tile_groups * p.k_slices                            # CTAs: tile groups x K slices
     # the K slices cover every group once, none empty, each at least 4 groups where K allows
     assert (p.k_slices - 1) * p.groups_per_slice < groups <= p.k_slices * p.groups_per_slice
     assert p.groups_per_slice >= min(4, groups)
-    assert 2 <= p.x_stages <= 4 and p.smem_bytes <= SMEM_MAX
+    # a K split never leaves CTAs for a second partial wave
+    assert p.k_slices == 1 or p.grid <= 152
+    assert 2 <= p.x_stages <= 4 and 2 <= p.w_stages <= 4 and p.smem_bytes <= SMEM_MAX
     # activation stage: n_pad rows x 128 B (twice with the remainder), a multiple of 1024 B
     stage = p.n_pad * 128 * (2 if x_lo else 1)
     assert stage % 1024 == 0
-    assert p.smem_bytes >= p.x_stages * stage + 2 * 3 * 128 * 128 + 3 * 3 * 4608   # + two A stages, three raw stages
+    # + two f16 A stages and the raw stages, sized for the largest CTA
+    assert p.smem_bytes >= p.x_stages * stage + 2 * p.tiles_big * 128 * 128 + p.w_stages * p.tiles_big * 4608
     # scratch: one fp32 partial tile per (K slice, 128-row tile)
     assert p.scratch_bytes == p.k_slices * p.n_pad * p.m_tiles * 128 * 4
 
 
-def test_plan_fills_the_sms_where_k_allows(lib):
-    lm = pkg.rows_matmul_plan(151936, 5120, 128, 0, 152)        # 1187 tiles in 396 groups of 3: no K split
-    assert (lm.m_tiles, lm.k_slices, lm.grid) == (1187, 1, 396)
-    qkv = pkg.rows_matmul_plan(7168, 5120, 160, 1, 152)         # 56 tiles (19 groups): split K 8 ways
-    assert (qkv.m_tiles, qkv.k_slices, qkv.groups_per_slice, qkv.grid) == (56, 8, 10, 152)
-    down = pkg.rows_matmul_plan(5120, 17408, 160, 0, 152)       # 40 tiles (14 groups) over 272 groups
-    assert down.k_slices == 11 and down.grid == 154
+def test_plan_shapes_of_the_drafter(lib):
+    """The cost model's choices on the 5120-wide drafter (152 SMs): no second partial wave."""
+    lm = pkg.rows_matmul_plan(151936, 5120, 128, 0, 152)        # 1187 tiles: 2 x 152 CTAs of 3, then CTAs of 2
+    assert (lm.m_tiles, lm.k_slices, lm.tiles_big, lm.big_groups, lm.tiles_small, lm.grid) == (1187, 1, 3, 304, 2, 442)
+    gu = pkg.rows_matmul_plan(34816, 5120, 160, 1, 152)         # 272 tiles: 136 CTAs of 2, K whole
+    assert (gu.k_slices, gu.tiles_big, gu.grid) == (1, 2, 136)
+    down = pkg.rows_matmul_plan(5120, 17408, 160, 0, 152)       # 40 tiles over 272 groups: 20 pairs x 7 slices
+    assert (down.tiles_big, down.k_slices, down.grid) == (2, 7, 140)
     tiny = pkg.rows_matmul_plan(16, 64, 1, 0, 152)              # one tile, one group
-    assert (tiny.grid, tiny.k_slices, tiny.n_pad) == (1, 1, 16)
+    assert (tiny.grid, tiny.k_slices, tiny.n_pad, tiny.tiles_big) == (1, 1, 16, 1)
 
 
 def test_plan_rejects_bad_sizes(lib):
@@ -74,7 +85,7 @@ def test_rows_matmul_validates_before_any_launch(lib):
 
 def test_large_batch_option_carves_the_contraction_scratch(lib):
     """large_batch_tc05 = 1 adds exactly the largest contraction scratch (the block projections and
-    the head at max_batch * gamma rows, capped at 160; W_c at 160 context rows) and the f16 copy of
+    the head at 33 .. max_batch * gamma rows, capped at 160; W_c at 33 .. 160 context rows) and the f16 copy of
     160 context-tap rows to the workspace. It adds nothing where the option does not apply (one
     request of 8 rows, 16-bit weights, or a Markov head)."""
     import dflash_synth as syn
@@ -90,8 +101,13 @@ def test_large_batch_option_carves_the_contraction_scratch(lib):
               (cfg.vocab, cfg.d)]
     n_sm = 148   # the library's default when no device is present
     mh = cfg.n_taps * cfg.target_hidden
-    want = max([pkg.rows_matmul_plan(n, k, rows, 0, n_sm).scratch_bytes for n, k in shapes] +
-               [pkg.rows_matmul_plan(cfg.d, mh, pkg.DFLASH_ROWS_MATMUL_MAX, 0, n_sm).scratch_bytes])  # W_c
+    # every many-row call size (33 rows up): the plan's K slices may grow as the rows shrink
+    lo = {(qkv, cfg.d): 1, (2 * cfg.inter, cfg.d): 1, (cfg.vocab, cfg.d): 1}
+    sizes = lambda top: [min(r, top) for r in range(33, top + 16, 16)]
+    want = max([pkg.rows_matmul_plan(n, k, r, lo.get((n, k), 0), n_sm).scratch_bytes for n, k in shapes
+                for r in sizes(rows)] +
+               [pkg.rows_matmul_plan(cfg.d, mh, r, 0, n_sm).scratch_bytes
+                for r in sizes(pkg.DFLASH_ROWS_MATMUL_MAX)])  # W_c
     want = -(-want // 256) * 256
     want += -(-(pkg.DFLASH_ROWS_MATMUL_MAX * mh * 2) // 256) * 256   # context taps converted to f16
     # the head's vocab states: one slice per row chunk (up to 8) of n_sm CTAs x 32 rows x (max, sum, index)
