@@ -304,7 +304,10 @@ typedef struct {
   int tiles_big;        /*   the first big_groups hold tiles_big tiles (1-3), */
   int big_groups;
   int tiles_small;      /*   the others tiles_small (the last possibly fewer) */
-  int w_stages;         /* ring depth of the raw 4-bit tiles */
+  int w_stages;         /* ring depth of the raw 4-bit tiles, w_groups 64-input groups per stage */
+  int w_groups;
+  int a_stages;         /* ring depth of the dequantised f16 tiles (one group per stage) */
+  int x_groups;         /* 64-input groups per activation stage */
   size_t smem_bytes;    /* dynamic shared memory per CTA */
   size_t scratch_bytes; /* scratch dflash_rows_matmul needs */
 } dflash_rows_plan;

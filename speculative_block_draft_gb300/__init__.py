@@ -115,7 +115,7 @@ class dflash_stats(ctypes.Structure):
 class dflash_rows_plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_pad", "m_tiles", "k_slices", "groups_per_slice", "grid",
                                             "x_stages", "tile_groups", "tiles_big", "big_groups", "tiles_small",
-                                            "w_stages")] + [("smem_bytes", ctypes.c_size_t),
+                                            "w_stages", "w_groups", "a_stages", "x_groups")] + [("smem_bytes", ctypes.c_size_t),
                                                             ("scratch_bytes", ctypes.c_size_t)]
 
 

@@ -396,15 +396,31 @@ int make_rows_map(const void* base, int k, int rows, int ld, int box_rows, CUten
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
 }
 
+// Activation rows (f16 [rows][ld]) as a 3-D map [k / 64][rows][64]: box 64 x box_rows x kx with the
+// 128-byte swizzle, i.e. kx consecutive 64-input groups per copy, each a K-major tile of box_rows
+// rows of 128 B (rows past `rows` read as zero).
+int make_rows_map_groups(const void* base, int k, int rows, int ld, int box_rows, int kx, CUtensorMap* map) {
+  EncodeTiled encode = tensor_map_encoder();
+  if (!encode) return DFLASH_ECUDA;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(k / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)kx};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
+}
+
 // A stored 4-bit matrix ([strip][group] tiles of 576 B) as a 3-D map of 32-bit words
-// [n_strips][groups][144], box 144 x 1 x 8: one group of a 128-row output tile per copy; strips past
-// the matrix read as zero.
-int make_q4_tile_map(const PackedMat& m, CUtensorMap* map) {
+// [n_strips][groups][144], box 144 x kw x (8 * tiles): kw consecutive groups of `tiles`
+// consecutive 128-row output tiles per copy; strips and groups past the matrix read as zero.
+int make_q4_tile_map(const PackedMat& m, int tiles, int kw, CUtensorMap* map) {
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return DFLASH_ECUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)(kQ4GroupBytes / 4), (cuuint64_t)m.groups, (cuuint64_t)m.n_strips};
   const cuuint64_t strides[2] = {(cuuint64_t)kQ4GroupBytes, (cuuint64_t)m.groups * kQ4GroupBytes};
-  const cuuint32_t box[3] = {kQ4GroupBytes / 4, 1, 8};
+  const cuuint32_t box[3] = {kQ4GroupBytes / 4, (cuuint32_t)kw, (cuuint32_t)(8 * tiles)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(m.w), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -558,9 +574,11 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   if (p.npad == 0 || p.scratch > h->tc05_scratch_bytes) return DFLASH_EINVAL;
   const void* xl = lo_off ? static_cast<const void*>(static_cast<const __half*>(x) + lo_off) : nullptr;
   Tc05Args a{};
-  if (make_rows_map(x, m.k, rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (xl && make_rows_map(xl, m.k, rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (make_q4_tile_map(m, &a.wmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_rows_map_groups(x, m.k, rows, ldx, p.npad, p.kx, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (xl && make_rows_map_groups(xl, m.k, rows, ldx, p.npad, p.kx, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_q4_tile_map(m, p.tiles_big, kTcKW, &a.wmap) != DFLASH_OK ||
+      make_q4_tile_map(m, p.tiles_small, kTcKW, &a.wmap_small) != DFLASH_OK)
+    return DFLASH_ECUDA;
   a.w = m.w;
   a.part = reinterpret_cast<float*>(h->tc05_scratch + p.part_off);
   a.err = h->err;
@@ -1432,6 +1450,9 @@ int dflash_rows_matmul_plan(int n_out, int k_in, int n_rows, int x_lo, int n_sm,
   plan->big_groups = p.groups_big;
   plan->tiles_small = p.tiles_small;
   plan->w_stages = p.sw;
+  plan->a_stages = p.sa;
+  plan->w_groups = kTcKW;
+  plan->x_groups = p.kx;
   plan->smem_bytes = p.smem;
   plan->scratch_bytes = p.scratch;
   return DFLASH_OK;
@@ -1461,9 +1482,12 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   if (p.npad == 0) return DFLASH_EINVAL;
   if (scratch_bytes < p.scratch) return DFLASH_ECAPACITY;
   Tc05Args a{};
-  if (make_rows_map(x, m->k, n_rows, ldx, p.npad, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (x_lo && make_rows_map(x_lo, m->k, n_rows, ldx, p.npad, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (make_q4_tile_map(*m, &a.wmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_rows_map_groups(x, m->k, n_rows, ldx, p.npad, p.kx, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (x_lo && make_rows_map_groups(x_lo, m->k, n_rows, ldx, p.npad, p.kx, &a.xlmap) != DFLASH_OK)
+    return DFLASH_ECUDA;
+  if (make_q4_tile_map(*m, p.tiles_big, kTcKW, &a.wmap) != DFLASH_OK ||
+      make_q4_tile_map(*m, p.tiles_small, kTcKW, &a.wmap_small) != DFLASH_OK)
+    return DFLASH_ECUDA;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   a.w = m->w;
   a.part = reinterpret_cast<float*>(sc + p.part_off);

@@ -57,9 +57,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // error word err[0] and return false: the caller stops issuing work and leaves. The limit is
 // err[1] microseconds when that word is nonzero (a test setting), else 1 s; a wait without an
 // error word (err == nullptr: draining a CTA's own copies before it leaves) always allows 1 s.
+// The first ~20000 cycles (~10 us) poll the barrier alone: reading the limit word is a global
+// load, and a pipeline's ordinary short waits must not each pay a memory round trip for it (under
+// a full HBM stream that is a microsecond). Limits are therefore at least ~10 us.
+constexpr long long kWaitFastCycles = 20000;
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned* err,
                                                   unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
+  const long long c0 = clock64();
+  do {
+    if (mbar_try_wait(bar, parity)) return true;
+  } while (clock64() - c0 < kWaitFastCycles);
   const uint64_t t0 = global_timer_ns();
   const unsigned limit_us = err ? *reinterpret_cast<volatile unsigned*>(err + 1) : 0u;
   const uint64_t limit_ns = limit_us ? (uint64_t)limit_us * 1000ull : 1000000000ull;
@@ -99,6 +107,14 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 }
 
 // 3-D tiled tensor copy global -> shared (TMA), completing on an mbarrier.
+// Tiled tensor prefetch of one 3-D box into L2; nothing waits for it.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                             uint32_t bar) {
   asm volatile(

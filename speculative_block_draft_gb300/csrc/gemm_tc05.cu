@@ -2,13 +2,14 @@
 // fifth-generation tensor cores (tcgen05), for batches of activation rows (up to 160) where the
 // skinny mma.sync GEMV runs into the legacy tensor path's ceiling.
 //
-// One CTA per (group of up to kTcTiles 128-row output tiles, K slice), ten warps. The tiles of a
+// One CTA per (group of up to kTcTiles 128-row output tiles, K slice), eleven warps. The tiles of a
 // CTA share every activation tile: it is loaded once per 64-input group for all of them, which
 // divides the activation traffic from L2 and the number of activation loads in flight by the
 // tile count.
-//  * warp 0 streams, per 64-input group, each tile's eight 4-bit (strip, group) tiles with one 3-D
-//    tensor copy, and the group's activation rows (f16, plus the f16 remainder where given) with
-//    2-D tensor copies in the 128-byte swizzle;
+//  * warp 0 streams the CTA's 4-bit (strip, group) tiles, two 64-input groups of all its tiles per
+//    3-D tensor copy, and keeps the following ones coming into L2 with tensor prefetches; warp 10
+//    streams the activation rows (f16, plus the f16 remainder where given), one or two groups per
+//    3-D tensor copy in the 128-byte swizzle;
 //  * warps 2-9 (strip w of every tile) dequantise the codes to f16 weights, w = s q + b with one
 //    rounding (the code q is made exact in f16 from its nibble with a magic-number lop3 and one
 //    exact subtraction, then one fused f16 multiply-add with the row's scale and bias), and store
@@ -74,9 +75,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int cb = a.tiles_big;                                   // tiles of the largest CTA: ring strides
-  const uint32_t a_stage = (uint32_t)cb * kTcTileA, w_stage = (uint32_t)cb * kTcTileW;
-  uint8_t* aring = sm;                                          // kTcSA x a_stage (1024-aligned)
-  uint8_t* xring = aring + kTcSA * a_stage;                     // a.sx x a.x_stage (1024-aligned)
+  const uint32_t a_stage = (uint32_t)cb * kTcTileA, w_stage = (uint32_t)(kTcKW * cb * kTcTileW);
+  uint8_t* aring = sm;                                          // a.sa x a_stage (1024-aligned)
+  uint8_t* xring = aring + (size_t)a.sa * a_stage;              // a.sx x a.x_stage (1024-aligned)
   uint8_t* wring = xring + (size_t)a.sx * a.x_stage;            // a.sw x w_stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(wring + (size_t)a.sw * w_stage);
   uint64_t* full_w = bars;
@@ -84,8 +85,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   uint64_t* full_x = empty_w + kTcMaxSW;
   uint64_t* empty_x = full_x + kTcMaxSX;
   uint64_t* full_a = empty_x + kTcMaxSX;
-  uint64_t* empty_a = full_a + kTcSA;
-  uint64_t* acc_done = empty_a + kTcSA;
+  uint64_t* empty_a = full_a + kTcMaxSA;
+  uint64_t* acc_done = empty_a + kTcMaxSA;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,6 +96,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   const int mt0 = tg < a.groups_big ? tg * cb : a.groups_big * cb + (tg - a.groups_big) * a.tiles_small;
   const int n_tiles = min(tg < a.groups_big ? cb : a.tiles_small, a.mtiles - mt0);
   const int g0 = slice * a.gps, ng = min(a.groups, g0 + a.gps) - g0;
+  // copies: raw weights kTcKW groups at a time (W step), activations a.kx groups at a time (x step)
+  const int kx = a.kx;
+  const int nsw = (ng + kTcKW - 1) / kTcKW, nsx = (ng + kx - 1) / kx;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.sw; i++) {
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
       mbar_init(smem_u32(&full_x[i]), 1);
       mbar_init(smem_u32(&empty_x[i]), 1);            // the MMA commit
     }
-    for (int i = 0; i < kTcSA; i++) {
+    for (int i = 0; i < a.sa; i++) {
       mbar_init(smem_u32(&full_a[i]), kTcStrips);     // the eight decoder warps
       mbar_init(smem_u32(&empty_a[i]), 1);            // the MMA commit
     }
@@ -121,32 +125,72 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   tc05_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Launched with programmatic dependent launch: the next kernel may start its prologue now, and
+  // this one may have started while the previous kernel drained. Nothing earlier kernels wrote
+  // (activation rows, the partial-tile scratch an earlier epilogue reads) is touched before
+  // pdl_wait(); the constant weights of the first stages are requested before it.
+  pdl_launch_dependents();
   if (warp == 0) {
-    // ---- copies: raw 4-bit tiles and activation tiles --------------------------------------------
+    // ---- copies: raw 4-bit tiles -------------------------------------------------------------------
     if (ng > 0) {
-      const uint32_t w_bytes = (uint32_t)(n_tiles * kTcTileW);   // whole boxes, zero-filled rows included
-      bool ok = true;
-      RingPos pw, px;
-      int nw = 0, nx = 0;   // fills issued
-      for (int i = 0; i < ng && ok; i++) {
-        const int g = g0 + i;
-        if (i >= a.sw)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[pw.stage]), pw.phase ^ 1u, a.err,
-                                                         kErrTimeoutTc05));
-        if (!ok) break;
+      // One tensor copy per W step: kTcKW groups of the 8 strips of each of the CTA's tiles (a box
+      // as tall as the CTA's tile count; strips and groups past the matrix read as zero, and a
+      // short last CTA reads only strips past the matrix beyond its own). Few large copies: each
+      // copy has a fixed cost of its own in the copy engine, whatever its size.
+      const bool big = tg < a.groups_big;
+      const CUtensorMap* wm = big ? &a.wmap : &a.wmap_small;
+      const uint32_t w_bytes = (uint32_t)(kTcKW * (big ? cb : a.tiles_small) * kTcTileW);   // whole box
+      auto issue_w = [&](int j, int stage) {
         if (lane == 0) {
-          in_bounds(mt0 < a.mtiles && g < a.groups, a.err);
-          const uint32_t fw = smem_u32(&full_w[pw.stage]);
+          in_bounds(mt0 < a.mtiles && g0 + j * kTcKW < a.groups, a.err);
+          const uint32_t fw = smem_u32(&full_w[stage]);
           mbar_arrive_expect_tx(fw, w_bytes);
-          // one tensor copy per tile: its 8 strips' tiles of group g (strips past the matrix: zeros)
-          for (int t = 0; t < n_tiles; t++)
-            tma_load_3d(smem_u32(wring + pw.stage * w_stage + t * kTcTileW), &a.wmap, 0, g, (mt0 + t) * kTcStrips,
-                        fw);
+          tma_load_3d(smem_u32(wring + stage * w_stage), wm, 0, g0 + j * kTcKW, mt0 * kTcStrips, fw);
         }
         __syncwarp();
-        nw = i + 1;
+      };
+      const int pre = min(a.sw, nsw);
+      for (int j = 0; j < pre; j++) issue_w(j, j);
+      // and the next a.pf steps into L2, so that the ring's copies find them there: the ring alone
+      // holds too few bytes per SM to cover HBM latency under a full stream
+      int npf = pre;
+      auto prefetch_next = [&]() {
+        if (lane == 0 && npf < nsw) tma_prefetch_3d(wm, 0, g0 + npf * kTcKW, mt0 * kTcStrips);
+        npf++;
+      };
+      while (npf < min(nsw, pre + a.pf)) prefetch_next();
+      pdl_wait();
+      bool ok = true;
+      RingPos pw;
+      for (int j = 0; j < pre; j++) pw.next(a.sw);
+      int nw = pre;   // fills issued
+      for (int j = pre; j < nsw && ok; j++) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_w[pw.stage]), pw.phase ^ 1u, a.err,
+                                                       kErrTimeoutTc05));
+        if (!ok) break;
+        issue_w(j, pw.stage);
+        nw = j + 1;
+        prefetch_next();
         pw.next(a.sw);
-        if (i >= a.sx)
+      }
+      // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
+      // the last fill of every stage has completed (earlier fills of a stage completed before
+      // its refill was issued); after a normal run these waits return at once
+      for (int j = nw > a.sw ? nw - a.sw : 0; j < nw; j++)
+        mbar_wait_bounded(smem_u32(&full_w[j % a.sw]), (j / a.sw) & 1, nullptr, 0);
+    } else {
+      pdl_wait();
+    }
+  } else if (warp == kTcWarps - 1) {
+    // ---- copies: activation tiles (a warp of their own, so that neither stream waits on the
+    // other's free stages) ------------------------------------------------------------------------
+    pdl_wait();
+    if (ng > 0) {
+      bool ok = true;
+      RingPos px;
+      int nx = 0;   // fills issued
+      for (int k = 0; k < nsx && ok; k++) {
+        if (k >= a.sx)
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&empty_x[px.stage]), px.phase ^ 1u, a.err,
                                                          kErrTimeoutTc05));
         if (!ok) break;
@@ -154,22 +198,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
           const uint32_t fx = smem_u32(&full_x[px.stage]);
           uint8_t* xst = xring + (size_t)px.stage * a.x_stage;
           mbar_arrive_expect_tx(fx, a.x_tx);
-          tma_load_2d(smem_u32(xst), &a.xmap, g * 64, 0, fx);
-          if (LO) tma_load_2d(smem_u32(xst + a.npad * 128), &a.xlmap, g * 64, 0, fx);
+          tma_load_3d(smem_u32(xst), &a.xmap, 0, 0, g0 + k * kx, fx);
+          if (LO) tma_load_3d(smem_u32(xst + kx * a.npad * 128), &a.xlmap, 0, 0, g0 + k * kx, fx);
         }
         __syncwarp();
-        nx = i + 1;
+        nx = k + 1;
         px.next(a.sx);
       }
-      // leave no copy in flight into this CTA's shared memory, also when a consumer gave up:
-      // the last fill of every stage has completed (earlier fills of a stage completed before
-      // its refill was issued); after a normal run these waits return at once
-      for (int j = nw > a.sw ? nw - a.sw : 0; j < nw; j++)
-        mbar_wait_bounded(smem_u32(&full_w[j % a.sw]), (j / a.sw) & 1, nullptr, 0);
       for (int j = nx > a.sx ? nx - a.sx : 0; j < nx; j++)
         mbar_wait_bounded(smem_u32(&full_x[j % a.sx]), (j / a.sx) & 1, nullptr, 0);
     }
   } else if (warp == 1) {
+    pdl_wait();
     // ---- MMA issue: accumulator t (tensor-memory columns t * npad ...) for tile t ----------------
     // The whole warp runs the loop; one elected lane issues each MMA and commit. Descriptors are
     // the rings' base descriptors plus start-address offsets (16-byte units in the low field;
@@ -177,18 +217,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     if (ng > 0) {
       const uint32_t idesc = umma_idesc_f16_f32(128, a.npad);
       const uint64_t a_base = umma_desc_sw128(smem_u32(aring)), x_base = umma_desc_sw128(smem_u32(xring));
-      const uint32_t a_step = a_stage >> 4, x_step = a.x_stage >> 4, lo_off = (uint32_t)a.npad * 8u;
+      const uint32_t a_step = a_stage >> 4, x_step = a.x_stage >> 4, x_tile = (uint32_t)a.npad * 8u;
+      const uint32_t lo_off = (uint32_t)kx * x_tile;   // the remainder rows follow the kx tiles
       bool ok = true;
       RingPos pa, px;
       int issued = 0;
       for (int i = 0; i < ng && ok; i++) {
+        const int kxi = i % kx;   // group within the x step
+        const bool x_last = kxi == kx - 1 || i + 1 == ng;
         ok = __all_sync(0xffffffffu,
                         mbar_wait_bounded(smem_u32(&full_a[pa.stage]), pa.phase, a.err, kErrTimeoutTc05) &&
                             mbar_wait_bounded(smem_u32(&full_x[px.stage]), px.phase, a.err, kErrTimeoutTc05));
         if (!ok) break;
         tc05_fence_after();
         const uint64_t ad = a_base + (uint64_t)(pa.stage * a_step);
-        const uint64_t xd = x_base + (uint64_t)(px.stage * x_step);
+        const uint64_t xd = x_base + (uint64_t)(px.stage * x_step + kxi * x_tile);
 #pragma unroll
         for (int t = 0; t < kTcTiles; t++) {
           if (t < n_tiles) {
@@ -202,17 +245,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
           }
         }
         umma_commit_warp(smem_u32(&empty_a[pa.stage]));
-        umma_commit_warp(smem_u32(&empty_x[px.stage]));
+        if (x_last) umma_commit_warp(smem_u32(&empty_x[px.stage]));
         if (i + 1 == ng) umma_commit_warp(smem_u32(acc_done));
         issued = i + 1;
-        pa.next(kTcSA);
-        px.next(a.sx);
+        pa.next(a.sa);
+        if (x_last) px.next(a.sx);
       }
       // nothing of this CTA may still be running on the tensor core when its memory is freed
-      if (issued > 0) mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % kTcSA]), ((issued - 1) / kTcSA) & 1, a.err,
+      if (issued > 0) mbar_wait_bounded(smem_u32(&empty_a[(issued - 1) % a.sa]), ((issued - 1) / a.sa) & 1, a.err,
                                         kErrTimeoutTc05);
     }
   } else {
+    pdl_wait();
     // ---- dequantise: 4-bit codes -> f16 weights, swizzled K-major A tiles -------------------------
     // Warp s (0-7) takes strip s of every tile. All of a group's words are read first, then
     // converted and stored, so the tiles' shared-memory latencies overlap.
@@ -221,8 +265,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
     bool ok = true;
     RingPos pw, pa;
     for (int i = 0; i < ng && ok; i++) {
+      const int kwi = i % kTcKW;   // group within the W step
+      const bool w_last = kwi == kTcKW - 1 || i + 1 == ng;
       ok = mbar_wait_bounded(smem_u32(&full_w[pw.stage]), pw.phase, a.err, kErrTimeoutTc05) &&
-           (i < kTcSA || mbar_wait_bounded(smem_u32(&empty_a[pa.stage]), pa.phase ^ 1u, a.err, kErrTimeoutTc05));
+           (i < a.sa || mbar_wait_bounded(smem_u32(&empty_a[pa.stage]), pa.phase ^ 1u, a.err, kErrTimeoutTc05));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       uint4 W[kTcTiles];
@@ -230,7 +276,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
 #pragma unroll
       for (int t = 0; t < kTcTiles; t++) {
         if (t < n_tiles) {
-          const uint8_t* gp = wring + pw.stage * w_stage + (t * kTcStrips + s) * kQ4GroupBytes;
+          const uint8_t* gp = wring + pw.stage * w_stage + ((t * kTcStrips + s) * kTcKW + kwi) * kQ4GroupBytes;
           W[t] = *reinterpret_cast<const uint4*>(gp + lane * 16);
           sbg[t] = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * g8);
           sb8[t] = *reinterpret_cast<const uint32_t*>(gp + 512 + 4 * (g8 + 8));
@@ -271,26 +317,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&full_a[pa.stage]));
-        mbar_arrive(smem_u32(&empty_w[pw.stage]));
+        if (w_last) mbar_arrive(smem_u32(&empty_w[pw.stage]));
       }
-      pw.next(a.sw);
-      pa.next(kTcSA);
+      if (w_last) pw.next(a.sw);
+      pa.next(a.sa);
     }
     if (warp >= 4 && warp < 8 && ok && ng > 0) {
-      // ---- the slice's partial tiles: tensor memory -> part[slice][column][output row] ----------
+      // ---- the slice's partial tiles: tensor memory -> part[slice][strip][column][16] -----------
+      // (a strip's 16 outputs of one activation row are 64 contiguous bytes, and a strip's rows
+      // follow each other: the epilogues read whole strips)
       const int quarter = warp & 3, n = quarter * 32 + lane;   // tile row = tensor-memory lane
       ok = mbar_wait_bounded(smem_u32(acc_done), 0, a.err, kErrTimeoutTc05);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc05_fence_after();
+        const size_t strips_pad = (size_t)a.n_out_pad / 16;
         for (int t = 0; t < n_tiles; t++) {
-          float* out = a.part + (size_t)slice * a.npad * a.n_out_pad + (size_t)(mt0 + t) * 128 + n;
+          const size_t strip = (size_t)(mt0 + t) * kTcStrips + n / 16;
+          float* out = a.part + ((size_t)slice * strips_pad + strip) * a.npad * 16 + (n & 15);
           const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * a.npad);
           for (int ch = 0; ch < a.npad / 16; ch++) {
             float v[16];
             tmem_ld16(tb + (uint32_t)(ch * 16), v);
 #pragma unroll
-            for (int e = 0; e < 16; e++) out[(size_t)(ch * 16 + e) * a.n_out_pad] = v[e];
+            for (int e = 0; e < 16; e++) out[(size_t)(ch * 16 + e) * 16] = v[e];
           }
         }
         tc05_fence_before();
@@ -317,7 +367,8 @@ __global__ void __launch_bounds__(256) tc05_reduce_kernel(const float* __restric
     int p = nn;
     if (half > 0) p = nn < half ? 16 * (nn / 8) + nn % 8 : 16 * ((nn - half) / 8) + 8 + (nn - half) % 8;
     float acc = 0.f;
-    for (int s = 0; s < slices; s++) acc += part[((size_t)s * npad + r) * n_out_pad + p];
+    const size_t strips_pad = (size_t)n_out_pad / 16;
+    for (int s = 0; s < slices; s++) acc += part[(((size_t)s * strips_pad + p / 16) * npad + r) * 16 + p % 16];
     y[(size_t)r * ldy + nn] = acc;
   }
 }
@@ -347,26 +398,80 @@ cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cu
 
 namespace {
 
-// Cost model of one launch, in SM cycles, for choosing a plan: per 64-input group a fixed ~150
-// cycles of waits and commits plus, per tile, the larger of its MMAs' issue time (measured on this
-// kernel's issue loop: ~50 + 0.19 N cycles per M = 128, K = 16 instruction) and its 4.6 KB share
-// of HBM; per CTA ~3000 cycles of start-up and the store of its partial tiles; per extra K slice
-// the partial tiles written and read once more. The CTAs are dispatched in index order to the SM
-// that frees first (one CTA per SM fits), which is what the makespan below simulates.
-struct CostModel {
-  double per_group, per_tile_group, per_cta, per_tile_out, hbm_bytes_per_cycle;
+// Shared memory of a CTA with cb tiles, sa f16 stages, sw raw stages (kTcKW groups each) and sx
+// activation stages.
+size_t tc05_smem(int cb, int sa, int sw, int sx, uint32_t x_stage) {
+  return 1024 /* alignment slack */ + (size_t)sa * cb * kTcTileA + (size_t)sw * kTcKW * cb * kTcTileW +
+         (size_t)sx * x_stage + (size_t)(2 * kTcMaxSW + 2 * kTcMaxSX + 2 * kTcMaxSA + 1) * 8 + 16;
+}
+
+// Ring depths of a CTA with cb tiles: as many f16 stages as fit in ~96 KB (the dequantisation of
+// group i + sa can only start when the MMAs of group i have completed, so the stage count divides
+// that round trip); activation copies of two groups where three or more groups then fit, else of
+// one; the rest of shared memory as raw stages (kTcKW groups each, at least two: with the L2
+// prefetch they cover HBM latency).
+struct Depths {
+  int sa = 0, sw = 0, sx = 0, kx = 0;
+  uint32_t x_stage = 0;
 };
 
-CostModel cost_model(int npad, int x_lo, int n_sm) {
+Depths pick_depths(int cb, int npad, int x_lo) {
+  const int sa_max = std::max(2, std::min(kTcMaxSA, 6 / cb));
+  const size_t w_stage = (size_t)kTcKW * cb * kTcTileW;
+  for (int sa = sa_max; sa >= 2; sa--)
+    for (int kx = 2; kx >= 1; kx--) {
+      const uint32_t xs = (uint32_t)(kx * npad * 128 * (x_lo ? 2 : 1));
+      for (int sx = kTcMaxSX; sx >= 2; sx--) {
+        if (kx * sx < 3) continue;
+        const size_t base = tc05_smem(cb, sa, 0, sx, xs);
+        if (base >= kTcSmemMax) continue;
+        const int sw = (int)std::min<size_t>(kTcMaxSW, (kTcSmemMax - base) / w_stage);
+        if (sw >= 2) return Depths{sa, sw, sx, kx, xs};
+      }
+    }
+  const uint32_t xs = (uint32_t)(npad * 128 * (x_lo ? 2 : 1));   // large tiles and rows: whatever fits
+  const size_t base = tc05_smem(cb, 2, 0, 2, xs);
+  if (base < kTcSmemMax && (kTcSmemMax - base) / w_stage >= 1)
+    return Depths{2, (int)std::min<size_t>(kTcMaxSW, (kTcSmemMax - base) / w_stage), 2, 1, xs};
+  return Depths{};
+}
+
+// Cost model of one launch, in SM cycles, for choosing a plan (constants measured on this kernel
+// with per-CTA clock stamps). Per 64-input group, a CTA with nt tiles takes the largest of: the
+// dequantisation (~290 cycles per tile), the MMAs' issue (~50 + 0.19 N cycles per M = 128, K = 16
+// instruction), the round trip dequantise -> MMA -> completion -> next dequantisation into the
+// same stage divided by the f16 stages, the tiles' share of HBM and the activation tile's share of
+// L2 bandwidth; plus ~150 cycles of waits. Per CTA: ~7000 cycles of start-up and pipeline fill
+// and the store of its partial tiles; per extra K slice the partial tiles written and read once
+// more. CTAs are dispatched in index order to the SM that frees first (one CTA per SM fits).
+struct CostModel {
+  double dq, mma, chain, hbm_tile, l2_x, copies, per_group, per_cta, per_tile_out, hbm_bytes_per_cycle;
+  int sa;
+};
+
+CostModel cost_model(int npad, int x_lo, int n_sm, const Depths& dp) {
   CostModel c{};
-  const double mma = 50.0 + 0.19 * npad;
+  const int sa = dp.sa;
+  const uint32_t x_stage = dp.x_stage / dp.kx;   // per group
   const double hbm = 6.6e12 / 2.07e9;   // bytes per SM cycle, whole GPU
+  const double l2 = 12e12 / 2.07e9;
+  c.dq = 290.0;
+  c.mma = 4.0 * (x_lo ? 2.0 : 1.0) * (50.0 + 0.19 * npad);
+  c.chain = 1100.0;
+  c.hbm_tile = kTcTileW / (hbm / n_sm);
+  c.l2_x = x_stage / (l2 / n_sm);
+  c.copies = 540.0 * (1.0 / kTcKW + (x_lo ? 2.0 : 1.0) / dp.kx);   // the copy engine's fixed cost per copy
   c.per_group = 150.0;
-  c.per_tile_group = std::max(4.0 * (x_lo ? 2.0 : 1.0) * mma, kTcTileW / (hbm / n_sm));
-  c.per_cta = 3000.0;
-  c.per_tile_out = 128.0 * npad * 4.0 / 40.0;
+  c.per_cta = 7000.0;
+  c.per_tile_out = 16.0 * npad;
   c.hbm_bytes_per_cycle = hbm;
+  c.sa = sa;
   return c;
+}
+
+double group_cycles(const CostModel& c, int nt) {
+  const double d = c.dq * nt, m = c.mma * nt;
+  return c.per_group + std::max({d, m, (d + m + c.chain) / c.sa, c.hbm_tile * nt, c.l2_x, c.copies});
 }
 
 double makespan(const CostModel& c, int n_sm, int mtiles, int cb, int nb, int cs, int groups, int gps) {
@@ -381,7 +486,7 @@ double makespan(const CostModel& c, int n_sm, int mtiles, int cb, int nb, int cs
     const int mt0 = tg < nb ? tg * cb : nb * cb + (tg - nb) * cs;
     const int nt = std::min(tg < nb ? cb : cs, mtiles - mt0);
     const int ng = std::min(groups, (sl + 1) * gps) - sl * gps;
-    const double cost = c.per_cta + ng * (c.per_group + nt * c.per_tile_group) + nt * c.per_tile_out;
+    const double cost = c.per_cta + ng * group_cycles(c, nt) + nt * c.per_tile_out;
     std::pop_heap(sm.begin(), sm.end(), cmp);
     sm.back() += cost;
     end = std::max(end, sm.back());
@@ -390,18 +495,11 @@ double makespan(const CostModel& c, int n_sm, int mtiles, int cb, int nb, int cs
   return end;
 }
 
-// Shared memory of a CTA with cb tiles, sw raw stages and sx activation stages.
-size_t tc05_smem(int cb, int sw, int sx, uint32_t x_stage) {
-  return 1024 /* alignment slack */ + (size_t)kTcSA * cb * kTcTileA + (size_t)sw * cb * kTcTileW +
-         (size_t)sx * x_stage + (size_t)(2 * kTcMaxSW + 2 * kTcMaxSX + 2 * kTcSA + 1) * 8 + 16;
-}
-
 }  // namespace
 
 Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_sm) {
   Tc05Plan p{};
   const int mtiles = (n_strips + kTcStrips - 1) / kTcStrips;
-  const CostModel cm = cost_model(npad, x_lo, n_sm);
   // Candidates: every CTA with c tiles (c = 3, 2, 1) and s K slices (each >= 4 groups long), or,
   // with one slice, k x n_sm CTAs of three tiles followed by CTAs of two.
   struct Cand {
@@ -409,6 +507,9 @@ Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_
     double t;
   } best{0, 0, 0, 0, 0.0};
   auto consider = [&](int cb, int nb, int cs, int gps) {
+    const Depths dp = pick_depths(cb, npad, x_lo);
+    if (dp.sa == 0) return;
+    const CostModel cm = cost_model(npad, x_lo, n_sm, dp);
     double t = makespan(cm, n_sm, mtiles, cb, nb, cs, groups, gps);
     const int slices = (groups + gps - 1) / gps;
     t += (slices - 1) * (double)npad * mtiles * 128 * 8.0 / cm.hbm_bytes_per_cycle;   // partials re-read
@@ -426,6 +527,7 @@ Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_
   }
   if (kTcTiles * npad <= 512)
     for (int k = 1; (long long)k * n_sm * kTcTiles < mtiles; k++) consider(kTcTiles, k * n_sm, 2, groups);
+  if (best.cb == 0) return p;
   p.npad = npad;
   p.mtiles = mtiles;
   p.tiles_big = best.cb;
@@ -436,21 +538,18 @@ Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_
   const int rest = mtiles - p.groups_big * p.tiles_big;
   p.tgroups = p.groups_big + (rest > 0 ? (rest + p.tiles_small - 1) / p.tiles_small : 0);
   p.grid = p.tgroups * p.slices;
-  p.x_stage = (uint32_t)npad * 128u * (x_lo ? 2u : 1u);   // a multiple of 2048 B
+  const Depths dp = pick_depths(p.tiles_big, npad, x_lo);
+  p.x_stage = dp.x_stage;   // a multiple of 2048 B
   p.x_tx = p.x_stage;
-  // raw stages: four when three activation stages still fit, else three (two activation stages
-  // at least)
-  p.sw = 0;
-  for (int sw = kTcMaxSW; sw >= 2 && p.sw == 0; sw--) {
-    const size_t base = tc05_smem(p.tiles_big, sw, 0, p.x_stage);
-    const int sx = base < kTcSmemMax ? (int)std::min<size_t>(kTcMaxSX, (kTcSmemMax - base) / p.x_stage) : 0;
-    if (sx >= 3 || (sw == 3 && sx >= 2) || (sw == 2 && sx >= 2)) {
-      p.sw = sw;
-      p.sx = sx;
-    }
-  }
+  p.sa = dp.sa;
+  p.sw = dp.sw;
+  p.sx = dp.sx;
+  p.kx = dp.kx;
+  // L2 prefetch distance: about kTcBytesInFlight of weights per SM requested ahead, ring included
   if (p.sw == 0) return Tc05Plan{};
-  p.smem = tc05_smem(p.tiles_big, p.sw, p.sx, p.x_stage);
+  p.smem = tc05_smem(p.tiles_big, p.sa, p.sw, p.sx, p.x_stage);
+  const int in_flight = (int)(kTcBytesInFlight / ((size_t)kTcKW * p.tiles_big * kTcTileW));   // W steps
+  p.pf = std::max(0, in_flight - p.sw);
   int cols = 32;
   while (cols < p.tiles_big * npad) cols *= 2;
   p.tmem_cols = cols;
@@ -490,6 +589,9 @@ void tc05_fill_args(const Tc05Plan& p, int has_lo, Tc05Args& a) {
   a.n_out_pad = p.mtiles * 128;
   a.sx = p.sx;
   a.sw = p.sw;
+  a.sa = p.sa;
+  a.pf = p.pf;
+  a.kx = p.kx;
   a.tmem_cols = p.tmem_cols;
   a.x_stage = p.x_stage;
   a.x_tx = p.x_tx;
@@ -501,13 +603,11 @@ cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t
   if (a.has_lo) {
     e = ensure_smem_limit(tc05_q4_kernel<true>, p.smem, smem_set[1]);
     if (e != cudaSuccess) return e;
-    tc05_q4_kernel<true><<<p.grid, kTcThreads, p.smem, s>>>(a);
-  } else {
-    e = ensure_smem_limit(tc05_q4_kernel<false>, p.smem, smem_set[0]);
-    if (e != cudaSuccess) return e;
-    tc05_q4_kernel<false><<<p.grid, kTcThreads, p.smem, s>>>(a);
+    return launch_pdl(tc05_q4_kernel<true>, dim3(p.grid), dim3(kTcThreads), p.smem, s, a);
   }
-  return cudaGetLastError();
+  e = ensure_smem_limit(tc05_q4_kernel<false>, p.smem, smem_set[0]);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tc05_q4_kernel<false>, dim3(p.grid), dim3(kTcThreads), p.smem, s, a);
 }
 
 cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_out, int half, float* y, int ldy,

@@ -9,22 +9,32 @@ namespace dfl {
 
 constexpr unsigned kErrTimeoutTc05 = 4u;  // device error word bit of this kernel's bounded waits
 
-constexpr int kTcWarps = 10;              // copies, MMA issue, 8 dequantising warps (4 of them also the epilogue)
+constexpr int kTcWarps = 11;              // weight copies, MMA issue, 8 dequantising warps (4 of them also the
+                                          // epilogue), activation copies
 constexpr int kTcMaxRows = 160;           // activation rows per call (the MMA's N, padded to 16)
 constexpr int kTcTiles = 3;               // 128-row output tiles per CTA, at most (3 x 160 accumulator columns <= 512)
-constexpr int kTcMaxSW = 4;               // raw 4-bit stages (one 64-input group of a CTA's tiles each), at most
-constexpr int kTcSA = 2;                  // dequantised f16 A stages
+#ifndef DFL_TC_KW
+#define DFL_TC_KW 2
+#endif
+constexpr int kTcKW = DFL_TC_KW;          // 64-input groups per raw-weight copy (and stage)
+constexpr int kTcMaxSW = 8;               // raw 4-bit stages (kTcKW groups of a CTA's tiles each), at most
+constexpr size_t kTcBytesInFlight = 96 * 1024;   // weights requested ahead per SM (ring + L2 prefetch)
+constexpr int kTcMaxSA = 6;               // dequantised f16 A stages, at most
 constexpr int kTcMaxSX = 4;               // activation stages, at most
 constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
 
 struct Tc05Args {
-  CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder: box 64 x npad, 128-byte swizzle
-  CUtensorMap wmap;          // the stored 4-bit matrix as [strip][group][144 words]: box 144 x 1 x 8 (one
-                             // group of a 128-row tile, 4608 B), rows past the matrix read as zero
+  CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder as [k / 64][rows][64]: box
+                             // 64 x npad x kx, 128-byte swizzle (kx groups per copy)
+  CUtensorMap wmap;          // the stored 4-bit matrix as [strip][group][144 words]: box 144 x kTcKW x
+                             // (8 x tiles_big), kTcKW groups of a big CTA's tiles per copy (rows and
+                             // groups past the matrix read as zero);
+  CUtensorMap wmap_small;    // the same with box 144 x kTcKW x (8 x tiles_small)
   const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
-  float* part;               // [slices][npad][n_out_pad] partial tiles (scratch)
+  float* part;               // [slices][n_out_pad / 16][npad][16] partial tiles (scratch): per 16-row
+                             // strip of the stored order, each activation row's 16 outputs
   unsigned* err;
-  int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, sw, tmem_cols;
+  int n_strips, groups, npad, gps, mtiles, has_lo, n_out_pad, sx, sw, sa, pf, kx, tmem_cols;
   // CTA b covers tile group b % tgroups and K slice b / tgroups; the first groups_big tile groups
   // hold tiles_big consecutive 128-row tiles, the others tiles_small (the last possibly fewer)
   int tgroups, tiles_big, groups_big, tiles_small;
@@ -32,7 +42,7 @@ struct Tc05Args {
 };
 
 struct Tc05Plan {
-  int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, sw = 0, tmem_cols = 0;   // npad == 0: no plan
+  int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, sw = 0, sa = 0, pf = 0, kx = 0, tmem_cols = 0;   // npad == 0: no plan
   int tgroups = 0, tiles_big = 0, groups_big = 0, tiles_small = 0;
   uint32_t x_stage = 0, x_tx = 0;
   size_t smem = 0, part_off = 0, scratch = 0;
@@ -44,7 +54,7 @@ Tc05Plan plan_tc05(int n_strips, int groups, int rows, int x_lo, int n_sm);
 // Copies the plan's shape into the kernel arguments (maps, pointers and sizes are the caller's).
 void tc05_fill_args(const Tc05Plan& p, int has_lo, Tc05Args& a);
 
-// The contraction: partial tiles [slices][npad][n_out_pad] in a.part (stored row order).
+// The contraction: partial tiles [slices][n_out_pad / 16][npad][16] in a.part (stored row order).
 cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t s);
 
 // launch_tc05_parts, then the ordered slice reduction into y [rows][ldy] (natural row order of

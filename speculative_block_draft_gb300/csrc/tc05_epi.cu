@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kF32Warps * 32)
   __shared__ float srow[kMaxRows];
   __shared__ LmState sm_lm[kF32Warps * kMaxRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  pdl_launch_dependents();
+  pdl_wait();   // the partial tiles and the row norms' sums of squares come from earlier kernels
   compute_row_scales(a, srow, RP);
   __syncthreads();
   LmState lm[NT][2];
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
   for (int nt = 0; nt < NT; nt++)
 #pragma unroll
     for (int p = 0; p < 2; p++) lm[nt][p] = LmState{-INFINITY, 0.f, 0x7fffffff};
-  const size_t slice_stride = (size_t)npad * n_out_pad;
+  const size_t slice_stride = (size_t)npad * n_out_pad;   // part[slice][strip][row][16]
   for (int sl = blockIdx.x * kF32Warps + warp; sl < a.n_strips; sl += gridDim.x * kF32Warps) {
     const int strip = a.strip0 + sl;
     float y[NT][4];
@@ -39,7 +41,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
         const int c = nt * 8 + 2 * t + p;
         float y0 = 0.f, y1 = 0.f;
         if (c < a.R) {
-          const float* src = part + (size_t)(row_base + map_row(a.xmap, c)) * n_out_pad + strip * 16 + g;
+          const float* src = part + ((size_t)strip * npad + row_base + map_row(a.xmap, c)) * 16 + g;
           for (int s = 0; s < slices; s++) {
             y0 += __ldcg(src + s * slice_stride);
             y1 += __ldcg(src + s * slice_stride + 8);
@@ -59,14 +61,14 @@ template <int EPI>
 cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad, int n_out_pad,
                        int grid, cudaStream_t s) {
   const dim3 g(grid, ch.n);
+  const dim3 b(kF32Warps * 32);
   switch (nt) {
-    case 1: tc05_epi_kernel<1, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
-    case 2: tc05_epi_kernel<2, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
-    case 3: tc05_epi_kernel<3, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
-    case 4: tc05_epi_kernel<4, EPI><<<g, kF32Warps * 32, 0, s>>>(ch, part, slices, npad, n_out_pad); break;
+    case 1: return launch_pdl(tc05_epi_kernel<1, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
+    case 2: return launch_pdl(tc05_epi_kernel<2, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
+    case 3: return launch_pdl(tc05_epi_kernel<3, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
+    case 4: return launch_pdl(tc05_epi_kernel<4, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
