@@ -641,10 +641,11 @@ int run_tc05_epi_chunks(dflash_handle* h, const GemvCall* calls, const int* r0, 
   }
   ch.n = n;
   if (grid_out) *grid_out = grid;
-  h->launches++;
+  h->launches += 2;   // the rows' norm scales, then the epilogue
   return status_of(launch_tc05_epilogue(calls[0].epi, nt, ch,
                                         reinterpret_cast<const float*>(h->tc05_scratch + p.part_off), p.slices,
-                                        p.npad, p.mtiles * 128, grid, s));
+                                        p.npad, p.mtiles * 128, grid,
+                                        reinterpret_cast<float*>(h->tc05_scratch + p.srow_off), s));
 }
 
 // The epilogue of one chunk of a projection (the context projection's chunks).

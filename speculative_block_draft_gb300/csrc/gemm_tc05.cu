@@ -6,8 +6,8 @@
 // CTA share every activation tile: it is loaded once per 64-input group for all of them, which
 // divides the activation traffic from L2 and the number of activation loads in flight by the
 // tile count.
-//  * warp 0 streams the CTA's 4-bit (strip, group) tiles, two 64-input groups of all its tiles per
-//    3-D tensor copy, and keeps the following ones coming into L2 with tensor prefetches; warp 10
+//  * warp 0 streams the CTA's 4-bit (strip, group) tiles, kTcKW 64-input groups of all its tiles
+//    per 3-D tensor copy, and keeps the following ones coming into L2 with tensor prefetches; warp 10
 //    streams the activation rows (f16, plus the f16 remainder where given), one or two groups per
 //    3-D tensor copy in the 128-byte swizzle;
 //  * warps 2-9 (strip w of every tile) dequantise the codes to f16 weights, w = s q + b with one
@@ -521,7 +521,7 @@ Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_
     for (int s = 1; s <= std::max(1, std::min(groups / 4, 64)); s++) {
       const int gps = (groups + s - 1) / s;
       if (s > 1 && (groups + gps - 1) / gps != s) continue;   // same slicing as a smaller s
-      if (s > 1 && (long long)tg * s > 3LL * n_sm) break;   // beyond ~3 waves more slices only add work
+      if (s > 1 && (long long)tg * s > n_sm) break;   // a K split fills at most one wave of CTAs
       consider(c, tg, c, gps);
     }
   }
@@ -554,7 +554,8 @@ Tc05Plan plan_tc05_uncached(int n_strips, int groups, int npad, int x_lo, int n_
   while (cols < p.tiles_big * npad) cols *= 2;
   p.tmem_cols = cols;
   p.part_off = 0;
-  p.scratch = (size_t)p.slices * npad * mtiles * 128 * 4;
+  p.srow_off = (size_t)p.slices * npad * mtiles * 128 * 4;
+  p.scratch = p.srow_off + (size_t)kTcMaxChunks * kMaxRows * 4;
   return p;
 }
 

@@ -14,7 +14,7 @@ constexpr int kTcWarps = 11;              // weight copies, MMA issue, 8 dequant
 constexpr int kTcMaxRows = 160;           // activation rows per call (the MMA's N, padded to 16)
 constexpr int kTcTiles = 3;               // 128-row output tiles per CTA, at most (3 x 160 accumulator columns <= 512)
 #ifndef DFL_TC_KW
-#define DFL_TC_KW 2
+#define DFL_TC_KW 1
 #endif
 constexpr int kTcKW = DFL_TC_KW;          // 64-input groups per raw-weight copy (and stage)
 constexpr int kTcMaxSW = 8;               // raw 4-bit stages (kTcKW groups of a CTA's tiles each), at most
@@ -45,7 +45,7 @@ struct Tc05Plan {
   int npad = 0, mtiles = 0, slices = 0, gps = 0, grid = 0, sx = 0, sw = 0, sa = 0, pf = 0, kx = 0, tmem_cols = 0;   // npad == 0: no plan
   int tgroups = 0, tiles_big = 0, groups_big = 0, tiles_small = 0;
   uint32_t x_stage = 0, x_tx = 0;
-  size_t smem = 0, part_off = 0, scratch = 0;
+  size_t smem = 0, part_off = 0, srow_off = 0, scratch = 0;   // scratch: partial tiles, then row scales
 };
 
 // The launch shape with the shortest modelled time: tiles per CTA, K slices, ring depths.
@@ -77,8 +77,9 @@ struct Tc05EpiChunks {
   int row_base[kTcMaxChunks];
   int n;
 };
+// srow: kTcMaxChunks x kMaxRows floats of scratch for the rows' norm scales.
 cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
-                                 int n_out_pad, int grid, cudaStream_t s);
+                                 int n_out_pad, int grid, float* srow, cudaStream_t s);
 
 // ---- skinny projections of the draft round on tcgen05 (proj_tc05.cu) ---------------------------
 constexpr unsigned kErrTimeoutProj = 8u;  // device error word bit of its bounded waits

@@ -1,6 +1,7 @@
 // Epilogues of the round's projections when they run on the many-row tcgen05 contraction. The K
 // slices' partial tiles are summed in slice order and handed, one 16-row strip per warp, to the
-// same strip epilogues the skinny GEMV fuses: context rows x ctx_norm with sums of squares,
+// same strip epilogues the skinny GEMV fuses (the rows' norm scales computed once per projection by
+// a one-CTA-per-chunk kernel before it): context rows x ctx_norm with sums of squares,
 // row-norm scale, Q/K/V split, residual with next norm input and sums of squares, gated FFN, and
 // vocab states. One launch covers every row chunk of a projection (grid.y = chunk); row c of
 // chunk j is contraction row row_base[j] + map_row(xmap_j, c).
@@ -11,19 +12,30 @@ namespace dfl {
 
 namespace {
 
+// The rows' norm scales of every chunk, once per projection (a CTA per chunk), instead of in each
+// of the epilogue's CTAs: they sum hundreds of per-strip partials per row.
+__global__ void __launch_bounds__(kF32Warps * 32)
+    tc05_rowscale_kernel(const __grid_constant__ Tc05EpiChunks ch, float* __restrict__ srow_out) {
+  __shared__ float srow[kMaxRows];
+  pdl_launch_dependents();
+  pdl_wait();   // the sums of squares come from earlier kernels
+  compute_row_scales(ch.a[blockIdx.x], srow, kMaxRows);
+  __syncthreads();
+  if (threadIdx.x < kMaxRows) srow_out[blockIdx.x * kMaxRows + threadIdx.x] = srow[threadIdx.x];
+}
+
 template <int NT, int EPI>
 __global__ void __launch_bounds__(kF32Warps * 32)
     tc05_epi_kernel(const __grid_constant__ Tc05EpiChunks ch, const float* __restrict__ part, int slices, int npad,
-                    int n_out_pad) {
-  constexpr int RP = NT * 8;
+                    int n_out_pad, const float* __restrict__ srow_in) {
   const GemvArgs& a = ch.a[blockIdx.y];   // this CTA's row chunk
   const int row_base = ch.row_base[blockIdx.y];
   __shared__ float srow[kMaxRows];
   __shared__ LmState sm_lm[kF32Warps * kMaxRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   pdl_launch_dependents();
-  pdl_wait();   // the partial tiles and the row norms' sums of squares come from earlier kernels
-  compute_row_scales(a, srow, RP);
+  pdl_wait();   // the partial tiles and the row scales come from earlier kernels
+  if (threadIdx.x < kMaxRows) srow[threadIdx.x] = srow_in[blockIdx.y * kMaxRows + threadIdx.x];
   __syncthreads();
   LmState lm[NT][2];
 #pragma unroll
@@ -57,16 +69,115 @@ __global__ void __launch_bounds__(kF32Warps * 32)
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
 }
 
+// The LM head's epilogue on the contraction's partial tiles, for every row chunk in one pass: a CTA
+// takes a range of strips (16 vocab entries each) and a thread one (chunk, row) pair (two threads
+// per pair, alternate strips, when there are at most 128 pairs), so that a warp reads whole 64-byte
+// row pieces of a strip, consecutive in memory; four strips' loads are in flight per thread. Each
+// thread folds its logits (partial sums over the K slices, times the row's norm scale; written out
+// when asked for) into a (max, sum, index) state; the CTA's state per row goes to the chunk's slice
+// of vocab states, merged later per row by lm_reduce_kernel. Same arithmetic per logit as the
+// generic epilogue; ties keep the lowest index.
+constexpr int kLmThreads = 256;
+__global__ void __launch_bounds__(kLmThreads)
+    tc05_lm_epi_kernel(const __grid_constant__ Tc05EpiChunks ch, const float* __restrict__ part, int slices, int npad,
+                       int n_out_pad, const float* __restrict__ srow_in, int n_pairs, int n_split) {
+  __shared__ LmState sm[kLmThreads];
+  pdl_launch_dependents();
+  pdl_wait();   // the partial tiles and the row scales come from earlier kernels
+  const int t = threadIdx.x;
+  const int q = t % n_pairs, sp = t / n_pairs;   // (chunk, row) pair and strip parity of this thread
+  const bool active = t < n_pairs * n_split;
+  int j = 0, c = q;
+  while (j + 1 < ch.n && c >= ch.a[j].R) {
+    c -= ch.a[j].R;
+    j++;
+  }
+  const GemvArgs& a = ch.a[j];
+  const EpiArgs& e = a.e;
+  const int row = ch.row_base[j] + map_row(a.xmap, c);
+  const float sc = active ? srow_in[j * kMaxRows + c] : 0.f;
+  const size_t slice_stride = (size_t)npad * n_out_pad;
+  const int per = (a.n_strips + gridDim.x - 1) / gridDim.x;
+  const int s_beg = blockIdx.x * per, s_end = min(a.n_strips, s_beg + per);
+  LmState st{-INFINITY, 0.f, 0x7fffffff};
+  float* lrow = e.logits ? e.logits + (size_t)c * (e.logit_row_stride ? e.logit_row_stride : e.vocab) : nullptr;
+  if (active) {
+    constexpr int U = 4;
+    for (int s0 = s_beg + sp; s0 < s_end; s0 += U * n_split) {
+      float4 v[U][4];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int sl = s0 + u * n_split;
+        const float4* src = reinterpret_cast<const float4*>(part + ((size_t)(a.strip0 + sl) * npad + row) * 16);
+#pragma unroll
+        for (int w = 0; w < 4; w++) v[u][w] = sl < s_end ? __ldcg(src + w) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int z = 1; z < slices; z++) {
+          if (sl >= s_end) break;
+#pragma unroll
+          for (int w = 0; w < 4; w++) {
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) +
+                                                                     z * slice_stride) + w);
+            v[u][w].x += o.x;
+            v[u][w].y += o.y;
+            v[u][w].z += o.z;
+            v[u][w].w += o.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int sl = s0 + u * n_split;
+        if (sl >= s_end) break;
+        const float y[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w,
+                             v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w, v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
+        const int n0 = (a.strip0 + sl) * 16 - e.row_base;
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+          const int n = n0 + k;
+          if (n < 0 || n >= e.n_rows) continue;
+          const float l = y[k] * sc;
+          if (lrow) lrow[n] = l;
+          lm_push(st, l, n);
+        }
+      }
+    }
+  }
+  // merge the strip parities of a pair, then write the CTA's state per row
+  sm[t] = st;
+  __syncthreads();
+  if (active && sp == 0) {
+    for (int o = 1; o < n_split; o++) lm_merge(st, sm[t + o * n_pairs]);
+    float* dst = e.lm_part + ((size_t)blockIdx.x * kMaxRows + c) * 3;
+    dst[0] = st.m;
+    dst[1] = st.s;
+    dst[2] = __int_as_float(st.i);
+  }
+}
+
 template <int EPI>
 cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad, int n_out_pad,
-                       int grid, cudaStream_t s) {
+                       int grid, float* srow, cudaStream_t s) {
   const dim3 g(grid, ch.n);
   const dim3 b(kF32Warps * 32);
+  const cudaError_t e = launch_pdl(tc05_rowscale_kernel, dim3(ch.n), b, 0, s, ch, srow);
+  if (e != cudaSuccess) return e;
+  if (EPI == EPI_LMHEAD) {
+    bool plain = true;   // the dedicated kernel: no logit bias, one output range for every chunk
+    int pairs = 0;
+    for (int j = 0; j < ch.n; j++) {
+      plain = plain && !ch.a[j].e.logit_bias && ch.a[j].strip0 == ch.a[0].strip0 &&
+              ch.a[j].n_strips == ch.a[0].n_strips && ch.a[j].R <= kMaxRows;
+      pairs += ch.a[j].R;
+    }
+    if (plain && pairs >= 1 && pairs <= kLmThreads)
+      return launch_pdl(tc05_lm_epi_kernel, dim3(grid), dim3(kLmThreads), 0, s, ch, part, slices, npad, n_out_pad,
+                        static_cast<const float*>(srow), pairs, kLmThreads / pairs > 1 ? 2 : 1);
+  }
   switch (nt) {
-    case 1: return launch_pdl(tc05_epi_kernel<1, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
-    case 2: return launch_pdl(tc05_epi_kernel<2, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
-    case 3: return launch_pdl(tc05_epi_kernel<3, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
-    case 4: return launch_pdl(tc05_epi_kernel<4, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad);
+    case 1: return launch_pdl(tc05_epi_kernel<1, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
+    case 2: return launch_pdl(tc05_epi_kernel<2, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
+    case 3: return launch_pdl(tc05_epi_kernel<3, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
+    case 4: return launch_pdl(tc05_epi_kernel<4, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -74,14 +185,14 @@ cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int s
 }  // namespace
 
 cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
-                                 int n_out_pad, int grid, cudaStream_t s) {
+                                 int n_out_pad, int grid, float* srow, cudaStream_t s) {
   if (ch.n < 1 || ch.n > kTcMaxChunks) return cudaErrorInvalidValue;
   switch (epi) {
-    case EPI_CTX: return launch_epi<EPI_CTX>(nt, ch, part, slices, npad, n_out_pad, grid, s);
-    case EPI_QKV: return launch_epi<EPI_QKV>(nt, ch, part, slices, npad, n_out_pad, grid, s);
-    case EPI_RESID: return launch_epi<EPI_RESID>(nt, ch, part, slices, npad, n_out_pad, grid, s);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, ch, part, slices, npad, n_out_pad, grid, s);
-    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, ch, part, slices, npad, n_out_pad, grid, s);
+    case EPI_CTX: return launch_epi<EPI_CTX>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
+    case EPI_QKV: return launch_epi<EPI_QKV>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
+    case EPI_RESID: return launch_epi<EPI_RESID>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
+    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
     default: return cudaErrorInvalidValue;
   }
 }
