@@ -432,12 +432,14 @@ int make_cache_map(dflash_handle* h, void* base, CUtensorMap* map) {
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return DFLASH_ECUDA;
   const dflash_config& c = h->cfg;
-  const cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)h->cap,
+  // [plane][cap][head_dim] viewed as [plane][head_dim / 64][cap][64]: one copy brings a 64-key tile
+  // with every 64-column part of the head (each a 64-row x 128-byte swizzled sub-tile)
+  const cuuint64_t dims[4] = {64, (cuuint64_t)h->cap, (cuuint64_t)(c.head_dim / 64),
                               (cuuint64_t)h->L * c.max_batch * c.n_kv_heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)h->cap * c.head_dim * 2};
-  const cuuint32_t box[3] = {64, 64, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+  const cuuint64_t strides[3] = {(cuuint64_t)c.head_dim * 2, 128, (cuuint64_t)h->cap * c.head_dim * 2};
+  const cuuint32_t box[4] = {64, 64, (cuuint32_t)(c.head_dim / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;

@@ -6,7 +6,8 @@
 //  * The CTA's query rows are the GQA group x gamma rows of one KV head (<= 64 rows, one 16-row
 //    m-tile per warp), held in shared memory.
 //  * Context K/V tiles of 64 rows x head_dim come from the per-layer ring cache
-//    [slot][Hkv][cap][hd] through 3-D TMA copies with the 128-byte swizzle (two stages), so
+//    [slot][Hkv][cap][hd] through 4-D TMA copies (one for K, one for V, every 64-column part of
+//    the head as its own sub-tile) with the 128-byte swizzle (two stages), so
 //    ldmatrix reads are bank-conflict free. A tile never crosses the ring's wrap point; rows past
 //    the ring end read as zeros and are masked.
 //  * The last split also takes the 16-row block tile (K_d, V_d of this block, not cached).
@@ -189,11 +190,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_tc_kernel(const __grid_c
     uint8_t* ks = stage_s + (i & 1) * 2 * NSUB * kSub;
     uint8_t* vs = ks + NSUB * kSub;
     mbar_arrive_expect_tx(bar, 2 * NSUB * kSub);
-#pragma unroll
-    for (int c = 0; c < NSUB; c++) {
-      tma_load_3d(smem_u32(ks + c * kSub), &kmap, c * 64, slot0, plane, bar);
-      tma_load_3d(smem_u32(vs + c * kSub), &vmap, c * 64, slot0, plane, bar);
-    }
+    // one copy each for K and V: all NSUB 64-column sub-tiles of the 64 keys (a copy has a fixed
+    // cost of its own in the copy engine, so fewer, larger copies keep the tiles coming)
+    tma_load_4d(smem_u32(ks), &kmap, 0, slot0, 0, plane, bar);
+    tma_load_4d(smem_u32(vs), &vmap, 0, slot0, 0, plane, bar);
   };
 
   if (threadIdx.x == 0) {
