@@ -63,6 +63,7 @@ struct dflash_handle {
   int ticket_count = 0, lm_grid_max = 0, att_pairs_max = 0;
   // many-row draft calls on the tcgen05 contraction (config large_batch_tc05)
   int tc05_on = 0, tc05_rows = 0;
+  int xw_rows = 0;   // context rows per input plane of xw (and rows of ssq_ctx)
   uint8_t* tc05_scratch = nullptr;
   size_t tc05_scratch_bytes = 0;
   void* tc05_taps = nullptr;    // [kTcMaxRows][n_taps * H] f16: context taps converted for TMA
@@ -194,6 +195,27 @@ bool valid_config(const dflash_config* c) {
 }
 
 // Lay out the workspace; with base == nullptr only sizes are computed.
+#ifndef DFL_ATTN_TILES_PER_SPLIT
+#define DFL_ATTN_TILES_PER_SPLIT 2
+#endif
+
+// Which projections also read the f16 remainder of their input. Rounding the inputs of the
+// projections that feed the attention scores (Q, K, V of the block and of the context rows) is
+// amplified by the softmax; with those and gate-up covered, the rms logit error of the 4-bit
+// 5120-wide drafter drops by 30% at no measured cost. out_proj and the LM head do not need it.
+#ifndef DFL_LO_MASK
+#define DFL_LO_MASK 11
+#endif
+enum { LO_QKV = 1, LO_GU = 2, LO_LM = 4, LO_CTXKV = 8, LO_OUTPROJ = 16 };
+long long lo_if(int bit, size_t off) { return (DFL_LO_MASK & bit) ? (long long)off : 0; }
+
+// The grouped context K/V contraction of `rows` context rows: the K/V strips of every layer's
+// Q/K/V matrix, planned as one layer's problem on its share of the SMs.
+Tc05Plan plan_kv_tc05(const dflash_handle* h, int rows) {
+  return plan_tc05((2 * h->kvd) / 16, h->qkv[0].groups, rows, (DFL_LO_MASK & LO_CTXKV) ? 1 : 0,
+                   std::max(1, h->n_sm / std::max(1, h->L)));
+}
+
 size_t carve(dflash_handle* h, uint8_t* base) {
   const dflash_config& c = h->cfg;
   Carver cv{base};
@@ -242,8 +264,13 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->tokrow = cv.take<float>((size_t)c.max_batch * h->d * 4);
   h->ssq_ld = (h->d + 15) / 16;
   h->ssq = cv.take<float>((size_t)R * h->ssq_ld * 4);
-  h->ssq_ctx = cv.take<float>((size_t)kMaxCtxChunk * h->ssq_ld * 2 * 4);
-  h->xw = cv.take<void>((size_t)h->L * kMaxCtxChunk * h->d * ab * 2);
+  // a context call on the tcgen05 contraction projects up to kTcMaxRows rows' context K/V of every
+  // layer in one grouped launch, from one input plane per layer
+  const bool tc_possible = c.large_batch_tc05 && h->fmt == FMT_Q4 && !h->act_f32 && h->d == h->H && !c.markov_rank &&
+                           std::min(c.max_batch * h->G, kTcMaxRows) > kMaxRows;
+  h->xw_rows = tc_possible ? kTcMaxRows : kMaxCtxChunk;
+  h->ssq_ctx = cv.take<float>((size_t)h->xw_rows * h->ssq_ld * 2 * 4);
+  h->xw = cv.take<void>((size_t)h->L * h->xw_rows * h->d * ab * 2);
   if (c.markov_rank) {
     h->mk_base = cv.take<float>((size_t)c.max_batch * h->nd * h->V * 4);
     h->mk_x = cv.take<void>((size_t)c.max_batch * c.markov_rank * ab * 2);
@@ -290,8 +317,6 @@ size_t carve(dflash_handle* h, uint8_t* base) {
   h->tickets = cv.take<int>((size_t)tk * 4);
   // vocab states per CTA and row; a many-row draft call on the tcgen05 contraction keeps one slice
   // per row chunk
-  const bool tc_possible = c.large_batch_tc05 && h->fmt == FMT_Q4 && !h->act_f32 && h->d == h->H && !c.markov_rank &&
-                           std::min(c.max_batch * h->G, kTcMaxRows) > kMaxRows;
   const int lm_slices = tc_possible ? kTcMaxChunks : 1;
   h->lm_part = cv.take<float>((size_t)lmg * kMaxRows * 3 * 4 * lm_slices);
   h->lm_strip = cv.take<float>((size_t)tk * kMaxRows * 3 * 4);
@@ -320,8 +345,11 @@ size_t carve(dflash_handle* h, uint8_t* base) {
     need(h->down[0], 0);
     need(h->lm, 1);
     for (int r = kMaxRows + 1; r <= kTcMaxRows + 15; r += 16) {   // context rows, in chunks of up to 160
-      const Tc05Plan pc = plan_tc05(h->wc.n_strips, h->wc.groups, std::min(r, kTcMaxRows), 0, h->n_sm);
+      const int rr = std::min(r, kTcMaxRows);
+      const Tc05Plan pc = plan_tc05(h->wc.n_strips, h->wc.groups, rr, 0, h->n_sm);
       sc = std::max(sc, pc.scratch);
+      const Tc05Plan pk = plan_kv_tc05(h, rr);   // every layer's context K/V, grouped
+      sc = std::max(sc, (size_t)h->L * pk.srow_off + (pk.scratch - pk.srow_off));
     }
     h->tc05_on = sc > 0;
     h->tc05_scratch_bytes = sc;
@@ -396,33 +424,40 @@ int make_rows_map(const void* base, int k, int rows, int ld, int box_rows, CUten
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
 }
 
-// Activation rows (f16 [rows][ld]) as a 3-D map [k / 64][rows][64]: box 64 x box_rows x kx with the
-// 128-byte swizzle, i.e. kx consecutive 64-input groups per copy, each a K-major tile of box_rows
-// rows of 128 B (rows past `rows` read as zero).
-int make_rows_map_groups(const void* base, int k, int rows, int ld, int box_rows, int kx, CUtensorMap* map) {
+// Activation rows (f16 [rows][ld], `layers` planes layer_stride bytes apart) as a 4-D map
+// [layer][k / 64][rows][64]: box 64 x box_rows x kx x 1 with the 128-byte swizzle, i.e. kx
+// consecutive 64-input groups of one plane per copy, each a K-major tile of box_rows rows of 128 B
+// (rows past `rows` read as zero).
+int make_rows_map_groups(const void* base, int k, int rows, int ld, int box_rows, int kx, int layers,
+                         size_t layer_stride, CUtensorMap* map) {
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return DFLASH_ECUDA;
-  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(k / 64)};
-  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)kx};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(k / 64), (cuuint64_t)layers};
+  const cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128,
+                                 (cuuint64_t)(layers > 1 ? layer_stride : round_up((size_t)rows * ld * 2, 16))};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)kx, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
 }
 
-// A stored 4-bit matrix ([strip][group] tiles of 576 B) as a 3-D map of 32-bit words
-// [n_strips][groups][144], box 144 x kw x (8 * tiles): kw consecutive groups of `tiles`
-// consecutive 128-row output tiles per copy; strips and groups past the matrix read as zero.
-int make_q4_tile_map(const PackedMat& m, int tiles, int kw, CUtensorMap* map) {
+// A stored 4-bit matrix ([strip][group] tiles of 576 B; `layers` matrices layer_stride bytes apart)
+// as a 4-D map of 32-bit words [layer][n_strips][groups][144], box 144 x kw x (8 * tiles) x 1: kw
+// consecutive groups of `tiles` consecutive 128-row output tiles of one matrix per copy; strips
+// and groups past the matrix read as zero.
+int make_q4_tile_map(const PackedMat& m, int tiles, int kw, int layers, size_t layer_stride, CUtensorMap* map) {
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return DFLASH_ECUDA;
-  const cuuint64_t dims[3] = {(cuuint64_t)(kQ4GroupBytes / 4), (cuuint64_t)m.groups, (cuuint64_t)m.n_strips};
-  const cuuint64_t strides[2] = {(cuuint64_t)kQ4GroupBytes, (cuuint64_t)m.groups * kQ4GroupBytes};
-  const cuuint32_t box[3] = {kQ4GroupBytes / 4, (cuuint32_t)kw, (cuuint32_t)(8 * tiles)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(m.w), dims, strides, box, estr,
+  const size_t mat_bytes = (size_t)m.n_strips * m.groups * kQ4GroupBytes;
+  const cuuint64_t dims[4] = {(cuuint64_t)(kQ4GroupBytes / 4), (cuuint64_t)m.groups, (cuuint64_t)m.n_strips,
+                              (cuuint64_t)layers};
+  const cuuint64_t strides[3] = {(cuuint64_t)kQ4GroupBytes, (cuuint64_t)m.groups * kQ4GroupBytes,
+                                 (cuuint64_t)(layers > 1 ? layer_stride : round_up(mat_bytes, 16))};
+  const cuuint32_t box[4] = {kQ4GroupBytes / 4, (cuuint32_t)kw, (cuuint32_t)(8 * tiles), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<uint8_t*>(m.w), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_ECUDA;
@@ -502,20 +537,8 @@ void probe_end(dflash_handle* h, int kind, cudaStream_t s) {
 }
 
 size_t xn_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->r_blk * h->d; }
-size_t xw_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->L * kMaxCtxChunk * h->d; }
+size_t xw_lo(const dflash_handle* h) { return h->act_f32 ? 0 : (size_t)h->L * h->xw_rows * h->d; }
 
-// Which projections also read the f16 remainder of their input. Rounding the inputs of the
-// projections that feed the attention scores (Q, K, V of the block and of the context rows) is
-// amplified by the softmax; with those and gate-up covered, the rms logit error of the 4-bit
-// 5120-wide drafter drops by 30% at no measured cost. out_proj and the LM head do not need it.
-#ifndef DFL_ATTN_TILES_PER_SPLIT
-#define DFL_ATTN_TILES_PER_SPLIT 2
-#endif
-#ifndef DFL_LO_MASK
-#define DFL_LO_MASK 11
-#endif
-enum { LO_QKV = 1, LO_GU = 2, LO_LM = 4, LO_CTXKV = 8, LO_OUTPROJ = 16 };
-long long lo_if(int bit, size_t off) { return (DFL_LO_MASK & bit) ? (long long)off : 0; }
 
 int run_gemv(dflash_handle* h, GemvCall& c, cudaStream_t s, GemvPlan* plan_out = nullptr) {
   const PackedMat& m = *c.m;
@@ -576,10 +599,10 @@ int run_tc05_parts(dflash_handle* h, const PackedMat& m, int rows, const void* x
   if (p.npad == 0 || p.scratch > h->tc05_scratch_bytes) return DFLASH_EINVAL;
   const void* xl = lo_off ? static_cast<const void*>(static_cast<const __half*>(x) + lo_off) : nullptr;
   Tc05Args a{};
-  if (make_rows_map_groups(x, m.k, rows, ldx, p.npad, p.kx, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (xl && make_rows_map_groups(xl, m.k, rows, ldx, p.npad, p.kx, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (make_q4_tile_map(m, p.tiles_big, kTcKW, &a.wmap) != DFLASH_OK ||
-      make_q4_tile_map(m, p.tiles_small, kTcKW, &a.wmap_small) != DFLASH_OK)
+  if (make_rows_map_groups(x, m.k, rows, ldx, p.npad, p.kx, 1, 0, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (xl && make_rows_map_groups(xl, m.k, rows, ldx, p.npad, p.kx, 1, 0, &a.xlmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (make_q4_tile_map(m, p.tiles_big, kTcKW, 1, 0, &a.wmap) != DFLASH_OK ||
+      make_q4_tile_map(m, p.tiles_small, kTcKW, 1, 0, &a.wmap_small) != DFLASH_OK)
     return DFLASH_ECUDA;
   a.w = m.w;
   a.part = reinterpret_cast<float*>(h->tc05_scratch + p.part_off);
@@ -598,8 +621,8 @@ GemvArgs tc05_epi_args(dflash_handle* h, const GemvCall& c, int chunk, int grid)
   const PackedMat& m = *c.m;
   GemvArgs a{};
   a.w = m.w;
-  a.strip0 = 0;
-  a.n_strips = m.n_strips;
+  a.strip0 = c.epi == EPI_KV ? c.strip0 : 0;   // the context K/V strips of a Q/K/V matrix
+  a.n_strips = c.epi == EPI_KV ? c.n_strips : m.n_strips;
   a.k = m.k;
   a.groups = m.groups;
   a.n_slices = 1;
@@ -623,7 +646,8 @@ GemvArgs tc05_epi_args(dflash_handle* h, const GemvCall& c, int chunk, int grid)
 }
 
 int tc05_epi_grid(const dflash_handle* h, const GemvCall& c) {
-  const int grid = (c.m->n_strips + kF32Warps - 1) / kF32Warps;
+  const int strips = c.epi == EPI_KV ? c.n_strips : c.m->n_strips;
+  const int grid = (strips + kF32Warps - 1) / kF32Warps;
   return std::max(1, std::min(grid, c.epi == EPI_LMHEAD ? h->lm_grid_max : 4 * h->n_sm));
 }
 
@@ -647,13 +671,63 @@ int run_tc05_epi_chunks(dflash_handle* h, const GemvCall* calls, const int* r0, 
   return status_of(launch_tc05_epilogue(calls[0].epi, nt, ch,
                                         reinterpret_cast<const float*>(h->tc05_scratch + p.part_off), p.slices,
                                         p.npad, p.mtiles * 128, grid,
-                                        reinterpret_cast<float*>(h->tc05_scratch + p.srow_off), s));
+                                        reinterpret_cast<float*>(h->tc05_scratch + p.srow_off), 1, 0, s));
 }
 
 // The epilogue of one chunk of a projection (the context projection's chunks).
 int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row_base, cudaStream_t s) {
   if (c.R <= 0) return DFLASH_OK;
   return run_tc05_epi_chunks(h, &c, &row_base, 1, p, s);
+}
+
+// The context K/V of `rows` context rows for every layer, on the tcgen05 contraction: one grouped
+// launch over the K/V strips of each layer's Q/K/V matrix, reading layer i's input plane of xw
+// (x * ctx_norm * attn_norm_i, f16 and its remainder), then one epilogue launch (grid.z = layer)
+// that scales by the rows' norm and appends to each layer's ring cache. calls[j] describes chunk j
+// (contraction rows r0[j] ...) as for the GEMV.
+int run_tc05_kv(dflash_handle* h, int rows, const GemvCall* calls, const int* r0, int n, cudaStream_t s) {
+  const int L = h->L;
+  const Tc05Plan p = plan_kv_tc05(h, rows);
+  if (p.npad == 0 || n < 1 || n > kTcMaxChunks) return DFLASH_EINVAL;
+  const size_t layer_bytes = p.srow_off;   // one layer's partial tiles
+  if ((size_t)L * layer_bytes + (p.scratch - p.srow_off) > h->tc05_scratch_bytes) return DFLASH_EINVAL;
+  const PackedMat& m = h->qkv[0];
+  const int lo = (DFL_LO_MASK & LO_CTXKV) ? 1 : 0;
+  const size_t plane = (size_t)h->xw_rows * h->d * 2;   // bytes between the layers' input planes
+  const size_t w_stride = L > 1 ? (size_t)(h->qkv[1].w - h->qkv[0].w) : 0;
+  Tc05Args a{};
+  if (make_rows_map_groups(h->xw, h->d, rows, h->d, p.npad, p.kx, L, plane, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (lo && make_rows_map_groups(static_cast<const __half*>(h->xw) + xw_lo(h), h->d, rows, h->d, p.npad, p.kx, L,
+                                 plane, &a.xlmap) != DFLASH_OK)
+    return DFLASH_ECUDA;
+  if (make_q4_tile_map(m, p.tiles_big, kTcKW, L, w_stride, &a.wmap) != DFLASH_OK ||
+      make_q4_tile_map(m, p.tiles_small, kTcKW, L, w_stride, &a.wmap_small) != DFLASH_OK)
+    return DFLASH_ECUDA;
+  a.w = m.w;
+  a.part = reinterpret_cast<float*>(h->tc05_scratch);
+  a.err = h->err;
+  a.n_strips = (2 * h->kvd) / 16;
+  a.groups = m.groups;
+  tc05_fill_args(p, lo, a);
+  a.n_layers = L;
+  a.w_strip0 = h->qd / 16;
+  a.part_layer_stride = layer_bytes / 4;
+  h->launches++;
+  int st = status_of(launch_tc05_parts(a, p, s));
+  if (st) return st;
+  static thread_local Tc05EpiChunks ch;
+  const int grid = tc05_epi_grid(h, calls[0]);
+  int nt = 1;
+  for (int j = 0; j < n; j++) {
+    ch.a[j] = tc05_epi_args(h, calls[j], j, grid);
+    ch.row_base[j] = r0[j];
+    nt = std::max(nt, nt_for(calls[j].R));
+  }
+  ch.n = n;
+  h->launches += 2;   // the rows' norm scales, then the epilogue
+  return status_of(launch_tc05_epilogue(EPI_KV, nt, ch, a.part, p.slices, p.npad, p.mtiles * 128, grid,
+                                        reinterpret_cast<float*>(h->tc05_scratch + (size_t)L * layer_bytes), L,
+                                        layer_bytes / 4, s));
 }
 
 // One projection of a draft call of at most kProjMaxRows block rows on the tcgen05 projection
@@ -853,10 +927,15 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   const bool tc = h->tc05_on && total > kMaxCtxChunk;
   Tc05Plan wcp{};
   int64_t tc_row0 = 0;
+  int tc_rows = 0;
+  GemvCall kv_calls[kTcMaxChunks];   // the tcgen05 block's context K/V epilogues, one per 32-row chunk
+  int kv_r0[kTcMaxChunks], n_kv = 0;
   while (row < total) {
     if (tc && (row == 0 || row - tc_row0 >= kTcMaxRows)) {
       tc_row0 = row;
       const int rows = (int)std::min<int64_t>(kTcMaxRows, total - row);
+      tc_rows = rows;
+      n_kv = 0;
       h->launches++;
       int st = status_of(launch_bf16_to_f16(tp + (size_t)row * h->mH * ab, (long long)rows * h->mH, h->tc05_taps, s));
       if (!st) st = run_tc05_parts(h, h->wc, rows, h->tc05_taps, h->mH, 0, s, &wcp);
@@ -886,13 +965,15 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.ldo = h->d;
     c1.e.ctx_norm = h->ctx_norm;
     // tensor-core path: one row x * ctx_norm, the K/V launch applies attn_norm_i to its input;
-    // CUDA-core path: one input row per layer
-    c1.e.attn_norms = h->act_f32 ? h->attn_norm : nullptr;
+    // CUDA-core path and the tcgen05 block: one input row per layer (x * ctx_norm * attn_norm_i),
+    // the block's rows at their offset in it
+    const size_t blk = tc ? (size_t)(row - tc_row0) : 0;
+    c1.e.attn_norms = (h->act_f32 || tc) ? h->attn_norm : nullptr;
     c1.e.n_layers = h->L;
-    c1.e.xw = h->xw;
-    c1.e.xw_rows = kMaxCtxChunk;
+    c1.e.xw = static_cast<uint8_t*>(h->xw) + blk * h->d * ab;
+    c1.e.xw_rows = h->xw_rows;
     c1.e.x_lo_off = xw_lo(h);
-    c1.e.ssq_out = h->ssq_ctx;
+    c1.e.ssq_out = h->ssq_ctx + blk * h->ssq_ld * 2;
     c1.e.ssq_ld = h->ssq_ld;
     probe_begin(h, DFLASH_PROBE_WC, s);
     int st = tc ? run_tc05_epi(h, c1, wcp, (int)(row - tc_row0), s) : run_gemv(h, c1, s);
@@ -904,7 +985,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     const bool grouped = !h->act_f32;
     for (int i = 0; i < (grouped ? 1 : h->L); i++) {
       GemvCall c2;
-      if (!h->act_f32) {
+      if (!h->act_f32 && !tc) {
         c2.grp_n = h->L;
         c2.grp_w_stride = h->L > 1 ? h->qkv[1].w - h->qkv[0].w : 0;
         c2.grp_x_stride = 0;   // the same input rows, scaled per layer by attn_norm_i
@@ -916,11 +997,11 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       c2.strip0 = h->qd / 16;
       c2.n_strips = (2 * h->kvd) / 16;
       c2.R = rc;
-      c2.x = static_cast<const uint8_t*>(h->xw) + (grouped ? 0 : (size_t)i * kMaxCtxChunk * h->d * ab);
+      c2.x = static_cast<const uint8_t*>(h->xw) + (grouped ? 0 : (size_t)i * h->xw_rows * h->d * ab);
       c2.ldx = h->d;
       c2.x_lo_off = lo_if(LO_CTXKV, xw_lo(h));
       c2.norm_mode = NORM_CTX;
-      c2.ssq = h->ssq_ctx;
+      c2.ssq = h->ssq_ctx + blk * h->ssq_ld * 2;
       c2.ssq_ld = h->ssq_ld;
       c2.ssq_parts = parts;
       c2.inv_dim = 1.f / h->d;
@@ -936,6 +1017,20 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       for (int r = 0; r < rc; r++) {
         c2.e.kv_slot[r] = slots[r];
         c2.e.kv_pos[r] = pos[r];
+      }
+      if (tc) {
+        // every layer's K/V of the whole tcgen05 block at once, after its last chunk
+        c2.e.kv_grp_stride = (long long)layer_cache;
+        kv_calls[n_kv] = c2;
+        kv_r0[n_kv] = (int)blk;
+        n_kv++;
+        if (row + rc == tc_row0 + tc_rows) {
+          probe_begin(h, DFLASH_PROBE_CTX_KV, s);
+          st = run_tc05_kv(h, tc_rows, kv_calls, kv_r0, n_kv, s);
+          if (st) return st;
+          probe_end(h, DFLASH_PROBE_CTX_KV, s);
+        }
+        continue;
       }
       probe_begin(h, DFLASH_PROBE_CTX_KV, s);
       st = run_gemv(h, c2, s);
@@ -1485,11 +1580,11 @@ int dflash_rows_matmul(dflash_handle* h, int matrix, int layer, int n_rows, cons
   if (p.npad == 0) return DFLASH_EINVAL;
   if (scratch_bytes < p.scratch) return DFLASH_ECAPACITY;
   Tc05Args a{};
-  if (make_rows_map_groups(x, m->k, n_rows, ldx, p.npad, p.kx, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
-  if (x_lo && make_rows_map_groups(x_lo, m->k, n_rows, ldx, p.npad, p.kx, &a.xlmap) != DFLASH_OK)
+  if (make_rows_map_groups(x, m->k, n_rows, ldx, p.npad, p.kx, 1, 0, &a.xmap) != DFLASH_OK) return DFLASH_ECUDA;
+  if (x_lo && make_rows_map_groups(x_lo, m->k, n_rows, ldx, p.npad, p.kx, 1, 0, &a.xlmap) != DFLASH_OK)
     return DFLASH_ECUDA;
-  if (make_q4_tile_map(*m, p.tiles_big, kTcKW, &a.wmap) != DFLASH_OK ||
-      make_q4_tile_map(*m, p.tiles_small, kTcKW, &a.wmap_small) != DFLASH_OK)
+  if (make_q4_tile_map(*m, p.tiles_big, kTcKW, 1, 0, &a.wmap) != DFLASH_OK ||
+      make_q4_tile_map(*m, p.tiles_small, kTcKW, 1, 0, &a.wmap_small) != DFLASH_OK)
     return DFLASH_ECUDA;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   a.w = m->w;

@@ -107,6 +107,14 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 }
 
 // 3-D tiled tensor copy global -> shared (TMA), completing on an mbarrier.
+// Tiled tensor prefetch of one 4-D box into L2; nothing waits for it.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 // Tiled tensor prefetch of one 3-D box into L2; nothing waits for it.
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(

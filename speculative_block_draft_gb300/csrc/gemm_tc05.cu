@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
   // CTA -> (tile group, K slice); the first a.groups_big tile groups hold tiles_big tiles, the
   // rest tiles_small (the last one possibly fewer)
   const int tg = blockIdx.x % a.tgroups, slice = blockIdx.x / a.tgroups;
+  const int layer = blockIdx.y;   // grouped launches: one problem (layer) per grid row
   const int mt0 = tg < a.groups_big ? tg * cb : a.groups_big * cb + (tg - a.groups_big) * a.tiles_small;
   const int n_tiles = min(tg < a.groups_big ? cb : a.tiles_small, a.mtiles - mt0);
   const int g0 = slice * a.gps, ng = min(a.groups, g0 + a.gps) - g0;
@@ -145,7 +146,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
           in_bounds(mt0 < a.mtiles && g0 + j * kTcKW < a.groups, a.err);
           const uint32_t fw = smem_u32(&full_w[stage]);
           mbar_arrive_expect_tx(fw, w_bytes);
-          tma_load_3d(smem_u32(wring + stage * w_stage), wm, 0, g0 + j * kTcKW, mt0 * kTcStrips, fw);
+          tma_load_4d(smem_u32(wring + stage * w_stage), wm, 0, g0 + j * kTcKW, a.w_strip0 + mt0 * kTcStrips, layer,
+                      fw);
         }
         __syncwarp();
       };
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
       // holds too few bytes per SM to cover HBM latency under a full stream
       int npf = pre;
       auto prefetch_next = [&]() {
-        if (lane == 0 && npf < nsw) tma_prefetch_3d(wm, 0, g0 + npf * kTcKW, mt0 * kTcStrips);
+        if (lane == 0 && npf < nsw) tma_prefetch_4d(wm, 0, g0 + npf * kTcKW, a.w_strip0 + mt0 * kTcStrips, layer);
         npf++;
       };
       while (npf < min(nsw, pre + a.pf)) prefetch_next();
@@ -198,8 +200,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
           const uint32_t fx = smem_u32(&full_x[px.stage]);
           uint8_t* xst = xring + (size_t)px.stage * a.x_stage;
           mbar_arrive_expect_tx(fx, a.x_tx);
-          tma_load_3d(smem_u32(xst), &a.xmap, 0, 0, g0 + k * kx, fx);
-          if (LO) tma_load_3d(smem_u32(xst + kx * a.npad * 128), &a.xlmap, 0, 0, g0 + k * kx, fx);
+          tma_load_4d(smem_u32(xst), &a.xmap, 0, 0, g0 + k * kx, layer, fx);
+          if (LO) tma_load_4d(smem_u32(xst + kx * a.npad * 128), &a.xlmap, 0, 0, g0 + k * kx, layer, fx);
         }
         __syncwarp();
         nx = k + 1;
@@ -334,7 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc05_q4_kernel(const __grid_con
         const size_t strips_pad = (size_t)a.n_out_pad / 16;
         for (int t = 0; t < n_tiles; t++) {
           const size_t strip = (size_t)(mt0 + t) * kTcStrips + n / 16;
-          float* out = a.part + ((size_t)slice * strips_pad + strip) * a.npad * 16 + (n & 15);
+          float* out = a.part + (size_t)layer * a.part_layer_stride + ((size_t)slice * strips_pad + strip) * a.npad * 16 +
+                       (n & 15);
           const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * a.npad);
           for (int ch = 0; ch < a.npad / 16; ch++) {
             float v[16];
@@ -593,6 +596,7 @@ void tc05_fill_args(const Tc05Plan& p, int has_lo, Tc05Args& a) {
   a.sa = p.sa;
   a.pf = p.pf;
   a.kx = p.kx;
+  if (a.n_layers < 1) a.n_layers = 1;
   a.tmem_cols = p.tmem_cols;
   a.x_stage = p.x_stage;
   a.x_tx = p.x_tx;
@@ -604,11 +608,11 @@ cudaError_t launch_tc05_parts(const Tc05Args& a, const Tc05Plan& p, cudaStream_t
   if (a.has_lo) {
     e = ensure_smem_limit(tc05_q4_kernel<true>, p.smem, smem_set[1]);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tc05_q4_kernel<true>, dim3(p.grid), dim3(kTcThreads), p.smem, s, a);
+    return launch_pdl(tc05_q4_kernel<true>, dim3(p.grid, a.n_layers), dim3(kTcThreads), p.smem, s, a);
   }
   e = ensure_smem_limit(tc05_q4_kernel<false>, p.smem, smem_set[0]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(tc05_q4_kernel<false>, dim3(p.grid), dim3(kTcThreads), p.smem, s, a);
+  return launch_pdl(tc05_q4_kernel<false>, dim3(p.grid, a.n_layers), dim3(kTcThreads), p.smem, s, a);
 }
 
 cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_out, int half, float* y, int ldy,

@@ -24,12 +24,12 @@ constexpr int kTcMaxSX = 4;               // activation stages, at most
 constexpr size_t kTcSmemMax = 232448;     // dynamic shared memory a CTA may opt into (227 KB)
 
 struct Tc05Args {
-  CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder as [k / 64][rows][64]: box
-                             // 64 x npad x kx, 128-byte swizzle (kx groups per copy)
-  CUtensorMap wmap;          // the stored 4-bit matrix as [strip][group][144 words]: box 144 x kTcKW x
-                             // (8 x tiles_big), kTcKW groups of a big CTA's tiles per copy (rows and
-                             // groups past the matrix read as zero);
-  CUtensorMap wmap_small;    // the same with box 144 x kTcKW x (8 x tiles_small)
+  CUtensorMap xmap, xlmap;   // activation rows (f16) and their f16 remainder as [layer][k / 64][rows][64]:
+                             // box 64 x npad x kx x 1, 128-byte swizzle (kx groups per copy)
+  CUtensorMap wmap;          // the stored 4-bit matrix as [layer][strip][group][144 words]: box 144 x kTcKW
+                             // x (8 x tiles_big) x 1, kTcKW groups of a big CTA's tiles per copy (rows
+                             // and groups past the matrix read as zero);
+  CUtensorMap wmap_small;    // the same with box 144 x kTcKW x (8 x tiles_small) x 1
   const uint8_t* w;          // stored 4-bit matrix: [strip][group] tiles of kQ4GroupBytes
   float* part;               // [slices][n_out_pad / 16][npad][16] partial tiles (scratch): per 16-row
                              // strip of the stored order, each activation row's 16 outputs
@@ -39,6 +39,11 @@ struct Tc05Args {
   // hold tiles_big consecutive 128-row tiles, the others tiles_small (the last possibly fewer)
   int tgroups, tiles_big, groups_big, tiles_small;
   uint32_t x_stage, x_tx;
+  // grouped launches (grid.y = n_layers): the same plan over n_layers equally spaced matrices and
+  // activation planes; partial tiles of layer l at part + l * part_layer_stride. w_strip0: the
+  // first stored strip of the row range the contraction covers (a part of a larger matrix).
+  int n_layers, w_strip0;
+  size_t part_layer_stride;
 };
 
 struct Tc05Plan {
@@ -65,7 +70,7 @@ cudaError_t launch_tc05(const Tc05Args& a, const Tc05Plan& p, int rows, int n_ou
 // bf16 -> f16 of n_elems (even) contiguous elements, as the skinny GEMV converts context taps.
 cudaError_t launch_bf16_to_f16(const void* src, long long n_elems, void* dst, cudaStream_t s);
 
-// A draft-round projection's epilogue (EPI_CTX, EPI_QKV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
+// A draft-round projection's epilogue (EPI_CTX, EPI_QKV, EPI_KV, EPI_RESID, EPI_SWIGLU or EPI_LMHEAD) from the
 // partial tiles, through the skinny GEMV's strip epilogues, for up to kTcMaxChunks row chunks in
 // one launch (grid.y = chunk): ch.a[j] describes chunk j as for the GEMV (a.R <= kMaxRows rows,
 // nt = n-tiles of 8 for the largest chunk) with a.n_slices == 1; its row c is contraction row
@@ -77,9 +82,12 @@ struct Tc05EpiChunks {
   int row_base[kTcMaxChunks];
   int n;
 };
-// srow: kTcMaxChunks x kMaxRows floats of scratch for the rows' norm scales.
+// srow: kTcMaxChunks x kMaxRows floats of scratch for the rows' norm scales. n_layers > 1: a grouped
+// launch (EPI_KV over every layer), layer l's partial tiles at part + l * part_layer_stride; strips
+// of the partial tiles count from the chunks' strip0.
 cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
-                                 int n_out_pad, int grid, float* srow, cudaStream_t s);
+                                 int n_out_pad, int grid, float* srow, int n_layers, size_t part_layer_stride,
+                                 cudaStream_t s);
 
 // ---- skinny projections of the draft round on tcgen05 (proj_tc05.cu) ---------------------------
 constexpr unsigned kErrTimeoutProj = 8u;  // device error word bit of its bounded waits

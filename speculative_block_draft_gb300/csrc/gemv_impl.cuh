@@ -148,7 +148,7 @@ __device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre
     } else {
       pre.cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
       pre.cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
-      if (std::is_same<XT, float>::value && e.attn_norms) {
+      if (e.attn_norms) {   // one input plane per layer (CUDA-core path, tcgen05 context K/V)
 #pragma unroll
         for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
           pre.an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
@@ -300,7 +300,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             e.h[idx] = hn;
             store_act_split<XT>(e.xnext, idx, e.x_lo_off, hn * wn[h]);
             s0 += hn * hn;
-          } else if (!std::is_same<XT, float>::value || !e.attn_norms) {
+          } else if (!e.attn_norms) {
             // one row x * ctx_norm; the consumer applies attn_norm_i
             store_act_split<XT>(e.xw, (size_t)c * e.ldo + nr, e.x_lo_off, v * cn[h]);
             s0 += v * v;

@@ -1,7 +1,7 @@
 // Epilogues of the round's projections when they run on the many-row tcgen05 contraction. The K
 // slices' partial tiles are summed in slice order and handed, one 16-row strip per warp, to the
 // same strip epilogues the skinny GEMV fuses (the rows' norm scales computed once per projection by
-// a one-CTA-per-chunk kernel before it): context rows x ctx_norm with sums of squares,
+// a one-CTA-per-chunk kernel before it), grid.z over the problems of a grouped launch: context rows x ctx_norm with sums of squares,
 // row-norm scale, Q/K/V split, residual with next norm input and sums of squares, gated FFN, and
 // vocab states. One launch covers every row chunk of a projection (grid.y = chunk); row c of
 // chunk j is contraction row row_base[j] + map_row(xmap_j, c).
@@ -27,8 +27,10 @@ __global__ void __launch_bounds__(kF32Warps * 32)
 template <int NT, int EPI>
 __global__ void __launch_bounds__(kF32Warps * 32)
     tc05_epi_kernel(const __grid_constant__ Tc05EpiChunks ch, const float* __restrict__ part, int slices, int npad,
-                    int n_out_pad, const float* __restrict__ srow_in) {
+                    int n_out_pad, const float* __restrict__ srow_in, size_t part_layer_stride) {
   const GemvArgs& a = ch.a[blockIdx.y];   // this CTA's row chunk
+  const int lyr = blockIdx.z;             // problem of a grouped launch (context K/V of every layer)
+  part += (size_t)lyr * part_layer_stride;
   const int row_base = ch.row_base[blockIdx.y];
   __shared__ float srow[kMaxRows];
   __shared__ LmState sm_lm[kF32Warps * kMaxRows];
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
         const int c = nt * 8 + 2 * t + p;
         float y0 = 0.f, y1 = 0.f;
         if (c < a.R) {
-          const float* src = part + ((size_t)strip * npad + row_base + map_row(a.xmap, c)) * 16 + g;
+          const float* src = part + ((size_t)sl * npad + row_base + map_row(a.xmap, c)) * 16 + g;
           for (int s = 0; s < slices; s++) {
             y0 += __ldcg(src + s * slice_stride);
             y1 += __ldcg(src + s * slice_stride + 8);
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kF32Warps * 32)
       }
     EpiPre<NT> pre;
     epi_preload<EPI, NT, __half>(a, strip, pre);
-    strip_epilogue<EPI, NT, __half>(a, strip, y, srow, lm, 0, pre);
+    strip_epilogue<EPI, NT, __half>(a, strip, y, srow, lm, lyr, pre);
   }
   if constexpr (EPI == EPI_LMHEAD) lm_finish<NT>(a, lm, sm_lm);
 }
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kLmThreads)
 #pragma unroll
       for (int u = 0; u < U; u++) {
         const int sl = s0 + u * n_split;
-        const float4* src = reinterpret_cast<const float4*>(part + ((size_t)(a.strip0 + sl) * npad + row) * 16);
+        const float4* src = reinterpret_cast<const float4*>(part + ((size_t)sl * npad + row) * 16);
 #pragma unroll
         for (int w = 0; w < 4; w++) v[u][w] = sl < s_end ? __ldcg(src + w) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int z = 1; z < slices; z++) {
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kLmThreads)
 
 template <int EPI>
 cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad, int n_out_pad,
-                       int grid, float* srow, cudaStream_t s) {
-  const dim3 g(grid, ch.n);
+                       int grid, float* srow, int n_layers, size_t part_layer_stride, cudaStream_t s) {
+  const dim3 g(grid, ch.n, n_layers);
   const dim3 b(kF32Warps * 32);
   const cudaError_t e = launch_pdl(tc05_rowscale_kernel, dim3(ch.n), b, 0, s, ch, srow);
   if (e != cudaSuccess) return e;
@@ -169,15 +171,23 @@ cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int s
               ch.a[j].n_strips == ch.a[0].n_strips && ch.a[j].R <= kMaxRows;
       pairs += ch.a[j].R;
     }
-    if (plain && pairs >= 1 && pairs <= kLmThreads)
+    if (plain && pairs >= 1 && pairs <= kLmThreads && n_layers == 1)
       return launch_pdl(tc05_lm_epi_kernel, dim3(grid), dim3(kLmThreads), 0, s, ch, part, slices, npad, n_out_pad,
                         static_cast<const float*>(srow), pairs, kLmThreads / pairs > 1 ? 2 : 1);
   }
   switch (nt) {
-    case 1: return launch_pdl(tc05_epi_kernel<1, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
-    case 2: return launch_pdl(tc05_epi_kernel<2, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
-    case 3: return launch_pdl(tc05_epi_kernel<3, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
-    case 4: return launch_pdl(tc05_epi_kernel<4, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow);
+    case 1:
+      return launch_pdl(tc05_epi_kernel<1, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow,
+                        part_layer_stride);
+    case 2:
+      return launch_pdl(tc05_epi_kernel<2, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow,
+                        part_layer_stride);
+    case 3:
+      return launch_pdl(tc05_epi_kernel<3, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow,
+                        part_layer_stride);
+    case 4:
+      return launch_pdl(tc05_epi_kernel<4, EPI>, g, b, 0, s, ch, part, slices, npad, n_out_pad, srow,
+                        part_layer_stride);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -185,16 +195,21 @@ cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int s
 }  // namespace
 
 cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
-                                 int n_out_pad, int grid, float* srow, cudaStream_t s) {
-  if (ch.n < 1 || ch.n > kTcMaxChunks) return cudaErrorInvalidValue;
+                                 int n_out_pad, int grid, float* srow, int n_layers, size_t part_layer_stride,
+                                 cudaStream_t s) {
+  if (ch.n < 1 || ch.n > kTcMaxChunks || n_layers < 1) return cudaErrorInvalidValue;
+#define DFL_EPI_CASE(E) \
+  case E: return launch_epi<E>(nt, ch, part, slices, npad, n_out_pad, grid, srow, n_layers, part_layer_stride, s);
   switch (epi) {
-    case EPI_CTX: return launch_epi<EPI_CTX>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
-    case EPI_QKV: return launch_epi<EPI_QKV>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
-    case EPI_RESID: return launch_epi<EPI_RESID>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
-    case EPI_LMHEAD: return launch_epi<EPI_LMHEAD>(nt, ch, part, slices, npad, n_out_pad, grid, srow, s);
+    DFL_EPI_CASE(EPI_CTX)
+    DFL_EPI_CASE(EPI_QKV)
+    DFL_EPI_CASE(EPI_KV)
+    DFL_EPI_CASE(EPI_RESID)
+    DFL_EPI_CASE(EPI_SWIGLU)
+    DFL_EPI_CASE(EPI_LMHEAD)
     default: return cudaErrorInvalidValue;
   }
+#undef DFL_EPI_CASE
 }
 
 }  // namespace dfl

@@ -90,8 +90,9 @@ def test_rows_matmul_validates_before_any_launch(lib):
 
 def test_large_batch_option_carves_the_contraction_scratch(lib):
     """large_batch_tc05 = 1 adds exactly the largest contraction scratch (the block projections and
-    the head at 33 .. max_batch * gamma rows, capped at 160; W_c at 33 .. 160 context rows) and the f16 copy of
-    160 context-tap rows to the workspace. It adds nothing where the option does not apply (one
+    the head at 33 .. max_batch * gamma rows, capped at 160; W_c and the grouped context K/V at 33 .. 160
+    context rows), the f16 copy of 160 context-tap rows, and room for 160 context rows in the per-layer input
+    planes and their sums of squares to the workspace. It adds nothing where the option does not apply (one
     request of 8 rows, 16-bit weights, or a Markov head)."""
     import dflash_synth as syn
     torch = pytest.importorskip("torch")
@@ -109,14 +110,22 @@ def test_large_batch_option_carves_the_contraction_scratch(lib):
     # every many-row call size (33 rows up): the plan's K slices may grow as the rows shrink
     lo = {(qkv, cfg.d): 1, (2 * cfg.inter, cfg.d): 1, (cfg.vocab, cfg.d): 1}
     sizes = lambda top: [min(r, top) for r in range(33, top + 16, 16)]
+    kvd = cfg.n_kv_heads * cfg.head_dim
+    kv = [pkg.rows_matmul_plan(2 * kvd, cfg.d, r, 1, n_sm // cfg.n_layers) for r in sizes(pkg.DFLASH_ROWS_MATMUL_MAX)]
     want = max([pkg.rows_matmul_plan(n, k, r, lo.get((n, k), 0), n_sm).scratch_bytes for n, k in shapes
                 for r in sizes(rows)] +
                [pkg.rows_matmul_plan(cfg.d, mh, r, 0, n_sm).scratch_bytes
-                for r in sizes(pkg.DFLASH_ROWS_MATMUL_MAX)])  # W_c
+                for r in sizes(pkg.DFLASH_ROWS_MATMUL_MAX)] +   # W_c
+               # every layer's context K/V in one grouped launch: each layer's partial tiles, one row-scale area
+               [cfg.n_layers * (p.scratch_bytes - 8 * 32 * 4) + 8 * 32 * 4 for p in kv])
     want = -(-want // 256) * 256
     want += -(-(pkg.DFLASH_ROWS_MATMUL_MAX * mh * 2) // 256) * 256   # context taps converted to f16
     # the head's vocab states: one slice per row chunk (up to 8) of n_sm CTAs x 32 rows x (max, sum, index)
     want += (8 - 1) * n_sm * 32 * 3 * 4
+    # context rows of a call: 160 instead of 32 per input plane (f16 + remainder, one plane per layer),
+    # and their sums of squares
+    ssq_ld = -(-cfg.d // 16)
+    want += cfg.n_layers * (160 - 32) * cfg.d * 2 * 2 + (160 - 32) * ssq_ld * 2 * 4
     diff = lib.dflash_workspace_bytes(ctypes.byref(on)) - lib.dflash_workspace_bytes(ctypes.byref(off))
     assert diff == want
     for over in (dict(batch=1, gamma=8), dict(wdtype="bf16"), dict(markov_rank=64)):
