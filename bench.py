@@ -110,7 +110,11 @@ def probe_classes(cfg, ctx_lens, ctx_rows_per_round):
     act = 4 if cfg.adtype == "f32" else 2
     keys = sum(min(int(P), cfg.window) if cfg.window else int(P) for P in ctx_lens)
     L, d, I = cfg.n_layers, cfg.d, cfg.inter
-    chunks = max(1, -(-int(round(ctx_rows_per_round)) // 32))
+    rows = int(round(ctx_rows_per_round))
+    # context calls of more than 32 rows on the tcgen05 path: W_c and every layer's K/V once per
+    # block of up to 160 rows (the probes bracket a whole block); otherwise once per 32-row chunk
+    tc = getattr(cfg, "large_batch_tc05", False) and cfg.wdtype == "q4" and rows > 32
+    chunks = max(1, -(-rows // (160 if tc else 32)))
     return [("lm_head", 0, 1, cfg.vocab * cfg.target_hidden * bpp),
             ("qkv", 1, L, (qd + 2 * kvd) * d * bpp),
             ("attention", 2, L, keys * kvd * 2 * act),

@@ -936,6 +936,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
       const int rows = (int)std::min<int64_t>(kTcMaxRows, total - row);
       tc_rows = rows;
       n_kv = 0;
+      probe_begin(h, DFLASH_PROBE_WC, s);   // the block's W_c: contraction and every chunk's epilogue
       h->launches++;
       int st = status_of(launch_bf16_to_f16(tp + (size_t)row * h->mH * ab, (long long)rows * h->mH, h->tc05_taps, s));
       if (!st) st = run_tc05_parts(h, h->wc, rows, h->tc05_taps, h->mH, 0, s, &wcp);
@@ -975,10 +976,10 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.e.x_lo_off = xw_lo(h);
     c1.e.ssq_out = h->ssq_ctx + blk * h->ssq_ld * 2;
     c1.e.ssq_ld = h->ssq_ld;
-    probe_begin(h, DFLASH_PROBE_WC, s);
+    if (!tc) probe_begin(h, DFLASH_PROBE_WC, s);
     int st = tc ? run_tc05_epi(h, c1, wcp, (int)(row - tc_row0), s) : run_gemv(h, c1, s);
     if (st) return st;
-    probe_end(h, DFLASH_PROBE_WC, s);
+    if (!tc || row + rc == tc_row0 + tc_rows) probe_end(h, DFLASH_PROBE_WC, s);
     // per layer: K_i, V_i of RMSNorm_attn_i(RMSNorm_ctx(x)), appended to the ring cache; the
     // tensor-core path runs every layer in one grouped launch over the same input rows (the
     // layers' packed Q/K/V matrices and caches are equally spaced; attn_norm_i scales the input)
