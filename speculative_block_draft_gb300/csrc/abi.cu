@@ -960,7 +960,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.x = tp + (size_t)row * h->mH * ab;
     c1.ldx = h->mH;
     c1.x_bf16 = !h->act_f32;   // caller taps are bf16; the tensor-core path computes in f16
-    c1.epi = EPI_CTX;
+    c1.epi = tc ? EPI_CTX_PLANES : EPI_CTX;
     c1.e.row_base = 0;
     c1.e.n_rows = h->d;
     c1.e.ldo = h->d;

@@ -202,6 +202,7 @@ cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const
   case E: return launch_epi<E>(nt, ch, part, slices, npad, n_out_pad, grid, srow, n_layers, part_layer_stride, s);
   switch (epi) {
     DFL_EPI_CASE(EPI_CTX)
+    DFL_EPI_CASE(EPI_CTX_PLANES)
     DFL_EPI_CASE(EPI_QKV)
     DFL_EPI_CASE(EPI_KV)
     DFL_EPI_CASE(EPI_RESID)
