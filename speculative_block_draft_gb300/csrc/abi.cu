@@ -925,6 +925,11 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
   // many rows: W_c runs once per kTcMaxRows rows on the tcgen05 contraction (a whole number of
   // chunks), then each chunk's epilogue and its context K/V launch as below
   const bool tc = h->tc05_on && total > kMaxCtxChunk;
+  // the grouped context K/V appends a whole block's rows in one launch, so no request may wrap its
+  // ring within the call (later rows must overwrite earlier ones in order: the chunked path then)
+  int max_new = 0;
+  for (int i = 0; i < n_req; i++) max_new = std::max(max_new, (int)n_new[i]);
+  const bool tc_kv = tc && max_new <= h->cap;
   Tc05Plan wcp{};
   int64_t tc_row0 = 0;
   int tc_rows = 0;
@@ -960,7 +965,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.x = tp + (size_t)row * h->mH * ab;
     c1.ldx = h->mH;
     c1.x_bf16 = !h->act_f32;   // caller taps are bf16; the tensor-core path computes in f16
-    c1.epi = tc ? EPI_CTX_PLANES : EPI_CTX;
+    c1.epi = tc_kv ? EPI_CTX_PLANES : EPI_CTX;
     c1.e.row_base = 0;
     c1.e.n_rows = h->d;
     c1.e.ldo = h->d;
@@ -968,8 +973,8 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     // tensor-core path: one row x * ctx_norm, the K/V launch applies attn_norm_i to its input;
     // CUDA-core path and the tcgen05 block: one input row per layer (x * ctx_norm * attn_norm_i),
     // the block's rows at their offset in it
-    const size_t blk = tc ? (size_t)(row - tc_row0) : 0;
-    c1.e.attn_norms = (h->act_f32 || tc) ? h->attn_norm : nullptr;
+    const size_t blk = tc_kv ? (size_t)(row - tc_row0) : 0;
+    c1.e.attn_norms = (h->act_f32 || tc_kv) ? h->attn_norm : nullptr;
     c1.e.n_layers = h->L;
     c1.e.xw = static_cast<uint8_t*>(h->xw) + blk * h->d * ab;
     c1.e.xw_rows = h->xw_rows;
@@ -986,7 +991,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     const bool grouped = !h->act_f32;
     for (int i = 0; i < (grouped ? 1 : h->L); i++) {
       GemvCall c2;
-      if (!h->act_f32 && !tc) {
+      if (!h->act_f32 && !tc_kv) {
         c2.grp_n = h->L;
         c2.grp_w_stride = h->L > 1 ? h->qkv[1].w - h->qkv[0].w : 0;
         c2.grp_x_stride = 0;   // the same input rows, scaled per layer by attn_norm_i
@@ -1019,7 +1024,7 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
         c2.e.kv_slot[r] = slots[r];
         c2.e.kv_pos[r] = pos[r];
       }
-      if (tc) {
+      if (tc_kv) {
         // every layer's K/V of the whole tcgen05 block at once, after its last chunk
         c2.e.kv_grp_stride = (long long)layer_cache;
         kv_calls[n_kv] = c2;

@@ -187,6 +187,19 @@ def test_large_batch_round_small_ragged():
     run(cfg, rounds=3, ctx_capacity=64)
 
 
+def test_large_batch_round_ring_wraps_within_a_call():
+    """Context calls on the contraction where one request appends more rows than its ring holds
+    (window 40, ring of 64 slots, 100 prefill rows in one call): the later rows must overwrite the
+    earlier ones in order, so the context K/V goes through the chunked path there; against the
+    oracle, error word clear."""
+    from test_gpu_parity import run, small
+    cfg = small("s_tc05_wrap", batch=8, ctx_len=100, ctx_min=30, window=40, append_min=1, append_max=8, agree=0.6,
+                large_batch_tc05=True)
+    lengths = syn.ctx_lengths(cfg)
+    assert int(lengths.sum()) > 160 and int(lengths.max()) > 64
+    run(cfg, rounds=3, ctx_capacity=64, lengths=lengths)
+
+
 def test_large_batch_round_gelu_all_rows():
     """The same path with the page's gated-GELU FFN and drafts from every block row (the LM head
     epilogue reads every row), 5 requests x gamma 8 = 40 rows, hd 128."""
