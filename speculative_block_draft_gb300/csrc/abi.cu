@@ -680,9 +680,10 @@ int run_tc05_epi(dflash_handle* h, const GemvCall& c, const Tc05Plan& p, int row
   return run_tc05_epi_chunks(h, &c, &row_base, 1, p, s);
 }
 
-// The context K/V of `rows` context rows for every layer, on the tcgen05 contraction: one grouped
-// launch over the K/V strips of each layer's Q/K/V matrix, reading layer i's input plane of xw
-// (x * ctx_norm * attn_norm_i, f16 and its remainder), then one epilogue launch (grid.z = layer)
+// The context K/V of `rows` context rows for every layer, on the tcgen05 contraction: one launch
+// makes layer i's input plane of xw (x * ctx_norm * attn_norm_i, f16 and its remainder) from the
+// context epilogue's plane, one grouped launch contracts the K/V strips of each layer's Q/K/V
+// matrix with its plane, then one epilogue launch (grid.z = layer)
 // that scales by the rows' norm and appends to each layer's ring cache. calls[j] describes chunk j
 // (contraction rows r0[j] ...) as for the GEMV.
 int run_tc05_kv(dflash_handle* h, int rows, const GemvCall* calls, const int* r0, int n, cudaStream_t s) {
@@ -703,6 +704,10 @@ int run_tc05_kv(dflash_handle* h, int rows, const GemvCall* calls, const int* r0
   if (make_q4_tile_map(m, p.tiles_big, kTcKW, L, w_stride, &a.wmap) != DFLASH_OK ||
       make_q4_tile_map(m, p.tiles_small, kTcKW, L, w_stride, &a.wmap_small) != DFLASH_OK)
     return DFLASH_ECUDA;
+  h->launches++;
+  int st = status_of(launch_tc05_kv_planes(h->xw, (long long)xw_lo(h), h->attn_norm, rows, h->d, L,
+                                           (long long)h->xw_rows * h->d, s));
+  if (st) return st;
   a.w = m.w;
   a.part = reinterpret_cast<float*>(h->tc05_scratch);
   a.err = h->err;
@@ -713,7 +718,7 @@ int run_tc05_kv(dflash_handle* h, int rows, const GemvCall* calls, const int* r0
   a.w_strip0 = h->qd / 16;
   a.part_layer_stride = layer_bytes / 4;
   h->launches++;
-  int st = status_of(launch_tc05_parts(a, p, s));
+  st = status_of(launch_tc05_parts(a, p, s));
   if (st) return st;
   static thread_local Tc05EpiChunks ch;
   const int grid = tc05_epi_grid(h, calls[0]);
@@ -965,16 +970,16 @@ int dflash_project_ctx(dflash_handle* h, int n_req, const int32_t* req_ids, cons
     c1.x = tp + (size_t)row * h->mH * ab;
     c1.ldx = h->mH;
     c1.x_bf16 = !h->act_f32;   // caller taps are bf16; the tensor-core path computes in f16
-    c1.epi = tc_kv ? EPI_CTX_PLANES : EPI_CTX;
+    c1.epi = EPI_CTX;
     c1.e.row_base = 0;
     c1.e.n_rows = h->d;
     c1.e.ldo = h->d;
     c1.e.ctx_norm = h->ctx_norm;
-    // tensor-core path: one row x * ctx_norm, the K/V launch applies attn_norm_i to its input;
-    // CUDA-core path and the tcgen05 block: one input row per layer (x * ctx_norm * attn_norm_i),
-    // the block's rows at their offset in it
+    // tensor-core path: one row x * ctx_norm, the K/V launch applies attn_norm_i to its input
+    // (the tcgen05 block: its rows at their offset in the block, every layer's plane made from
+    // them before the grouped K/V); CUDA-core path: one input row per layer
     const size_t blk = tc_kv ? (size_t)(row - tc_row0) : 0;
-    c1.e.attn_norms = (h->act_f32 || tc_kv) ? h->attn_norm : nullptr;
+    c1.e.attn_norms = h->act_f32 ? h->attn_norm : nullptr;
     c1.e.n_layers = h->L;
     c1.e.xw = static_cast<uint8_t*>(h->xw) + blk * h->d * ab;
     c1.e.xw_rows = h->xw_rows;

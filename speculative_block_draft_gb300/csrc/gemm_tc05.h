@@ -82,6 +82,11 @@ struct Tc05EpiChunks {
   int row_base[kTcMaxChunks];
   int n;
 };
+// One f16 (+ remainder) input plane per layer, planes `plane` elements apart, for the grouped
+// context K/V: plane i = plane 0 (x * ctx_norm, in place) * attn_norm_i, rows [0, rows) of width d.
+cudaError_t launch_tc05_kv_planes(void* xw, long long lo_off, const float* attn_norm, int rows, int d, int n_layers,
+                                  long long plane, cudaStream_t s);
+
 // srow: kTcMaxChunks x kMaxRows floats of scratch for the rows' norm scales. n_layers > 1: a grouped
 // launch (EPI_KV over every layer), layer l's partial tiles at part + l * part_layer_stride; strips
 // of the partial tiles count from the chunks' strip0.

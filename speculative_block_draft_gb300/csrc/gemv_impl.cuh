@@ -124,11 +124,10 @@ struct EpiPre {
   float an[DFLASH_MAX_LAYERS][2];     // per-layer norm weights of rows nr0, nr1 (CTX, CUDA-core path)
 };
 
-// XT = float is the CUDA-core path, which writes one context row per layer (EPI_CTX); on the f16
-// paths only EPI_CTX_PLANES (the tcgen05 context calls) does.
+// XT = float is the CUDA-core path, which alone writes one context row per layer (EPI_CTX).
 template <int EPI, int NT, typename XT>
 __device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre<NT>& pre) {
-  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX || EPI == EPI_CTX_PLANES) {
+  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
     const EpiArgs& e = a.e;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int nr0 = strip * 16 + g - e.row_base, nr1 = nr0 + 8;
@@ -149,7 +148,7 @@ __device__ __forceinline__ void epi_preload(const GemvArgs& a, int strip, EpiPre
     } else {
       pre.cn[0] = v0 ? e.ctx_norm[nr0] : 0.f;
       pre.cn[1] = v1 ? e.ctx_norm[nr1] : 0.f;
-      if ((std::is_same<XT, float>::value || EPI == EPI_CTX_PLANES) && e.attn_norms) {   // one input plane per layer
+      if (std::is_same<XT, float>::value && e.attn_norms) {
 #pragma unroll
         for (int i = 0; i < DFLASH_MAX_LAYERS; i++) {
           pre.an[i][0] = (i < e.n_layers && v0) ? e.attn_norms[(size_t)i * e.ldo + nr0] : 0.f;
@@ -275,7 +274,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
       }
     }
   }
-  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX || EPI == EPI_CTX_PLANES) {
+  if constexpr (EPI == EPI_RESID || EPI == EPI_CTX) {
     // residual update / context rows, then this strip's sum-of-squares partial per column
     const auto& hv = pre.hv;
     const auto& wn = pre.wn;
@@ -301,7 +300,7 @@ __device__ __forceinline__ void strip_epilogue(const GemvArgs& a, int strip, flo
             e.h[idx] = hn;
             store_act_split<XT>(e.xnext, idx, e.x_lo_off, hn * wn[h]);
             s0 += hn * hn;
-          } else if ((!std::is_same<XT, float>::value && EPI != EPI_CTX_PLANES) || !e.attn_norms) {
+          } else if (!std::is_same<XT, float>::value || !e.attn_norms) {
             // one row x * ctx_norm; the consumer applies attn_norm_i
             store_act_split<XT>(e.xw, (size_t)c * e.ldo + nr, e.x_lo_off, v * cn[h]);
             s0 += v * v;

@@ -55,8 +55,7 @@ __host__ __device__ constexpr int gemv_warps(int nt) { return nt == 1 ? kWarps :
 constexpr int kF32Warps = 8;
 
 enum Fmt { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q4 = 2 };
-enum Epi { EPI_STORE = 0, EPI_CTX = 1, EPI_KV = 2, EPI_QKV = 3, EPI_RESID = 4, EPI_SWIGLU = 5, EPI_LMHEAD = 6,
-           EPI_CTX_PLANES = 7 };   // EPI_CTX writing one f16 input plane per layer (tcgen05 context calls)
+enum Epi { EPI_STORE = 0, EPI_CTX = 1, EPI_KV = 2, EPI_QKV = 3, EPI_RESID = 4, EPI_SWIGLU = 5, EPI_LMHEAD = 6 };
 enum NormMode { NORM_NONE = 0, NORM_ONE = 1, NORM_CTX = 2 };
 
 // Device error word bits.

@@ -12,6 +12,48 @@ namespace dfl {
 
 namespace {
 
+// One input plane per layer for the grouped context K/V: plane i of row r = (x_r * ctx_norm) *
+// attn_norm_i, from the context epilogue's single plane (f16 and its f16 remainder), split again
+// into f16 and remainder exactly as the skinny GEMV's K/V launch rescales its staged input. Plane 0
+// overwrites the input in place (each element is read, then written, by the same thread).
+__global__ void __launch_bounds__(256) tc05_kv_planes_kernel(__half* xw, long long lo_off, const float* attn_norm,
+                                                             int rows, int d, int n_layers, long long plane) {
+  pdl_launch_dependents();
+  pdl_wait();   // the context epilogue wrote the input plane
+  const int per_row = d / 8;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < (long long)rows * per_row;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / per_row), k8 = (int)(idx % per_row) * 8;
+    const size_t off = (size_t)r * d + k8;
+    const uint4 h4 = *reinterpret_cast<const uint4*>(xw + off);
+    const uint4 l4 = *reinterpret_cast<const uint4*>(xw + lo_off + off);
+    const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, lw[4] = {l4.x, l4.y, l4.z, l4.w};
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hw[q]));
+      const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&lw[q]));
+      v[2 * q] = fh.x + fl.x;
+      v[2 * q + 1] = fh.y + fl.y;
+    }
+    for (int i = n_layers - 1; i >= 0; i--) {   // plane 0 last: it is the input
+      const float4 a0 = *reinterpret_cast<const float4*>(attn_norm + (size_t)i * d + k8);
+      const float4 a1 = *reinterpret_cast<const float4*>(attn_norm + (size_t)i * d + k8 + 4);
+      const float w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      uint32_t oh[4], ol[4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const float va = v[2 * q] * w[2 * q], vb = v[2 * q + 1] * w[2 * q + 1];
+        const __half ha = from_f<__half>(va), hb = from_f<__half>(vb);
+        oh[q] = pack_f16x2(__half2float(ha), __half2float(hb));
+        ol[q] = pack_f16x2(va - __half2float(ha), vb - __half2float(hb));
+      }
+      *reinterpret_cast<uint4*>(xw + (size_t)i * plane + off) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      *reinterpret_cast<uint4*>(xw + lo_off + (size_t)i * plane + off) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    }
+  }
+}
+
 // The rows' norm scales of every chunk, once per projection (a CTA per chunk), instead of in each
 // of the epilogue's CTAs: they sum hundreds of per-strip partials per row.
 __global__ void __launch_bounds__(kF32Warps * 32)
@@ -194,6 +236,15 @@ cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int s
 
 }  // namespace
 
+cudaError_t launch_tc05_kv_planes(void* xw, long long lo_off, const float* attn_norm, int rows, int d, int n_layers,
+                                  long long plane, cudaStream_t s) {
+  if (rows < 1 || d % 8 || n_layers < 1) return cudaErrorInvalidValue;
+  const long long work = (long long)rows * (d / 8);
+  const int blocks = (int)std::min<long long>(1024, (work + 255) / 256);
+  return launch_pdl(tc05_kv_planes_kernel, dim3(blocks), dim3(256), 0, s, static_cast<__half*>(xw), lo_off,
+                    attn_norm, rows, d, n_layers, plane);
+}
+
 cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad,
                                  int n_out_pad, int grid, float* srow, int n_layers, size_t part_layer_stride,
                                  cudaStream_t s) {
@@ -202,7 +253,6 @@ cudaError_t launch_tc05_epilogue(int epi, int nt, const Tc05EpiChunks& ch, const
   case E: return launch_epi<E>(nt, ch, part, slices, npad, n_out_pad, grid, srow, n_layers, part_layer_stride, s);
   switch (epi) {
     DFL_EPI_CASE(EPI_CTX)
-    DFL_EPI_CASE(EPI_CTX_PLANES)
     DFL_EPI_CASE(EPI_QKV)
     DFL_EPI_CASE(EPI_KV)
     DFL_EPI_CASE(EPI_RESID)
