@@ -198,6 +198,108 @@ __global__ void __launch_bounds__(kLmThreads)
   }
 }
 
+// Q/K/V and gated-FFN epilogues on the contraction's partial tiles, one thread per (row, strip): it
+// reads the strip's 16 outputs of its row (64 contiguous bytes per K slice, consecutive rows in
+// consecutive threads), scales them by the row's norm scale and writes them with 16-byte stores.
+// Same arithmetic per element as the strip epilogues.
+template <int EPI>
+__global__ void __launch_bounds__(256)
+    tc05_rowstrip_epi_kernel(const __grid_constant__ Tc05EpiChunks ch, const float* __restrict__ part, int slices,
+                             int npad, int n_out_pad, const float* __restrict__ srow_in, int n_pairs) {
+  static_assert(EPI == EPI_QKV || EPI == EPI_SWIGLU, "row-by-strip epilogues: Q/K/V and the gated FFN");
+  pdl_launch_dependents();
+  pdl_wait();   // the partial tiles and the row scales come from earlier kernels
+  const int n_strips = ch.a[0].n_strips;
+  const long long total = (long long)n_pairs * n_strips;
+  const size_t slice_stride = (size_t)npad * n_out_pad;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int sl = (int)(idx / n_pairs);
+    int c = (int)(idx - (long long)sl * n_pairs), j = 0;
+    while (j + 1 < ch.n && c >= ch.a[j].R) {
+      c -= ch.a[j].R;
+      j++;
+    }
+    const GemvArgs& a = ch.a[j];
+    const EpiArgs& e = a.e;
+    const int row = ch.row_base[j] + map_row(a.xmap, c);
+    const float sc = srow_in[j * kMaxRows + c];
+    const float4* src = reinterpret_cast<const float4*>(part + ((size_t)sl * npad + row) * 16);
+    // the K slices in order, four slices' loads in flight at a time
+    float4 v4[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
+                    make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int z0 = 0; z0 < slices; z0 += 4) {
+      float4 t[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+#pragma unroll
+        for (int w = 0; w < 4; w++)
+          t[u][w] = z0 + u < slices
+                        ? __ldcg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) +
+                                                                 (z0 + u) * slice_stride) + w)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+          v4[w].x += t[u][w].x;
+          v4[w].y += t[u][w].y;
+          v4[w].z += t[u][w].z;
+          v4[w].w += t[u][w].w;
+        }
+    }
+    float y[16];
+#pragma unroll
+    for (int w = 0; w < 4; w++) {
+      y[4 * w] = v4[w].x * sc;
+      y[4 * w + 1] = v4[w].y * sc;
+      y[4 * w + 2] = v4[w].z * sc;
+      y[4 * w + 3] = v4[w].w * sc;
+    }
+    const int strip = a.strip0 + sl;
+    const int n0 = strip * 16 - e.row_base;   // first output feature of the strip
+    if constexpr (EPI == EPI_SWIGLU) {
+      // strip rows 0-7 are gate rows, 8-15 the matching up rows; outputs strip * 8 + k
+      const int j0 = strip * 8;
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++) {
+        const float g = y[k];
+        const float ga = e.ffn_act == DFLASH_FFN_GELU
+                             ? 0.5f * g * (1.0f + tanhf(0.7978845608028654f * fmaf(0.044715f * g, g * g, g)))
+                             : g / (1.0f + __expf(-g));
+        o[k] = ga * y[k + 8];
+      }
+      __half* dst = static_cast<__half*>(e.act) + (size_t)c * e.inter + j0;
+      if (j0 + 8 <= e.inter) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) pk[q] = pack_f16x2(__half2float(from_f<__half>(o[2 * q])),
+                                                       __half2float(from_f<__half>(o[2 * q + 1])));
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      } else {
+        for (int k = 0; k < 8 && j0 + k < e.inter; k++) dst[k] = from_f<__half>(o[k]);
+      }
+    } else if constexpr (EPI == EPI_QKV) {
+      // qd and kvd are multiples of 16: a strip lies in one of q, k, v
+      __half* dst;
+      if (n0 < e.qd) dst = static_cast<__half*>(e.q) + (size_t)c * e.qd + n0;
+      else if (n0 < e.qd + e.kvd) dst = static_cast<__half*>(e.kb) + (size_t)c * e.kvd + n0 - e.qd;
+      else dst = static_cast<__half*>(e.vb) + (size_t)c * e.kvd + n0 - e.qd - e.kvd;
+      if (n0 + 16 <= e.n_rows) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) pk[q] = pack_f16x2(__half2float(from_f<__half>(y[2 * q])),
+                                                       __half2float(from_f<__half>(y[2 * q + 1])));
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      } else {
+        for (int k = 0; k < 16 && n0 + k < e.n_rows; k++) dst[k] = from_f<__half>(y[k]);
+      }
+    }
+  }
+}
+
 template <int EPI>
 cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int slices, int npad, int n_out_pad,
                        int grid, float* srow, int n_layers, size_t part_layer_stride, cudaStream_t s) {
@@ -216,6 +318,22 @@ cudaError_t launch_epi(int nt, const Tc05EpiChunks& ch, const float* part, int s
     if (plain && pairs >= 1 && pairs <= kLmThreads && n_layers == 1)
       return launch_pdl(tc05_lm_epi_kernel, dim3(grid), dim3(kLmThreads), 0, s, ch, part, slices, npad, n_out_pad,
                         static_cast<const float*>(srow), pairs, kLmThreads / pairs > 1 ? 2 : 1);
+  }
+  // the row-by-strip kernel for Q/K/V and the gated FFN (measured faster); the residual epilogues
+  // (O, down: several K slices) stay on the strip kernel, which was faster there
+  if constexpr (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+    int pairs = 0;
+    bool same = true;
+    for (int j = 0; j < ch.n; j++) {
+      pairs += ch.a[j].R;
+      same = same && ch.a[j].strip0 == ch.a[0].strip0 && ch.a[j].n_strips == ch.a[0].n_strips;
+    }
+    if (same && n_layers == 1 && pairs >= 1) {
+      const long long total = (long long)pairs * ch.a[0].n_strips;
+      const int blocks = (int)std::min<long long>(2048, (total + 255) / 256);
+      return launch_pdl(tc05_rowstrip_epi_kernel<EPI>, dim3(blocks), dim3(256), 0, s, ch, part, slices, npad,
+                        n_out_pad, static_cast<const float*>(srow), pairs);
+    }
   }
   switch (nt) {
     case 1:
