@@ -7,23 +7,26 @@
 // divides the activation traffic from L2 and the number of activation loads in flight by the
 // tile count.
 //  * warp 0 streams the CTA's 4-bit (strip, group) tiles, kTcKW 64-input groups of all its tiles
-//    per 3-D tensor copy, and keeps the following ones coming into L2 with tensor prefetches; warp 10
+//    per tensor copy, and keeps the following ones coming into L2 with tensor prefetches; warp 10
 //    streams the activation rows (f16, plus the f16 remainder where given), one or two groups per
-//    3-D tensor copy in the 128-byte swizzle;
+//    tensor copy in the 128-byte swizzle (4-D maps: a grouped launch's layer is the outer
+//    coordinate, grid.y);
 //  * warps 2-9 (strip w of every tile) dequantise the codes to f16 weights, w = s q + b with one
 //    rounding (the code q is made exact in f16 from its nibble with a magic-number lop3 and one
 //    exact subtraction, then one fused f16 multiply-add with the row's scale and bias), and store
 //    them as the MMAs' K-major A tiles in the same swizzle (the stored word order of a lane covers
 //    whole 16-byte chunks of a row);
-//  * warp 1 allocates tensor memory and one of its lanes issues tcgen05.mma kind::f16 (M = 128
-//    output rows, N = the activation rows padded to 16, K = 16), one fp32 accumulator per tile
-//    over the whole K slice, then commits to the stages' mbarriers;
+//  * warp 1 allocates tensor memory and, converged, issues tcgen05.mma kind::f16 through one
+//    elected lane (M = 128 output rows, N = the activation rows padded to 16, K = 16), one fp32
+//    accumulator per tile over the whole K slice, then commits to the stages' mbarriers;
 //  * warps 4-7 (tensor-memory lane quarters 0-3) finally read the accumulators and store the
-//    slice's partial tiles.
+//    slice's partial tiles, strip-major ([slice][strip][row][16]).
 // The copy and MMA warps run their loops with all 32 lanes (one lane issues): a lone lane whose
 // warp-mates wait at a block barrier is scheduled far too rarely for an issue loop. Every mbarrier
 // wait is bounded (error word + early exit); tensor memory is freed at the end. The K slices'
-// partial tiles are summed in slice order by a separate kernel.
+// partial tiles are summed in slice order by the reduction kernel below (dflash_rows_matmul) or by
+// the draft round's epilogues (tc05_epi.cu). The launch shape (tiles per CTA, K slices, ring
+// depths) comes from plan_tc05's cost model.
 #include <cuda.h>
 
 #include <algorithm>
