@@ -79,6 +79,21 @@ def test_probe_classes_cover_the_round_bytes():
     assert abs(cls["ctx_kv"][2] - 5 * 2 * 1024 * 5120 * bench.Q4_BYTES_PER_PARAM) < 1
 
 
+def test_probe_classes_count_context_blocks_on_the_tcgen05_path():
+    """Context calls of more than 32 rows on the tcgen05 path run W_c and every layer's K/V once per
+    block of up to 160 rows; the GEMV path once per 32-row chunk."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    cfg = syn.CONFIGS["c5"]
+    tc = syn.with_overrides(cfg, large_batch_tc05=True)
+    for rows, gemv_n, tc_n in ((144.0, 5, 1), (200.0, 7, 2), (20.0, 1, 1)):
+        g = {name: n for name, _, n, _ in bench.probe_classes(cfg, [4096] * 32, rows)}
+        t = {name: n for name, _, n, _ in bench.probe_classes(tc, [4096] * 32, rows)}
+        assert g["w_c"] == g["ctx_kv"] == gemv_n, rows
+        assert t["w_c"] == t["ctx_kv"] == tc_n, rows
+
+
 def test_oracle_table_one_core_and_all_cores():
     """The oracle timing table (1 core and all cores per workload) on the tiny fp32 drafter."""
     import bench
