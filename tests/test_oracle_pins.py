@@ -312,6 +312,82 @@ def test_block_scores_from_live_q_k_v_projections(hq, hkv, window, n_ctx):
     assert np.allclose(out["trace"][1], h0 + att, rtol=0, atol=1e-12)
 
 
+def _torch_drafter(cfg, m, anchor, tap_rows, all_rows=False, gelu=False):
+    """The whole draft block written with torch's own routines (F.linear, F.rms_norm, SDPA,
+    SiLU / GELU, softmax) in float64 from the raw matrices: the context rows' projection and
+    norms (Eq 2 of the dflash.ts page), the block rows, every layer of Eq 3 with its gated FFN,
+    out_norm (+ out_proj) and the borrowed head."""
+    F = torch.nn.functional
+    T = lambda a: torch.tensor(np.asarray(a, dtype=np.float64))
+    W = lambda n: T(_raw(m.mats[n]))
+    vec = lambda n: T(m.vecs[n])
+    eps, d, hd = cfg.eps, cfg.d, cfg.head_dim
+    hq, hkv, G = cfg.n_q_heads, cfg.n_kv_heads, cfg.gamma
+    hctx = F.rms_norm(F.linear(T(tap_rows), W("W_c")), (d,), vec("ctx_norm"), eps)
+    e = W("embed")[anchor]
+    h = torch.empty(G, d, dtype=torch.float64)
+    h[0] = (F.linear(e, W("tok_proj")) if cfg.target_hidden != d else e) + vec("block_pos")[0]
+    for k in range(1, G):
+        h[k] = vec("mask_emb")[k - 1] + vec("block_pos")[k]
+    n_ctx = hctx.shape[0]
+    lo = max(0, n_ctx - cfg.window) if cfg.window else 0
+    for i in range(cfg.n_layers):
+        an = vec(f"bb.{i}.attn_norm")
+        nc = F.rms_norm(hctx[lo:], (d,), an, eps)
+        n = F.rms_norm(h, (d,), an, eps)
+        q = F.linear(n, W(f"bb.{i}.q"))
+        k = torch.cat([F.linear(nc, W(f"bb.{i}.k")), F.linear(n, W(f"bb.{i}.k"))])
+        v = torch.cat([F.linear(nc, W(f"bb.{i}.v")), F.linear(n, W(f"bb.{i}.v"))])
+        tq = q.view(G, hq, hd).transpose(0, 1)
+        tk = k.view(-1, hkv, hd).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+        tv = v.view(-1, hkv, hd).transpose(0, 1).repeat_interleave(hq // hkv, dim=0)
+        att = F.scaled_dot_product_attention(tq, tk, tv, is_causal=False).transpose(0, 1).reshape(G, hq * hd)
+        h = h + F.linear(att, W(f"bb.{i}.o"))
+        n2 = F.rms_norm(h, (d,), vec(f"bb.{i}.ff_norm"), eps)
+        g = F.linear(n2, W(f"bb.{i}.gate"))
+        act = F.gelu(g, approximate="tanh") if gelu else F.silu(g)
+        h = h + F.linear(act * F.linear(n2, W(f"bb.{i}.up")), W(f"bb.{i}.down"))
+    rows = h if all_rows else h[1:]
+    hn = F.rms_norm(rows, (d,), vec("out_norm"), eps)
+    if cfg.target_hidden != d:
+        hn = F.linear(hn, W("out_proj"))
+    logits = F.linear(hn, W("lm_head"))
+    p = torch.softmax(logits, dim=-1)
+    return logits.numpy(), p.argmax(dim=-1).numpy(), p.max(dim=-1).values.numpy()
+
+
+@pytest.mark.parametrize("H,hq,hkv,window,n_ctx,ffn,all_rows", [
+    (64, 4, 2, 0, 6, "swiglu", False),
+    (128, 4, 2, 3, 7, "swiglu", False),
+    (64, 4, 4, 0, 0, "gelu", False),
+    (96, 4, 1, 4, 9, "swiglu", True),
+    (64, 2, 2, 2, 5, "gelu", True),
+])
+def test_full_drafter_vs_torch_restatement(H, hq, hkv, window, n_ctx, ffn, all_rows):
+    """Every weight live at once (jittered norms, two layers, context rows, windowed keys,
+    d == H and d != H, both FFN gates, GQA and MHA, drafts from rows 1..gamma-1 or from all
+    rows): the oracle's logits, tokens and confidences equal the torch restatement above.
+    The other pins fix one piece each with the rest switched off; this one catches a mistake
+    in how the pieces are chained (a norm weight of the wrong layer, the residual taken from
+    the wrong stream, context keys normed with the wrong vector, the head fed unnormed rows)."""
+    cfg = syn.with_overrides(tiny(H=H, hq=hq, hkv=hkv, window=window, gamma=5), ffn=ffn,
+                             draft_all_rows=all_rows)
+    m = model(cfg)
+    for i in range(cfg.n_layers):
+        m.mats[f"bb.{i}.q"].data[:] *= 6.0        # scores far from uniform
+        m.mats[f"bb.{i}.k"].data[:] *= 6.0
+    o = oracle.Oracle(m)
+    t = taps(cfg, n_ctx)
+    out = o.draft(13, *o.ctx_rows(t))
+    logits, tok, conf = _torch_drafter(cfg, m, 13, t.reshape(n_ctx, cfg.n_taps * H), all_rows, ffn == "gelu")
+    assert out["logits"].shape == logits.shape == (cfg.gamma if all_rows else cfg.gamma - 1, cfg.vocab)
+    scale = float(np.abs(logits).max())
+    assert scale > 1e-3
+    assert np.allclose(out["logits"], logits, rtol=0, atol=1e-12 * max(1.0, scale))
+    assert np.array_equal(out["tokens"], tok)
+    assert np.allclose(out["conf"], conf, rtol=1e-11, atol=0)
+
+
 def test_non_causal_block():
     """is_causal is false: block row 1 (draft 1) depends on block row gamma-1, which only
     mask_emb[gamma-2] feeds. A causal variant of the same oracle shows no such dependence."""
