@@ -100,7 +100,10 @@ typedef struct {
                          and LM-head projections once over all its rows on the tcgen05 contraction
                          (as dflash_rows_matmul), followed by the same epilogues; likewise
                          dflash_project_ctx runs W_c once per 160 context rows when a call appends
-                         more than 32. It applies to 4-bit weights with d == H and no Markov head;
+                         more than 32, and every layer's context K/V of those rows in one grouped
+                         launch (the 32-row GEMV chunks instead when a request's ring would wrap
+                         within the call, so later rows overwrite earlier ones in order). It
+                         applies to 4-bit weights with d == H and no Markov head;
                          other calls use the GEMV. The workspace grows by the contraction's scratch
                          and an f16 copy of 160 tap rows. */
   int skinny_tc05;    /* 0: calls of at most 32 block rows run every projection as the mma.sync
