@@ -1,5 +1,5 @@
 """The bench's host logic on CPU: the multi-GPU replicas (max elapsed over ranks, units summed;
-gloo, world size 2) and the oracle timing table."""
+gloo, world size 2), the oracle timing table and the reference arm's line."""
 import os
 import sys
 
@@ -102,3 +102,40 @@ def test_oracle_table_one_core_and_all_cores():
     assert {r["threads"] for r in rows} == {1, t["cores"]}
     for r in rows:
         assert r["config"] == "c1" and r["round_s"] > 0 and abs(r["blocks_per_s"] * r["round_s"] - 1) < 1e-9
+
+
+def _run_bench(args, env_extra):
+    import json
+    import subprocess
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                       env=env, cwd=ROOT, timeout=600)
+    lines = [json.loads(s) for s in r.stdout.splitlines() if s.startswith("{")]
+    return r.returncode, lines, r.stderr
+
+
+def test_reference_arm_line_on_the_small_drafter():
+    """`bench.py --impl reference` times the oracle on the host and prints one JSON line with the
+    contract's keys: impl, metric/unit/value, the cpu_baseline that describes this run (its value is
+    the line's), and an e2e object with no host-device copies."""
+    rc, lines, err = _run_bench(["--impl", "reference", "--config", "c1", "--steps", "2", "--warmup", "3"],
+                                {"RANK": "0", "WORLD_SIZE": "1"})
+    assert rc == 0, err
+    assert len(lines) == 1
+    ln = lines[0]
+    assert ln["impl"] == "reference" and ln["unit"] == "blocks/s" and ln["higher_is_better"] is True
+    assert ln["steps"] == 2 and ln["warmup"] == 3 and ln["dtype"] == "f64" and ln["value"] > 0
+    assert ln["config"]["workload"].startswith("c1")
+    cb = ln["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == ln["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert ln["e2e"] == {"value": ln["value"], "unit": "blocks/s", "h2d_bytes_per_step": 0,
+                         "d2h_bytes_per_step": 0}
+    assert abs(ln["ms_per_step"] - 1e3 / ln["value"]) < 1e-6 * ln["ms_per_step"]
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    """Under torchrun only rank 0 runs the reference arm and prints; the other ranks exit 0 silently."""
+    rc, lines, err = _run_bench(["--impl", "reference", "--config", "c1", "--steps", "2", "--warmup", "3"],
+                                {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert rc == 0, err
+    assert lines == []
