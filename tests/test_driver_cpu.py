@@ -73,3 +73,76 @@ def test_closed_loop_pruning_caps_acceptance():
     assert list(res.keep) == [2] and list(res.accepted) == [2] and list(res.next_anchor) == [3]
     loop.commit(res)
     assert loop.req[0].pending == 3 and loop.req[0].anchor == 3
+
+
+class RecordingTarget(SyntheticTarget):
+    """The synthetic target, recording which positions' taps the driver asks for."""
+
+    def __init__(self, cfg, agree):
+        super().__init__(cfg, agree=agree)
+        self.tap_calls = []
+
+    def taps(self, req, pos0, count):
+        self.tap_calls.append((req, pos0, count))
+        return super().taps(req, pos0, count)
+
+
+class RandomDraftSession(FakeSession):
+    """Fresh random drafts and confidences every call (the synthetic target agrees with each draft
+    with its probability p, so blocks are accepted at many lengths)."""
+
+    def __init__(self, cfg, rng):
+        super().__init__(cfg, None, None)
+        self.rng = rng
+
+    def draft(self, reqs, anchors, logits=False):
+        self.drafted_anchors.append(list(anchors))
+        n = self.cfg.n_draft
+        d = self.rng.integers(0, self.cfg.vocab, size=(len(reqs), n), dtype=np.int32)
+        c = self.rng.uniform(0.0, 1.0, size=(len(reqs), n)).astype(np.float32)
+        return {"rc": 0, "tokens": d, "conf": c}
+
+
+def test_closed_loop_many_rounds_bookkeeping():
+    """Twenty rounds of four requests with random blocks, with and without pruning: every committed
+    position's taps are appended exactly once and in order; each round commits the anchor and the
+    accepted drafts (each equal to the target's token there); the bonus token is the next anchor."""
+    c = cfg()
+    for min_conf in (None, 0.3):
+        rng = np.random.default_rng(11)
+        target = RecordingTarget(c, agree=0.7)
+        s = RandomDraftSession(c, rng)
+        loop = ClosedLoop(s, target, min_conf=min_conf)
+        prompts = {0: 8, 1: 1, 2: 5, 3: 13}
+        for b, p in prompts.items():
+            loop.start(b, p, anchor=20 + b)
+        expect_committed = {b: [] for b in prompts}
+        seen_a = set()
+        for r in range(20):
+            anchors_before = {b: loop.req[b].anchor for b in prompts}
+            res = loop.step()
+            assert s.drafted_anchors[-1] == [anchors_before[b] for b in sorted(prompts)]
+            for i, b in enumerate(sorted(prompts)):
+                a, keep = int(res.accepted[i]), int(res.keep[i])
+                assert 0 <= a <= keep <= c.n_draft
+                if min_conf is None:
+                    assert keep == c.n_draft
+                assert list(res.drafts[i][:a]) == list(res.targets[i][:a])
+                assert a == keep or res.drafts[i][a] != res.targets[i][a]
+                assert res.next_anchor[i] == res.targets[i][a]
+                seen_a.add(a)
+                expect_committed[b] += [anchors_before[b]] + [int(x) for x in res.drafts[i][:a]]
+            loop.commit(res)
+            for i, b in enumerate(sorted(prompts)):
+                assert loop.req[b].anchor == res.next_anchor[i]
+                assert loop.req[b].committed == expect_committed[b]
+        assert len(seen_a) >= 3           # short and long accepted prefixes both occurred
+        # taps: per request one contiguous run of positions 0 .. prompt + committed - 1 (the last
+        # round's commits are still pending), each position once
+        for b, p in prompts.items():
+            calls = [(p0, n) for rb, p0, n in target.tap_calls if rb == b]
+            pos = 0
+            for p0, n in calls:
+                assert p0 == pos and n > 0
+                pos += n
+            assert pos == loop.req[b].pos == p + len(expect_committed[b]) - loop.req[b].pending
