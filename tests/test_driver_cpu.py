@@ -146,3 +146,66 @@ def test_closed_loop_many_rounds_bookkeeping():
                 assert p0 == pos and n > 0
                 pos += n
             assert pos == loop.req[b].pos == p + len(expect_committed[b]) - loop.req[b].pending
+
+
+class GreedyTarget(SyntheticTarget):
+    """A deterministic stand-in target: its greedy token at position q of request b is a fixed hash
+    f(b, q), whatever came before. It tracks the position of each request's anchor itself."""
+
+    def __init__(self, cfg, prompts):
+        super().__init__(cfg)
+        self.q = {b: p - 1 for b, p in prompts.items()}      # the anchor is the prompt's last token
+
+    def f(self, b, q):
+        return int((b * 1000003 + q * 7919 + 17) % self.cfg.vocab)
+
+    def verify(self, rnd, b, drafts):
+        q = self.q[b]
+        t = np.array([self.f(b, q + 1 + k) for k in range(self.cfg.n_draft + 1)], dtype=np.int32)
+        a = 0
+        while a < len(drafts) and drafts[a] == t[a]:
+            a += 1
+        self.q[b] = q + a + 1                                  # a drafts and the bonus token commit
+        return t
+
+
+class PeekingSession(FakeSession):
+    """Drafts that equal the target's tokens with probability 0.6 each, else random."""
+
+    def __init__(self, cfg, target, rng):
+        super().__init__(cfg, None, None)
+        self.t, self.rng = target, rng
+
+    def draft(self, reqs, anchors, logits=False):
+        n = self.cfg.n_draft
+        d = self.rng.integers(0, self.cfg.vocab, size=(len(reqs), n)).astype(np.int32)
+        for i, b in enumerate(reqs):
+            for k in range(n):
+                if self.rng.uniform() < 0.6:
+                    d[i, k] = self.t.f(b, self.t.q[b] + 1 + k)
+        return {"rc": 0, "tokens": d, "conf": self.rng.uniform(0.0, 1.0, size=(len(reqs), n)).astype(np.float32)}
+
+
+def test_closed_loop_output_is_the_targets_greedy_sequence():
+    """Greedy speculative decoding changes only how many tokens a round commits, never which: with
+    random drafts, with and without confidence pruning (which keeps position 0 and only shortens
+    what the target verifies), every request's committed tokens are the target's own greedy
+    sequence from the prompt's last token on."""
+    c = cfg()
+    prompts = {0: 8, 1: 3, 2: 6}
+    for min_conf in (None, 0.5):
+        target = GreedyTarget(c, prompts)
+        loop = ClosedLoop(PeekingSession(c, target, np.random.default_rng(5)), target, min_conf=min_conf)
+        for b, p in prompts.items():
+            loop.start(b, p, anchor=target.f(b, p - 1))
+        lengths = []
+        for _ in range(25):
+            res = loop.step()
+            if min_conf is not None:
+                assert np.all(res.keep >= 1)
+            loop.commit(res)
+            lengths += [int(x) + 1 for x in res.accepted]
+        for b, p in prompts.items():
+            got = loop.req[b].committed + [loop.req[b].anchor]
+            assert got == [target.f(b, p - 1 + j) for j in range(len(got))]
+        assert max(lengths) > 1 and min(lengths) == 1        # rounds of several tokens and of one
