@@ -83,3 +83,12 @@ def test_debug_build_exports_the_same_symbols():
     assert path == pkg.LIB_PATH_DEBUG
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
     assert set(declared()) <= set(re.findall(r" T (dflash_\w+)", out))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """With the compiled library absent the binding raises; there is no CPU fallback to take."""
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "libdflash.so"))
+    monkeypatch.setattr(pkg, "LIB_PATH_DEBUG", str(tmp_path / "libdflash_debug.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        pkg.lib()
