@@ -101,6 +101,36 @@ def load_traffic(kernel: str):
 LM_HEAD_SOURCES = ("common.cuh", "gemv_f32.cu", "gemv_impl.cuh", "gemv_q4.cu", "internal.h")
 ATTN_SOURCES = ("attn.cu", "common.cuh", "internal.h")
 
+def on_tc05(cfg) -> bool:
+    """Whether the library's many-row option applies to this drafter (4-bit weights, d == H, no
+    Markov head): calls of more than 32 rows then run on the tcgen05 contraction."""
+    return (bool(getattr(cfg, "large_batch_tc05", False)) and cfg.wdtype == "q4" and cfg.d == cfg.target_hidden
+            and not getattr(cfg, "markov_rank", 0))
+
+
+def ctx_calls(cfg, ctx_rows_per_round):
+    """(launches per round, rows per launch) of the context classes: one per block of up to 160
+    rows on the tcgen05 path (calls of more than 32 rows), else one per 32-row chunk."""
+    rows = int(round(ctx_rows_per_round))
+    tc = on_tc05(cfg) and rows > 32
+    chunks = max(1, -(-rows // (160 if tc else 32)))
+    return chunks, ctx_rows_per_round / chunks, tc
+
+
+def tc05_classes(cfg, ctx_rows_per_round) -> set:
+    """The probed classes that run on the tcgen05 contraction: every block projection and the head
+    when a draft call carries 33-160 block rows, the context classes when a context call carries
+    more than 32 rows."""
+    if not on_tc05(cfg):
+        return set()
+    out = set()
+    if 32 < cfg.batch * cfg.gamma <= 160:
+        out |= {"qkv", "o", "gate_up", "down", "lm_head"}
+    if ctx_calls(cfg, ctx_rows_per_round)[2]:
+        out |= {"w_c", "ctx_kv"}
+    return out
+
+
 # Kernel classes of a round that bench.py times live (dflash_set_probe kinds): name, probe kind,
 # launches per round, algorithmic bytes per launch (weights at their stored size; attention: the
 # window's context K and V rows of one layer).
@@ -110,11 +140,9 @@ def probe_classes(cfg, ctx_lens, ctx_rows_per_round):
     act = 4 if cfg.adtype == "f32" else 2
     keys = sum(min(int(P), cfg.window) if cfg.window else int(P) for P in ctx_lens)
     L, d, I = cfg.n_layers, cfg.d, cfg.inter
-    rows = int(round(ctx_rows_per_round))
     # context calls of more than 32 rows on the tcgen05 path: W_c and every layer's K/V once per
     # block of up to 160 rows (the probes bracket a whole block); otherwise once per 32-row chunk
-    tc = getattr(cfg, "large_batch_tc05", False) and cfg.wdtype == "q4" and rows > 32
-    chunks = max(1, -(-rows // (160 if tc else 32)))
+    chunks = ctx_calls(cfg, ctx_rows_per_round)[0]
     return [("lm_head", 0, 1, cfg.vocab * cfg.target_hidden * bpp),
             ("qkv", 1, L, (qd + 2 * kvd) * d * bpp),
             ("attention", 2, L, keys * kvd * 2 * act),
@@ -123,6 +151,77 @@ def probe_classes(cfg, ctx_lens, ctx_rows_per_round):
             ("down", 5, L, d * I * bpp),
             ("w_c", 6, chunks, d * cfg.n_taps * cfg.target_hidden * bpp),
             ("ctx_kv", 7, chunks, L * 2 * kvd * d * bpp)]
+
+
+def class_flops(cfg, ctx_lens, ctx_rows_per_round) -> dict:
+    """Algorithmic FLOP per launch of each probed class (2 per weight and activation row; attention:
+    QK^T and PV over the window's keys plus the block's own). Summed with the launches per round of
+    probe_classes they give round_flops' total (d == H)."""
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    L, d, I = cfg.n_layers, cfg.d, cfg.inter
+    rows_b, rows_d = cfg.batch * cfg.gamma, cfg.batch * cfg.n_draft
+    keys = sum((min(int(P), cfg.window) if cfg.window else int(P)) + cfg.gamma for P in ctx_lens)
+    rows_c = ctx_calls(cfg, ctx_rows_per_round)[1]
+    return {"lm_head": 2.0 * rows_d * cfg.vocab * cfg.target_hidden,
+            "qkv": 2.0 * rows_b * (qd + 2 * kvd) * d,
+            "attention": 4.0 * cfg.n_q_heads * cfg.gamma * keys * cfg.head_dim,
+            "o": 2.0 * rows_b * d * qd,
+            "gate_up": 2.0 * rows_b * 2 * I * d,
+            "down": 2.0 * rows_b * d * I,
+            "w_c": 2.0 * rows_c * d * cfg.n_taps * cfg.target_hidden,
+            "ctx_kv": 2.0 * rows_c * L * 2 * kvd * d}
+
+
+GEMV_LABELS = {"lm_head": "4-bit GEMV + fused argmax/softmax confidence, then the vocab merge",
+               "attention": "block attention over the window (+ split merge)",
+               "w_c": "4-bit GEMV, context projection (Eq 2) + ctx norm sums",
+               "ctx_kv": "4-bit GEMV, context K/V of every layer, one grouped launch"}
+TC05_LABELS = {"lm_head": "tcgen05 contraction over every drafting row + vocab-state epilogue, then the vocab merge",
+               "w_c": "tcgen05 contraction, context projection (Eq 2) of a block of up to 160 rows + chunk epilogues",
+               "ctx_kv": "tcgen05 contraction, context K/V of every layer in one grouped launch + epilogue"}
+
+
+def class_rooflines(cfg, classes, class_ms, t_round_ms, peaks, ctx_lens, ctx_rows_per_round):
+    """Per probed class: live time, share of the round, algorithmic bytes and FLOP per launch and
+    both fractions; and the roofline object of the class with the largest share. A class on the
+    tcgen05 contraction whose FLOP per byte is above the ridge (tensor peak / HBM peak) is reported
+    against the tensor peak (the burst bf16 figure: f16 operands run at the bf16 rate), every other
+    class against the HBM copy bandwidth."""
+    flops = class_flops(cfg, ctx_lens, ctx_rows_per_round)
+    tc = tc05_classes(cfg, ctx_rows_per_round)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    by_kernel = {}
+    for name, kind, per_round, nbytes in classes:
+        ms = class_ms[name]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        tfs = flops[name] / (ms / 1e3) / 1e12
+        bound = "tensor" if name in tc and flops[name] / nbytes > ridge else "hbm"
+        by_kernel[name] = {"avg_launch_us": 1e3 * ms, "launches_per_round": per_round,
+                           "share_of_round": ms * per_round / t_round_ms, "algorithmic_bytes_per_launch": nbytes,
+                           "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+                           "algorithmic_flop_per_launch": flops[name], "achieved_tflops": tfs,
+                           "tensor_frac": tfs / peaks["bf16_tflops"],
+                           "path": "tcgen05" if name in tc else ("attention" if name == "attention" else "gemv"),
+                           "bound": bound}
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["share_of_round"])
+    dk = by_kernel[dom]
+    labels = TC05_LABELS if dom in tc else GEMV_LABELS
+    default = ("tcgen05 contraction over every block row + fused epilogue, layer 0 (the layers are identical)"
+               if dom in tc else "4-bit GEMV with fused epilogue, layer 0 (the layers are identical)")
+    roof = {"kernel": f"{dom}: " + labels.get(dom, default), "bound": dk["bound"]}
+    if dk["bound"] == "tensor":
+        roof.update({"achieved": dk["achieved_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": dk["tensor_frac"], "traffic": None,
+                     "algorithmic_flop_per_launch": dk["algorithmic_flop_per_launch"],
+                     "hbm_frac": dk["frac"],
+                     "peak_source": f"{peaks['source']} (cuBLAS bf16 burst, MEASURED_PEAKS.json bf16_tflops)"})
+    else:
+        roof.update({"achieved": dk["achieved_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": dk["frac"], "traffic": None if dom in tc else load_traffic(dom),
+                     "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"],
+                     "peak_source": f"{peaks['source']} (burst copy, MEASURED_PEAKS.json hbm_gbs)"})
+    roof.update({"avg_launch_ms": dk["avg_launch_us"] / 1e3, "share_of_round": dk["share_of_round"]})
+    return by_kernel, roof
 
 
 def kernel_source_hash(names=LM_HEAD_SOURCES) -> str:
@@ -627,25 +726,7 @@ def main():
     # the class that takes the largest share of the round (launch time x launches per round)
     class_ms["lm_head"] = lm_ms
     t_round_ms = 1e3 * t_max / args.steps
-    by_kernel = {}
-    for name, kind, per_round, nbytes in classes:
-        ms = class_ms[name]
-        gbs = nbytes / (ms / 1e3) / 1e9
-        by_kernel[name] = {"avg_launch_us": 1e3 * ms, "launches_per_round": per_round,
-                           "share_of_round": ms * per_round / t_round_ms, "algorithmic_bytes_per_launch": nbytes,
-                           "achieved_gbs": gbs, "frac": gbs / peaks["hbm_gbs"]}
-    dom = max(by_kernel, key=lambda k: by_kernel[k]["share_of_round"])
-    dk = by_kernel[dom]
-    roof = {"kernel": f"{dom}: " + {"lm_head": "4-bit GEMV + fused argmax/softmax confidence, then the vocab merge",
-                                    "attention": "block attention over the window (+ split merge)",
-                                    "w_c": "4-bit GEMV, context projection (Eq 2) + ctx norm sums",
-                                    "ctx_kv": "4-bit GEMV, context K/V of every layer, one grouped launch"}.get(
-                dom, "4-bit GEMV with fused epilogue, layer 0 (the layers are identical)"),
-            "bound": "hbm", "achieved": dk["achieved_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": dk["frac"], "traffic": load_traffic(dom),
-            "algorithmic_bytes_per_launch": dk["algorithmic_bytes_per_launch"],
-            "avg_launch_ms": dk["avg_launch_us"] / 1e3, "share_of_round": dk["share_of_round"],
-            "peak_source": f"{peaks['source']} (burst copy, MEASURED_PEAKS.json hbm_gbs)"}
+    by_kernel, roof = class_rooflines(cfg, classes, class_ms, t_round_ms, peaks, lengths, ctx_rows)
     line = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,

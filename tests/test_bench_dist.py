@@ -139,3 +139,73 @@ def test_reference_arm_other_ranks_exit_without_work():
                                 {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert rc == 0, err
     assert lines == []
+
+
+def _classes_and_times(cfg, lengths, ctx_rows, dominant):
+    import bench
+    classes = bench.probe_classes(cfg, lengths, ctx_rows)
+    ms = {name: 0.01 for name, _, _, _ in classes}
+    ms[dominant] = 0.1
+    return classes, ms
+
+
+@pytest.mark.parametrize("name,tc", [("c3", False), ("c5", False), ("c5", True)])
+def test_class_flops_add_up_to_the_round(name, tc):
+    """Per-launch FLOP of the probed classes times their launches per round equal the round's
+    algorithmic FLOP, on either projection path."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    cfg = syn.with_overrides(syn.CONFIGS[name], large_batch_tc05=tc)
+    lengths = [4096] * cfg.batch
+    ctx_rows = 144.0 if cfg.batch > 1 else 8.0
+    fl = bench.class_flops(cfg, lengths, ctx_rows)
+    total = sum(fl[n] * per_round for n, _, per_round, _ in bench.probe_classes(cfg, lengths, ctx_rows))
+    assert abs(total - bench.round_flops(cfg, lengths, ctx_rows)["total"]) <= 1e-9 * total
+
+
+def test_rooflines_gemv_round_is_hbm_bound():
+    """The 8-row round (one request): every class on the GEMV, the dominant one reported in GB/s
+    against the copy bandwidth, with its ncu traffic lookup."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    cfg = syn.CONFIGS["c3"]
+    classes, ms = _classes_and_times(cfg, [4096], 8.0, "gate_up")
+    peaks = {"hbm_gbs": 6660.3, "bf16_tflops": 1884.6, "bf16_tflops_sustained": 1723.8, "source": "measured"}
+    by, roof = bench.class_rooflines(cfg, classes, ms, 0.58, peaks, [4096], 8.0)
+    assert all(v["path"] in ("gemv", "attention") and v["bound"] == "hbm" for v in by.values())
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["kernel"].startswith("gate_up: 4-bit GEMV")
+    nbytes = 2 * cfg.inter * cfg.d * 0.5625
+    assert abs(roof["achieved"] - nbytes / 1e-4 / 1e9) < 1e-6 * roof["achieved"]
+    assert abs(roof["frac"] - roof["achieved"] / 6660.3) < 1e-12
+    assert "traffic" in roof and abs(by["gate_up"]["share_of_round"] - 0.1 * 5 / 0.58) < 1e-12
+
+
+def test_rooflines_batched_tcgen05_round_is_tensor_bound():
+    """The batched round on the tcgen05 path (160 block rows, 144 context rows per round): the
+    block projections, the head and the context classes are contractions above the ridge, reported
+    in TFLOP/s against the burst tensor peak; attention stays HBM-bound; without the option the same
+    round is all GEMV."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import dflash_synth as syn
+    peaks = {"hbm_gbs": 6660.3, "bf16_tflops": 1884.6, "bf16_tflops_sustained": 1723.8, "source": "measured"}
+    cfg = syn.with_overrides(syn.CONFIGS["c5"], large_batch_tc05=True)
+    lengths = [4096] * 32
+    assert bench.tc05_classes(cfg, 144.0) == {"qkv", "o", "gate_up", "down", "lm_head", "w_c", "ctx_kv"}
+    assert bench.tc05_classes(cfg, 20.0) == {"qkv", "o", "gate_up", "down", "lm_head"}
+    classes, ms = _classes_and_times(cfg, lengths, 144.0, "gate_up")
+    by, roof = bench.class_rooflines(cfg, classes, ms, 2.0, peaks, lengths, 144.0)
+    assert by["attention"]["bound"] == "hbm" and by["attention"]["path"] == "attention"
+    assert all(by[n]["bound"] == "tensor" and by[n]["path"] == "tcgen05" for n in ("qkv", "o", "gate_up", "down", "lm_head"))
+    assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s" and roof["traffic"] is None
+    assert roof["kernel"].startswith("gate_up: tcgen05 contraction")
+    flop = 2.0 * 160 * 2 * cfg.inter * cfg.d
+    assert abs(roof["achieved"] - flop / 1e-4 / 1e12) < 1e-9 * roof["achieved"]
+    assert abs(roof["frac"] - roof["achieved"] / 1884.6) < 1e-12 and roof["peak"] == 1884.6
+    off = syn.CONFIGS["c5"]
+    assert bench.tc05_classes(off, 144.0) == set()
+    by_off, roof_off = bench.class_rooflines(off, *_classes_and_times(off, lengths, 144.0, "gate_up"), 2.0, peaks,
+                                             lengths, 144.0)
+    assert roof_off["bound"] == "hbm" and all(v["path"] != "tcgen05" for v in by_off.values())
